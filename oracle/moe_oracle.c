@@ -1,0 +1,311 @@
+/*
+ * moe_oracle.c -- plain, slow, fp64 oracle of the MoE FFN layer forward.
+ *
+ * TEST INFRASTRUCTURE, NOT PART OF THE LIBRARY.  Only the tests, the smoke
+ * check and the benchmark's CPU-baseline leg may load or call this code.  It
+ * shares nothing with the CUDA path: no header, helper, table or constant.
+ *
+ * What it computes, step by step, in the order the Colibri pages give the
+ * MoE pipeline ("Colibri：面向MoE架构的C语言级高效推理引擎" §2.1: router logits,
+ * top-k, dispatch to the k experts, k expert matmuls, weighted sum):
+ *
+ *  1. router logits  l[t][e] = sum_i x[t][i] * Wr[e][i] + b[e]
+ *     (the router's linear projection with bias, same page §3.2; Wr stored
+ *     as [E][d] out-by-in, the channel-last rule of §3.1)
+ *  2. gating: softmax over the E logits, then top-k, weights renormalised
+ *     over the k ("Colibri：面向MoE模型的高性能C语言推理引擎" §1, §2.1).
+ *     Experts are ordered by (logit descending, index ascending), so ties go
+ *     to the lower index; slot s is the s-th expert in that order.  Because
+ *     softmax is monotone and its full denominator cancels after the
+ *     renormalisation, w[t][s] = exp(l_s - l_0) / sum_{j<k} exp(l_j - l_0).
+ *     A NaN logit ranks below every number; among NaNs the lower index wins.
+ *  3. dispatch (the dispatch kernel of the first page's §2.3): per-expert
+ *     counts, exclusive prefix-sum offsets, and the canonical permutation:
+ *     rows of expert e hold its tokens in ascending token order.
+ *     tok[row] = token, inv[t][s] = row.
+ *  4. expert FFN per routed row (SwiGLU with w1 = gate, w3 = up,
+ *     w2 = down, second page §4.2): g_j = sum_i x_i Wg[e][j][i],
+ *     u_j = sum_i x_i Wu[e][j][i], h_j = SiLU(g_j) u_j with
+ *     SiLU(z) = z / (1 + exp(-z)), y_c = sum_j h_j Wd[e][c][j].
+ *     int8 experts (symmetric per-output-channel, "lshu.cn/news/53496" §4.3):
+ *     W[e][j][i] = s[e][j] * Q[e][j][i], so g_j = s_g[e][j] * sum_i x_i Q_g.
+ *     Mode EXACT keeps h in double; mode BF16H rounds each h_j to bf16
+ *     (round to nearest even) before the down projection, which is the
+ *     precision the layer's bf16 down-projection operand holds.
+ *  5. combine (the combine kernel of the first page's §2.3):
+ *     o[t] = sum_s w[t][s] * y(t, s).
+ *
+ * Every sum is a plain sequential loop in double.  Inputs are bf16 bit
+ * patterns (uint16) or int8 codes with float scales.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+typedef struct {
+  int32_t T, d, f, E, k;
+  int32_t wdtype;                 /* 0 = bf16 weights, 1 = int8 + scales */
+  const uint16_t *x;              /* [T][d] bf16 bits                    */
+  const uint16_t *wr;             /* [E][d] bf16 bits                    */
+  const float *bias;              /* [E] or NULL                         */
+  const void *wg, *wu;            /* [E][f][d] bf16 bits or int8         */
+  const void *wd;                 /* [E][d][f]                           */
+  const float *sg, *su;           /* [E][f] (int8 only)                  */
+  const float *sd;                /* [E][d] (int8 only)                  */
+} moe_oracle_layer_t;
+
+enum { ORACLE_EXACT = 0, ORACLE_BF16H = 1 };
+
+/* ---------------------------------------------------------------- threads */
+void moe_oracle_set_threads(int n) {
+#ifdef _OPENMP
+  if (n > 0) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}
+
+int moe_oracle_get_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+/* ---------------------------------------------------------------- numbers */
+static double bf16_value(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return (double)f;
+}
+
+/* Round a double to the nearest bf16 value (ties to even), returned as a
+ * double.  Normal range: clear the low 45 of the 52 fraction bits with
+ * round-half-even on the bit pattern; subnormal range: the 2^-133 grid. */
+double moe_oracle_round_bf16(double v) {
+  if (isnan(v) || isinf(v) || v == 0.0) return v;
+  double a = fabs(v);
+  if (a < 0x1p-126) return copysign(nearbyint(a * 0x1p133) * 0x1p-133, v);
+  uint64_t b;
+  memcpy(&b, &v, 8);
+  uint64_t lsb = (b >> 45) & 1u;
+  b += ((uint64_t)1 << 44) - 1u + lsb;
+  b &= ~(((uint64_t)1 << 45) - 1u);
+  double r;
+  memcpy(&r, &b, 8);
+  if (fabs(r) > 0x1.FEp127) return copysign(INFINITY, v);
+  return r;
+}
+
+/* bf16 bit pattern of a value already on the bf16 grid */
+uint16_t moe_oracle_bf16_bits(double v) {
+  double r = moe_oracle_round_bf16(v);
+  float f = (float)r;
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  if (isnan(v)) return 0x7FC0;
+  return (uint16_t)(u >> 16);
+}
+
+static double weight_elem(const moe_oracle_layer_t *L, const void *w, int64_t idx) {
+  if (L->wdtype == 0) return bf16_value(((const uint16_t *)w)[idx]);
+  return (double)((const int8_t *)w)[idx];
+}
+
+/* ---------------------------------------------------------- 1. the router */
+/* logits of token t into l[0..E) */
+static void router_logits_row(const moe_oracle_layer_t *L, int64_t t, double *l) {
+  const uint16_t *xr = L->x + t * (int64_t)L->d;
+  for (int e = 0; e < L->E; ++e) {
+    const uint16_t *wr = L->wr + (int64_t)e * L->d;
+    double acc = 0.0;
+    for (int i = 0; i < L->d; ++i) acc += bf16_value(xr[i]) * bf16_value(wr[i]);
+    if (L->bias) acc += (double)L->bias[e];
+    l[e] = acc;
+  }
+}
+
+/* ---------------------------------------------------------- 2. top-k gate */
+/* 1 if expert (a, ia) ranks before (b, ib) */
+static int ranks_before(double a, int ia, double b, int ib) {
+  int na = isnan(a), nb = isnan(b);
+  if (na != nb) return nb;          /* the number beats the NaN */
+  if (na && nb) return ia < ib;
+  if (a != b) return a > b;
+  return ia < ib;
+}
+
+/* Full order of the E experts by insertion sort on ranks_before. */
+static void order_experts(int E, const double *l, int *order) {
+  for (int e = 0; e < E; ++e) {
+    int j = e;
+    while (j > 0 && ranks_before(l[e], e, l[order[j - 1]], order[j - 1])) {
+      order[j] = order[j - 1];
+      --j;
+    }
+    order[j] = e;
+  }
+}
+
+/* One token's gate: ids[k], w[k]; gap_k = l(k-1) - l(k) in the sorted order
+ * (+inf when k == E), gap_slot = smallest adjacent gap among the k chosen
+ * (+inf when k == 1).  Returns 0, or -1 on bad sizes. */
+int moe_oracle_gate(int E, int k, const double *l, int32_t *ids, double *w,
+                    double *gap_k, double *gap_slot) {
+  if (E <= 0 || k <= 0 || k > E) return -1;
+  int *order = (int *)malloc(sizeof(int) * (size_t)E);
+  if (!order) return -1;
+  order_experts(E, l, order);
+  double l0 = l[order[0]];
+  double den = 0.0;
+  for (int s = 0; s < k; ++s) den += exp(l[order[s]] - l0);
+  for (int s = 0; s < k; ++s) {
+    ids[s] = order[s];
+    w[s] = exp(l[order[s]] - l0) / den;
+  }
+  if (gap_k) *gap_k = (k < E) ? l[order[k - 1]] - l[order[k]] : INFINITY;
+  if (gap_slot) {
+    double g = INFINITY;
+    for (int s = 0; s + 1 < k; ++s) {
+      double dg = l[order[s]] - l[order[s + 1]];
+      if (dg < g) g = dg;
+    }
+    *gap_slot = g;
+  }
+  free(order);
+  return 0;
+}
+
+/* Route tokens tokens[0..n) (or 0..n when tokens == NULL).  Outputs are
+ * indexed by position in the list; logits may be NULL. */
+int moe_oracle_route(const moe_oracle_layer_t *L, const int32_t *tokens, int64_t n,
+                     double *logits, int32_t *ids, double *w, double *gap_k, double *gap_slot) {
+  int bad = 0;
+  #pragma omp parallel
+  {
+    double *l = (double *)malloc(sizeof(double) * (size_t)L->E);
+    #pragma omp for schedule(dynamic, 16)
+    for (int64_t p = 0; p < n; ++p) {
+      int64_t t = tokens ? tokens[p] : p;
+      if (!l || t < 0 || t >= L->T) { bad = 1; continue; }
+      router_logits_row(L, t, l);
+      if (logits) memcpy(logits + p * L->E, l, sizeof(double) * (size_t)L->E);
+      if (moe_oracle_gate(L->E, L->k, l, ids + p * L->k, w + p * L->k,
+                          gap_k ? gap_k + p : NULL, gap_slot ? gap_slot + p : NULL))
+        bad = 1;
+    }
+    free(l);
+  }
+  return bad ? -1 : 0;
+}
+
+/* ---------------------------------------------------------- 3. dispatch */
+/* Counting sort of the T*k (token, slot) pairs by expert, stable in token
+ * order.  cnt[E], off[E+1], tok[T*k], inv[T*k].  Returns -1 on an id out of
+ * range or a token holding one expert twice. */
+int moe_oracle_dispatch(int64_t T, int E, int k, const int32_t *ids,
+                        int32_t *cnt, int32_t *off, int32_t *tok, int32_t *inv) {
+  if (E <= 0 || k <= 0 || T < 0) return -1;
+  for (int e = 0; e < E; ++e) cnt[e] = 0;
+  for (int64_t t = 0; t < T; ++t)
+    for (int s = 0; s < k; ++s) {
+      int32_t e = ids[t * k + s];
+      if (e < 0 || e >= E) return -1;
+      for (int s2 = 0; s2 < s; ++s2)
+        if (ids[t * k + s2] == e) return -1;
+      cnt[e] += 1;
+    }
+  off[0] = 0;
+  for (int e = 0; e < E; ++e) off[e + 1] = off[e] + cnt[e];
+  int32_t *fill = (int32_t *)calloc((size_t)E, sizeof(int32_t));
+  if (!fill) return -1;
+  for (int64_t t = 0; t < T; ++t)
+    for (int s = 0; s < k; ++s) {
+      int32_t e = ids[t * k + s];
+      int32_t r = off[e] + fill[e]++;
+      tok[r] = (int32_t)t;
+      inv[t * k + s] = r;
+    }
+  free(fill);
+  return 0;
+}
+
+/* ---------------------------------------------------------- 4. one expert */
+/* y[d] = FFN_e(xrow).  h is scratch of f doubles. */
+static void expert_row(const moe_oracle_layer_t *L, int e, const double *xv, int mode,
+                       double *h, double *y) {
+  const int d = L->d, f = L->f;
+  const int64_t gbase = (int64_t)e * f * d, dbase = (int64_t)e * d * f;
+  for (int j = 0; j < f; ++j) {
+    double g = 0.0, u = 0.0;
+    for (int i = 0; i < d; ++i) {
+      g += xv[i] * weight_elem(L, L->wg, gbase + (int64_t)j * d + i);
+      u += xv[i] * weight_elem(L, L->wu, gbase + (int64_t)j * d + i);
+    }
+    if (L->wdtype == 1) {
+      g *= (double)L->sg[(int64_t)e * f + j];
+      u *= (double)L->su[(int64_t)e * f + j];
+    }
+    double silu = g / (1.0 + exp(-g));
+    double hj = silu * u;
+    h[j] = (mode == ORACLE_BF16H) ? moe_oracle_round_bf16(hj) : hj;
+  }
+  for (int c = 0; c < d; ++c) {
+    double acc = 0.0;
+    for (int j = 0; j < f; ++j) acc += h[j] * weight_elem(L, L->wd, dbase + (int64_t)c * f + j);
+    if (L->wdtype == 1) acc *= (double)L->sd[(int64_t)e * d + c];
+    y[c] = acc;
+  }
+}
+
+/* Expert e applied to an arbitrary bf16 row (d elements). */
+void moe_oracle_expert(const moe_oracle_layer_t *L, int e, const uint16_t *xrow, int mode, double *y) {
+  double *xv = (double *)malloc(sizeof(double) * (size_t)L->d);
+  double *h = (double *)malloc(sizeof(double) * (size_t)L->f);
+  for (int i = 0; i < L->d; ++i) xv[i] = bf16_value(xrow[i]);
+  expert_row(L, e, xv, mode, h, y);
+  free(xv);
+  free(h);
+}
+
+/* ---------------------------------------------------------- 5. the layer */
+/* Layer output for tokens[0..n) (all tokens when NULL): out[n][d] in double,
+ * plus the gate's ids[n][k] and w[n][k] (either may be NULL). */
+int moe_oracle_forward(const moe_oracle_layer_t *L, const int32_t *tokens, int64_t n, int mode,
+                       double *out, int32_t *ids_out, double *w_out) {
+  const int d = L->d, E = L->E, k = L->k;
+  int bad = 0;
+  #pragma omp parallel
+  {
+    double *l = (double *)malloc(sizeof(double) * (size_t)E);
+    double *xv = (double *)malloc(sizeof(double) * (size_t)d);
+    double *h = (double *)malloc(sizeof(double) * (size_t)L->f);
+    double *y = (double *)malloc(sizeof(double) * (size_t)d);
+    int32_t *ids = (int32_t *)malloc(sizeof(int32_t) * (size_t)k);
+    double *w = (double *)malloc(sizeof(double) * (size_t)k);
+    #pragma omp for schedule(dynamic, 1)
+    for (int64_t p = 0; p < n; ++p) {
+      int64_t t = tokens ? tokens[p] : p;
+      if (!l || !xv || !h || !y || !ids || !w || t < 0 || t >= L->T) { bad = 1; continue; }
+      router_logits_row(L, t, l);
+      if (moe_oracle_gate(E, k, l, ids, w, NULL, NULL)) { bad = 1; continue; }
+      for (int i = 0; i < d; ++i) xv[i] = bf16_value(L->x[t * (int64_t)d + i]);
+      double *o = out + p * d;
+      for (int c = 0; c < d; ++c) o[c] = 0.0;
+      for (int s = 0; s < k; ++s) {
+        expert_row(L, ids[s], xv, mode, h, y);
+        for (int c = 0; c < d; ++c) o[c] += w[s] * y[c];
+      }
+      if (ids_out) memcpy(ids_out + p * k, ids, sizeof(int32_t) * (size_t)k);
+      if (w_out) memcpy(w_out + p * k, w, sizeof(double) * (size_t)k);
+    }
+    free(l); free(xv); free(h); free(y); free(ids); free(w);
+  }
+  return bad ? -1 : 0;
+}

@@ -1,0 +1,59 @@
+"""Plant plausible mistakes in a copy of the oracle (on the CPU) and check that
+each one fails at least one pin: the pins are strong enough to notice a dropped
+term, a wrong sign or index, a transposed operand or a wrong rounding."""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+import oracle_pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "moe_oracle.c")
+
+MUTANTS = {
+    "gate_up_swapped": ("double silu = g / (1.0 + exp(-g));\n    double hj = silu * u;",
+                        "double silu = u / (1.0 + exp(-u));\n    double hj = silu * g;"),
+    "silu_sign": ("double silu = g / (1.0 + exp(-g));", "double silu = g / (1.0 + exp(g));"),
+    "bias_dropped": ("if (L->bias) acc += (double)L->bias[e];", ""),
+    "tie_to_higher_index": ("if (a != b) return a > b;\n  return ia < ib;", "if (a != b) return a > b;\n  return ia > ib;"),
+    "nan_ranks_first": ("if (na != nb) return nb;", "if (na != nb) return na;"),
+    "not_renormalised": ("for (int s = 0; s < k; ++s) den += exp(l[order[s]] - l0);",
+                         "for (int s = 0; s < E; ++s) den += exp(l[order[s]] - l0);"),
+    "weights_reversed": ("w[s] = exp(l[order[s]] - l0) / den;", "w[s] = exp(l[order[k - 1 - s]] - l0) / den;"),
+    "gate_transposed": ("g += xv[i] * weight_elem(L, L->wg, gbase + (int64_t)j * d + i);",
+                        "g += xv[i] * weight_elem(L, L->wg, gbase + (int64_t)i * f + j);"),
+    "down_transposed": ("weight_elem(L, L->wd, dbase + (int64_t)c * f + j)",
+                        "weight_elem(L, L->wd, dbase + (int64_t)j * d + c)"),
+    "bf16_truncates": ("b += ((uint64_t)1 << 44) - 1u + lsb;", ""),
+    "bf16_ties_away": ("b += ((uint64_t)1 << 44) - 1u + lsb;", "b += ((uint64_t)1 << 44);"),
+    "int8_gate_uses_up_scale": ("g *= (double)L->sg[(int64_t)e * f + j];", "g *= (double)L->su[(int64_t)e * f + j];"),
+    "int8_down_scale_index": ("acc *= (double)L->sd[(int64_t)e * d + c];", "acc *= (double)L->sd[(int64_t)e * d];"),
+    "dispatch_reversed_order": ("int32_t r = off[e] + fill[e]++;", "int32_t r = off[e + 1] - 1 - fill[e]++;"),
+    "combine_drops_weight": ("for (int c = 0; c < d; ++c) o[c] += w[s] * y[c];",
+                             "for (int c = 0; c < d; ++c) o[c] += y[c];"),
+    "router_wrong_row": ("const uint16_t *xr = L->x + t * (int64_t)L->d;", "const uint16_t *xr = L->x;"),
+    "bf16h_skips_rounding": ("h[j] = (mode == ORACLE_BF16H) ? moe_oracle_round_bf16(hj) : hj;", "h[j] = hj;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site for {name} not unique"
+    mpath = tmp_path / "mutant.c"
+    mpath.write_text(src.replace(old, new))
+    so = tmp_path / "libmutant.so"
+    subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11", "-fno-fast-math",
+                           "-ffp-contract=off", str(mpath), "-o", str(so), "-lm"],
+                          stderr=subprocess.DEVNULL)
+    lib = oracle.load(str(so))
+    caught = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(lib)
+        except (AssertionError, ValueError, RuntimeError) as ex:
+            caught.append(pin.__name__)
+            break
+    assert caught, f"mutant {name} passed every pin"

@@ -1,0 +1,67 @@
+"""The seeded input generator against its own published definition (CPU only)."""
+import math
+
+import numpy as np
+
+import synth
+
+M64 = (1 << 64) - 1
+
+
+def _mix(z):
+    z ^= z >> 30; z = (z * 0xBF58476D1CE4E5B9) & M64
+    z ^= z >> 27; z = (z * 0x94D049BB133111EB) & M64
+    return z ^ (z >> 31)
+
+
+def test_stream_words_follow_splitmix64():
+    seed, tid = 1234, 5
+    key = _mix(seed ^ _mix((tid + 0x632BE59BD9B4E019) & M64))
+    want = [_mix((key + (i + 1) * 0x9E3779B97F4A7C15) & M64) for i in range(64)]
+    assert synth.raw_bits(seed, tid, 64).tolist() == want
+    # counter based: any slice equals the same slice of the whole stream
+    assert synth.raw_bits(seed, tid, 10, offset=50).tolist() == want[50:60]
+
+
+def test_box_muller_values_and_moments():
+    seed, tid = 99, 3
+    bits = synth.raw_bits(seed, tid, 8)
+    u = ((bits >> np.uint64(11)).astype(np.float64) + 0.5) * 2.0 ** -53
+    z = synth.normal_f64(seed, tid, 1.0, (8,))
+    for j in range(4):
+        r = math.sqrt(-2.0 * math.log(u[2 * j]))
+        assert math.isclose(z[2 * j], r * math.cos(2 * math.pi * u[2 * j + 1]), rel_tol=1e-14, abs_tol=1e-15)
+        assert math.isclose(z[2 * j + 1], r * math.sin(2 * math.pi * u[2 * j + 1]), rel_tol=1e-14, abs_tol=1e-15)
+    big = synth.normal_f64(seed, tid, 1.0, (400000,))
+    assert abs(big.mean()) < 0.01 and abs(big.std() - 1.0) < 0.01
+
+
+def test_bf16_and_int8_rounding_of_draws():
+    import torch
+    z = synth.normal_f64(7, 1, 0.02, (50000,))
+    b = synth.normal_bf16(7, 1, 0.02, (50000,))
+    got = synth.bf16_bits_to_f32(b).astype(np.float64)
+    # nearest bf16 value: no bf16 neighbour is closer (ties are measure-zero here)
+    up = synth.bf16_bits_to_f32((b.astype(np.int32) + 1).astype(np.uint16)).astype(np.float64)
+    dn = synth.bf16_bits_to_f32((b.astype(np.int32) - 1).astype(np.uint16)).astype(np.float64)
+    err = np.abs(got - z)
+    assert np.all(err <= np.abs(up - z)) and np.all(err <= np.abs(dn - z))
+    # agrees with torch wherever the float32 rounding cannot matter
+    ref = torch.from_numpy(z.astype(np.float32)).to(torch.bfloat16).float().numpy().astype(np.float64)
+    assert np.mean(ref == got) > 0.999
+    q = synth.int8_codes(7, 2, 40.0, (50000,))
+    zq = synth.normal_f64(7, 2, 40.0, (50000,))
+    assert np.array_equal(q.astype(np.float64), np.clip(np.rint(zq), -127, 127))
+    s = synth.uniform_f32(7, 3, 0.5e-3, 1e-3, (10000,))
+    assert s.min() >= 0.5e-3 and s.max() <= 1e-3
+
+
+def test_workload_shapes():
+    w = synth.WORKLOADS
+    assert (w["mixtral_prefill"].T, w["mixtral_prefill"].d, w["mixtral_prefill"].f) == (4096, 4096, 14336)
+    assert (w["skewed"].E, w["skewed"].k, w["skewed"].bias) == (128, 4, True)
+    assert (w["int8"].wdtype, w["int8"].k, w["int8"].E) == ("int8", 6, 64)
+    b = synth.skew_bias(128)
+    assert b[0] == 0.0 and math.isclose(b[127], 2 * math.log(1 / 128), rel_tol=1e-7)
+    L = synth.make_layer(w["tiny"])
+    assert L.x.shape == (64, 256) and L.wg.shape == (8, 512, 256) and L.wd.shape == (8, 256, 512)
