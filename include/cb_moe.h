@@ -1,0 +1,162 @@
+/*
+ * cb_moe.h -- C ABI of a GB300 (sm_103a) Mixture-of-Experts FFN layer forward.
+ *
+ * The layer (the MoE pipeline of "Colibri：面向MoE架构的C语言级高效推理引擎" §2.1,
+ * with the init / infer / free host interface of its §2.3):
+ *
+ *   l[t][e]   = sum_i x[t][i] Wr[e][i] + b[e]                (fp32 logits)
+ *   ids[t][:] = the k experts with the largest logits, ties to the lower
+ *               index, in (logit descending, index ascending) order
+ *   w[t][s]   = exp(l[t][ids[t][s]] - l[t][ids[t][0]]) / sum_{j<k} (same)
+ *               (softmax, top-k, renormalised over the k: the gate of
+ *               "Colibri：面向MoE模型的高性能C语言推理引擎" §1 and §2.1)
+ *   dispatch  : per-expert counts, prefix-sum offsets, and a stable
+ *               permutation (expert ascending, then token ascending)
+ *   H[r]      = bf16( SiLU(Xp[r] Wg[e]^T) * (Xp[r] Wu[e]^T) )  (SwiGLU,
+ *               w1 = gate, w3 = up, w2 = down: same page §4.2)
+ *   Y[r]      = H[r] Wd[e]^T                                  (fp32)
+ *   out[t]    = bf16( sum_s w[t][s] Y[row(t,s)] )             (combine)
+ *
+ * int8 experts: W[e][j][i] = s[e][j] * Q[e][j][i] with one fp32 scale per
+ * output channel (symmetric per-channel int8, "lshu.cn/news/53496" §4.3);
+ * the codes become bf16 exactly inside the GEMM and the scale multiplies the
+ * fp32 accumulator.
+ *
+ * Conventions for every call below:
+ *  - bf16 means IEEE bfloat16 stored as 16-bit words; all matrices are
+ *    row-major, weights channel-last [out_features][in_features] (first
+ *    page §3.1).
+ *  - "device" pointers are CUDA device (or managed) memory on the handle's
+ *    device, 16-byte aligned; "host" pointers are ordinary host memory
+ *    (pinned for asynchronous copies).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  All work is enqueued on it; no call below synchronises the
+ *    device except cb_moe_init, cb_moe_free and cb_moe_last_error.
+ *  - Errors in arguments are reported before anything is enqueued.  A
+ *    non-zero status never leaves a partial forward behind.
+ *  - A handle is not thread safe; one forward may be in flight per handle
+ *    (each forward reuses the handle's workspace).
+ */
+#ifndef CB_MOE_H
+#define CB_MOE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define CB_API __attribute__((visibility("default")))
+#else
+#define CB_API
+#endif
+
+typedef enum {
+  CB_OK = 0,
+  CB_ERR_INVALID_ARG = 1,  /* NULL pointer, negative size, k > E, x aliasing out        */
+  CB_ERR_UNSUPPORTED = 2,  /* d_model or d_ff not a multiple of 256, E > 256, k > 16,
+                              wrong GPU (not compute capability 10.3), missing scales     */
+  CB_ERR_ALIGNMENT = 3,    /* a pointer not 16-byte aligned                               */
+  CB_ERR_OOM = 4,          /* a device allocation in cb_moe_init failed                   */
+  CB_ERR_CUDA = 5,         /* a CUDA runtime call or kernel launch failed                 */
+  CB_ERR_TIMEOUT = 6,      /* a device-side wait ran past its bound (cb_moe_last_error)   */
+  CB_ERR_DEVICE = 7        /* a device-side range check failed, e.g. an expert id out of
+                              range or a row past the workspace (cb_moe_last_error)      */
+} cb_status_t;
+
+typedef enum { CB_W_BF16 = 0, CB_W_INT8 = 1 } cb_wdtype_t;
+
+/* config.flags */
+#define CB_FLAG_KEEP_LOGITS 0x1u   /* also store the fp32 router logits [T][E] */
+
+typedef struct {
+  int32_t n_tokens;   /* T: tokens in every forward on this handle (>= 0)         */
+  int32_t d_model;    /* d: multiple of 256                                      */
+  int32_t d_ff;       /* f: multiple of 256                                      */
+  int32_t n_experts;  /* E: 1..256                                               */
+  int32_t top_k;      /* k: 1..min(E, 16)                                        */
+  int32_t wdtype;     /* cb_wdtype_t of the expert weights                       */
+  int32_t device;     /* CUDA device ordinal                                     */
+  uint32_t flags;     /* CB_FLAG_*                                               */
+} cb_moe_config_t;
+
+/* Expert and router weights: device pointers, read only during cb_moe_init. */
+typedef struct {
+  const void *w_router;     /* bf16 [E][d]                                        */
+  const float *router_bias; /* fp32 [E], or NULL for no bias                      */
+  const void *w_gate;       /* bf16 or int8 [E][f][d]   (w1)                      */
+  const void *w_up;         /* bf16 or int8 [E][f][d]   (w3)                      */
+  const void *w_down;       /* bf16 or int8 [E][d][f]   (w2)                      */
+  const float *s_gate;      /* fp32 [E][f]  int8 only, else NULL                  */
+  const float *s_up;        /* fp32 [E][f]  int8 only, else NULL                  */
+  const float *s_down;      /* fp32 [E][d]  int8 only, else NULL                  */
+} cb_moe_weights_t;
+
+typedef struct cb_moe cb_moe_t;   /* opaque handle */
+
+/*
+ * Create a layer.  Validates the config (sizes, alignment, GPU), allocates
+ * every device buffer the layer will ever use (weights, workspace sized for
+ * n_tokens), and copies the weights into handle-owned memory, re-laid out
+ * for the GEMMs (gate and up rows interleaved in blocks of 128).  The caller
+ * may free its own weight buffers when this returns.  Synchronous.
+ * Returns CB_OK and *out, or an error with *out = NULL and nothing leaked.
+ */
+CB_API cb_status_t cb_moe_init(const cb_moe_config_t *cfg, const cb_moe_weights_t *weights, cb_moe_t **out);
+
+/*
+ * One forward pass: x bf16 [T][d] (device) -> out bf16 [T][d] (device).
+ * x and out are caller-owned, must not overlap, and must stay valid until
+ * the stream has run the work.  Asynchronous on `stream`; no allocation,
+ * no host synchronisation.  Device-side failures (bounds, timeouts) are
+ * reported later by cb_moe_last_error.
+ */
+CB_API cb_status_t cb_moe_forward(cb_moe_t *h, const void *x, void *out, void *stream);
+
+/* Same pass with the combine storing fp32 instead of bf16: out fp32 [T][d]. */
+CB_API cb_status_t cb_moe_forward_f32out(cb_moe_t *h, const void *x, float *out, void *stream);
+
+/*
+ * Same pass from host memory: copies x_host (bf16 [T][d]) to a handle-owned
+ * device buffer, runs cb_moe_forward, and copies the bf16 result back to
+ * out_host, all on `stream`.  Asynchronous when both host buffers are pinned;
+ * the caller synchronises the stream before reading out_host.
+ */
+CB_API cb_status_t cb_moe_forward_host(cb_moe_t *h, const void *x_host, void *out_host, void *stream);
+
+/* Device pointers of the routing of the last forward (valid until the next
+ * forward or cb_moe_free; read after synchronising its stream). */
+typedef struct {
+  const int32_t *ids;       /* [T][k] expert ids, slot order                       */
+  const float *w;           /* [T][k] renormalised gate weights                    */
+  const int32_t *counts;    /* [E]   rows per expert                               */
+  const int32_t *offsets;   /* [E+1] exclusive prefix sum of counts                */
+  const int32_t *tok;       /* [T*k] token of each row (expert-major, stable)      */
+  const int32_t *inv;       /* [T][k] row of each (token, slot)                    */
+  const float *logits;      /* [T][E] fp32 logits with bias, or NULL unless
+                               CB_FLAG_KEEP_LOGITS                                */
+  const int32_t *tile_offsets; /* [E+1] prefix sum of ceil(counts/128): the
+                               expert-aligned 128-row tiles of the GEMM layout   */
+} cb_routing_view_t;
+
+CB_API cb_status_t cb_moe_routing(const cb_moe_t *h, cb_routing_view_t *view);
+
+/* Synchronise the device, return the handle's device status word (CB_OK,
+ * CB_ERR_TIMEOUT or CB_ERR_DEVICE) and clear it. */
+CB_API cb_status_t cb_moe_last_error(cb_moe_t *h);
+
+/* Bytes of device memory a handle with this config holds (weights + workspace). */
+CB_API cb_status_t cb_moe_device_bytes(const cb_moe_config_t *cfg, uint64_t *bytes);
+
+/* Free every buffer of the handle (synchronises the device first).  NULL is OK. */
+CB_API cb_status_t cb_moe_free(cb_moe_t *h);
+
+/* Static description of a status code. */
+CB_API const char *cb_status_string(cb_status_t s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CB_MOE_H */

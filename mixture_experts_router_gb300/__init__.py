@@ -1,0 +1,180 @@
+"""Python binding of libcbmoe.so, the GB300 MoE FFN layer (C ABI in include/cb_moe.h).
+
+Argument marshalling only: every step of the layer runs in the library's CUDA
+kernels.  PyTorch is used by callers for device memory and streams; this module
+takes raw pointers (ints) or torch tensors and forwards them.  There is no
+fallback: if the shared library is missing or fails to load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libcbmoe.so")
+
+CB_OK, CB_ERR_INVALID_ARG, CB_ERR_UNSUPPORTED, CB_ERR_ALIGNMENT = 0, 1, 2, 3
+CB_ERR_OOM, CB_ERR_CUDA, CB_ERR_TIMEOUT, CB_ERR_DEVICE = 4, 5, 6, 7
+CB_W_BF16, CB_W_INT8 = 0, 1
+CB_FLAG_KEEP_LOGITS = 0x1
+
+# every symbol include/cb_moe.h declares
+ABI_SYMBOLS = ("cb_moe_init", "cb_moe_forward", "cb_moe_forward_f32out", "cb_moe_forward_host",
+               "cb_moe_routing", "cb_moe_last_error", "cb_moe_device_bytes", "cb_moe_free",
+               "cb_status_string")
+
+
+class cb_moe_config_t(ctypes.Structure):
+    _fields_ = [("n_tokens", ctypes.c_int32), ("d_model", ctypes.c_int32), ("d_ff", ctypes.c_int32),
+                ("n_experts", ctypes.c_int32), ("top_k", ctypes.c_int32), ("wdtype", ctypes.c_int32),
+                ("device", ctypes.c_int32), ("flags", ctypes.c_uint32)]
+
+
+class cb_moe_weights_t(ctypes.Structure):
+    _fields_ = [("w_router", ctypes.c_void_p), ("router_bias", ctypes.c_void_p),
+                ("w_gate", ctypes.c_void_p), ("w_up", ctypes.c_void_p), ("w_down", ctypes.c_void_p),
+                ("s_gate", ctypes.c_void_p), ("s_up", ctypes.c_void_p), ("s_down", ctypes.c_void_p)]
+
+
+class cb_routing_view_t(ctypes.Structure):
+    _fields_ = [("ids", ctypes.c_void_p), ("w", ctypes.c_void_p), ("counts", ctypes.c_void_p),
+                ("offsets", ctypes.c_void_p), ("tok", ctypes.c_void_p), ("inv", ctypes.c_void_p),
+                ("logits", ctypes.c_void_p), ("tile_offsets", ctypes.c_void_p)]
+
+
+class CbMoeError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {cb_status_string(status)} (status {status})")
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libcbmoe.so (build it first with __graft_entry__.build() or build.py)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"libcbmoe.so is not built ({path}); run mixture_experts_router_gb300/build.py")
+    lib = ctypes.CDLL(path)
+    vp, i32 = ctypes.c_void_p, ctypes.c_int
+    lib.cb_moe_init.argtypes = [ctypes.POINTER(cb_moe_config_t), ctypes.POINTER(cb_moe_weights_t),
+                                ctypes.POINTER(vp)]
+    lib.cb_moe_forward.argtypes = [vp, vp, vp, vp]
+    lib.cb_moe_forward_f32out.argtypes = [vp, vp, vp, vp]
+    lib.cb_moe_forward_host.argtypes = [vp, vp, vp, vp]
+    lib.cb_moe_routing.argtypes = [vp, ctypes.POINTER(cb_routing_view_t)]
+    lib.cb_moe_last_error.argtypes = [vp]
+    lib.cb_moe_device_bytes.argtypes = [ctypes.POINTER(cb_moe_config_t), ctypes.POINTER(ctypes.c_uint64)]
+    lib.cb_moe_free.argtypes = [vp]
+    for name in ("cb_moe_init", "cb_moe_forward", "cb_moe_forward_f32out", "cb_moe_forward_host",
+                 "cb_moe_routing", "cb_moe_last_error", "cb_moe_device_bytes", "cb_moe_free"):
+        getattr(lib, name).restype = i32
+    lib.cb_status_string.argtypes = [i32]
+    lib.cb_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+# --------------------------------------------------------- same-name calls
+def cb_status_string(status: int) -> str:
+    return load_library().cb_status_string(int(status)).decode()
+
+
+def cb_moe_init(cfg: cb_moe_config_t, weights: cb_moe_weights_t):
+    """Returns (status, handle); handle is None unless status == CB_OK."""
+    h = ctypes.c_void_p()
+    st = load_library().cb_moe_init(ctypes.byref(cfg), ctypes.byref(weights), ctypes.byref(h))
+    return st, (h.value if st == CB_OK else None)
+
+
+def cb_moe_forward(handle, x_ptr: int, out_ptr: int, stream: int = 0) -> int:
+    return load_library().cb_moe_forward(handle, x_ptr, out_ptr, stream)
+
+
+def cb_moe_forward_f32out(handle, x_ptr: int, out_ptr: int, stream: int = 0) -> int:
+    return load_library().cb_moe_forward_f32out(handle, x_ptr, out_ptr, stream)
+
+
+def cb_moe_forward_host(handle, x_host_ptr: int, out_host_ptr: int, stream: int = 0) -> int:
+    return load_library().cb_moe_forward_host(handle, x_host_ptr, out_host_ptr, stream)
+
+
+def cb_moe_routing(handle):
+    v = cb_routing_view_t()
+    st = load_library().cb_moe_routing(handle, ctypes.byref(v))
+    return st, v
+
+
+def cb_moe_last_error(handle) -> int:
+    return load_library().cb_moe_last_error(handle)
+
+
+def cb_moe_device_bytes(cfg: cb_moe_config_t):
+    b = ctypes.c_uint64()
+    st = load_library().cb_moe_device_bytes(ctypes.byref(cfg), ctypes.byref(b))
+    return st, b.value
+
+
+def cb_moe_free(handle) -> int:
+    return load_library().cb_moe_free(handle)
+
+
+# ------------------------------------------------------- torch convenience
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+class MoELayer:
+    """One layer handle over torch device tensors (bf16 as torch.bfloat16 or int16 bits,
+    int8 as torch.int8).  Raises CbMoeError on any non-zero status."""
+
+    def __init__(self, T, d, f, E, k, w_router, w_gate, w_up, w_down, router_bias=None,
+                 s_gate=None, s_up=None, s_down=None, device=0, keep_logits=False):
+        self.cfg = cb_moe_config_t(T, d, f, E, k, CB_W_INT8 if s_gate is not None else CB_W_BF16,
+                                   device, CB_FLAG_KEEP_LOGITS if keep_logits else 0)
+        w = cb_moe_weights_t(_ptr(w_router), _ptr(router_bias), _ptr(w_gate), _ptr(w_up), _ptr(w_down),
+                             _ptr(s_gate), _ptr(s_up), _ptr(s_down))
+        st, h = cb_moe_init(self.cfg, w)
+        if st != CB_OK:
+            raise CbMoeError(st, "cb_moe_init")
+        self.handle = h
+
+    def forward(self, x, out, stream=None, f32out=False):
+        s = 0 if stream is None else stream.cuda_stream
+        fn = cb_moe_forward_f32out if f32out else cb_moe_forward
+        st = fn(self.handle, x.data_ptr(), out.data_ptr(), s)
+        if st != CB_OK:
+            raise CbMoeError(st, "cb_moe_forward")
+        return out
+
+    def forward_host(self, x_host, out_host, stream=None):
+        s = 0 if stream is None else stream.cuda_stream
+        st = cb_moe_forward_host(self.handle, x_host.data_ptr(), out_host.data_ptr(), s)
+        if st != CB_OK:
+            raise CbMoeError(st, "cb_moe_forward_host")
+        return out_host
+
+    def routing(self):
+        st, v = cb_moe_routing(self.handle)
+        if st != CB_OK:
+            raise CbMoeError(st, "cb_moe_routing")
+        return v
+
+    def last_error(self) -> int:
+        return cb_moe_last_error(self.handle)
+
+    def close(self):
+        if getattr(self, "handle", None) is not None:
+            st = cb_moe_free(self.handle)
+            self.handle = None
+            if st != CB_OK:
+                raise CbMoeError(st, "cb_moe_free")
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,449 @@
+// Host side of the C ABI in cb_moe.h: argument validation, the one-time
+// allocation of every device buffer, the weight re-layout, the TMA tensor
+// maps, and the launch sequence of one forward pass.
+//
+// Mirrors the init / infer / free triple and the "C decides, CUDA executes"
+// split of "Colibri：面向MoE架构的C语言级高效推理引擎" §2.2-§2.3: the host fixes
+// launch shapes from (T, d, f, E, k) once, and every forward only enqueues
+// kernels on the caller's stream.  All memory is taken at init
+// ("discosf.com/news/4774337" §3.1) from one allocation carved into
+// 256-byte-aligned regions (the memory-pool offsets of "lshu.cn/news/53496"
+// §3), and dimensions must be multiples of 256 (same page, §3).
+#include <cudaTypedefs.h>
+
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "cb_moe.h"
+#include "internal.h"
+
+using namespace cbmoe;
+
+struct cb_moe {
+  cb_moe_config_t cfg;
+  int num_sms;
+  char* block;
+  uint64_t block_bytes;
+  // weights (handle-owned copies)
+  uint16_t* wr;
+  float* bias;
+  void* wgu;  // [E][f/128][2][128][d]: gate rows then up rows per 128-block
+  void* wd;   // [E][d][f]
+  float *sg, *su, *sd;
+  // workspace
+  uint16_t* xp;  // [mpad][d]
+  uint16_t* hb;  // [mpad][f]
+  float* y;      // [mpad][d]
+  int32_t* ids;
+  float* w;
+  float* logits;
+  int32_t *chunk, *counts, *offsets, *mtile_off, *mtile_expert, *tok, *inv;
+  int* err;
+  uint16_t *x_stage, *out_stage;
+  int32_t max_mtiles, n_chunks;
+  CUtensorMap tm_a_gu, tm_b_gu, tm_a_dn, tm_b_dn;
+};
+
+namespace {
+
+struct Layout {
+  uint64_t off_wr, off_bias, off_wgu, off_wd, off_sg, off_su, off_sd;
+  uint64_t off_xp, off_hb, off_y, off_ids, off_w, off_logits, off_chunk, off_counts, off_offsets, off_mtile_off,
+      off_mtile_expert, off_tok, off_inv, off_err, off_xs, off_os;
+  uint64_t total;
+  int32_t max_mtiles, n_chunks;
+};
+
+uint64_t align256(uint64_t v) { return (v + 255) & ~uint64_t(255); }
+
+Layout plan(const cb_moe_config_t& c) {
+  Layout L{};
+  const uint64_t T = c.n_tokens, d = c.d_model, f = c.d_ff, E = c.n_experts, k = c.top_k;
+  const uint64_t eb = (c.wdtype == CB_W_INT8) ? 1 : 2;
+  const uint64_t M = T * k;
+  L.max_mtiles = static_cast<int32_t>((M + E * (kTileM - 1)) / kTileM + 1);
+  L.n_chunks = static_cast<int32_t>((M + kDispatchChunk - 1) / kDispatchChunk);
+  const uint64_t mpad = static_cast<uint64_t>(L.max_mtiles) * kTileM;
+  uint64_t o = 0;
+  auto take = [&](uint64_t bytes) {
+    const uint64_t at = o;
+    o = align256(o + bytes);
+    return at;
+  };
+  L.off_wr = take(E * d * 2);
+  L.off_bias = take(E * 4);
+  L.off_wgu = take(E * 2 * f * d * eb);
+  L.off_wd = take(E * d * f * eb);
+  L.off_sg = take(c.wdtype == CB_W_INT8 ? E * f * 4 : 0);
+  L.off_su = take(c.wdtype == CB_W_INT8 ? E * f * 4 : 0);
+  L.off_sd = take(c.wdtype == CB_W_INT8 ? E * d * 4 : 0);
+  L.off_xp = take(mpad * d * 2);
+  L.off_hb = take(mpad * f * 2);
+  L.off_y = take(mpad * d * 4);
+  L.off_ids = take(M * 4);
+  L.off_w = take(M * 4);
+  L.off_logits = take((c.flags & CB_FLAG_KEEP_LOGITS) ? T * E * 4 : 0);
+  L.off_chunk = take(static_cast<uint64_t>(L.n_chunks) * E * 4);
+  L.off_counts = take(E * 4);
+  L.off_offsets = take((E + 1) * 4);
+  L.off_mtile_off = take((E + 1) * 4);
+  L.off_mtile_expert = take(static_cast<uint64_t>(L.max_mtiles) * 4);
+  L.off_tok = take(M * 4);
+  L.off_inv = take(M * 4);
+  L.off_err = take(64);
+  L.off_xs = take(T * d * 2);
+  L.off_os = take(T * d * 2);
+  L.total = o;
+  return L;
+}
+
+cb_status_t validate_config(const cb_moe_config_t* c) {
+  if (c == nullptr) return CB_ERR_INVALID_ARG;
+  if (c->n_tokens < 0 || c->d_model <= 0 || c->d_ff <= 0 || c->n_experts <= 0 || c->top_k <= 0)
+    return CB_ERR_INVALID_ARG;
+  if (c->top_k > c->n_experts) return CB_ERR_INVALID_ARG;
+  if (c->wdtype != CB_W_BF16 && c->wdtype != CB_W_INT8) return CB_ERR_INVALID_ARG;
+  if (c->d_model % 256 != 0 || c->d_ff % 256 != 0) return CB_ERR_UNSUPPORTED;
+  if (c->n_experts > 256 || c->top_k > 16) return CB_ERR_UNSUPPORTED;
+  if ((c->flags & ~CB_FLAG_KEEP_LOGITS) != 0) return CB_ERR_INVALID_ARG;
+  // 32-bit row and tile indices everywhere
+  const uint64_t M = static_cast<uint64_t>(c->n_tokens) * c->top_k;
+  const uint64_t rows = M + static_cast<uint64_t>(c->n_experts) * kTileM;
+  if (rows >= (1ull << 31) || static_cast<uint64_t>(c->n_experts) * 2 * c->d_ff >= (1ull << 31) ||
+      static_cast<uint64_t>(c->n_experts) * c->d_model >= (1ull << 31))
+    return CB_ERR_UNSUPPORTED;
+  return CB_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool fault_injected(const char* what) {
+  const char* v = std::getenv("CB_MOE_INJECT_FAULT");
+  return v != nullptr && std::strcmp(v, what) == 0;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D row-major tensor [outer][inner] with a box of box_outer x box_inner
+// elements and the 128-byte swizzle.
+bool make_tmap(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint64_t elem_bytes, uint64_t inner,
+               uint64_t outer, uint32_t box_inner, uint32_t box_outer) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * elem_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = false;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    ok = cudaSetDevice(dev) == cudaSuccess;
+  }
+  ~DeviceGuard() {
+    if (prev >= 0) cudaSetDevice(prev);
+  }
+};
+
+cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, cudaStream_t s) {
+  const cb_moe_config_t& c = h->cfg;
+  if (fault_injected("launch")) return CB_ERR_CUDA;
+
+  RouterArgs ra{};
+  ra.x = static_cast<const uint16_t*>(x);
+  ra.wr = h->wr;
+  ra.bias = h->bias;
+  ra.T = c.n_tokens;
+  ra.d = c.d_model;
+  ra.E = c.n_experts;
+  ra.k = c.top_k;
+  ra.ids = h->ids;
+  ra.w = h->w;
+  ra.logits = h->logits;
+  ra.err = h->err;
+  if (launch_router(ra, s) != cudaSuccess) return CB_ERR_CUDA;
+
+  DispatchArgs da{};
+  da.ids = h->ids;
+  da.x = static_cast<const uint16_t*>(x);
+  da.T = c.n_tokens;
+  da.k = c.top_k;
+  da.E = c.n_experts;
+  da.d = c.d_model;
+  da.n_chunks = h->n_chunks;
+  da.chunk = h->chunk;
+  da.counts = h->counts;
+  da.offsets = h->offsets;
+  da.mtile_off = h->mtile_off;
+  da.mtile_expert = h->mtile_expert;
+  da.max_mtiles = h->max_mtiles;
+  da.tok = h->tok;
+  da.inv = h->inv;
+  da.xp = h->xp;
+  da.gather_blocks = h->num_sms * 4;
+  da.err = h->err;
+  if (launch_dispatch(da, s) != cudaSuccess) return CB_ERR_CUDA;
+
+  const bool int8w = c.wdtype == CB_W_INT8;
+  GemmArgs ga{};
+  ga.mtile_off = h->mtile_off;
+  ga.mtile_expert = h->mtile_expert;
+  ga.E = c.n_experts;
+  ga.n_tiles = c.d_ff / grouped_gemm_tile_n(kGateUpSwiGLU);
+  ga.k_blocks = c.d_model / 64;
+  ga.b_rows_per_expert = 2 * c.d_ff;
+  ga.out = h->hb;
+  ga.ld_out = c.d_ff;
+  ga.scale0 = h->sg;
+  ga.scale1 = h->su;
+  ga.err = h->err;
+  ga.wait_limit_ns = kWaitLimitNs;
+  ga.grid = h->num_sms;
+  if (launch_grouped_gemm(kGateUpSwiGLU, int8w, h->tm_a_gu, h->tm_b_gu, ga, s) != cudaSuccess) return CB_ERR_CUDA;
+
+  GemmArgs gd = ga;
+  gd.n_tiles = c.d_model / grouped_gemm_tile_n(kDownF32);
+  gd.k_blocks = c.d_ff / 64;
+  gd.b_rows_per_expert = c.d_model;
+  gd.out = h->y;
+  gd.ld_out = c.d_model;
+  gd.scale0 = h->sd;
+  gd.scale1 = nullptr;
+  if (launch_grouped_gemm(kDownF32, int8w, h->tm_a_dn, h->tm_b_dn, gd, s) != cudaSuccess) return CB_ERR_CUDA;
+
+  CombineArgs ca{};
+  ca.y = h->y;
+  ca.w = h->w;
+  ca.ids = h->ids;
+  ca.inv = h->inv;
+  ca.offsets = h->offsets;
+  ca.mtile_off = h->mtile_off;
+  ca.T = c.n_tokens;
+  ca.k = c.top_k;
+  ca.d = c.d_model;
+  ca.out = out;
+  ca.out_f32 = f32out ? 1 : 0;
+  if (launch_combine(ca, s) != cudaSuccess) return CB_ERR_CUDA;
+  return CB_OK;
+}
+
+cb_status_t check_forward_args(const cb_moe_t* h, const void* x, const void* out, uint64_t out_elem_bytes) {
+  if (h == nullptr || x == nullptr || out == nullptr) return CB_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(out)) return CB_ERR_ALIGNMENT;
+  const uint64_t xb = static_cast<uint64_t>(h->cfg.n_tokens) * h->cfg.d_model * 2;
+  const uint64_t ob = static_cast<uint64_t>(h->cfg.n_tokens) * h->cfg.d_model * out_elem_bytes;
+  const uintptr_t xa = reinterpret_cast<uintptr_t>(x), oa = reinterpret_cast<uintptr_t>(out);
+  if (xb > 0 && xa < oa + ob && oa < xa + xb) return CB_ERR_INVALID_ARG;  // overlap
+  return CB_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* cb_status_string(cb_status_t s) {
+  switch (s) {
+    case CB_OK: return "ok";
+    case CB_ERR_INVALID_ARG: return "invalid argument";
+    case CB_ERR_UNSUPPORTED: return "unsupported configuration or device";
+    case CB_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case CB_ERR_OOM: return "device allocation failed";
+    case CB_ERR_CUDA: return "CUDA call or kernel launch failed";
+    case CB_ERR_TIMEOUT: return "device-side wait timed out";
+    case CB_ERR_DEVICE: return "device-side range check failed";
+  }
+  return "unknown status";
+}
+
+cb_status_t cb_moe_device_bytes(const cb_moe_config_t* cfg, uint64_t* bytes) {
+  if (bytes == nullptr) return CB_ERR_INVALID_ARG;
+  const cb_status_t st = validate_config(cfg);
+  if (st != CB_OK) return st;
+  *bytes = plan(*cfg).total;
+  return CB_OK;
+}
+
+cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts, cb_moe_t** out) {
+  if (out == nullptr) return CB_ERR_INVALID_ARG;
+  *out = nullptr;
+  cb_status_t st = validate_config(cfg);
+  if (st != CB_OK) return st;
+  if (wts == nullptr || wts->w_router == nullptr || wts->w_gate == nullptr || wts->w_up == nullptr ||
+      wts->w_down == nullptr)
+    return CB_ERR_INVALID_ARG;
+  const bool int8w = cfg->wdtype == CB_W_INT8;
+  if (int8w && (wts->s_gate == nullptr || wts->s_up == nullptr || wts->s_down == nullptr))
+    return CB_ERR_UNSUPPORTED;
+  const void* ptrs[] = {wts->w_router, wts->router_bias, wts->w_gate, wts->w_up, wts->w_down,
+                        wts->s_gate,   wts->s_up,        wts->s_down};
+  for (const void* p : ptrs)
+    if (p != nullptr && !aligned16(p)) return CB_ERR_ALIGNMENT;
+
+  DeviceGuard guard(cfg->device);
+  if (!guard.ok) return CB_ERR_UNSUPPORTED;
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, cfg->device) != cudaSuccess) return CB_ERR_CUDA;
+  if (prop.major != 10 || prop.minor != 3) return CB_ERR_UNSUPPORTED;
+  if (int8w) return CB_ERR_UNSUPPORTED;  // the int8 GEMM variant is not built yet
+
+  const Layout L = plan(*cfg);
+  cb_moe_t* h = new (std::nothrow) cb_moe_t();
+  if (h == nullptr) return CB_ERR_OOM;
+  h->cfg = *cfg;
+  h->num_sms = prop.multiProcessorCount;
+  h->max_mtiles = L.max_mtiles;
+  h->n_chunks = L.n_chunks;
+  h->block_bytes = L.total;
+  if (fault_injected("oom") || cudaMalloc(&h->block, L.total) != cudaSuccess) {
+    cudaGetLastError();
+    delete h;
+    return CB_ERR_OOM;
+  }
+  char* b = h->block;
+  h->wr = reinterpret_cast<uint16_t*>(b + L.off_wr);
+  h->bias = wts->router_bias ? reinterpret_cast<float*>(b + L.off_bias) : nullptr;
+  h->wgu = b + L.off_wgu;
+  h->wd = b + L.off_wd;
+  h->sg = int8w ? reinterpret_cast<float*>(b + L.off_sg) : nullptr;
+  h->su = int8w ? reinterpret_cast<float*>(b + L.off_su) : nullptr;
+  h->sd = int8w ? reinterpret_cast<float*>(b + L.off_sd) : nullptr;
+  h->xp = reinterpret_cast<uint16_t*>(b + L.off_xp);
+  h->hb = reinterpret_cast<uint16_t*>(b + L.off_hb);
+  h->y = reinterpret_cast<float*>(b + L.off_y);
+  h->ids = reinterpret_cast<int32_t*>(b + L.off_ids);
+  h->w = reinterpret_cast<float*>(b + L.off_w);
+  h->logits = (cfg->flags & CB_FLAG_KEEP_LOGITS) ? reinterpret_cast<float*>(b + L.off_logits) : nullptr;
+  h->chunk = reinterpret_cast<int32_t*>(b + L.off_chunk);
+  h->counts = reinterpret_cast<int32_t*>(b + L.off_counts);
+  h->offsets = reinterpret_cast<int32_t*>(b + L.off_offsets);
+  h->mtile_off = reinterpret_cast<int32_t*>(b + L.off_mtile_off);
+  h->mtile_expert = reinterpret_cast<int32_t*>(b + L.off_mtile_expert);
+  h->tok = reinterpret_cast<int32_t*>(b + L.off_tok);
+  h->inv = reinterpret_cast<int32_t*>(b + L.off_inv);
+  h->err = reinterpret_cast<int*>(b + L.off_err);
+  h->x_stage = reinterpret_cast<uint16_t*>(b + L.off_xs);
+  h->out_stage = reinterpret_cast<uint16_t*>(b + L.off_os);
+
+  const uint64_t E = cfg->n_experts, d = cfg->d_model, f = cfg->d_ff;
+  const uint64_t eb = int8w ? 1 : 2;
+  bool ok = cudaMemset(h->block + L.off_xp, 0, L.off_ids - L.off_xp) == cudaSuccess &&
+            cudaMemset(h->block + L.off_ids, 0, L.total - L.off_ids) == cudaSuccess;
+  ok = ok && cudaMemcpy(h->wr, wts->w_router, E * d * 2, cudaMemcpyDeviceToDevice) == cudaSuccess;
+  if (ok && h->bias) ok = cudaMemcpy(h->bias, wts->router_bias, E * 4, cudaMemcpyDeviceToDevice) == cudaSuccess;
+  ok = ok && cudaMemcpy(h->wd, wts->w_down, E * d * f * eb, cudaMemcpyDeviceToDevice) == cudaSuccess;
+  if (ok && int8w) {
+    ok = cudaMemcpy(h->sg, wts->s_gate, E * f * 4, cudaMemcpyDeviceToDevice) == cudaSuccess &&
+         cudaMemcpy(h->su, wts->s_up, E * f * 4, cudaMemcpyDeviceToDevice) == cudaSuccess &&
+         cudaMemcpy(h->sd, wts->s_down, E * d * 4, cudaMemcpyDeviceToDevice) == cudaSuccess;
+  }
+  // gate/up interleave: block n of expert e = gate rows [128n, 128n+128) then the same up rows
+  const uint64_t blk = 128 * d * eb;  // bytes of 128 weight rows
+  const uint64_t nblk = E * (f / 128);
+  ok = ok && cudaMemcpy2D(h->wgu, 2 * blk, wts->w_gate, blk, blk, nblk, cudaMemcpyDeviceToDevice) == cudaSuccess;
+  ok = ok && cudaMemcpy2D(static_cast<char*>(h->wgu) + blk, 2 * blk, wts->w_up, blk, blk, nblk,
+                          cudaMemcpyDeviceToDevice) == cudaSuccess;
+  const uint64_t mpad = static_cast<uint64_t>(h->max_mtiles) * kTileM;
+  const CUtensorMapDataType wdt = int8w ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  ok = ok && make_tmap(&h->tm_a_gu, h->xp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, mpad, 64, 128);
+  ok = ok && make_tmap(&h->tm_b_gu, h->wgu, wdt, eb, d, E * 2 * f, 64, 256);
+  ok = ok && make_tmap(&h->tm_a_dn, h->hb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, f, mpad, 64, 128);
+  ok = ok && make_tmap(&h->tm_b_dn, h->wd, wdt, eb, f, E * d, 64, 256);
+  ok = ok && grouped_gemm_prepare() == cudaSuccess && router_prepare() == cudaSuccess;
+  ok = ok && cudaDeviceSynchronize() == cudaSuccess;
+  if (!ok) {
+    cudaGetLastError();
+    cudaFree(h->block);
+    delete h;
+    return CB_ERR_CUDA;
+  }
+  *out = h;
+  return CB_OK;
+}
+
+cb_status_t cb_moe_forward(cb_moe_t* h, const void* x, void* out, void* stream) {
+  const cb_status_t st = check_forward_args(h, x, out, 2);
+  if (st != CB_OK) return st;
+  if (h->cfg.n_tokens == 0) return CB_OK;
+  DeviceGuard guard(h->cfg.device);
+  if (!guard.ok) return CB_ERR_CUDA;
+  return enqueue_forward(h, x, out, false, static_cast<cudaStream_t>(stream));
+}
+
+cb_status_t cb_moe_forward_f32out(cb_moe_t* h, const void* x, float* out, void* stream) {
+  const cb_status_t st = check_forward_args(h, x, out, 4);
+  if (st != CB_OK) return st;
+  if (h->cfg.n_tokens == 0) return CB_OK;
+  DeviceGuard guard(h->cfg.device);
+  if (!guard.ok) return CB_ERR_CUDA;
+  return enqueue_forward(h, x, out, true, static_cast<cudaStream_t>(stream));
+}
+
+cb_status_t cb_moe_forward_host(cb_moe_t* h, const void* x_host, void* out_host, void* stream) {
+  if (h == nullptr || x_host == nullptr || out_host == nullptr) return CB_ERR_INVALID_ARG;
+  if (h->cfg.n_tokens == 0) return CB_OK;
+  DeviceGuard guard(h->cfg.device);
+  if (!guard.ok) return CB_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const uint64_t bytes = static_cast<uint64_t>(h->cfg.n_tokens) * h->cfg.d_model * 2;
+  if (cudaMemcpyAsync(h->x_stage, x_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return CB_ERR_CUDA;
+  const cb_status_t st = enqueue_forward(h, h->x_stage, h->out_stage, false, s);
+  if (st != CB_OK) return st;
+  if (cudaMemcpyAsync(out_host, h->out_stage, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) return CB_ERR_CUDA;
+  return CB_OK;
+}
+
+cb_status_t cb_moe_routing(const cb_moe_t* h, cb_routing_view_t* v) {
+  if (h == nullptr || v == nullptr) return CB_ERR_INVALID_ARG;
+  v->ids = h->ids;
+  v->w = h->w;
+  v->counts = h->counts;
+  v->offsets = h->offsets;
+  v->tok = h->tok;
+  v->inv = h->inv;
+  v->logits = h->logits;
+  v->tile_offsets = h->mtile_off;
+  return CB_OK;
+}
+
+cb_status_t cb_moe_last_error(cb_moe_t* h) {
+  if (h == nullptr) return CB_ERR_INVALID_ARG;
+  DeviceGuard guard(h->cfg.device);
+  if (!guard.ok || cudaDeviceSynchronize() != cudaSuccess) return CB_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, h->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return CB_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpy(h->err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return CB_ERR_CUDA;
+  return static_cast<cb_status_t>(v);
+}
+
+cb_status_t cb_moe_free(cb_moe_t* h) {
+  if (h == nullptr) return CB_OK;
+  cb_status_t st = CB_OK;
+  {
+    DeviceGuard guard(h->cfg.device);
+    if (!guard.ok || cudaDeviceSynchronize() != cudaSuccess) st = CB_ERR_CUDA;
+    if (cudaFree(h->block) != cudaSuccess) st = CB_ERR_CUDA;
+  }
+  delete h;
+  return st;
+}
+
+}  // extern "C"

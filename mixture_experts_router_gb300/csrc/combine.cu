@@ -1,0 +1,80 @@
+// Combine: out[t] = sum_s w[t][s] * Y[row(t, s)], the weighted sum of the k
+// expert outputs by gating score (the combine kernel of
+// "Colibri：面向MoE架构的C语言级高效推理引擎" §2.3).  Y is fp32; the sum is fp32
+// FMA in slot order, rounded once to bf16 (or stored as fp32).
+//
+// One block per token: the k padded row indices are resolved once into
+// shared memory (row = tile_base(e) + (inv - offset(e))), then each thread
+// streams 8 columns at a time with 16-byte loads from the k rows.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+
+namespace cbmoe {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kMaxK = 16;
+
+template <bool F32OUT>
+__global__ void __launch_bounds__(kThreads) combine_kernel(CombineArgs a) {
+  __shared__ int64_t rows[kMaxK];
+  __shared__ float ws[kMaxK];
+  const int t = blockIdx.x;
+  if (threadIdx.x < a.k) {
+    const int s = threadIdx.x;
+    const int e = a.ids[static_cast<int64_t>(t) * a.k + s];
+    const int r = a.inv[static_cast<int64_t>(t) * a.k + s];
+    rows[s] = static_cast<int64_t>(a.mtile_off[e]) * kTileM + (r - a.offsets[e]);
+    ws[s] = a.w[static_cast<int64_t>(t) * a.k + s];
+  }
+  __syncthreads();
+  const int nvec = a.d / 8;
+  for (int v = threadIdx.x; v < nvec; v += kThreads) {
+    float acc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+    for (int s = 0; s < a.k; ++s) {
+      const float4* src = reinterpret_cast<const float4*>(a.y + rows[s] * a.d) + 2 * v;
+      const float4 p = __ldg(src), q = __ldg(src + 1);
+      const float wv = ws[s];
+      acc[0] = fmaf(wv, p.x, acc[0]);
+      acc[1] = fmaf(wv, p.y, acc[1]);
+      acc[2] = fmaf(wv, p.z, acc[2]);
+      acc[3] = fmaf(wv, p.w, acc[3]);
+      acc[4] = fmaf(wv, q.x, acc[4]);
+      acc[5] = fmaf(wv, q.y, acc[5]);
+      acc[6] = fmaf(wv, q.z, acc[6]);
+      acc[7] = fmaf(wv, q.w, acc[7]);
+    }
+    if constexpr (F32OUT) {
+      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + static_cast<int64_t>(t) * a.d) + 2 * v;
+      dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    } else {
+      uint4 o;
+      __nv_bfloat162 b0 = __floats2bfloat162_rn(acc[0], acc[1]);
+      __nv_bfloat162 b1 = __floats2bfloat162_rn(acc[2], acc[3]);
+      __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[4], acc[5]);
+      __nv_bfloat162 b3 = __floats2bfloat162_rn(acc[6], acc[7]);
+      o.x = *reinterpret_cast<uint32_t*>(&b0);
+      o.y = *reinterpret_cast<uint32_t*>(&b1);
+      o.z = *reinterpret_cast<uint32_t*>(&b2);
+      o.w = *reinterpret_cast<uint32_t*>(&b3);
+      reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + static_cast<int64_t>(t) * a.d)[v] = o;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s) {
+  if (a.T <= 0) return cudaSuccess;
+  if (a.out_f32)
+    combine_kernel<true><<<a.T, kThreads, 0, s>>>(a);
+  else
+    combine_kernel<false><<<a.T, kThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace cbmoe

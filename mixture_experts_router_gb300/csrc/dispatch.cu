@@ -1,0 +1,186 @@
+// Token dispatch: per-expert histogram, prefix sums and a stable permutation
+// of the T*k (token, slot) pairs, then the row gather that builds the
+// expert-grouped activations.  This is the dispatch kernel of
+// "Colibri：面向MoE架构的C语言级高效推理引擎" §2.3 (scatter each token to its k
+// experts' input buffers), whose irregular scatter and warp divergence that
+// page's §2.1 names as the cost.  Here the ranks come from warp match/ballot
+// prefix counts in flat (token, slot) order, so the permutation is
+// deterministic (expert ascending, then token ascending) and the row copies
+// are plain coalesced 16-byte moves.
+//
+//   dispatch_count   : per chunk of 2048 pairs, counts per expert
+//   dispatch_scan    : one block: per-expert totals, offsets, per-chunk row
+//                      bases, the expert-aligned 128-row tile prefix and the
+//                      tile -> expert map used by the grouped GEMMs
+//   dispatch_scatter : per chunk: warp-aggregated ranks -> tok[], inv[]
+//   dispatch_gather  : Xp[row] = x[tok[row]] over the padded row space
+#include "internal.h"
+
+namespace cbmoe {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kPerWarp = kDispatchChunk / kWarps;  // 256 pairs, 8 rounds of 32
+
+__global__ void __launch_bounds__(kThreads) dispatch_count(DispatchArgs a) {
+  __shared__ int hist[256];
+  for (int e = threadIdx.x; e < a.E; e += kThreads) hist[e] = 0;
+  __syncthreads();
+  const int64_t M = static_cast<int64_t>(a.T) * a.k;
+  const int64_t base = static_cast<int64_t>(blockIdx.x) * kDispatchChunk;
+  for (int i = threadIdx.x; i < kDispatchChunk; i += kThreads) {
+    const int64_t p = base + i;
+    if (p < M) {
+      const int e = a.ids[p];
+      if (e >= 0 && e < a.E)
+        atomicAdd(&hist[e], 1);
+      else
+        set_error(a.err, kErrDevice);
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < a.E; e += kThreads)
+    a.chunk[static_cast<int64_t>(blockIdx.x) * a.E + e] = hist[e];
+}
+
+// exclusive scan of one value per thread over a 256-thread block
+__device__ int block_exclusive_scan(int v, int* tmp) {
+  const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) tmp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int s = (lane < kWarps) ? tmp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    if (lane < kWarps) tmp[lane] = s;
+  }
+  __syncthreads();
+  const int r = x - v + (warp > 0 ? tmp[warp - 1] : 0);
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(kThreads) dispatch_scan(DispatchArgs a) {
+  __shared__ int tmp[kWarps];
+  const int e = threadIdx.x;
+  int total = 0;
+  if (e < a.E) {
+    for (int b = 0; b < a.n_chunks; ++b) {
+      int* slot = a.chunk + static_cast<int64_t>(b) * a.E + e;
+      const int c = *slot;
+      *slot = total;  // exclusive within this expert
+      total += c;
+    }
+  }
+  const int mt = (total + kTileM - 1) / kTileM;
+  const int off = block_exclusive_scan(e < a.E ? total : 0, tmp);
+  const int moff = block_exclusive_scan(e < a.E ? mt : 0, tmp);
+  if (e < a.E) {
+    a.counts[e] = total;
+    a.offsets[e] = off;
+    a.mtile_off[e] = moff;
+    if (e == a.E - 1) {
+      a.offsets[a.E] = off + total;
+      a.mtile_off[a.E] = moff + mt;
+      if (moff + mt > a.max_mtiles) set_error(a.err, kErrDevice);
+    }
+    for (int b = 0; b < a.n_chunks; ++b) a.chunk[static_cast<int64_t>(b) * a.E + e] += off;
+    for (int i = moff; i < moff + mt && i < a.max_mtiles; ++i) a.mtile_expert[i] = e;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) dispatch_scatter(DispatchArgs a) {
+  __shared__ int wh[kWarps][256];
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  for (int i = threadIdx.x; i < kWarps * 256; i += kThreads) (&wh[0][0])[i] = 0;
+  __syncthreads();
+  const int64_t M = static_cast<int64_t>(a.T) * a.k;
+  const int64_t wbase = static_cast<int64_t>(blockIdx.x) * kDispatchChunk + warp * kPerWarp;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+
+  // pass 1: this warp's count per expert
+  for (int r = 0; r < kPerWarp / 32; ++r) {
+    const int64_t p = wbase + r * 32 + lane;
+    int e = (p < M) ? a.ids[p] : -1;
+    if (e < 0 || e >= a.E) e = -1;
+    const uint32_t m = __match_any_sync(0xffffffffu, e);
+    if (e >= 0 && (__ffs(m) - 1) == lane) wh[warp][e] += __popc(m);
+  }
+  __syncthreads();
+  // per expert: exclusive over the warps, starting at this chunk's row base
+  for (int e = threadIdx.x; e < a.E; e += kThreads) {
+    int base = a.chunk[static_cast<int64_t>(blockIdx.x) * a.E + e];
+    for (int w = 0; w < kWarps; ++w) {
+      const int c = wh[w][e];
+      wh[w][e] = base;
+      base += c;
+    }
+  }
+  __syncthreads();
+  // pass 2: ranks in flat (token, slot) order
+  for (int r = 0; r < kPerWarp / 32; ++r) {
+    const int64_t p = wbase + r * 32 + lane;
+    int e = (p < M) ? a.ids[p] : -1;
+    if (e < 0 || e >= a.E) e = -1;
+    const uint32_t m = __match_any_sync(0xffffffffu, e);
+    int rank = 0;
+    if (e >= 0) rank = wh[warp][e] + __popc(m & lt_mask);
+    __syncwarp();
+    if (e >= 0 && (__ffs(m) - 1) == lane) wh[warp][e] += __popc(m);
+    __syncwarp();
+    if (e >= 0) {
+      if (rank < 0 || rank >= M) {
+        set_error(a.err, kErrDevice);
+      } else {
+        a.tok[rank] = static_cast<int32_t>(p / a.k);
+        a.inv[p] = rank;
+      }
+    }
+  }
+}
+
+// One warp per padded row: copy x[tok] into Xp with 16-byte vectors.
+__global__ void __launch_bounds__(kThreads) dispatch_gather(DispatchArgs a) {
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int total_tiles = min(a.mtile_off[a.E], a.max_mtiles);
+  const int64_t rows = static_cast<int64_t>(total_tiles) * kTileM;
+  const int vec_per_row = a.d / 8;
+  for (int64_t row = static_cast<int64_t>(blockIdx.x) * kWarps + warp; row < rows;
+       row += static_cast<int64_t>(gridDim.x) * kWarps) {
+    const int mt = static_cast<int>(row / kTileM);
+    const int e = a.mtile_expert[mt];
+    const int local = static_cast<int>(row - static_cast<int64_t>(a.mtile_off[e]) * kTileM);
+    if (local >= a.counts[e]) continue;  // padding row of the expert's last tile
+    const int t = a.tok[a.offsets[e] + local];
+    if (t < 0 || t >= a.T) {
+      if (lane == 0) set_error(a.err, kErrDevice);
+      continue;
+    }
+    const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<int64_t>(t) * a.d);
+    uint4* dst = reinterpret_cast<uint4*>(a.xp + row * a.d);
+    for (int v = lane; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s) {
+  if (a.n_chunks <= 0) return cudaSuccess;
+  dispatch_count<<<a.n_chunks, kThreads, 0, s>>>(a);
+  dispatch_scan<<<1, kThreads, 0, s>>>(a);
+  dispatch_scatter<<<a.n_chunks, kThreads, 0, s>>>(a);
+  dispatch_gather<<<a.gather_blocks, kThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace cbmoe

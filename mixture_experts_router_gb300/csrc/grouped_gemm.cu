@@ -1,0 +1,275 @@
+// Grouped expert GEMMs on the 5th-generation tensor cores (tcgen05).
+//
+// The expert matmuls of the MoE layer (the expert GEMM kernel of
+// "Colibri：面向MoE架构的C语言级高效推理引擎" §2.3, fused with the activation as in
+// "discosf.com/news/4774337" §3.2, which hand-wrote its MMA in PTX for the same
+// reason) run as one persistent kernel per projection over all experts:
+//
+//   gate/up : H[r, n*128 + j] = bf16( SiLU(acc[j]) * acc[128 + j] ),
+//             acc = Xp[r] . Wgu[e][n]^T, where the repacked weight block n of
+//             expert e holds gate rows n*128..n*128+127 followed by the same
+//             up rows, so one 128x256 accumulator carries matching gate and
+//             up columns (SwiGLU, w1 gate, w3 up:
+//             "Colibri：面向MoE模型的高性能C语言推理引擎" §4.2)
+//   down    : Y[r, n*256 + c] = acc[c], acc = H[r] . Wd[e][n]^T (fp32 out)
+//
+// Rows are the expert-grouped activations; every expert's block starts on a
+// 128-row boundary, so an M-tile belongs to exactly one expert, and the tile
+// list (expert-major, then N, then M) is derived on the device from the
+// dispatch's tile prefix sums: the host never learns the expert counts.
+//
+// Per CTA (one per SM, persistent, static round-robin over tiles):
+//   warp 0      : TMA producer (one thread): A 128x64 and B 256x64 bf16 boxes,
+//                 128-byte swizzle, into a 4-stage ring guarded by mbarriers
+//   warp 1      : owns the 512 TMEM columns; one thread issues
+//                 tcgen05.mma.cta_group::1.kind::f16 (M=128, N=256, K=16) x4
+//                 per stage and commits stage release / accumulator ready
+//   warps 2..5  : epilogue: tcgen05.ld 32 lanes x 32 columns, SwiGLU or fp32,
+//                 16-byte global stores; two accumulators alternate so the
+//                 epilogue of tile i overlaps the mainloop of tile i+1
+// Every wait is bounded; a wait that runs out records CB_ERR_TIMEOUT in the
+// status word and the CTA winds down (waiting for its own loads in flight
+// and freeing its TMEM).
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace cbmoe {
+namespace {
+
+constexpr int BM = kTileM;               // 128 rows per tile
+constexpr int BK = 64;                   // 64 bf16 = one 128-byte swizzled row
+constexpr int BN = 256;                  // accumulator columns per tile
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;     // 16 KB
+constexpr int B_BYTES = BN * BK * 2;     // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int THREADS = 192;
+constexpr uint32_t TMEM_COLS = 2 * BN;   // two fp32 accumulators of 256 columns
+constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+
+struct TileCoord {
+  int m_tile;  // global 128-row tile index in the grouped rows
+  int e;       // expert
+  int n;       // N tile within the expert
+};
+
+__device__ __forceinline__ TileCoord decode_tile(int tile, const GemmArgs& p) {
+  const int e = p.mtile_expert[tile / p.n_tiles];
+  const int base = p.mtile_off[e];
+  const int mt = p.mtile_off[e + 1] - base;
+  const int local = tile - base * p.n_tiles;
+  TileCoord c;
+  c.e = e;
+  c.n = local / mt;
+  c.m_tile = base + local % mt;
+  return c;
+}
+
+__device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&b);
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(THREADS, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                        const GemmArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sa = smem;
+  uint8_t* sb = smem + STAGES * A_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 128);
+    }
+    fence_barrier_init();
+    prefetch_tensormap(&tm_a);
+    prefetch_tensormap(&tm_b);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total_tiles = p.mtile_off[p.E] * p.n_tiles;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------ TMA producer
+      int stage = 0;
+      uint32_t phase = 0;
+      int64_t issued = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+        const TileCoord c = decode_tile(tile, p);
+        const int a_row = c.m_tile * BM;
+        const int b_row = c.e * p.b_rows_per_expert + c.n * BN;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, p.wait_limit_ns)) {
+            set_error(p.err, kErrTimeout);
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+          tma_load_2d(sa + stage * A_BYTES, &tm_a, &full[stage], kb * BK, a_row);
+          tma_load_2d(sb + stage * B_BYTES, &tm_b, &full[stage], kb * BK, b_row);
+          ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // No load of ours may still be landing in shared memory when the CTA
+      // exits: wait for the last load issued into each stage.
+      for (int64_t i = (issued > STAGES ? issued - STAGES : 0); i < issued; ++i) {
+        if (!mbar_wait(&full[i % STAGES], static_cast<uint32_t>((i / STAGES) & 1), p.wait_limit_ns))
+          set_error(p.err, kErrTimeout);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------- MMA issuer
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, p.wait_limit_ns)) {
+          set_error(p.err, kErrTimeout);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait(&full[stage], phase, p.wait_limit_ns)) {
+            set_error(p.err, kErrTimeout);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t adesc = sw128_desc(smem_u32(sa + stage * A_BYTES));
+          const uint64_t bdesc = sw128_desc(smem_u32(sb + stage * B_BYTES));
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            tc_mma_f16(d_tmem, adesc + 2 * k, bdesc + 2 * k, IDESC, (kb | k) != 0 ? 1u : 0u);
+          tc_commit(&empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(&tfull[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // this warp's quarter of the 128 TMEM lanes
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+      const TileCoord c = decode_tile(tile, p);
+      if (!mbar_wait(&tfull[acc], acc_phase, p.wait_limit_ns)) {
+        set_error(p.err, kErrTimeout);
+        break;
+      }
+      tc_fence_after();
+      const int64_t row = static_cast<int64_t>(c.m_tile) * BM + q * 32 + lane;
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      if constexpr (KIND == kGateUpSwiGLU) {
+        uint16_t* out_row = static_cast<uint16_t*>(p.out) + row * p.ld_out + c.n * (BN / 2);
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN / 2; c0 += 32) {
+          uint32_t g[32], u[32];
+          tmem_load32(tbase + c0, g);
+          tmem_load32(tbase + BN / 2 + c0, u);
+          uint32_t h[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float h0 = silu(__uint_as_float(g[2 * j])) * __uint_as_float(u[2 * j]);
+            const float h1 = silu(__uint_as_float(g[2 * j + 1])) * __uint_as_float(u[2 * j + 1]);
+            h[j] = pack_bf16x2(h0, h1);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(out_row + c0);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) dst[j] = make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
+        }
+      } else {
+        float* out_row = static_cast<float*>(p.out) + row * p.ld_out + c.n * BN;
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          uint32_t r[32];
+          tmem_load32(tbase + c0, r);
+          float4* dst = reinterpret_cast<float4*>(out_row + c0);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                 __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+}  // namespace
+
+int grouped_gemm_tile_n(GemmKind kind) { return kind == kGateUpSwiGLU ? BN / 2 : BN; }
+
+cudaError_t grouped_gemm_prepare() {
+  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<kGateUpSwiGLU>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(grouped_gemm_kernel<kDownF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              SMEM_BYTES);
+}
+
+cudaError_t launch_grouped_gemm(GemmKind kind, bool int8_weights, const CUtensorMap& tm_a, const CUtensorMap& tm_b,
+                                const GemmArgs& a, cudaStream_t s) {
+  if (int8_weights) return cudaErrorNotSupported;
+  if (kind == kGateUpSwiGLU)
+    grouped_gemm_kernel<kGateUpSwiGLU><<<a.grid, THREADS, SMEM_BYTES, s>>>(tm_a, tm_b, a);
+  else
+    grouped_gemm_kernel<kDownF32><<<a.grid, THREADS, SMEM_BYTES, s>>>(tm_a, tm_b, a);
+  return cudaGetLastError();
+}
+
+}  // namespace cbmoe

@@ -1,0 +1,95 @@
+// Declarations shared by the library's own translation units: the launchers
+// of each kernel and the argument blocks they take.  Not part of the ABI.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace cbmoe {
+
+// Rows of one GEMM M-tile; every expert's block of rows in the permuted
+// activations is padded to a multiple of it, so no tile spans two experts.
+constexpr int kTileM = 128;
+// Device status codes written by kernels (same values as cb_status_t).
+constexpr int kErrTimeout = 6;
+constexpr int kErrDevice = 7;
+// Default bound on any device-side wait.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+// Record a device-side error: the first one wins.
+__device__ __forceinline__ void set_error(int* err, int code) {
+  if (err) atomicCAS(err, 0, code);
+}
+
+// ------------------------------------------------------------------ router
+struct RouterArgs {
+  const uint16_t* x;     // bf16 [T][d]
+  const uint16_t* wr;    // bf16 [E][d]
+  const float* bias;     // [E] or nullptr
+  int32_t T, d, E, k;
+  int32_t* ids;          // [T][k]
+  float* w;              // [T][k]
+  float* logits;         // [T][E] or nullptr
+  int* err;
+};
+cudaError_t launch_router(const RouterArgs& a, cudaStream_t s);
+cudaError_t router_prepare();  // one-time function attributes
+
+// ---------------------------------------------------------------- dispatch
+struct DispatchArgs {
+  const int32_t* ids;    // [T*k]
+  const uint16_t* x;     // bf16 [T][d]
+  int32_t T, k, E, d;
+  int32_t n_chunks;      // ceil(T*k / kDispatchChunk)
+  int32_t* chunk;        // [n_chunks][E] per-chunk counts, then per-chunk row bases
+  int32_t* counts;       // [E]
+  int32_t* offsets;      // [E+1]
+  int32_t* mtile_off;    // [E+1] prefix sum of ceil(counts/kTileM)
+  int32_t* mtile_expert; // [max_mtiles] expert owning each m-tile
+  int32_t max_mtiles;
+  int32_t* tok;          // [T*k]
+  int32_t* inv;          // [T*k]
+  uint16_t* xp;          // bf16 [max_mtiles*kTileM][d]
+  int32_t gather_blocks;
+  int* err;
+};
+constexpr int kDispatchChunk = 2048;
+cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s);
+
+// ----------------------------------------------------------------- combine
+struct CombineArgs {
+  const float* y;        // fp32 [max_mtiles*kTileM][d]
+  const float* w;        // [T][k]
+  const int32_t* ids;    // [T][k]
+  const int32_t* inv;    // [T][k]
+  const int32_t* offsets;   // [E+1]
+  const int32_t* mtile_off; // [E+1]
+  int32_t T, k, d;
+  void* out;             // bf16 or fp32 [T][d]
+  int out_f32;
+};
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s);
+
+// ------------------------------------------------------------ grouped GEMM
+struct GemmArgs {
+  const int32_t* mtile_off;     // [E+1]
+  const int32_t* mtile_expert;  // [max_mtiles]
+  int32_t E;
+  int32_t n_tiles;              // N tiles per expert
+  int32_t k_blocks;             // K / 64
+  int32_t b_rows_per_expert;    // rows of the B operand per expert
+  void* out;                    // H bf16 or Y fp32
+  int64_t ld_out;               // elements per output row
+  const float* scale0;          // int8: gate (or down) per-channel scales
+  const float* scale1;          // int8: up scales
+  int* err;
+  uint64_t wait_limit_ns;
+  int32_t grid;                 // persistent CTAs
+};
+enum GemmKind { kGateUpSwiGLU = 0, kDownF32 = 1 };
+cudaError_t launch_grouped_gemm(GemmKind kind, bool int8_weights, const CUtensorMap& tm_a,
+                                const CUtensorMap& tm_b, const GemmArgs& a, cudaStream_t s);
+cudaError_t grouped_gemm_prepare();  // one-time function attributes
+int grouped_gemm_tile_n(GemmKind kind);  // output columns per tile
+
+}  // namespace cbmoe

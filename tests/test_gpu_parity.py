@@ -1,0 +1,119 @@
+"""CUDA layer vs the fp64 oracle through the C ABI (needs a GB300)."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+
+pytestmark = pytest.mark.gpu
+
+gh = pytest.importorskip("gpu_harness")
+
+SMALL = {
+    "tiny": synth.WORKLOADS["tiny"],
+    # several M, N and K tiles with ragged per-expert tails
+    "ragged_mid": synth.custom_shape("ragged_mid", T=300, d=512, f=768, E=8, k=2, seed=21),
+    "one_expert": synth.custom_shape("one_expert", T=130, d=256, f=256, E=1, k=1, seed=22),
+    "k_equals_E": synth.custom_shape("k_equals_E", T=200, d=256, f=512, E=4, k=4, seed=23),
+    # skewed bias: most of the 128 experts get no rows
+    "skewed_small": synth.custom_shape("skewed_small", T=1000, d=256, f=256, E=128, k=4, bias=True, seed=24),
+    "e256_k16": synth.custom_shape("e256_k16", T=257, d=256, f=256, E=256, k=16, seed=25),
+    "odd_T": synth.custom_shape("odd_T", T=1, d=512, f=512, E=8, k=2, seed=26),
+}
+
+FULL = {  # workload: tokens sampled for the output check
+    "mixtral_decode": 24,
+    "skewed": 64,
+    "mixtral_prefill": 24,
+}
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_parity_small(name):
+    rep = gh.full_check(synth.make_layer(SMALL[name]))
+    print(name, rep)
+
+
+@pytest.mark.parametrize("name", list(FULL))
+def test_parity_full_size(name):
+    layer = synth.make_layer(synth.WORKLOADS[name])
+    rep = gh.full_check(layer, sample=FULL[name])
+    print(name, rep)
+
+
+def test_deterministic_and_host_entry_point():
+    layer = synth.make_layer(SMALL["ragged_mid"])
+    gl = gh.GpuLayer(layer)
+    try:
+        gl.run(f32=False)
+        a = gl.out.clone()
+        gl.run(f32=False)
+        assert torch.equal(a.view(torch.int16), gl.out.view(torch.int16))
+        xh = torch.from_numpy(layer.x.view(np.int16)).pin_memory()
+        oh = torch.empty_like(xh).pin_memory()
+        gl.m.forward_host(xh, oh)
+        torch.cuda.synchronize()
+        assert torch.equal(oh, a.view(torch.int16).cpu())
+    finally:
+        gl.close()
+
+
+def test_token_permutation_equivariance():
+    layer = synth.make_layer(SMALL["ragged_mid"])
+    gl = gh.GpuLayer(layer)
+    try:
+        gl.run(f32=False)
+        base = gl.out.clone()
+        p = torch.randperm(gl.T, generator=torch.Generator().manual_seed(3))
+        gl.x.copy_(gl.x[p.to(gl.x.device)])
+        gl.run(f32=False)
+        assert torch.equal(gl.out.view(torch.int16), base[p.to(base.device)].view(torch.int16))
+    finally:
+        gl.close()
+
+
+def test_empty_token_count():
+    import mixture_experts_router_gb300 as cb
+    layer = synth.make_layer(synth.custom_shape("empty", T=4, d=256, f=256, E=4, k=2, seed=5))
+    w = {n: gh.to_dev(getattr(layer, n)) for n in ("wr", "wg", "wu", "wd")}
+    m = cb.MoELayer(0, 256, 256, 4, 2, w["wr"], w["wg"], w["wu"], w["wd"])
+    x = torch.empty((0, 256), dtype=torch.bfloat16, device="cuda")
+    x16 = torch.empty((16,), dtype=torch.bfloat16, device="cuda")
+    o16 = torch.empty((16,), dtype=torch.bfloat16, device="cuda")
+    m.forward(x16, o16)
+    torch.cuda.synchronize()
+    assert m.last_error() == cb.CB_OK
+    m.close()
+    del x
+
+
+def test_argument_errors_on_device():
+    import mixture_experts_router_gb300 as cb
+    layer = synth.make_layer(synth.custom_shape("args", T=16, d=256, f=256, E=4, k=2, seed=6))
+    gl = gh.GpuLayer(layer)
+    try:
+        h = gl.m.handle
+        buf = torch.empty(16 * 256 + 64, dtype=torch.bfloat16, device="cuda")
+        assert cb.cb_moe_forward(h, gl.x.data_ptr() + 2, gl.out.data_ptr(), 0) == cb.CB_ERR_ALIGNMENT
+        assert cb.cb_moe_forward(h, buf.data_ptr(), buf.data_ptr() + 32, 0) == cb.CB_ERR_INVALID_ARG
+        assert cb.cb_moe_forward(h, 0, gl.out.data_ptr(), 0) == cb.CB_ERR_INVALID_ARG
+        assert cb.cb_moe_forward(None, gl.x.data_ptr(), gl.out.data_ptr(), 0) == cb.CB_ERR_INVALID_ARG
+    finally:
+        gl.close()
+
+
+def test_injected_host_faults(monkeypatch):
+    import mixture_experts_router_gb300 as cb
+    layer = synth.make_layer(synth.custom_shape("faults", T=16, d=256, f=256, E=4, k=2, seed=7))
+    monkeypatch.setenv("CB_MOE_INJECT_FAULT", "oom")
+    with pytest.raises(cb.CbMoeError) as ei:
+        gh.GpuLayer(layer)
+    assert ei.value.status == cb.CB_ERR_OOM
+    monkeypatch.setenv("CB_MOE_INJECT_FAULT", "launch")
+    gl = gh.GpuLayer(layer)
+    try:
+        assert cb.cb_moe_forward(gl.m.handle, gl.x.data_ptr(), gl.out.data_ptr(), 0) == cb.CB_ERR_CUDA
+        monkeypatch.delenv("CB_MOE_INJECT_FAULT")
+        gl.run()
+    finally:
+        gl.close()
