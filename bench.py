@@ -1,0 +1,445 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 MoE FFN layer forward (router -> dispatch -> grouped
+SwiGLU GEMMs -> combine) through the C ABI of libcbmoe.so.
+
+One step = one forward of the whole layer over one batch of T tokens of the
+workload (default: the Mixtral-8x7B-shaped prefill layer, T=4096, d=4096,
+f=14336, E=8, top-2, bf16).  Inputs are seeded synthetic data resident in HBM;
+L2 is flushed (a 512 MB write) between timed steps, outside the timed events.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Under torchrun each rank runs an independent replica of the layer on its own
+GPU over its own T tokens (weak scaling, no collective in the data path); the
+time is the max over ranks and `value` counts the tokens of all ranks.
+`--impl reference` times the fp64 CPU oracle on the host cores instead
+(rank 0 only).  Prints one JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+from datetime import datetime
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s; grouped-GEMM % of bf16 TC peak; decode weight GB/s % HBM"
+DEFAULT_WORKLOAD = "mixtral_prefill"
+KERNELS_PER_FORWARD = 8   # router, 4 dispatch kernels, 2 grouped GEMMs, combine
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+GEMM_SOURCE = os.path.join(ROOT, "mixture_experts_router_gb300", "csrc", "grouped_gemm.cu")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--shape", default=None, help="T,d,f,E,k of a custom bf16 layer (profiling cases)")
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--l2-flush-mb", type=int, default=512)
+    p.add_argument("--e2e-steps", type=int, default=50)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU work of the oracle baseline")
+    return p.parse_args(argv)
+
+
+# ------------------------------------------------------------------ helpers
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def algorithmic_work(shape, counts):
+    """Algorithmic bytes / flops of each stage for one forward.  Expert FLOPs
+    count routed rows only (padding rows of the 128-row tiles are waste)."""
+    T, d, f, E, k = shape.T, shape.d, shape.f, shape.E, shape.k
+    M = T * k
+    eb = 1 if shape.wdtype == "int8" else 2
+    active = sum(1 for c in counts if c > 0)
+    wbytes = active * 3 * d * f * eb + (active * (2 * f + d) * 4 if eb == 1 else 0)
+    return {
+        "router_bytes": T * d * 2 + E * d * 2 + T * k * 8,
+        "dispatch_bytes": T * d * 2 + M * d * 2 + 16 * M,
+        "gateup_flops": 4 * d * f * M,
+        "down_flops": 2 * d * f * M,
+        "combine_bytes": M * d * 4 + 8 * M + T * d * 2,
+        "active_expert_weight_bytes": wbytes,
+        "gateup_weight_bytes": active * 2 * d * f * eb,
+        "down_weight_bytes": active * d * f * eb,
+    }
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 100 ms) of SM clock and throttle reasons."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "100", "-i", str(device)], stdout=self.file,
+                                         stderr=subprocess.DEVNULL)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.file.flush()
+
+    def summary(self, t0, t1):
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    ts = datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    rows.append((ts, float(parts[1]), float(parts[2]), parts[5:9]))
+                except ValueError:
+                    continue
+        os.unlink(self.file.name)
+        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05] or rows
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in inside for n, v in zip(names, r[3]) if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": reasons, "samples": len(inside)}
+
+
+def measured_traffic(kernel_key):
+    """DRAM bytes per launch of a kernel from the committed ncu summary, or None
+    when the kernel's source changed since the counters were taken."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(TRAFFIC_FILE) as f:
+        data = json.load(f)
+    entry = data.get(kernel_key)
+    if not entry:
+        return None
+    with open(GEMM_SOURCE, "rb") as f:
+        digest = hashlib.sha256(f.read()).hexdigest()[:16]
+    if entry.get("source_sha256_16") != digest:
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    """Max of a float over all ranks (a measurement collective, not part of the layer)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def config_block(shape, l2_mb):
+    return {"workload": shape.name, "T": shape.T, "d_model": shape.d, "d_ff": shape.f, "n_experts": shape.E,
+            "top_k": shape.k, "expert_weights": shape.wdtype, "router_bias": shape.bias,
+            "l2": f"flushed between timed steps ({l2_mb} MB write, outside the timed events)",
+            "parallelism": "replicas (token-sharded, no collective)"}
+
+
+# ------------------------------------------------------- CPU oracle baseline
+def oracle_baseline(shape, layer, target_seconds=15.0, threads=None):
+    """Time the fp64 oracle (as it stands) on a bounded sample of tokens."""
+    import numpy as np
+    import oracle
+    lib = oracle.load()
+    threads = threads or host_cores()
+    oracle.set_threads(threads)
+    orc = oracle.Oracle(layer, lib)
+    rng = np.random.default_rng(0)
+    n = threads
+    t0 = time.perf_counter()
+    orc.forward(tokens=rng.choice(shape.T, n, replace=False).astype(np.int32))
+    first = time.perf_counter() - t0
+    more = max(0, int(n * (target_seconds - first) / max(first, 1e-6)))
+    more = min(more, shape.T - n)
+    total_tokens, total_time = n, first
+    if more > 0:
+        toks = rng.choice(shape.T, more, replace=False).astype(np.int32)
+        t0 = time.perf_counter()
+        orc.forward(tokens=toks)
+        total_time += time.perf_counter() - t0
+        total_tokens += more
+    return {"value": total_tokens / total_time, "unit": "tokens/s", "cores": oracle.get_threads(lib),
+            "kind": "oracle",
+            "sample": f"{total_tokens} of the {shape.T} tokens (routing + k experts + combine per token, fp64, "
+                      f"OpenMP over tokens), {total_time:.1f} s"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import numpy as np
+    import oracle
+    import synth
+    shape = workload_shape(args)
+    layer = synth.make_layer(shape)
+    threads = host_cores()
+    lib = oracle.load()
+    oracle.set_threads(threads)
+    orc = oracle.Oracle(layer, lib)
+    rng = np.random.default_rng(1)
+    per_step = threads        # one token per thread: a bounded sample of the batch
+    for _ in range(min(args.warmup, 3)):
+        orc.forward(tokens=rng.choice(shape.T, per_step, replace=False).astype(np.int32))
+    times = []
+    for _ in range(args.steps):
+        toks = rng.choice(shape.T, per_step, replace=False).astype(np.int32)
+        t0 = time.perf_counter()
+        orc.forward(tokens=toks)
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = per_step * args.steps / total
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded SplitMix64/Box-Muller, bf16 inputs)",
+            "config": config_block(shape, 0),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.get_threads(lib), "kind": "oracle",
+                             "sample": f"{per_step} tokens per step of the {shape.T}-token batch"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args):
+    import numpy as np
+    import torch
+    import mixture_experts_router_gb300 as cb
+    import synth
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    device = torch.device("cuda", local)
+    shape = workload_shape(args)
+    layer = synth.make_layer(shape)
+
+    def dev(a):
+        if a is None:
+            return None
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).to(device).view(torch.bfloat16)
+        return torch.from_numpy(a).to(device)
+
+    w = {n: dev(getattr(layer, n)) for n in ("wr", "bias", "wg", "wu", "wd", "sg", "su", "sd")}
+    m = cb.MoELayer(shape.T, shape.d, shape.f, shape.E, shape.k, w["wr"], w["wg"], w["wu"], w["wd"],
+                    router_bias=w["bias"], s_gate=w["sg"], s_up=w["su"], s_down=w["sd"], device=local,
+                    stage_timing=True)
+    del w
+    torch.cuda.empty_cache()
+    x = dev(layer.x)
+    out = torch.empty((shape.T, shape.d), dtype=torch.bfloat16, device=device)
+    flush = torch.empty(args.l2_flush_mb << 20, dtype=torch.uint8, device=device)
+    stream = torch.cuda.Stream(device)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            flush.zero_()
+            m.forward(x, out, stream=stream)
+        stream.synchronize()
+        st = m.last_error()
+        if st != cb.CB_OK:
+            raise cb.CbMoeError(st, "warm-up forward")
+
+        sampler = ClockSampler(local)
+        time.sleep(0.3)
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        t_wall0 = time.time()
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        stage_ms = []
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            m.forward(x, out, stream=stream)
+            ends[i].record(stream)
+            stage_ms.append(m.stage_times())   # waits for this step's last stage event
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        t_wall1 = time.time()
+        time.sleep(0.2)
+        sampler.stop()
+        clocks = sampler.summary(t_wall0, t_wall1)
+        st = m.last_error()
+        if st != cb.CB_OK:
+            raise cb.CbMoeError(st, "timed forward")
+        step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+        total_ms = max_over_ranks(sum(step_ms), world)
+
+        # end to end through the host-buffer entry point (pinned host memory)
+        xh = torch.from_numpy(layer.x.view(np.int16)).pin_memory()
+        oh = torch.empty_like(xh).pin_memory()
+        k2 = max(1, min(args.e2e_steps, args.steps))
+        for _ in range(3):
+            m.forward_host(xh, oh, stream=stream)
+        e_s = [torch.cuda.Event(enable_timing=True) for _ in range(k2)]
+        e_e = [torch.cuda.Event(enable_timing=True) for _ in range(k2)]
+        torch.cuda.synchronize()
+        for i in range(k2):
+            flush.zero_()
+            e_s[i].record(stream)
+            m.forward_host(xh, oh, stream=stream)
+            e_e[i].record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in zip(e_s, e_e)), world)
+        st = m.last_error()
+        if st != cb.CB_OK:
+            raise cb.CbMoeError(st, "host forward")
+        routing = m.routing()
+        counts = torch.empty(shape.E, dtype=torch.int32, device=device)
+        cb.copy_from_device(counts, routing.counts, 4 * shape.E)
+        counts = counts.cpu().tolist()
+
+    m.close()
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return 0
+
+    pk, pk_kind = peaks()
+    hbm = pk["hbm_gbs"]
+    tc_sus = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+    tc_burst = pk["bf16_tflops"]
+    work = algorithmic_work(shape, counts)
+    mean = [statistics.mean(s[i] for s in stage_ms) for i in range(5)]
+    names = cb.STAGE_NAMES
+    stages = {}
+    for i, n in enumerate(names):
+        s = mean[i] / 1e3
+        if n in ("gateup_gemm", "down_gemm"):
+            fl = work["gateup_flops" if n == "gateup_gemm" else "down_flops"]
+            wb = work["gateup_weight_bytes" if n == "gateup_gemm" else "down_weight_bytes"]
+            stages[n] = {"ms": mean[i], "tflops": fl / s / 1e12, "frac_tc_sustained": fl / s / 1e12 / tc_sus,
+                         "weight_gbs": wb / s / 1e9, "frac_hbm_weights": wb / s / 1e9 / hbm}
+        else:
+            b = work[n + "_bytes"]
+            stages[n] = {"ms": mean[i], "gbs": b / s / 1e9, "frac_hbm": b / s / 1e9 / hbm}
+    gemm_s = (mean[2] + mean[3]) / 1e3
+    stages["grouped_gemms"] = {"ms": mean[2] + mean[3],
+                               "tflops": (work["gateup_flops"] + work["down_flops"]) / gemm_s / 1e12,
+                               "frac_tc_sustained": (work["gateup_flops"] + work["down_flops"]) / gemm_s / 1e12 / tc_sus,
+                               "weight_gbs": work["active_expert_weight_bytes"] / gemm_s / 1e9,
+                               "frac_hbm_weights": work["active_expert_weight_bytes"] / gemm_s / 1e9 / hbm}
+
+    # dominant kernel: the longest stage
+    dom = max(range(5), key=lambda i: mean[i])
+    dname = names[dom]
+    # a GEMM is tensor-bound when its FLOPs per weight byte exceed the ridge point
+    intensity = (work["gateup_flops"] + work["down_flops"]) / max(1, work["active_expert_weight_bytes"])
+    ridge = tc_sus * 1e12 / (hbm * 1e9)
+    if dname in ("gateup_gemm", "down_gemm") and intensity >= ridge:
+        fl = work["gateup_flops" if dname == "gateup_gemm" else "down_flops"]
+        achieved = fl / (mean[dom] / 1e3) / 1e12
+        roof = {"kernel": dname, "bound": "tensor", "achieved": achieved, "peak": tc_sus, "unit": "TFLOP/s",
+                "frac": achieved / tc_sus, "peak_kind": f"{pk_kind} bf16 sustained",
+                "frac_of_burst": achieved / tc_burst}
+    elif dname in ("gateup_gemm", "down_gemm"):
+        wb = work["gateup_weight_bytes" if dname == "gateup_gemm" else "down_weight_bytes"]
+        achieved = wb / (mean[dom] / 1e3) / 1e9
+        roof = {"kernel": dname, "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm, "peak_kind": f"{pk_kind} HBM copy"}
+    else:
+        b = work[dname + "_bytes"]
+        achieved = b / (mean[dom] / 1e3) / 1e9
+        roof = {"kernel": dname, "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm, "peak_kind": f"{pk_kind} HBM copy"}
+    roof["traffic"] = measured_traffic(f"{dname}:{shape.name}")
+    roof["algorithmic_per_launch"] = (work["gateup_flops"] if dname == "gateup_gemm" else
+                                      work["down_flops"] if dname == "down_gemm" else work[dname + "_bytes"])
+
+    value = shape.T * world * args.steps / (total_ms / 1e3)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int8" if shape.wdtype == "int8" else "bf16",
+        "data": "synthetic (seeded SplitMix64/Box-Muller; x ~ N(0,1), weights ~ N(0, 0.02^2), bf16)",
+        "config": config_block(shape, args.l2_flush_mb),
+        "e2e": {"value": shape.T * world * k2 / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": shape.T * shape.d * 2, "d2h_bytes_per_step": shape.T * shape.d * 2,
+                "steps": k2, "api": "cb_moe_forward_host (pinned host x and out, copies on the stream)"},
+        "gpu_launches": KERNELS_PER_FORWARD * args.steps,
+        "roofline": roof,
+        "stages": stages,
+        "expert_rows": {"active_experts": sum(1 for c in counts if c > 0), "max_rows": max(counts),
+                        "min_rows": min(counts)},
+        "clocks": clocks,
+        "peaks": {"hbm_gbs": hbm, "bf16_tflops": tc_burst, "bf16_tflops_sustained": tc_sus, "kind": pk_kind},
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = oracle_baseline(shape, layer, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def workload_shape(args):
+    import synth
+    if args.shape:
+        T, d, f, E, k = (int(v) for v in args.shape.split(","))
+        return synth.custom_shape(f"custom_T{T}_d{d}_f{f}_E{E}_k{k}", T=T, d=d, f=f, E=E, k=k, seed=1100)
+    return synth.WORKLOADS[args.workload]
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

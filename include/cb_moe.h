@@ -69,6 +69,8 @@ typedef enum { CB_W_BF16 = 0, CB_W_INT8 = 1 } cb_wdtype_t;
 
 /* config.flags */
 #define CB_FLAG_KEEP_LOGITS 0x1u   /* also store the fp32 router logits [T][E] */
+#define CB_FLAG_STAGE_TIMING 0x2u  /* record CUDA events between the stages of each
+                                      forward (see cb_moe_stage_times)          */
 
 typedef struct {
   int32_t n_tokens;   /* T: tokens in every forward on this handle (>= 0)         */
@@ -141,6 +143,16 @@ typedef struct {
 } cb_routing_view_t;
 
 CB_API cb_status_t cb_moe_routing(const cb_moe_t *h, cb_routing_view_t *view);
+
+/*
+ * Durations in milliseconds of the stages of the last forward on a handle
+ * created with CB_FLAG_STAGE_TIMING, measured by CUDA events recorded on the
+ * forward's stream: ms[0] router, ms[1] dispatch (count, scan, scatter,
+ * gather), ms[2] gate/up GEMM + SwiGLU, ms[3] down GEMM, ms[4] combine.
+ * Waits for the last event.  n must be >= CB_N_STAGES.
+ */
+#define CB_N_STAGES 5
+CB_API cb_status_t cb_moe_stage_times(cb_moe_t *h, float *ms, int32_t n);
 
 /* Synchronise the device, return the handle's device status word (CB_OK,
  * CB_ERR_TIMEOUT or CB_ERR_DEVICE) and clear it. */

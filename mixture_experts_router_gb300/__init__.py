@@ -17,11 +17,14 @@ CB_OK, CB_ERR_INVALID_ARG, CB_ERR_UNSUPPORTED, CB_ERR_ALIGNMENT = 0, 1, 2, 3
 CB_ERR_OOM, CB_ERR_CUDA, CB_ERR_TIMEOUT, CB_ERR_DEVICE = 4, 5, 6, 7
 CB_W_BF16, CB_W_INT8 = 0, 1
 CB_FLAG_KEEP_LOGITS = 0x1
+CB_FLAG_STAGE_TIMING = 0x2
+CB_N_STAGES = 5
+STAGE_NAMES = ("router", "dispatch", "gateup_gemm", "down_gemm", "combine")
 
 # every symbol include/cb_moe.h declares
 ABI_SYMBOLS = ("cb_moe_init", "cb_moe_forward", "cb_moe_forward_f32out", "cb_moe_forward_host",
-               "cb_moe_routing", "cb_moe_last_error", "cb_moe_device_bytes", "cb_moe_free",
-               "cb_status_string")
+               "cb_moe_routing", "cb_moe_stage_times", "cb_moe_last_error", "cb_moe_device_bytes",
+               "cb_moe_free", "cb_status_string")
 
 
 class cb_moe_config_t(ctypes.Structure):
@@ -66,11 +69,13 @@ def load_library(path: str = LIB_PATH):
     lib.cb_moe_forward_f32out.argtypes = [vp, vp, vp, vp]
     lib.cb_moe_forward_host.argtypes = [vp, vp, vp, vp]
     lib.cb_moe_routing.argtypes = [vp, ctypes.POINTER(cb_routing_view_t)]
+    lib.cb_moe_stage_times.argtypes = [vp, ctypes.POINTER(ctypes.c_float), ctypes.c_int32]
     lib.cb_moe_last_error.argtypes = [vp]
     lib.cb_moe_device_bytes.argtypes = [ctypes.POINTER(cb_moe_config_t), ctypes.POINTER(ctypes.c_uint64)]
     lib.cb_moe_free.argtypes = [vp]
     for name in ("cb_moe_init", "cb_moe_forward", "cb_moe_forward_f32out", "cb_moe_forward_host",
-                 "cb_moe_routing", "cb_moe_last_error", "cb_moe_device_bytes", "cb_moe_free"):
+                 "cb_moe_routing", "cb_moe_stage_times", "cb_moe_last_error", "cb_moe_device_bytes",
+                 "cb_moe_free"):
         getattr(lib, name).restype = i32
     lib.cb_status_string.argtypes = [i32]
     lib.cb_status_string.restype = ctypes.c_char_p
@@ -108,6 +113,13 @@ def cb_moe_routing(handle):
     return st, v
 
 
+def cb_moe_stage_times(handle):
+    """Returns (status, [router, dispatch, gate/up, down, combine] ms)."""
+    ms = (ctypes.c_float * CB_N_STAGES)()
+    st = load_library().cb_moe_stage_times(handle, ms, CB_N_STAGES)
+    return st, list(ms)
+
+
 def cb_moe_last_error(handle) -> int:
     return load_library().cb_moe_last_error(handle)
 
@@ -123,6 +135,38 @@ def cb_moe_free(handle) -> int:
 
 
 # ------------------------------------------------------- torch convenience
+_cudart = None
+
+
+def copy_from_device(dst_tensor, src_ptr: int, nbytes: int) -> None:
+    """Copy nbytes of library-owned device memory (e.g. a cb_routing_view_t
+    array) into a torch CUDA tensor, with the CUDA runtime torch has loaded."""
+    global _cudart
+    if _cudart is None:
+        import glob
+        import sys
+        names = ["libcudart.so.13", "libcudart.so.12", "libcudart.so"]
+        for p in sys.path:
+            names += glob.glob(os.path.join(p, "nvidia", "cu*", "lib", "libcudart.so*"))
+            names += glob.glob(os.path.join(p, "nvidia", "cuda_runtime", "lib", "libcudart.so*"))
+        names += glob.glob("/usr/local/cuda/lib64/libcudart.so*")
+        for n in names:
+            try:
+                lib = ctypes.CDLL(n)
+                break
+            except OSError:
+                continue
+        else:
+            raise RuntimeError("no CUDA runtime library found")
+        lib.cudaMemcpy.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int]
+        lib.cudaMemcpy.restype = ctypes.c_int
+        _cudart = lib
+    if nbytes:
+        rc = _cudart.cudaMemcpy(dst_tensor.data_ptr(), src_ptr, nbytes, 3)  # device to device
+        if rc != 0:
+            raise RuntimeError(f"cudaMemcpy failed ({rc})")
+
+
 def _ptr(t):
     return None if t is None else t.data_ptr()
 
@@ -132,9 +176,10 @@ class MoELayer:
     int8 as torch.int8).  Raises CbMoeError on any non-zero status."""
 
     def __init__(self, T, d, f, E, k, w_router, w_gate, w_up, w_down, router_bias=None,
-                 s_gate=None, s_up=None, s_down=None, device=0, keep_logits=False):
+                 s_gate=None, s_up=None, s_down=None, device=0, keep_logits=False, stage_timing=False):
+        flags = (CB_FLAG_KEEP_LOGITS if keep_logits else 0) | (CB_FLAG_STAGE_TIMING if stage_timing else 0)
         self.cfg = cb_moe_config_t(T, d, f, E, k, CB_W_INT8 if s_gate is not None else CB_W_BF16,
-                                   device, CB_FLAG_KEEP_LOGITS if keep_logits else 0)
+                                   device, flags)
         w = cb_moe_weights_t(_ptr(w_router), _ptr(router_bias), _ptr(w_gate), _ptr(w_up), _ptr(w_down),
                              _ptr(s_gate), _ptr(s_up), _ptr(s_down))
         st, h = cb_moe_init(self.cfg, w)
@@ -162,6 +207,12 @@ class MoELayer:
         if st != CB_OK:
             raise CbMoeError(st, "cb_moe_routing")
         return v
+
+    def stage_times(self):
+        st, ms = cb_moe_stage_times(self.handle)
+        if st != CB_OK:
+            raise CbMoeError(st, "cb_moe_stage_times")
+        return ms
 
     def last_error(self) -> int:
         return cb_moe_last_error(self.handle)

@@ -42,6 +42,8 @@ struct cb_moe {
   int* err;
   uint16_t *x_stage, *out_stage;
   int32_t max_mtiles, n_chunks;
+  cudaEvent_t ev[CB_N_STAGES + 1];
+  bool timing;
   CUtensorMap tm_a_gu, tm_b_gu, tm_a_dn, tm_b_dn;
 };
 
@@ -106,7 +108,7 @@ cb_status_t validate_config(const cb_moe_config_t* c) {
   if (c->wdtype != CB_W_BF16 && c->wdtype != CB_W_INT8) return CB_ERR_INVALID_ARG;
   if (c->d_model % 256 != 0 || c->d_ff % 256 != 0) return CB_ERR_UNSUPPORTED;
   if (c->n_experts > 256 || c->top_k > 16) return CB_ERR_UNSUPPORTED;
-  if ((c->flags & ~CB_FLAG_KEEP_LOGITS) != 0) return CB_ERR_INVALID_ARG;
+  if ((c->flags & ~(CB_FLAG_KEEP_LOGITS | CB_FLAG_STAGE_TIMING)) != 0) return CB_ERR_INVALID_ARG;
   // 32-bit row and tile indices everywhere
   const uint64_t M = static_cast<uint64_t>(c->n_tokens) * c->top_k;
   const uint64_t rows = M + static_cast<uint64_t>(c->n_experts) * kTileM;
@@ -166,6 +168,8 @@ struct DeviceGuard {
 cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, cudaStream_t s) {
   const cb_moe_config_t& c = h->cfg;
   if (fault_injected("launch")) return CB_ERR_CUDA;
+  auto mark = [&](int i) { return !h->timing || cudaEventRecord(h->ev[i], s) == cudaSuccess; };
+  if (!mark(0)) return CB_ERR_CUDA;
 
   RouterArgs ra{};
   ra.x = static_cast<const uint16_t*>(x);
@@ -179,7 +183,7 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
   ra.w = h->w;
   ra.logits = h->logits;
   ra.err = h->err;
-  if (launch_router(ra, s) != cudaSuccess) return CB_ERR_CUDA;
+  if (launch_router(ra, s) != cudaSuccess || !mark(1)) return CB_ERR_CUDA;
 
   DispatchArgs da{};
   da.ids = h->ids;
@@ -200,7 +204,7 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
   da.xp = h->xp;
   da.gather_blocks = h->num_sms * 4;
   da.err = h->err;
-  if (launch_dispatch(da, s) != cudaSuccess) return CB_ERR_CUDA;
+  if (launch_dispatch(da, s) != cudaSuccess || !mark(2)) return CB_ERR_CUDA;
 
   const bool int8w = c.wdtype == CB_W_INT8;
   GemmArgs ga{};
@@ -217,7 +221,8 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
   ga.err = h->err;
   ga.wait_limit_ns = kWaitLimitNs;
   ga.grid = h->num_sms;
-  if (launch_grouped_gemm(kGateUpSwiGLU, int8w, h->tm_a_gu, h->tm_b_gu, ga, s) != cudaSuccess) return CB_ERR_CUDA;
+  if (launch_grouped_gemm(kGateUpSwiGLU, int8w, h->tm_a_gu, h->tm_b_gu, ga, s) != cudaSuccess || !mark(3))
+    return CB_ERR_CUDA;
 
   GemmArgs gd = ga;
   gd.n_tiles = c.d_model / grouped_gemm_tile_n(kDownF32);
@@ -227,7 +232,8 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
   gd.ld_out = c.d_model;
   gd.scale0 = h->sd;
   gd.scale1 = nullptr;
-  if (launch_grouped_gemm(kDownF32, int8w, h->tm_a_dn, h->tm_b_dn, gd, s) != cudaSuccess) return CB_ERR_CUDA;
+  if (launch_grouped_gemm(kDownF32, int8w, h->tm_a_dn, h->tm_b_dn, gd, s) != cudaSuccess || !mark(4))
+    return CB_ERR_CUDA;
 
   CombineArgs ca{};
   ca.y = h->y;
@@ -241,7 +247,7 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
   ca.d = c.d_model;
   ca.out = out;
   ca.out_f32 = f32out ? 1 : 0;
-  if (launch_combine(ca, s) != cudaSuccess) return CB_ERR_CUDA;
+  if (launch_combine(ca, s) != cudaSuccess || !mark(5)) return CB_ERR_CUDA;
   return CB_OK;
 }
 
@@ -367,6 +373,8 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
   ok = ok && make_tmap(&h->tm_a_dn, h->hb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, f, mpad, 64, 128);
   ok = ok && make_tmap(&h->tm_b_dn, h->wd, wdt, eb, f, E * d, 64, 256);
   ok = ok && grouped_gemm_prepare() == cudaSuccess && router_prepare() == cudaSuccess;
+  h->timing = (cfg->flags & CB_FLAG_STAGE_TIMING) != 0;
+  for (int i = 0; ok && h->timing && i <= CB_N_STAGES; ++i) ok = cudaEventCreate(&h->ev[i]) == cudaSuccess;
   ok = ok && cudaDeviceSynchronize() == cudaSuccess;
   if (!ok) {
     cudaGetLastError();
@@ -423,6 +431,16 @@ cb_status_t cb_moe_routing(const cb_moe_t* h, cb_routing_view_t* v) {
   return CB_OK;
 }
 
+cb_status_t cb_moe_stage_times(cb_moe_t* h, float* ms, int32_t n) {
+  if (h == nullptr || ms == nullptr || n < CB_N_STAGES) return CB_ERR_INVALID_ARG;
+  if (!h->timing) return CB_ERR_INVALID_ARG;
+  DeviceGuard guard(h->cfg.device);
+  if (!guard.ok || cudaEventSynchronize(h->ev[CB_N_STAGES]) != cudaSuccess) return CB_ERR_CUDA;
+  for (int i = 0; i < CB_N_STAGES; ++i)
+    if (cudaEventElapsedTime(&ms[i], h->ev[i], h->ev[i + 1]) != cudaSuccess) return CB_ERR_CUDA;
+  return CB_OK;
+}
+
 cb_status_t cb_moe_last_error(cb_moe_t* h) {
   if (h == nullptr) return CB_ERR_INVALID_ARG;
   DeviceGuard guard(h->cfg.device);
@@ -440,6 +458,8 @@ cb_status_t cb_moe_free(cb_moe_t* h) {
   {
     DeviceGuard guard(h->cfg.device);
     if (!guard.ok || cudaDeviceSynchronize() != cudaSuccess) st = CB_ERR_CUDA;
+    for (int i = 0; h->timing && i <= CB_N_STAGES; ++i)
+      if (h->ev[i] != nullptr) cudaEventDestroy(h->ev[i]);
     if (cudaFree(h->block) != cudaSuccess) st = CB_ERR_CUDA;
   }
   delete h;

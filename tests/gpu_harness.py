@@ -65,8 +65,7 @@ class GpuLayer:
 
         def grab(ptr, n, dt):
             t = torch.empty(n, dtype=dt, device=self.dev)
-            if n:
-                _memcpy_d2d(t.data_ptr(), ptr, n * t.element_size())
+            cb.copy_from_device(t, ptr, n * t.element_size())
             return t.cpu().numpy()
 
         r = dict(ids=grab(v.ids, T * k, torch.int32).reshape(T, k),
@@ -82,39 +81,6 @@ class GpuLayer:
 
     def close(self):
         self.m.close()
-
-
-_cudart = None
-
-
-def _memcpy_d2d(dst, src, nbytes):
-    """Device-to-device copy of library-owned memory into a torch tensor."""
-    global _cudart
-    import ctypes
-    import glob
-    import os
-    if _cudart is None:
-        for soname in ("libcudart.so.13", "libcudart.so.12", "libcudart.so"):
-            try:
-                _cudart = ctypes.CDLL(soname)
-                break
-            except OSError:
-                pass
-    if _cudart is None:
-        cands = [os.path.join(os.path.dirname(torch.__file__), "lib", n) for n in ("libcudart.so.13", "libcudart.so")]
-        cands += glob.glob("/usr/local/cuda/lib64/libcudart.so*")
-        for c in cands:
-            if os.path.exists(c):
-                _cudart = ctypes.CDLL(c)
-                break
-    if _cudart is None:
-        raise RuntimeError("no libcudart found")
-    if not hasattr(_cudart, "_cb_ready"):
-        _cudart._cb_ready = True
-        _cudart.cudaMemcpy.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int]
-        _cudart.cudaMemcpy.restype = ctypes.c_int
-    rc = _cudart.cudaMemcpy(dst, src, nbytes, 3)  # cudaMemcpyDeviceToDevice
-    assert rc == 0, f"cudaMemcpy failed {rc}"
 
 
 def half_ulp_bf16(ref):
