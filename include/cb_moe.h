@@ -158,6 +158,36 @@ CB_API cb_status_t cb_moe_stage_times(cb_moe_t *h, float *ms, int32_t n);
  * CB_ERR_TIMEOUT or CB_ERR_DEVICE) and clear it. */
 CB_API cb_status_t cb_moe_last_error(cb_moe_t *h);
 
+/*
+ * Dispatch without any device allocation (the pages have no counterpart of
+ * this call; it exists for callers that cannot allocate device memory, such
+ * as a host program whose own allocator has reserved the GPU's memory, or a
+ * loop that cannot afford cudaMalloc's implicit synchronisation).
+ *
+ * From routing ids[T][k] (device, each row k distinct experts in [0, E)) it
+ * writes counts[E], offsets[E+1], tok[T*k] and inv[T][k] exactly as the
+ * dispatch of cb_moe_forward does (rows of expert e in ascending token
+ * order).  `status` (device int32, or NULL) receives 0 or CB_ERR_DEVICE
+ * (an id out of range) once the stream has run the call.  All pointers are
+ * caller-owned device memory, 4-byte aligned; the call is asynchronous on
+ * `stream` and runs on the current device.
+ *
+ * Scratch lives in one static device array of CB_NOALLOC_SCRATCH_BYTES per
+ * GPU, held until the process exits; the call returns CB_ERR_UNSUPPORTED
+ * without launching anything when
+ *   ceil(T*k/2048)*E + (E+1) + ((T*k + 127*E)/128 + 1) + 1
+ * 32-bit words exceed it (about T*k <= 2 million pairs at E = 256).  The
+ * first call on each device looks the array's address up (and may load the
+ * library's kernels there): make it before any stream capture.  All calls
+ * share the array, so calls that overlap on the GPU race: keep them on one
+ * stream.  Returns CB_ERR_INVALID_ARG / CB_ERR_UNSUPPORTED / CB_ERR_ALIGNMENT
+ * on bad arguments, CB_ERR_CUDA if a launch fails.
+ */
+#define CB_NOALLOC_SCRATCH_BYTES (1u << 20)
+CB_API cb_status_t cb_moe_dispatch_noalloc(const int32_t *ids, int32_t n_tokens, int32_t top_k, int32_t n_experts,
+                                           int32_t *counts, int32_t *offsets, int32_t *tok, int32_t *inv,
+                                           int32_t *status, void *stream);
+
 /* Bytes of device memory a handle with this config holds (weights + workspace). */
 CB_API cb_status_t cb_moe_device_bytes(const cb_moe_config_t *cfg, uint64_t *bytes);
 

@@ -24,7 +24,7 @@ STAGE_NAMES = ("router", "dispatch", "gateup_gemm", "down_gemm", "combine")
 # every symbol include/cb_moe.h declares
 ABI_SYMBOLS = ("cb_moe_init", "cb_moe_forward", "cb_moe_forward_f32out", "cb_moe_forward_host",
                "cb_moe_routing", "cb_moe_stage_times", "cb_moe_last_error", "cb_moe_device_bytes",
-               "cb_moe_free", "cb_status_string")
+               "cb_moe_free", "cb_status_string", "cb_moe_dispatch_noalloc")
 
 
 class cb_moe_config_t(ctypes.Structure):
@@ -73,6 +73,9 @@ def load_library(path: str = LIB_PATH):
     lib.cb_moe_last_error.argtypes = [vp]
     lib.cb_moe_device_bytes.argtypes = [ctypes.POINTER(cb_moe_config_t), ctypes.POINTER(ctypes.c_uint64)]
     lib.cb_moe_free.argtypes = [vp]
+    lib.cb_moe_dispatch_noalloc.argtypes = [vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, vp, vp, vp, vp,
+                                            vp, vp]
+    lib.cb_moe_dispatch_noalloc.restype = i32
     for name in ("cb_moe_init", "cb_moe_forward", "cb_moe_forward_f32out", "cb_moe_forward_host",
                  "cb_moe_routing", "cb_moe_stage_times", "cb_moe_last_error", "cb_moe_device_bytes",
                  "cb_moe_free"):
@@ -132,6 +135,13 @@ def cb_moe_device_bytes(cfg: cb_moe_config_t):
 
 def cb_moe_free(handle) -> int:
     return load_library().cb_moe_free(handle)
+
+
+def cb_moe_dispatch_noalloc(ids_ptr, n_tokens, top_k, n_experts, counts_ptr, offsets_ptr, tok_ptr, inv_ptr,
+                            status_ptr=None, stream: int = 0) -> int:
+    """Dispatch of routing ids with no device allocation (static scratch); see cb_moe.h."""
+    return load_library().cb_moe_dispatch_noalloc(ids_ptr, n_tokens, top_k, n_experts, counts_ptr, offsets_ptr,
+                                                  tok_ptr, inv_ptr, status_ptr, stream)
 
 
 # ------------------------------------------------------- torch convenience

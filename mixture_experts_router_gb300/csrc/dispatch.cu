@@ -174,6 +174,14 @@ __global__ void __launch_bounds__(kThreads) dispatch_gather(DispatchArgs a) {
 
 }  // namespace
 
+cudaError_t launch_dispatch_ranks(const DispatchArgs& a, cudaStream_t s) {
+  if (a.n_chunks <= 0) return cudaSuccess;
+  dispatch_count<<<a.n_chunks, kThreads, 0, s>>>(a);
+  dispatch_scan<<<1, kThreads, 0, s>>>(a);
+  dispatch_scatter<<<a.n_chunks, kThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s) {
   if (a.n_chunks <= 0) return cudaSuccess;
   dispatch_count<<<a.n_chunks, kThreads, 0, s>>>(a);

@@ -55,6 +55,8 @@ struct DispatchArgs {
 };
 constexpr int kDispatchChunk = 2048;
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s);
+// histogram, prefix sums and ranks only (no row gather; x and xp unused)
+cudaError_t launch_dispatch_ranks(const DispatchArgs& a, cudaStream_t s);
 
 // ----------------------------------------------------------------- combine
 struct CombineArgs {
