@@ -139,17 +139,18 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // 2-D row-major tensor [outer][inner] with a box of box_outer x box_inner
-// elements and the 128-byte swizzle.
+// elements, 128-byte swizzled (bf16 operands) or unswizzled (int8 staging).
 bool make_tmap(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint64_t elem_bytes, uint64_t inner,
-               uint64_t outer, uint32_t box_inner, uint32_t box_outer) {
+               uint64_t outer, uint32_t box_inner, uint32_t box_outer,
+               CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto enc = tensor_map_encoder();
   if (enc == nullptr) return false;
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {inner * elem_bytes};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t es[2] = {1, 1};
-  return enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  return enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -308,7 +309,6 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
   cudaDeviceProp prop;
   if (cudaGetDeviceProperties(&prop, cfg->device) != cudaSuccess) return CB_ERR_CUDA;
   if (prop.major != 10 || prop.minor != 3) return CB_ERR_UNSUPPORTED;
-  if (int8w) return CB_ERR_UNSUPPORTED;  // the int8 GEMM variant is not built yet
 
   const Layout L = plan(*cfg);
   cb_moe_t* h = new (std::nothrow) cb_moe_t();
@@ -369,9 +369,10 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
   const uint64_t mpad = static_cast<uint64_t>(h->max_mtiles) * kTileM;
   const CUtensorMapDataType wdt = int8w ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   ok = ok && make_tmap(&h->tm_a_gu, h->xp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, mpad, 64, 128);
-  ok = ok && make_tmap(&h->tm_b_gu, h->wgu, wdt, eb, d, E * 2 * f, 64, 256);
+  const CUtensorMapSwizzle wsw = int8w ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B;
+  ok = ok && make_tmap(&h->tm_b_gu, h->wgu, wdt, eb, d, E * 2 * f, 64, 256, wsw);
   ok = ok && make_tmap(&h->tm_a_dn, h->hb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, f, mpad, 64, 128);
-  ok = ok && make_tmap(&h->tm_b_dn, h->wd, wdt, eb, f, E * d, 64, 256);
+  ok = ok && make_tmap(&h->tm_b_dn, h->wd, wdt, eb, f, E * d, 64, 256, wsw);
   ok = ok && grouped_gemm_prepare() == cudaSuccess && router_prepare() == cudaSuccess;
   h->timing = (cfg->flags & CB_FLAG_STAGE_TIMING) != 0;
   for (int i = 0; ok && h->timing && i <= CB_N_STAGES; ++i) ok = cudaEventCreate(&h->ev[i]) == cudaSuccess;

@@ -5,11 +5,22 @@
 // over the k ("Colibri：面向MoE模型的高性能C语言推理引擎" §2.1); since its full
 // denominator cancels, w_s = exp(l_s - l_0) / sum_{j<k} exp(l_j - l_0).
 //
-// One block owns a tile of TT tokens and all E experts.  The logit GEMM runs
-// on CUDA cores in fp32 (bf16 products are exact in fp32) with a per-32
-// partial sum, keeping the logit error near 1e-6.  The logits stay in shared
-// memory; one warp per token then takes k rounds of a warp arg-max in the
-// order (number before NaN, larger first, lower index on ties).
+// The logit GEMM [T x d] x [d x E] runs on the tensor cores with
+// mma.sync m16n8k16 (bf16 products are exact, fp32 accumulation).  It is a
+// thin GEMM (E <= 256 columns): the operands go straight from global memory
+// into registers, no shared-memory staging.  Because a dot product does not
+// depend on the order of its terms, the MMA's 16 k-slots are mapped onto d
+// so that each thread's four k-slots of one MMA are four consecutive
+// elements: a thread loads 8 consecutive bf16 (16 bytes) of a row of x and of
+// Wr per 32-element step and feeds two MMAs from them.
+//
+// Each warp computes a 16-token m-tile against NTW n-tiles of 8 experts over
+// a slice of d.  A block of 8 warps splits d KS ways (memory parallelism for
+// small E, where the kernel is bound by reading x) and the experts NS ways
+// (register budget for E > 128).  Partial logits are summed in a fixed order
+// in shared memory, the bias is added, and one warp per token takes k rounds
+// of a warp arg-max in the order (number before NaN, larger first, lower
+// index on ties).
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -18,8 +29,7 @@ namespace cbmoe {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kDK = 32;  // d elements per shared-memory step
-
+constexpr int kWarps = kThreads / 32;
 
 struct Cand {
   float v;
@@ -33,136 +43,146 @@ __device__ __forceinline__ bool ranks_before(const Cand& a, const Cand& b) {
   return a.idx < b.idx;
 }
 
-template <int EX, int TN, int TM>
-struct RouterCfg {
-  static constexpr int ROWS = kThreads / EX;  // thread rows over tokens
-  static constexpr int TT = ROWS * TM;        // tokens per block
-  static constexpr int EP = EX * TN;          // padded expert count
-  static constexpr int GEMM_FLOATS = kDK * (TT + EP);
-  static constexpr int LOGIT_FLOATS = TT * (EP + 1);
-  static constexpr int SMEM_BYTES = 4 * (GEMM_FLOATS > LOGIT_FLOATS ? GEMM_FLOATS : LOGIT_FLOATS);
+__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// NT: n-tiles of 8 experts in total (E padded to 8 NT); KS: d split; NS:
+// expert split; MTB: 16-token m-tiles per block.  KS * NS * MTB == 8 warps.
+template <int NT, int KS, int NS, int MTB>
+struct RCfg {
+  static_assert(KS * NS * MTB == kWarps, "8 warps per block");
+  static constexpr int NTW = NT / NS;      // n-tiles per warp
+  static constexpr int EP = NT * 8;        // padded experts
+  static constexpr int TB = 16 * MTB;      // tokens per block
+  static constexpr int SMEM = KS * TB * EP * 4;
 };
 
-template <int EX, int TN, int TM>
-__global__ void __launch_bounds__(kThreads) router_topk_kernel(RouterArgs a) {
-  using C = RouterCfg<EX, TN, TM>;
-  constexpr int ROWS = C::ROWS, TT = C::TT, EP = C::EP;
-  extern __shared__ float sm[];
-  float* xs = sm;             // [kDK][TT]
-  float* ws = sm + kDK * TT;  // [kDK][EP]
-  const int tid = threadIdx.x;
-  const int tx = tid % EX, ty = tid / EX;
-  const int t0 = blockIdx.x * TT;
+template <int NT, int KS, int NS, int MTB>
+__global__ void __launch_bounds__(kThreads) router_mma_kernel(RouterArgs a) {
+  using C = RCfg<NT, KS, NS, MTB>;
+  constexpr int NTW = C::NTW, EP = C::EP, TB = C::TB;
+  extern __shared__ float part[];  // [KS][TB][EP], then part[0] holds the logits
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int g = lane >> 2, q = lane & 3;
+  const int ks = warp % KS;
+  const int ns = (warp / KS) % NS;
+  const int mt = warp / (KS * NS);
+  const int tok0 = blockIdx.x * TB + mt * 16;
+  const int dslice = a.d / KS;
+  const int dbeg = ks * dslice;
 
-  float acc[TM][TN];
+  const int r0 = tok0 + g, r1 = tok0 + g + 8;
+  const uint4* xa_ptr = reinterpret_cast<const uint4*>(a.x + static_cast<int64_t>(min(r0, a.T - 1)) * a.d + dbeg + 8 * q);
+  const uint4* xb_ptr = reinterpret_cast<const uint4*>(a.x + static_cast<int64_t>(min(r1, a.T - 1)) * a.d + dbeg + 8 * q);
+  const bool va = r0 < a.T, vb = r1 < a.T;
+  const uint4* w_ptr[NTW];
+  bool wv[NTW];
 #pragma unroll
-  for (int i = 0; i < TM; ++i)
-#pragma unroll
-    for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
-
-  for (int k0 = 0; k0 < a.d; k0 += kDK) {
-    for (int v = tid; v < TT * (kDK / 8); v += kThreads) {
-      const int r = v / (kDK / 8), c8 = v % (kDK / 8);
-      const int t = t0 + r;
-      uint4 q = make_uint4(0, 0, 0, 0);
-      if (t < a.T) q = __ldg(reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(t) * a.d + k0 + c8 * 8));
-      const uint32_t u[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        xs[(c8 * 8 + 2 * j) * TT + r] = __uint_as_float(u[j] << 16);
-        xs[(c8 * 8 + 2 * j + 1) * TT + r] = __uint_as_float(u[j] & 0xFFFF0000u);
-      }
-    }
-    for (int v = tid; v < EP * (kDK / 8); v += kThreads) {
-      const int e = v / (kDK / 8), c8 = v % (kDK / 8);
-      uint4 q = make_uint4(0, 0, 0, 0);
-      if (e < a.E) q = __ldg(reinterpret_cast<const uint4*>(a.wr + static_cast<size_t>(e) * a.d + k0 + c8 * 8));
-      const uint32_t u[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        ws[(c8 * 8 + 2 * j) * EP + e] = __uint_as_float(u[j] << 16);
-        ws[(c8 * 8 + 2 * j + 1) * EP + e] = __uint_as_float(u[j] & 0xFFFF0000u);
-      }
-    }
-    __syncthreads();
-    float part[TM][TN];
-#pragma unroll
-    for (int i = 0; i < TM; ++i)
-#pragma unroll
-      for (int j = 0; j < TN; ++j) part[i][j] = 0.f;
-#pragma unroll 8
-    for (int kk = 0; kk < kDK; ++kk) {
-      float xv[TM], wv[TN];
-#pragma unroll
-      for (int i = 0; i < TM; ++i) xv[i] = xs[kk * TT + ty + i * ROWS];
-#pragma unroll
-      for (int j = 0; j < TN; ++j) wv[j] = ws[kk * EP + tx + j * EX];
-#pragma unroll
-      for (int i = 0; i < TM; ++i)
-#pragma unroll
-        for (int j = 0; j < TN; ++j) part[i][j] = fmaf(xv[i], wv[j], part[i][j]);
-    }
-#pragma unroll
-    for (int i = 0; i < TM; ++i)
-#pragma unroll
-      for (int j = 0; j < TN; ++j) acc[i][j] += part[i][j];
-    __syncthreads();
+  for (int j = 0; j < NTW; ++j) {
+    const int e = (ns * NTW + j) * 8 + g;
+    wv[j] = e < a.E;
+    w_ptr[j] = reinterpret_cast<const uint4*>(a.wr + static_cast<int64_t>(min(e, a.E - 1)) * a.d + dbeg + 8 * q);
   }
 
-  float* ls = sm;  // [TT][EP + 1]
+  float acc[NTW][4];
 #pragma unroll
-  for (int i = 0; i < TM; ++i)
+  for (int j = 0; j < NTW; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+
+  // UNR 32-element steps per iteration: all their loads are issued before
+  // any MMA, so each thread keeps several 16-byte loads in flight.
+  constexpr int UNR = NTW <= 2 ? 4 : (NTW <= 4 ? 2 : 1);
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+  for (int c = 0; c < dslice; c += 32 * UNR) {
+    uint4 xa[UNR], xb[UNR], wr[UNR][NTW];
 #pragma unroll
-    for (int j = 0; j < TN; ++j) {
-      const int r = ty + i * ROWS, e = tx + j * EX;
-      float v = acc[i][j];
-      if (a.bias != nullptr && e < a.E) v += __ldg(a.bias + e);
-      ls[r * (EP + 1) + e] = v;
+    for (int u = 0; u < UNR; ++u) {
+      const bool in = c + 32 * u < dslice;
+      const int off = (c + 32 * u) / 8;  // in uint4 units
+      xa[u] = (in && va) ? __ldg(xa_ptr + off) : zero;
+      xb[u] = (in && vb) ? __ldg(xb_ptr + off) : zero;
+#pragma unroll
+      for (int j = 0; j < NTW; ++j) wr[u][j] = (in && wv[j]) ? __ldg(w_ptr[j] + off) : zero;
     }
+#pragma unroll
+    for (int u = 0; u < UNR; ++u)
+#pragma unroll
+      for (int j = 0; j < NTW; ++j) {
+        mma_bf16(acc[j], xa[u].x, xb[u].x, xa[u].y, xb[u].y, wr[u][j].x, wr[u][j].y);
+        mma_bf16(acc[j], xa[u].z, xb[u].z, xa[u].w, xb[u].w, wr[u][j].z, wr[u][j].w);
+      }
+  }
+
+  // partial logits -> shared memory
+  float* mine = part + (static_cast<int64_t>(ks) * TB + mt * 16) * EP;
+#pragma unroll
+  for (int j = 0; j < NTW; ++j) {
+    const int col = (ns * NTW + j) * 8 + 2 * q;
+    mine[g * EP + col] = acc[j][0];
+    mine[g * EP + col + 1] = acc[j][1];
+    mine[(g + 8) * EP + col] = acc[j][2];
+    mine[(g + 8) * EP + col + 1] = acc[j][3];
+  }
   __syncthreads();
+  // sum the KS partials in a fixed order, add the bias
+  for (int i = threadIdx.x; i < TB * EP; i += kThreads) {
+    float v = part[i];
+#pragma unroll
+    for (int s = 1; s < KS; ++s) v += part[static_cast<int64_t>(s) * TB * EP + i];
+    const int e = i % EP;
+    if (a.bias != nullptr && e < a.E) v += __ldg(a.bias + e);
+    part[i] = v;
+  }
+  __syncthreads();
+  const float* ls = part;  // [TB][EP]
+  const int t_base = blockIdx.x * TB;
 
   if (a.logits != nullptr) {
-    for (int v = tid; v < TT * a.E; v += kThreads) {
-      const int r = v / a.E, e = v % a.E, t = t0 + r;
-      if (t < a.T) a.logits[static_cast<size_t>(t) * a.E + e] = ls[r * (EP + 1) + e];
+    for (int i = threadIdx.x; i < TB * a.E; i += kThreads) {
+      const int r = i / a.E, e = i % a.E, t = t_base + r;
+      if (t < a.T) a.logits[static_cast<int64_t>(t) * a.E + e] = ls[r * EP + e];
     }
   }
 
   constexpr int PER = (EP + 31) / 32;
-  const int warp = tid / 32, lane = tid % 32;
-  for (int r = warp; r < TT; r += kThreads / 32) {
-    const int t = t0 + r;
+  for (int r = warp; r < TB; r += kWarps) {
+    const int t = t_base + r;
     if (t >= a.T) break;
-    Cand c[PER];
+    Cand cand[PER];
 #pragma unroll
     for (int p = 0; p < PER; ++p) {
       const int e = lane + 32 * p;
       if (e < a.E) {
-        const float v = ls[r * (EP + 1) + e];
-        c[p] = Cand{v, e, isnan(v) ? 1 : 0};
+        const float v = ls[r * EP + e];
+        cand[p] = Cand{v, e, isnan(v) ? 1 : 0};
       } else {
-        c[p] = Cand{0.f, e, 2};
+        cand[p] = Cand{0.f, e, 2};
       }
     }
     float my_v = 0.f, l0 = 0.f;
     int my_i = 0;
     for (int s = 0; s < a.k; ++s) {
-      Cand b = c[0];
+      Cand b = cand[0];
 #pragma unroll
       for (int p = 1; p < PER; ++p)
-        if (ranks_before(c[p], b)) b = c[p];
+        if (ranks_before(cand[p], b)) b = cand[p];
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        Cand o;
-        o.v = __shfl_xor_sync(0xffffffffu, b.v, off);
-        o.idx = __shfl_xor_sync(0xffffffffu, b.idx, off);
-        o.cls = __shfl_xor_sync(0xffffffffu, b.cls, off);
-        if (ranks_before(o, b)) b = o;
+      for (int o = 16; o > 0; o >>= 1) {
+        Cand other;
+        other.v = __shfl_xor_sync(0xffffffffu, b.v, o);
+        other.idx = __shfl_xor_sync(0xffffffffu, b.idx, o);
+        other.cls = __shfl_xor_sync(0xffffffffu, b.cls, o);
+        if (ranks_before(other, b)) b = other;
       }
       if ((b.idx & 31) == lane) {
 #pragma unroll
         for (int p = 0; p < PER; ++p)
-          if (p == (b.idx >> 5)) c[p].cls = 2;
+          if (p == (b.idx >> 5)) cand[p].cls = 2;
       }
       if (s == 0) l0 = b.v;
       if (lane == s) {
@@ -173,34 +193,59 @@ __global__ void __launch_bounds__(kThreads) router_topk_kernel(RouterArgs a) {
     const float ex = (lane < a.k) ? expf(my_v - l0) : 0.f;
     float sum = ex;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
     if (lane < a.k) {
-      a.ids[static_cast<size_t>(t) * a.k + lane] = my_i;
-      a.w[static_cast<size_t>(t) * a.k + lane] = ex / sum;
+      a.ids[static_cast<int64_t>(t) * a.k + lane] = my_i;
+      a.w[static_cast<int64_t>(t) * a.k + lane] = ex / sum;
     }
   }
 }
 
-template <int EX, int TN, int TM>
+template <int NT, int KS, int NS, int MTB>
 cudaError_t launch_cfg(const RouterArgs& a, cudaStream_t s) {
-  using C = RouterCfg<EX, TN, TM>;
-  const int blocks = (a.T + C::TT - 1) / C::TT;
+  using C = RCfg<NT, KS, NS, MTB>;
+  const int blocks = (a.T + C::TB - 1) / C::TB;
   if (blocks == 0) return cudaSuccess;
-  router_topk_kernel<EX, TN, TM><<<blocks, kThreads, C::SMEM_BYTES, s>>>(a);
+  router_mma_kernel<NT, KS, NS, MTB><<<blocks, kThreads, C::SMEM, s>>>(a);
   return cudaGetLastError();
+}
+
+template <int NT, int KS, int NS, int MTB>
+cudaError_t prepare_cfg() {
+  using C = RCfg<NT, KS, NS, MTB>;
+  return cudaFuncSetAttribute(router_mma_kernel<NT, KS, NS, MTB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              C::SMEM);
 }
 
 }  // namespace
 
-cudaError_t router_prepare() { return cudaSuccess; }
+// Configurations by expert count: small E splits d 8 ways over 16 tokens
+// per block; large E keeps up to 16 n-tiles (128 experts) per warp.
+#define CBMOE_ROUTER_CONFIGS(X) \
+  X(1, 8, 1, 1)                 \
+  X(2, 8, 1, 1)                 \
+  X(4, 4, 1, 2)                 \
+  X(8, 2, 1, 4)                 \
+  X(16, 2, 1, 4)                \
+  X(32, 1, 2, 4)
+
+cudaError_t router_prepare() {
+  cudaError_t e = cudaSuccess;
+#define X(nt, ks, ns, mtb) \
+  if (e == cudaSuccess) e = prepare_cfg<nt, ks, ns, mtb>();
+  CBMOE_ROUTER_CONFIGS(X)
+#undef X
+  return e;
+}
 
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t s) {
-  if (a.E <= 8) return launch_cfg<8, 1, 1>(a, s);
-  if (a.E <= 16) return launch_cfg<16, 1, 2>(a, s);
-  if (a.E <= 32) return launch_cfg<16, 2, 2>(a, s);
-  if (a.E <= 64) return launch_cfg<16, 4, 4>(a, s);
-  if (a.E <= 128) return launch_cfg<16, 8, 4>(a, s);
-  return launch_cfg<16, 16, 2>(a, s);
+  const int nt = (a.E + 7) / 8;
+  if (nt <= 1) return launch_cfg<1, 8, 1, 1>(a, s);
+  if (nt <= 2) return launch_cfg<2, 8, 1, 1>(a, s);
+  if (nt <= 4) return launch_cfg<4, 4, 1, 2>(a, s);
+  if (nt <= 8) return launch_cfg<8, 2, 1, 4>(a, s);
+  if (nt <= 16) return launch_cfg<16, 2, 1, 4>(a, s);
+  return launch_cfg<32, 1, 2, 4>(a, s);
 }
 
 }  // namespace cbmoe

@@ -19,12 +19,16 @@ SMALL = {
     "skewed_small": synth.custom_shape("skewed_small", T=1000, d=256, f=256, E=128, k=4, bias=True, seed=24),
     "e256_k16": synth.custom_shape("e256_k16", T=257, d=256, f=256, E=256, k=16, seed=25),
     "odd_T": synth.custom_shape("odd_T", T=1, d=512, f=512, E=8, k=2, seed=26),
+    # int8 experts with per-channel scales: several tiles, ragged tails
+    "int8_mid": synth.custom_shape("int8_mid", T=300, d=512, f=768, E=8, k=2, wdtype="int8", seed=27),
+    "int8_k6": synth.custom_shape("int8_k6", T=700, d=256, f=512, E=64, k=6, wdtype="int8", seed=28),
 }
 
 FULL = {  # workload: tokens sampled for the output check
     "mixtral_decode": 24,
     "skewed": 64,
     "mixtral_prefill": 24,
+    "int8": 48,
 }
 
 
