@@ -46,7 +46,9 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
-    p.add_argument("--shape", default=None, help="T,d,f,E,k of a custom bf16 layer (profiling cases)")
+    p.add_argument("--shape", default=None, help="T,d,f,E,k of a custom layer (profiling cases)")
+    p.add_argument("--wdtype", default="bf16", choices=["bf16", "int8"], help="expert weights of a --shape layer")
+    p.add_argument("--bias", action="store_true", help="skewed router bias on a --shape layer")
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--l2-flush-mb", type=int, default=512)
     p.add_argument("--e2e-steps", type=int, default=50)
@@ -430,7 +432,9 @@ def workload_shape(args):
     import synth
     if args.shape:
         T, d, f, E, k = (int(v) for v in args.shape.split(","))
-        return synth.custom_shape(f"custom_T{T}_d{d}_f{f}_E{E}_k{k}", T=T, d=d, f=f, E=E, k=k, seed=1100)
+        name = f"custom_T{T}_d{d}_f{f}_E{E}_k{k}" + ("_int8" if args.wdtype == "int8" else "") + \
+            ("_bias" if args.bias else "")
+        return synth.custom_shape(name, T=T, d=d, f=f, E=E, k=k, wdtype=args.wdtype, bias=args.bias, seed=1100)
     return synth.WORKLOADS[args.workload]
 
 

@@ -50,19 +50,26 @@ namespace {
 constexpr int BM = kTileM;               // 128 rows per tile
 constexpr int BK = 64;                   // 64 bf16 = one 128-byte swizzled row
 constexpr int BN = 256;                  // accumulator columns per tile
-constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;     // 16 KB
 constexpr int B_BYTES = BN * BK * 2;     // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int I8_SLOTS = 2;
 constexpr int I8_BYTES = BN * BK;        // 16 KB of int8 per staged B tile
-constexpr int N_XFORM_WARPS = 4;
+constexpr int N_XFORM_WARPS = 8;
 constexpr uint32_t TMEM_COLS = 2 * BN;   // two fp32 accumulators of 256 columns
 constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
 
+// bf16 weights: a 4-stage ring of (A, B) tiles filled by one TMA thread.
+// int8 weights: a 3-stage (A, bf16 B) ring for the MMA plus a 5-slot ring of
+// int8 B tiles with its own TMA thread, so weight loads run up to five
+// k-blocks ahead of the MMA (about a DRAM latency) while the transform warps
+// fill the bf16 B stages.
 template <bool INT8>
 struct Shape {
-  static constexpr int THREADS = INT8 ? 192 + 32 * N_XFORM_WARPS : 192;
+  static constexpr int STAGES = INT8 ? 3 : 4;
+  static constexpr int I8_SLOTS = INT8 ? 5 : 1;
+  static constexpr int XFORM_WARP0 = 6;
+  static constexpr int BPROD_WARP = XFORM_WARP0 + N_XFORM_WARPS;
+  static constexpr int THREADS = INT8 ? 32 * (BPROD_WARP + 1) : 192;
   static constexpr int RING_BYTES = STAGES * STAGE_BYTES + (INT8 ? I8_SLOTS * I8_BYTES : 0);
   static constexpr int SMEM_BYTES = RING_BYTES + 1024 + 256;
 };
@@ -108,6 +115,8 @@ template <int KIND, bool INT8>
 __global__ void __launch_bounds__(Shape<INT8>::THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                         const GemmArgs p) {
+  constexpr int STAGES = Shape<INT8>::STAGES;
+  constexpr int I8_SLOTS = Shape<INT8>::I8_SLOTS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sa = smem;
@@ -151,7 +160,7 @@ __global__ void __launch_bounds__(Shape<INT8>::THREADS, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      // ------------------------------------------------------ TMA producer
+      // ------------------------------------------ TMA producer (A, and bf16 B)
       int64_t issued = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
@@ -167,17 +176,8 @@ __global__ void __launch_bounds__(Shape<INT8>::THREADS, 1)
             break;
           }
           if constexpr (INT8) {
-            const int slot = static_cast<int>(issued % I8_SLOTS);
-            const uint32_t sphase = static_cast<uint32_t>((issued / I8_SLOTS) & 1);
-            if (!mbar_wait(&i8_empty[slot], sphase ^ 1u, p.wait_limit_ns)) {
-              set_error(p.err, kErrTimeout);
-              ok = false;
-              break;
-            }
             mbar_arrive_expect_tx(&full[stage], A_BYTES);
             tma_load_2d(sa + stage * A_BYTES, &tm_a, &full[stage], kb * BK, a_row);
-            mbar_arrive_expect_tx(&i8_full[slot], I8_BYTES);
-            tma_load_2d(s8 + slot * I8_BYTES, &tm_b, &i8_full[slot], kb * BK, b_row);
           } else {
             mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
             tma_load_2d(sa + stage * A_BYTES, &tm_a, &full[stage], kb * BK, a_row);
@@ -187,15 +187,10 @@ __global__ void __launch_bounds__(Shape<INT8>::THREADS, 1)
         }
       }
       // No load of ours may still be landing in shared memory when the CTA
-      // exits: wait for the last load issued into each slot.
+      // exits: wait for the last load issued into each stage.
       for (int64_t i = (issued > STAGES ? issued - STAGES : 0); i < issued; ++i)
         if (!mbar_wait(&full[i % STAGES], static_cast<uint32_t>((i / STAGES) & 1), p.wait_limit_ns))
           set_error(p.err, kErrTimeout);
-      if constexpr (INT8) {
-        for (int64_t i = (issued > I8_SLOTS ? issued - I8_SLOTS : 0); i < issued; ++i)
-          if (!mbar_wait(&i8_full[i % I8_SLOTS], static_cast<uint32_t>((i / I8_SLOTS) & 1), p.wait_limit_ns))
-            set_error(p.err, kErrTimeout);
-      }
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -303,42 +298,70 @@ __global__ void __launch_bounds__(Shape<INT8>::THREADS, 1)
       }
     }
   } else if constexpr (INT8) {
-    // ------------------------------------------- int8 -> bf16 transform
-    // 128 threads; thread x handles the 16-byte output chunks x, x+128, ...
-    // of the 256 rows x 8 chunks: chunk (r, c) takes the 8 int8 codes at
-    // staged bytes r*64 + 8c and lands at r*128 + 16*(c ^ (r & 7)), the
-    // 128-byte-swizzled position of K elements 8c..8c+7 of row r.
-    const int xt = threadIdx.x - 192;
-    int64_t it = 0;
-    bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-      for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
-        const int stage = static_cast<int>(it % STAGES);
-        const uint32_t phase = static_cast<uint32_t>((it / STAGES) & 1);
-        const int slot = static_cast<int>(it % I8_SLOTS);
-        const uint32_t sphase = static_cast<uint32_t>((it / I8_SLOTS) & 1);
-        if (!mbar_wait(&i8_full[slot], sphase, p.wait_limit_ns) ||
-            !mbar_wait(&empty[stage], phase ^ 1u, p.wait_limit_ns)) {
-          set_error(p.err, kErrTimeout);
-          ok = false;
-          break;
+    if (warp == Shape<INT8>::BPROD_WARP) {
+      if (lane == 0) {
+        // --------------------------------------------- TMA producer (int8 B)
+        int64_t issued = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+          const TileCoord c = decode_tile(tile, p);
+          const int b_row = c.e * p.b_rows_per_expert + c.n * BN;
+          for (int kb = 0; kb < p.k_blocks; ++kb) {
+            const int slot = static_cast<int>(issued % I8_SLOTS);
+            const uint32_t sphase = static_cast<uint32_t>((issued / I8_SLOTS) & 1);
+            if (!mbar_wait(&i8_empty[slot], sphase ^ 1u, p.wait_limit_ns)) {
+              set_error(p.err, kErrTimeout);
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&i8_full[slot], I8_BYTES);
+            tma_load_2d(s8 + slot * I8_BYTES, &tm_b, &i8_full[slot], kb * BK, b_row);
+            ++issued;
+          }
         }
-        const uint8_t* src = s8 + slot * I8_BYTES;
-        uint8_t* dst = sb + stage * B_BYTES;
-#pragma unroll 4
-        for (int ch = xt; ch < BN * 8; ch += 32 * N_XFORM_WARPS) {
-          const int r = ch >> 3, cc = ch & 7;
-          const uint2 w = *reinterpret_cast<const uint2*>(src + r * 64 + cc * 8);
-          uint4 o;
-          int8x4_to_bf16x4(w.x, o.x, o.y);
-          int8x4_to_bf16x4(w.y, o.z, o.w);
-          *reinterpret_cast<uint4*>(dst + r * 128 + 16 * (cc ^ (r & 7))) = o;
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&i8_empty[slot]);
-          mbar_arrive(&full[stage]);
+        for (int64_t i = (issued > I8_SLOTS ? issued - I8_SLOTS : 0); i < issued; ++i)
+          if (!mbar_wait(&i8_full[i % I8_SLOTS], static_cast<uint32_t>((i / I8_SLOTS) & 1), p.wait_limit_ns))
+            set_error(p.err, kErrTimeout);
+      }
+    } else {
+      // ----------------------------------------- int8 -> bf16 transform
+      // N_XFORM_WARPS warps; thread x handles the 16-byte output chunks x,
+      // x + 32 N_XFORM_WARPS, ... of the 256 rows x 8 chunks: chunk (r, c)
+      // takes the 8 int8 codes at staged bytes r*64 + 8c and lands at
+      // r*128 + 16*(c ^ (r & 7)), the 128-byte-swizzled position of K
+      // elements 8c..8c+7 of row r.
+      const int xt = threadIdx.x - 32 * Shape<INT8>::XFORM_WARP0;
+      int64_t it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+        for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
+          const int stage = static_cast<int>(it % STAGES);
+          const uint32_t phase = static_cast<uint32_t>((it / STAGES) & 1);
+          const int slot = static_cast<int>(it % I8_SLOTS);
+          const uint32_t sphase = static_cast<uint32_t>((it / I8_SLOTS) & 1);
+          if (!mbar_wait(&i8_full[slot], sphase, p.wait_limit_ns) ||
+              !mbar_wait(&empty[stage], phase ^ 1u, p.wait_limit_ns)) {
+            set_error(p.err, kErrTimeout);
+            ok = false;
+            break;
+          }
+          const uint8_t* src = s8 + slot * I8_BYTES;
+          uint8_t* dst = sb + stage * B_BYTES;
+#pragma unroll
+          for (int ch = xt; ch < BN * 8; ch += 32 * N_XFORM_WARPS) {
+            const int r = ch >> 3, cc = ch & 7;
+            const uint2 w = *reinterpret_cast<const uint2*>(src + ch * 8);
+            uint4 o;
+            int8x4_to_bf16x4(w.x, o.x, o.y);
+            int8x4_to_bf16x4(w.y, o.z, o.w);
+            *reinterpret_cast<uint4*>(dst + r * 128 + 16 * (cc ^ (r & 7))) = o;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&i8_empty[slot]);
+            mbar_arrive(&full[stage]);
+          }
         }
       }
     }
