@@ -28,7 +28,7 @@ struct cb_moe {
   // weights (handle-owned copies)
   uint16_t* wr;
   float* bias;
-  void* wgu;  // [E][f/128][2][128][d]: gate rows then up rows per 128-block
+  void* wgu;  // [E][f/B][2][B][d]: gate rows then up rows per B-row block (B = 128 bf16, 64 int8)
   void* wd;   // [E][d][f]
   float *sg, *su, *sd;
   // workspace
@@ -38,7 +38,7 @@ struct cb_moe {
   int32_t* ids;
   float* w;
   float* logits;
-  int32_t *chunk, *counts, *offsets, *mtile_off, *mtile_expert, *tok, *inv;
+  int32_t *chunk, *counts, *offsets, *mtile_off, *mtile_expert, *ptile_off, *ptile_expert, *tok, *inv;
   int* err;
   uint16_t *x_stage, *out_stage;
   int32_t max_mtiles, n_chunks;
@@ -52,7 +52,7 @@ namespace {
 struct Layout {
   uint64_t off_wr, off_bias, off_wgu, off_wd, off_sg, off_su, off_sd;
   uint64_t off_xp, off_hb, off_y, off_ids, off_w, off_logits, off_chunk, off_counts, off_offsets, off_mtile_off,
-      off_mtile_expert, off_tok, off_inv, off_err, off_xs, off_os;
+      off_mtile_expert, off_ptile_off, off_ptile_expert, off_tok, off_inv, off_err, off_xs, off_os;
   uint64_t total;
   int32_t max_mtiles, n_chunks;
 };
@@ -91,6 +91,8 @@ Layout plan(const cb_moe_config_t& c) {
   L.off_offsets = take((E + 1) * 4);
   L.off_mtile_off = take((E + 1) * 4);
   L.off_mtile_expert = take(static_cast<uint64_t>(L.max_mtiles) * 4);
+  L.off_ptile_off = take((E + 1) * 4);
+  L.off_ptile_expert = take(static_cast<uint64_t>(L.max_mtiles) * 4);
   L.off_tok = take(M * 4);
   L.off_inv = take(M * 4);
   L.off_err = take(64);
@@ -200,6 +202,8 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
   da.mtile_off = h->mtile_off;
   da.mtile_expert = h->mtile_expert;
   da.max_mtiles = h->max_mtiles;
+  da.ptile_off = h->ptile_off;
+  da.ptile_expert = h->ptile_expert;
   da.tok = h->tok;
   da.inv = h->inv;
   da.xp = h->xp;
@@ -211,8 +215,10 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
   GemmArgs ga{};
   ga.mtile_off = h->mtile_off;
   ga.mtile_expert = h->mtile_expert;
+  ga.ptile_off = h->ptile_off;
+  ga.ptile_expert = h->ptile_expert;
   ga.E = c.n_experts;
-  ga.n_tiles = c.d_ff / grouped_gemm_tile_n(kGateUpSwiGLU);
+  ga.n_tiles = c.d_ff / (int8w ? grouped_gemm_int8_tile_n(kGateUpSwiGLU) : grouped_gemm_tile_n(kGateUpSwiGLU));
   ga.k_blocks = c.d_model / 64;
   ga.b_rows_per_expert = 2 * c.d_ff;
   ga.out = h->hb;
@@ -222,19 +228,21 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
   ga.err = h->err;
   ga.wait_limit_ns = kWaitLimitNs;
   ga.grid = h->num_sms;
-  if (launch_grouped_gemm(kGateUpSwiGLU, int8w, h->tm_a_gu, h->tm_b_gu, ga, s) != cudaSuccess || !mark(3))
-    return CB_ERR_CUDA;
+  const cudaError_t e1 = int8w ? launch_grouped_gemm_int8(kGateUpSwiGLU, h->tm_a_gu, h->tm_b_gu, ga, s)
+                               : launch_grouped_gemm(kGateUpSwiGLU, false, h->tm_a_gu, h->tm_b_gu, ga, s);
+  if (e1 != cudaSuccess || !mark(3)) return CB_ERR_CUDA;
 
   GemmArgs gd = ga;
-  gd.n_tiles = c.d_model / grouped_gemm_tile_n(kDownF32);
+  gd.n_tiles = c.d_model / (int8w ? grouped_gemm_int8_tile_n(kDownF32) : grouped_gemm_tile_n(kDownF32));
   gd.k_blocks = c.d_ff / 64;
   gd.b_rows_per_expert = c.d_model;
   gd.out = h->y;
   gd.ld_out = c.d_model;
   gd.scale0 = h->sd;
   gd.scale1 = nullptr;
-  if (launch_grouped_gemm(kDownF32, int8w, h->tm_a_dn, h->tm_b_dn, gd, s) != cudaSuccess || !mark(4))
-    return CB_ERR_CUDA;
+  const cudaError_t e2 = int8w ? launch_grouped_gemm_int8(kDownF32, h->tm_a_dn, h->tm_b_dn, gd, s)
+                               : launch_grouped_gemm(kDownF32, false, h->tm_a_dn, h->tm_b_dn, gd, s);
+  if (e2 != cudaSuccess || !mark(4)) return CB_ERR_CUDA;
 
   CombineArgs ca{};
   ca.y = h->y;
@@ -342,6 +350,8 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
   h->offsets = reinterpret_cast<int32_t*>(b + L.off_offsets);
   h->mtile_off = reinterpret_cast<int32_t*>(b + L.off_mtile_off);
   h->mtile_expert = reinterpret_cast<int32_t*>(b + L.off_mtile_expert);
+  h->ptile_off = reinterpret_cast<int32_t*>(b + L.off_ptile_off);
+  h->ptile_expert = reinterpret_cast<int32_t*>(b + L.off_ptile_expert);
   h->tok = reinterpret_cast<int32_t*>(b + L.off_tok);
   h->inv = reinterpret_cast<int32_t*>(b + L.off_inv);
   h->err = reinterpret_cast<int*>(b + L.off_err);
@@ -360,9 +370,10 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
          cudaMemcpy(h->su, wts->s_up, E * f * 4, cudaMemcpyDeviceToDevice) == cudaSuccess &&
          cudaMemcpy(h->sd, wts->s_down, E * d * 4, cudaMemcpyDeviceToDevice) == cudaSuccess;
   }
-  // gate/up interleave: block n of expert e = gate rows [128n, 128n+128) then the same up rows
-  const uint64_t blk = 128 * d * eb;  // bytes of 128 weight rows
-  const uint64_t nblk = E * (f / 128);
+  // gate/up interleave: block n of expert e = gate rows [Bn, Bn+B) then the same up rows
+  const uint64_t brows = int8w ? grouped_gemm_int8_gateup_block() : 128;
+  const uint64_t blk = brows * d * eb;  // bytes of one block of weight rows
+  const uint64_t nblk = E * (f / brows);
   ok = ok && cudaMemcpy2D(h->wgu, 2 * blk, wts->w_gate, blk, blk, nblk, cudaMemcpyDeviceToDevice) == cudaSuccess;
   ok = ok && cudaMemcpy2D(static_cast<char*>(h->wgu) + blk, 2 * blk, wts->w_up, blk, blk, nblk,
                           cudaMemcpyDeviceToDevice) == cudaSuccess;
@@ -370,10 +381,12 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
   const CUtensorMapDataType wdt = int8w ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   ok = ok && make_tmap(&h->tm_a_gu, h->xp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, mpad, 64, 128);
   const CUtensorMapSwizzle wsw = int8w ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B;
-  ok = ok && make_tmap(&h->tm_b_gu, h->wgu, wdt, eb, d, E * 2 * f, 64, 256, wsw);
+  const uint32_t brows_box = int8w ? 128 : 256;
+  ok = ok && make_tmap(&h->tm_b_gu, h->wgu, wdt, eb, d, E * 2 * f, 64, brows_box, wsw);
   ok = ok && make_tmap(&h->tm_a_dn, h->hb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, f, mpad, 64, 128);
-  ok = ok && make_tmap(&h->tm_b_dn, h->wd, wdt, eb, f, E * d, 64, 256, wsw);
-  ok = ok && grouped_gemm_prepare() == cudaSuccess && router_prepare() == cudaSuccess;
+  ok = ok && make_tmap(&h->tm_b_dn, h->wd, wdt, eb, f, E * d, 64, brows_box, wsw);
+  ok = ok && grouped_gemm_prepare() == cudaSuccess && grouped_gemm_int8_prepare() == cudaSuccess &&
+       router_prepare() == cudaSuccess;
   h->timing = (cfg->flags & CB_FLAG_STAGE_TIMING) != 0;
   for (int i = 0; ok && h->timing && i <= CB_N_STAGES; ++i) ok = cudaEventCreate(&h->ev[i]) == cudaSuccess;
   ok = ok && cudaDeviceSynchronize() == cudaSuccess;

@@ -83,8 +83,10 @@ __global__ void __launch_bounds__(kThreads) dispatch_scan(DispatchArgs a) {
     }
   }
   const int mt = (total + kTileM - 1) / kTileM;
+  const int pt = (mt + 1) / 2;
   const int off = block_exclusive_scan(e < a.E ? total : 0, tmp);
   const int moff = block_exclusive_scan(e < a.E ? mt : 0, tmp);
+  const int poff = block_exclusive_scan(e < a.E ? pt : 0, tmp);
   if (e < a.E) {
     a.counts[e] = total;
     a.offsets[e] = off;
@@ -96,6 +98,11 @@ __global__ void __launch_bounds__(kThreads) dispatch_scan(DispatchArgs a) {
     }
     for (int b = 0; b < a.n_chunks; ++b) a.chunk[static_cast<int64_t>(b) * a.E + e] += off;
     for (int i = moff; i < moff + mt && i < a.max_mtiles; ++i) a.mtile_expert[i] = e;
+    if (a.ptile_off != nullptr) {
+      a.ptile_off[e] = poff;
+      if (e == a.E - 1) a.ptile_off[a.E] = poff + pt;
+      for (int i = poff; i < poff + pt && i < a.max_mtiles; ++i) a.ptile_expert[i] = e;
+    }
   }
 }
 

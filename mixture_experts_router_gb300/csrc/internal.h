@@ -47,6 +47,8 @@ struct DispatchArgs {
   int32_t* mtile_off;    // [E+1] prefix sum of ceil(counts/kTileM)
   int32_t* mtile_expert; // [max_mtiles] expert owning each m-tile
   int32_t max_mtiles;
+  int32_t* ptile_off;    // [E+1] prefix sum of ceil(mtiles/2): pairs of m-tiles (or nullptr)
+  int32_t* ptile_expert; // [max_mtiles] expert owning each pair (or nullptr)
   int32_t* tok;          // [T*k]
   int32_t* inv;          // [T*k]
   uint16_t* xp;          // bf16 [max_mtiles*kTileM][d]
@@ -76,6 +78,8 @@ cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s);
 struct GemmArgs {
   const int32_t* mtile_off;     // [E+1]
   const int32_t* mtile_expert;  // [max_mtiles]
+  const int32_t* ptile_off;     // [E+1] m-tile pairs (int8 kernels)
+  const int32_t* ptile_expert;  // [max_mtiles]
   int32_t E;
   int32_t n_tiles;              // N tiles per expert
   int32_t k_blocks;             // K / 64
@@ -93,5 +97,11 @@ cudaError_t launch_grouped_gemm(GemmKind kind, bool int8_weights, const CUtensor
                                 const CUtensorMap& tm_b, const GemmArgs& a, cudaStream_t s);
 cudaError_t grouped_gemm_prepare();  // one-time function attributes
 int grouped_gemm_tile_n(GemmKind kind);  // output columns per tile
+// int8 weights: tiles are pairs of m-tiles against 128 weight rows
+cudaError_t launch_grouped_gemm_int8(GemmKind kind, const CUtensorMap& tm_a, const CUtensorMap& tm_b,
+                                     const GemmArgs& a, cudaStream_t s);
+cudaError_t grouped_gemm_int8_prepare();
+int grouped_gemm_int8_tile_n(GemmKind kind);
+int grouped_gemm_int8_gateup_block();  // gate/up rows interleaved in blocks of this size
 
 }  // namespace cbmoe
