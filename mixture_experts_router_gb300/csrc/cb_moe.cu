@@ -44,7 +44,9 @@ struct cb_moe {
   int32_t max_mtiles, n_chunks;
   cudaEvent_t ev[CB_N_STAGES + 1];
   bool timing;
-  CUtensorMap tm_a_gu, tm_b_gu, tm_a_dn, tm_b_dn;
+  bool router_tc;          // tcgen05 router (else the mma.sync router)
+  const void* tm_x_src;    // x pointer tm_x was encoded for
+  CUtensorMap tm_a_gu, tm_b_gu, tm_a_dn, tm_b_dn, tm_y, tm_x, tm_wr;
 };
 
 namespace {
@@ -186,7 +188,16 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
   ra.w = h->w;
   ra.logits = h->logits;
   ra.err = h->err;
-  if (launch_router(ra, s) != cudaSuccess || !mark(1)) return CB_ERR_CUDA;
+  if (h->router_tc) {
+    if (h->tm_x_src != x) {
+      if (!make_tmap(&h->tm_x, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c.d_model, c.n_tokens, 64, 128))
+        return CB_ERR_CUDA;
+      h->tm_x_src = x;
+    }
+    if (launch_router_tc(h->tm_x, h->tm_wr, ra, h->num_sms, s) != cudaSuccess || !mark(1)) return CB_ERR_CUDA;
+  } else {
+    if (launch_router(ra, s) != cudaSuccess || !mark(1)) return CB_ERR_CUDA;
+  }
 
   DispatchArgs da{};
   da.ids = h->ids;
@@ -228,8 +239,8 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
   ga.err = h->err;
   ga.wait_limit_ns = kWaitLimitNs;
   ga.grid = h->num_sms;
-  const cudaError_t e1 = int8w ? launch_grouped_gemm_int8(kGateUpSwiGLU, h->tm_a_gu, h->tm_b_gu, ga, s)
-                               : launch_grouped_gemm(kGateUpSwiGLU, false, h->tm_a_gu, h->tm_b_gu, ga, s);
+  const cudaError_t e1 = int8w ? launch_grouped_gemm_int8(kGateUpSwiGLU, h->tm_a_gu, h->tm_b_gu, h->tm_y, ga, s)
+                               : launch_grouped_gemm(kGateUpSwiGLU, false, h->tm_a_gu, h->tm_b_gu, h->tm_y, ga, s);
   if (e1 != cudaSuccess || !mark(3)) return CB_ERR_CUDA;
 
   GemmArgs gd = ga;
@@ -240,8 +251,8 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
   gd.ld_out = c.d_model;
   gd.scale0 = h->sd;
   gd.scale1 = nullptr;
-  const cudaError_t e2 = int8w ? launch_grouped_gemm_int8(kDownF32, h->tm_a_dn, h->tm_b_dn, gd, s)
-                               : launch_grouped_gemm(kDownF32, false, h->tm_a_dn, h->tm_b_dn, gd, s);
+  const cudaError_t e2 = int8w ? launch_grouped_gemm_int8(kDownF32, h->tm_a_dn, h->tm_b_dn, h->tm_y, gd, s)
+                               : launch_grouped_gemm(kDownF32, false, h->tm_a_dn, h->tm_b_dn, h->tm_y, gd, s);
   if (e2 != cudaSuccess || !mark(4)) return CB_ERR_CUDA;
 
   CombineArgs ca{};
@@ -385,8 +396,20 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
   ok = ok && make_tmap(&h->tm_b_gu, h->wgu, wdt, eb, d, E * 2 * f, 64, brows_box, wsw);
   ok = ok && make_tmap(&h->tm_a_dn, h->hb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, f, mpad, 64, 128);
   ok = ok && make_tmap(&h->tm_b_dn, h->wd, wdt, eb, f, E * d, 64, brows_box, wsw);
+  ok = ok && make_tmap(&h->tm_y, h->y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, mpad, 32, 32);
   ok = ok && grouped_gemm_prepare() == cudaSuccess && grouped_gemm_int8_prepare() == cudaSuccess &&
-       router_prepare() == cudaSuccess;
+       router_prepare() == cudaSuccess && router_tc_prepare() == cudaSuccess;
+  // router: tcgen05 for wide expert counts, the mma.sync split-K router for
+  // E <= 16 (bound by reading x, where more CTAs help); CB_MOE_ROUTER=tc|mma
+  // overrides the choice
+  {
+    const char* rv = std::getenv("CB_MOE_ROUTER");
+    h->router_tc = cfg->n_experts > 16;
+    if (rv != nullptr && std::strcmp(rv, "tc") == 0) h->router_tc = true;
+    if (rv != nullptr && std::strcmp(rv, "mma") == 0) h->router_tc = false;
+  }
+  ok = ok && make_tmap(&h->tm_wr, h->wr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, E, 64,
+                       static_cast<uint32_t>(router_tc_rows(cfg->n_experts)));
   h->timing = (cfg->flags & CB_FLAG_STAGE_TIMING) != 0;
   for (int i = 0; ok && h->timing && i <= CB_N_STAGES; ++i) ok = cudaEventCreate(&h->ev[i]) == cudaSuccess;
   ok = ok && cudaDeviceSynchronize() == cudaSuccess;

@@ -48,7 +48,13 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int THREADS = 192;
 constexpr uint32_t TMEM_COLS = 2 * BN;   // two fp32 accumulators of 256 columns
 constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+constexpr int STG_BYTES = 4 * 2 * 32 * 128;  // down epilogue: 4 warps x 2 buffers x 32 rows x 128 B
+template <int KIND>
+struct Smem {
+  static constexpr int RING = STAGES * STAGE_BYTES;
+  static constexpr int STAGING = KIND == kDownF32 ? STG_BYTES : 0;
+  static constexpr int BYTES = RING + STAGING + 1024 + 256;
+};
 
 struct TileCoord {
   int m_tile;  // global 128-row tile index in the grouped rows
@@ -78,12 +84,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 template <int KIND>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                        const GemmArgs p) {
+                        const __grid_constant__ CUtensorMap tm_out, const GemmArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sa = smem;
   uint8_t* sb = smem + STAGES * A_BYTES;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint8_t* staging = smem + Smem<KIND>::RING;  // down: per-warp store buffers
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Smem<KIND>::RING + Smem<KIND>::STAGING);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
@@ -102,6 +109,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     fence_barrier_init();
     prefetch_tensormap(&tm_a);
     prefetch_tensormap(&tm_b);
+    if (KIND == kDownF32) prefetch_tensormap(&tm_out);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, TMEM_COLS);
@@ -193,6 +201,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int q = warp & 3;  // this warp's quarter of the 128 TMEM lanes
     int acc = 0;
     uint32_t acc_phase = 0;
+    int n_stores = 0;  // bulk stores issued by this warp (down only)
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
       const TileCoord c = decode_tile(tile, p);
       if (!mbar_wait(&tfull[acc], acc_phase, p.wait_limit_ns)) {
@@ -221,17 +230,31 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int j = 0; j < 4; ++j) dst[j] = make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
         }
       } else {
-        float* out_row = static_cast<float*>(p.out) + row * p.ld_out + c.n * BN;
+        // TMA-store epilogue: this warp's 32 rows x 32 fp32 columns go through
+        // a 128-byte-swizzled staging buffer (two per warp, alternating), then
+        // one bulk tensor store writes whole 128-byte row segments.
+        const int row0 = c.m_tile * BM + q * 32;
 #pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 32) {
+        for (int c0 = 0; c0 < BN; c0 += 32, ++n_stores) {
           uint32_t r[32];
           tmem_load32(tbase + c0, r);
-          float4* dst = reinterpret_cast<float4*>(out_row + c0);
+          uint8_t* buf = staging + (q * 2 + (n_stores & 1)) * 4096;
+          if (n_stores >= 2) {
+            if (lane == 0) bulk_wait_group_read<1>();
+            __syncwarp();
+          }
 #pragma unroll
           for (int j = 0; j < 8; ++j)
-            dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                 __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+            *reinterpret_cast<uint4*>(buf + lane * 128 + 16 * (j ^ (lane & 7))) =
+                make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tm_out, buf, c.n * BN + c0, row0);
+            bulk_commit_group();
+          }
         }
+        (void)row;
       }
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
@@ -240,6 +263,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         acc_phase ^= 1u;
       }
     }
+    if (KIND == kDownF32 && lane == 0) bulk_wait_group<0>();
   }
 
   tc_fence_before();
@@ -256,19 +280,19 @@ int grouped_gemm_tile_n(GemmKind kind) { return kind == kGateUpSwiGLU ? BN / 2 :
 
 cudaError_t grouped_gemm_prepare() {
   cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<kGateUpSwiGLU>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<kGateUpSwiGLU>::BYTES);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(grouped_gemm_kernel<kDownF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              SMEM_BYTES);
+                              Smem<kDownF32>::BYTES);
 }
 
 cudaError_t launch_grouped_gemm(GemmKind kind, bool int8_weights, const CUtensorMap& tm_a, const CUtensorMap& tm_b,
-                                const GemmArgs& a, cudaStream_t s) {
+                                const CUtensorMap& tm_out, const GemmArgs& a, cudaStream_t s) {
   if (int8_weights) return cudaErrorNotSupported;
   if (kind == kGateUpSwiGLU)
-    grouped_gemm_kernel<kGateUpSwiGLU><<<a.grid, THREADS, SMEM_BYTES, s>>>(tm_a, tm_b, a);
+    grouped_gemm_kernel<kGateUpSwiGLU><<<a.grid, THREADS, Smem<kGateUpSwiGLU>::BYTES, s>>>(tm_a, tm_b, tm_out, a);
   else
-    grouped_gemm_kernel<kDownF32><<<a.grid, THREADS, SMEM_BYTES, s>>>(tm_a, tm_b, a);
+    grouped_gemm_kernel<kDownF32><<<a.grid, THREADS, Smem<kDownF32>::BYTES, s>>>(tm_a, tm_b, tm_out, a);
   return cudaGetLastError();
 }
 

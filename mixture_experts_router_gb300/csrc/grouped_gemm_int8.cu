@@ -23,8 +23,10 @@
 //   warps 6..9  : int8 -> bf16 transform of each staged weight tile into the
 //                 stage's 128-byte-swizzled B buffer, then fence to the async
 //                 proxy and arrive on the stage barrier
-//   warp 10     : TMA producer of the int8 weight tiles (128x64) into an
-//                 8-slot ring, running up to 8 k-blocks ahead
+//   warp 10     : TMA producer of the int8 weight tiles (128x64) into a
+//                 6-slot ring, running up to 6 k-blocks ahead
+// The down kernel's epilogue stages each warp's 32x32 fp32 blocks in
+// 128-byte-swizzled shared memory and writes them with bulk tensor stores.
 // Every wait is bounded (CB_ERR_TIMEOUT in the status word on expiry).
 #include <cuda_bf16.h>
 
@@ -41,7 +43,7 @@ constexpr int STAGES = 3;
 constexpr int A_BYTES = BM * BK * 2;  // 16 KB per m-tile
 constexpr int B_BYTES = BN * BK * 2;  // 16 KB bf16
 constexpr int STAGE_BYTES = 2 * A_BYTES + B_BYTES;
-constexpr int I8_SLOTS = 8;
+constexpr int I8_SLOTS = 6;
 constexpr int I8_BYTES = BN * BK;     // 8 KB int8
 constexpr int N_XFORM_WARPS = 4;
 constexpr int XFORM_WARP0 = 6;
@@ -50,7 +52,12 @@ constexpr int THREADS = 32 * (BPROD_WARP + 1);
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
 constexpr int RING_BYTES = STAGES * STAGE_BYTES + I8_SLOTS * I8_BYTES;
-constexpr int SMEM_BYTES = RING_BYTES + 1024 + 256;
+constexpr int STG_BYTES = 4 * 2 * 32 * 128;  // down epilogue: 4 warps x 2 buffers x 32 rows x 128 B
+template <int KIND>
+struct Smem {
+  static constexpr int STAGING = KIND == kDownF32 ? STG_BYTES : 0;
+  static constexpr int BYTES = RING_BYTES + STAGING + 1024 + 256;
+};
 
 struct PairCoord {
   int m0;      // first m-tile (global index)
@@ -96,12 +103,13 @@ __device__ __forceinline__ void int8x4_to_bf16x4(uint32_t w, uint32_t& lo, uint3
 template <int KIND>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_int8_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                             const GemmArgs p) {
+                             const __grid_constant__ CUtensorMap tm_out, const GemmArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   // stage s: A0 at s*STAGE_BYTES, A1 at +A_BYTES, B at +2*A_BYTES (all 1024-aligned)
   uint8_t* s8 = smem + STAGES * STAGE_BYTES;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + RING_BYTES);
+  uint8_t* staging = smem + RING_BYTES;  // down: per-warp store buffers
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + RING_BYTES + Smem<KIND>::STAGING);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
@@ -126,6 +134,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     fence_barrier_init();
     prefetch_tensormap(&tm_a);
     prefetch_tensormap(&tm_b);
+    if (KIND == kDownF32) prefetch_tensormap(&tm_out);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, TMEM_COLS);
@@ -214,6 +223,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int q = warp & 3;
     int acc = 0;
     uint32_t acc_phase = 0;
+    int n_stores = 0;  // bulk stores issued by this warp (down only)
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
       const PairCoord c = decode_pair(tile, p);
       if (!mbar_wait(&tfull[acc], acc_phase, p.wait_limit_ns)) {
@@ -251,20 +261,32 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         } else {
           const int64_t col = static_cast<int64_t>(c.n) * BN;
-          float* out_row = static_cast<float*>(p.out) + row * p.ld_out + col;
           const float* sd = p.scale0 + static_cast<int64_t>(c.e) * p.ld_out + col;
+          const int row0 = (c.m0 + j) * BM + q * 32;
 #pragma unroll 1
-          for (int c0 = 0; c0 < BN; c0 += 32) {
+          for (int c0 = 0; c0 < BN; c0 += 32, ++n_stores) {
             uint32_t r[32];
             tmem_load32(tbase + c0, r);
-            float4* dst = reinterpret_cast<float4*>(out_row + c0);
+            uint8_t* buf = staging + (q * 2 + (n_stores & 1)) * 4096;
+            if (n_stores >= 2) {
+              if (lane == 0) bulk_wait_group_read<1>();
+              __syncwarp();
+            }
 #pragma unroll
             for (int v = 0; v < 8; ++v) {
               const float4 s4 = __ldg(reinterpret_cast<const float4*>(sd + c0 + 4 * v));
-              dst[v] = make_float4(__uint_as_float(r[4 * v]) * s4.x, __uint_as_float(r[4 * v + 1]) * s4.y,
-                                   __uint_as_float(r[4 * v + 2]) * s4.z, __uint_as_float(r[4 * v + 3]) * s4.w);
+              *reinterpret_cast<float4*>(buf + lane * 128 + 16 * (v ^ (lane & 7))) =
+                  make_float4(__uint_as_float(r[4 * v]) * s4.x, __uint_as_float(r[4 * v + 1]) * s4.y,
+                              __uint_as_float(r[4 * v + 2]) * s4.z, __uint_as_float(r[4 * v + 3]) * s4.w);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tm_out, buf, static_cast<int32_t>(col) + c0, row0);
+              bulk_commit_group();
             }
           }
+          (void)row;
         }
       }
       tc_fence_before();
@@ -274,6 +296,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         acc_phase ^= 1u;
       }
     }
+    if (KIND == kDownF32 && lane == 0) bulk_wait_group<0>();
   } else if (warp == BPROD_WARP) {
     if (lane == 0) {
       // --------------------------------------------- int8 weight producer
@@ -360,18 +383,19 @@ int grouped_gemm_int8_gateup_block() { return BN / 2; }
 
 cudaError_t grouped_gemm_int8_prepare() {
   cudaError_t e = cudaFuncSetAttribute(grouped_gemm_int8_kernel<kGateUpSwiGLU>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<kGateUpSwiGLU>::BYTES);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(grouped_gemm_int8_kernel<kDownF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              SMEM_BYTES);
+                              Smem<kDownF32>::BYTES);
 }
 
 cudaError_t launch_grouped_gemm_int8(GemmKind kind, const CUtensorMap& tm_a, const CUtensorMap& tm_b,
-                                     const GemmArgs& a, cudaStream_t s) {
+                                     const CUtensorMap& tm_out, const GemmArgs& a, cudaStream_t s) {
   if (kind == kGateUpSwiGLU)
-    grouped_gemm_int8_kernel<kGateUpSwiGLU><<<a.grid, THREADS, SMEM_BYTES, s>>>(tm_a, tm_b, a);
+    grouped_gemm_int8_kernel<kGateUpSwiGLU>
+        <<<a.grid, THREADS, Smem<kGateUpSwiGLU>::BYTES, s>>>(tm_a, tm_b, tm_out, a);
   else
-    grouped_gemm_int8_kernel<kDownF32><<<a.grid, THREADS, SMEM_BYTES, s>>>(tm_a, tm_b, a);
+    grouped_gemm_int8_kernel<kDownF32><<<a.grid, THREADS, Smem<kDownF32>::BYTES, s>>>(tm_a, tm_b, tm_out, a);
   return cudaGetLastError();
 }
 

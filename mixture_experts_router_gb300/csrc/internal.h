@@ -34,6 +34,12 @@ struct RouterArgs {
 };
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t s);
 cudaError_t router_prepare();  // one-time function attributes
+// tcgen05 router: x and Wr through TMA (tm_x: [T][d] box 64x128; tm_w: [E][d]
+// box 64 x router_tc_rows(E)), one CTA per 128-token tile, persistent
+cudaError_t launch_router_tc(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const RouterArgs& a, int num_sms,
+                             cudaStream_t s);
+cudaError_t router_tc_prepare();
+int router_tc_rows(int E);
 
 // ---------------------------------------------------------------- dispatch
 struct DispatchArgs {
@@ -93,13 +99,16 @@ struct GemmArgs {
   int32_t grid;                 // persistent CTAs
 };
 enum GemmKind { kGateUpSwiGLU = 0, kDownF32 = 1 };
+// tm_out: the fp32 output Y [rows][d] with a 32 x 32 box and the 128-byte
+// swizzle, used by the down kernels' TMA-store epilogue (ignored by gate/up)
 cudaError_t launch_grouped_gemm(GemmKind kind, bool int8_weights, const CUtensorMap& tm_a,
-                                const CUtensorMap& tm_b, const GemmArgs& a, cudaStream_t s);
+                                const CUtensorMap& tm_b, const CUtensorMap& tm_out, const GemmArgs& a,
+                                cudaStream_t s);
 cudaError_t grouped_gemm_prepare();  // one-time function attributes
 int grouped_gemm_tile_n(GemmKind kind);  // output columns per tile
 // int8 weights: tiles are pairs of m-tiles against 128 weight rows
 cudaError_t launch_grouped_gemm_int8(GemmKind kind, const CUtensorMap& tm_a, const CUtensorMap& tm_b,
-                                     const GemmArgs& a, cudaStream_t s);
+                                     const CUtensorMap& tm_out, const GemmArgs& a, cudaStream_t s);
 cudaError_t grouped_gemm_int8_prepare();
 int grouped_gemm_int8_tile_n(GemmKind kind);
 int grouped_gemm_int8_gateup_block();  // gate/up rows interleaved in blocks of this size

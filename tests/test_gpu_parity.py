@@ -121,3 +121,23 @@ def test_injected_host_faults(monkeypatch):
         gl.run()
     finally:
         gl.close()
+
+
+ROUTER_CASES = {
+    "e8_small": synth.custom_shape("r_e8", T=333, d=512, f=256, E=8, k=2, seed=41),
+    "e16_k4": synth.custom_shape("r_e16", T=200, d=256, f=256, E=16, k=4, seed=42),
+    "e40_bias": synth.custom_shape("r_e40", T=257, d=768, f=256, E=40, k=3, bias=True, seed=43),
+    "e128_k4": synth.custom_shape("r_e128", T=300, d=1024, f=256, E=128, k=4, bias=True, seed=44),
+    "e256_k16": synth.custom_shape("r_e256", T=130, d=256, f=256, E=256, k=16, seed=45),
+}
+
+
+@pytest.mark.parametrize("router", ["mma", "tc"])
+@pytest.mark.parametrize("name", list(ROUTER_CASES))
+def test_both_routers(name, router, monkeypatch):
+    """The mma.sync split-K router and the tcgen05 router both match the oracle
+    (the library picks one by expert count; CB_MOE_ROUTER forces either)."""
+    monkeypatch.setenv("CB_MOE_ROUTER", router)
+    rep = gh.full_check(synth.make_layer(ROUTER_CASES[name]))
+    print(name, router, rep)
+    assert rep.get("logit_max_err", 0.0) <= 5e-6
