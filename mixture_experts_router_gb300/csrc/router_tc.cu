@@ -37,20 +37,25 @@ struct RtCfg {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES_RAW = (200 * 1024) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
   static constexpr int CW = NP < 32 ? NP : 32;  // epilogue column chunk
+  static constexpr int STG_FLOATS = 128 * (CW + 1);  // per-row logit staging, padded
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STG_FLOATS * 4 + 1024 + 256;
 };
 
-struct Cand {
-  float v;
-  int idx;
-  int cls;  // 0 number, 1 NaN, 3 empty slot
-};
-
-__device__ __forceinline__ bool ranks_before(const Cand& a, const Cand& b) {
-  if (a.cls != b.cls) return a.cls < b.cls;
-  if (a.cls == 0 && a.v != b.v) return a.v > b.v;
-  return a.idx < b.idx;
+// A candidate (logit v, expert e) as one 64-bit key whose unsigned order is
+// the routing order: numbers by value (larger first; -0 folded into +0 so
+// the two zeros tie), then NaN, then an empty slot (key 0); on equal values
+// the lower expert index has the larger key.
+__device__ __forceinline__ uint64_t rank_key(float v, int e) {
+  uint32_t hi;
+  if (isnan(v)) {
+    hi = 1u;
+  } else {
+    const uint32_t b = __float_as_uint(v + 0.0f);
+    hi = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+    hi = hi < 2u ? 2u : hi;  // stay above NaN and empty (only -inf maps below)
+  }
+  return (static_cast<uint64_t>(hi) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(e));
 }
 
 template <int CW>
@@ -70,7 +75,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   constexpr uint32_t IDESC = idesc_bf16_f32(BM, NP);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES);
+  float* stg = reinterpret_cast<float*>(smem + STAGES * C::STAGE_BYTES);  // [128][CW + 1]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES + C::STG_FLOATS * 4);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 1;
@@ -170,9 +176,15 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       const int t = tile * BM + q * 32 + lane;
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-      Cand top[KMAX];
+      uint64_t top[KMAX];   // sorted, best first
+      float topv[KMAX];
 #pragma unroll
-      for (int j = 0; j < KMAX; ++j) top[j] = Cand{0.f, 0x7fffffff, 3};
+      for (int j = 0; j < KMAX; ++j) {
+        top[j] = 0;
+        topv[j] = 0.f;
+      }
+      uint64_t thr = 0;  // key of the k-th best so far
+      float* my = stg + (q * 32 + lane) * (CW + 1);
       for (int c0 = 0; c0 < NP; c0 += CW) {
         if (c0 >= a.E) break;  // uniform across the warp
         float sum[CW];
@@ -185,37 +197,49 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int j = 0; j < CW; ++j) sum[j] += __uint_as_float(r[j]);
         }
 #pragma unroll
-        for (int j = 0; j < CW; ++j) {
+        for (int j = 0; j < CW; ++j) my[j] = sum[j];
+        __syncwarp();
+        const int nj = a.E - c0 < CW ? a.E - c0 : CW;
+#pragma unroll 1
+        for (int j = 0; j < nj; ++j) {
           const int e = c0 + j;
-          if (e < a.E) {
-            if (a.bias != nullptr) sum[j] += __ldg(a.bias + e);
-            if (a.logits != nullptr && t < a.T) a.logits[static_cast<int64_t>(t) * a.E + e] = sum[j];
-            Cand c{sum[j], e, isnan(sum[j]) ? 1 : 0};
+          float v = my[j];
+          if (a.bias != nullptr) v += __ldg(a.bias + e);
+          if (a.logits != nullptr && t < a.T) a.logits[static_cast<int64_t>(t) * a.E + e] = v;
+          uint64_t key = rank_key(v, e);
+          if (key > thr) {
+            float kv = v;
 #pragma unroll
-            for (int s = 0; s < KMAX; ++s) {
-              if (s < a.k && ranks_before(c, top[s])) {
-                const Cand tmp = top[s];
-                top[s] = c;
-                c = tmp;
-              }
+            for (int s2 = 0; s2 < KMAX; ++s2) {
+              const bool better = s2 < a.k && key > top[s2];
+              const uint64_t tk = top[s2];
+              const float tv = topv[s2];
+              top[s2] = better ? key : tk;
+              topv[s2] = better ? kv : tv;
+              key = better ? tk : key;
+              kv = better ? tv : kv;
             }
+#pragma unroll
+            for (int s2 = 0; s2 < KMAX; ++s2)
+              if (s2 == a.k - 1) thr = top[s2];
           }
         }
+        __syncwarp();
       }
       if (t < a.T) {
-        const float l0 = top[0].v;
+        const float l0 = topv[0];
         float ex[KMAX];
         float den = 0.f;
 #pragma unroll
-        for (int s = 0; s < KMAX; ++s) {
-          ex[s] = (s < a.k) ? expf(top[s].v - l0) : 0.f;
-          den += ex[s];
+        for (int s2 = 0; s2 < KMAX; ++s2) {
+          ex[s2] = (s2 < a.k) ? expf(topv[s2] - l0) : 0.f;
+          den += ex[s2];
         }
 #pragma unroll
-        for (int s = 0; s < KMAX; ++s) {
-          if (s < a.k) {
-            a.ids[static_cast<int64_t>(t) * a.k + s] = top[s].idx;
-            a.w[static_cast<int64_t>(t) * a.k + s] = ex[s] / den;
+        for (int s2 = 0; s2 < KMAX; ++s2) {
+          if (s2 < a.k) {
+            a.ids[static_cast<int64_t>(t) * a.k + s2] = static_cast<int>(~static_cast<uint32_t>(top[s2]));
+            a.w[static_cast<int64_t>(t) * a.k + s2] = ex[s2] / den;
           }
         }
       }
