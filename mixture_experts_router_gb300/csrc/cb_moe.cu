@@ -46,7 +46,7 @@ struct cb_moe {
   bool timing;
   bool router_tc;          // tcgen05 router (else the mma.sync router)
   const void* tm_x_src;    // x pointer tm_x was encoded for
-  CUtensorMap tm_a_gu, tm_b_gu, tm_a_dn, tm_b_dn, tm_y, tm_x, tm_wr;
+  CUtensorMap tm_a_gu, tm_b_gu, tm_a_dn, tm_b_dn, tm_b_dn64, tm_y, tm_x, tm_wr;
 };
 
 namespace {
@@ -240,7 +240,8 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
   ga.wait_limit_ns = kWaitLimitNs;
   ga.grid = h->num_sms;
   const cudaError_t e1 = int8w ? launch_grouped_gemm_int8(kGateUpSwiGLU, h->tm_a_gu, h->tm_b_gu, h->tm_y, ga, s)
-                               : launch_grouped_gemm(kGateUpSwiGLU, false, h->tm_a_gu, h->tm_b_gu, h->tm_y, ga, s);
+                               : launch_grouped_gemm(kGateUpSwiGLU, false, h->tm_a_gu, h->tm_b_gu, h->tm_y,
+                                                     h->tm_b_dn64, ga, s);
   if (e1 != cudaSuccess || !mark(3)) return CB_ERR_CUDA;
 
   GemmArgs gd = ga;
@@ -252,7 +253,8 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
   gd.scale0 = h->sd;
   gd.scale1 = nullptr;
   const cudaError_t e2 = int8w ? launch_grouped_gemm_int8(kDownF32, h->tm_a_dn, h->tm_b_dn, h->tm_y, gd, s)
-                               : launch_grouped_gemm(kDownF32, false, h->tm_a_dn, h->tm_b_dn, h->tm_y, gd, s);
+                               : launch_grouped_gemm(kDownF32, false, h->tm_a_dn, h->tm_b_dn, h->tm_y, h->tm_b_dn64,
+                                                     gd, s);
   if (e2 != cudaSuccess || !mark(4)) return CB_ERR_CUDA;
 
   CombineArgs ca{};
@@ -397,6 +399,7 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
   ok = ok && make_tmap(&h->tm_a_dn, h->hb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, f, mpad, 64, 128);
   ok = ok && make_tmap(&h->tm_b_dn, h->wd, wdt, eb, f, E * d, 64, brows_box, wsw);
   ok = ok && make_tmap(&h->tm_y, h->y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, mpad, 32, 32);
+  ok = ok && make_tmap(&h->tm_b_dn64, h->wd, wdt, eb, f, E * d, 64, 64, wsw);
   ok = ok && grouped_gemm_prepare() == cudaSuccess && grouped_gemm_int8_prepare() == cudaSuccess &&
        router_prepare() == cudaSuccess && router_tc_prepare() == cudaSuccess;
   // router: tcgen05 for wide expert counts, the mma.sync split-K router for

@@ -22,6 +22,7 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kPerWarp = kDispatchChunk / kWarps;  // 256 pairs, 8 rounds of 32
+constexpr int64_t kSmallM = 65536;  // T*k handled by the one-block kernel
 
 __global__ void __launch_bounds__(kThreads) dispatch_count(DispatchArgs a) {
   __shared__ int hist[256];
@@ -44,7 +45,8 @@ __global__ void __launch_bounds__(kThreads) dispatch_count(DispatchArgs a) {
     a.chunk[static_cast<int64_t>(blockIdx.x) * a.E + e] = hist[e];
 }
 
-// exclusive scan of one value per thread over a 256-thread block
+// exclusive scan of one value per thread over a block of NW warps
+template <int NW = kWarps>
 __device__ int block_exclusive_scan(int v, int* tmp) {
   const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
   int x = v;
@@ -56,13 +58,13 @@ __device__ int block_exclusive_scan(int v, int* tmp) {
   if (lane == 31) tmp[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    int s = (lane < kWarps) ? tmp[lane] : 0;
+    int s = (lane < NW) ? tmp[lane] : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, s, o);
       if (lane >= o) s += y;
     }
-    if (lane < kWarps) tmp[lane] = s;
+    if (lane < NW) tmp[lane] = s;
   }
   __syncthreads();
   const int r = x - v + (warp > 0 ? tmp[warp - 1] : 0);
@@ -156,7 +158,87 @@ __global__ void __launch_bounds__(kThreads) dispatch_scatter(DispatchArgs a) {
   }
 }
 
-// One warp per padded row: copy x[tok] into Xp with 16-byte vectors.
+// Count, scan and ranks in one 1024-thread block, for T*k <= kSmallM: the
+// 32 warps take consecutive runs of the flat (token, slot) pairs, so the
+// warp-aggregated ranks come out in token order exactly as in the chunked
+// kernels above.
+constexpr int kSmallThreads = 1024;
+constexpr int kSmallWarps = kSmallThreads / 32;
+
+__global__ void __launch_bounds__(kSmallThreads) dispatch_small(DispatchArgs a) {
+  __shared__ int wh[kSmallWarps][256];
+  __shared__ int tmp[kSmallWarps];
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  for (int i = threadIdx.x; i < kSmallWarps * 256; i += kSmallThreads) (&wh[0][0])[i] = 0;
+  __syncthreads();
+  const int64_t M = static_cast<int64_t>(a.T) * a.k;
+  const int64_t per_warp = ((M + kSmallWarps - 1) / kSmallWarps + 31) / 32 * 32;
+  const int64_t wbase = warp * per_warp;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  for (int64_t r = 0; r < per_warp; r += 32) {
+    const int64_t p = wbase + r + lane;
+    int e = (p < M) ? a.ids[p] : -1;
+    if (p < M && (e < 0 || e >= a.E)) set_error(a.err, kErrDevice);
+    if (e < 0 || e >= a.E) e = -1;
+    const uint32_t m = __match_any_sync(0xffffffffu, e);
+    if (e >= 0 && (__ffs(m) - 1) == lane) wh[warp][e] += __popc(m);
+  }
+  __syncthreads();
+  int total = 0;
+  const int e = threadIdx.x;
+  if (e < a.E) {
+    for (int w = 0; w < kSmallWarps; ++w) {
+      const int c = wh[w][e];
+      wh[w][e] = total;
+      total += c;
+    }
+  }
+  const int mt = (total + kTileM - 1) / kTileM;
+  const int pt = (mt + 1) / 2;
+  const int off = block_exclusive_scan<kSmallWarps>(e < a.E ? total : 0, tmp);
+  const int moff = block_exclusive_scan<kSmallWarps>(e < a.E ? mt : 0, tmp);
+  const int poff = block_exclusive_scan<kSmallWarps>(e < a.E ? pt : 0, tmp);
+  if (e < a.E) {
+    a.counts[e] = total;
+    a.offsets[e] = off;
+    a.mtile_off[e] = moff;
+    if (e == a.E - 1) {
+      a.offsets[a.E] = off + total;
+      a.mtile_off[a.E] = moff + mt;
+      if (moff + mt > a.max_mtiles) set_error(a.err, kErrDevice);
+    }
+    for (int i = moff; i < moff + mt && i < a.max_mtiles; ++i) a.mtile_expert[i] = e;
+    if (a.ptile_off != nullptr) {
+      a.ptile_off[e] = poff;
+      if (e == a.E - 1) a.ptile_off[a.E] = poff + pt;
+      for (int i = poff; i < poff + pt && i < a.max_mtiles; ++i) a.ptile_expert[i] = e;
+    }
+    for (int w = 0; w < kSmallWarps; ++w) wh[w][e] += off;
+  }
+  __syncthreads();
+  for (int64_t r = 0; r < per_warp; r += 32) {
+    const int64_t p = wbase + r + lane;
+    int e2 = (p < M) ? a.ids[p] : -1;
+    if (e2 < 0 || e2 >= a.E) e2 = -1;
+    const uint32_t m = __match_any_sync(0xffffffffu, e2);
+    int rank = 0;
+    if (e2 >= 0) rank = wh[warp][e2] + __popc(m & lt_mask);
+    __syncwarp();
+    if (e2 >= 0 && (__ffs(m) - 1) == lane) wh[warp][e2] += __popc(m);
+    __syncwarp();
+    if (e2 >= 0) {
+      if (rank < 0 || rank >= M) {
+        set_error(a.err, kErrDevice);
+      } else {
+        a.tok[rank] = static_cast<int32_t>(p / a.k);
+        a.inv[p] = rank;
+      }
+    }
+  }
+}
+
+// One warp per padded row: copy x[tok] into Xp with 16-byte vectors, up to
+// eight loads in flight per lane before the stores (d <= 2048: one round).
 __global__ void __launch_bounds__(kThreads) dispatch_gather(DispatchArgs a) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int total_tiles = min(a.mtile_off[a.E], a.max_mtiles);
@@ -175,7 +257,19 @@ __global__ void __launch_bounds__(kThreads) dispatch_gather(DispatchArgs a) {
     }
     const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<int64_t>(t) * a.d);
     uint4* dst = reinterpret_cast<uint4*>(a.xp + row * a.d);
-    for (int v = lane; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
+    for (int v0 = 0; v0 < vec_per_row; v0 += 32 * 8) {
+      uint4 buf[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int v = v0 + u * 32 + lane;
+        if (v < vec_per_row) buf[u] = __ldg(src + v);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int v = v0 + u * 32 + lane;
+        if (v < vec_per_row) dst[v] = buf[u];
+      }
+    }
   }
 }
 
@@ -191,9 +285,13 @@ cudaError_t launch_dispatch_ranks(const DispatchArgs& a, cudaStream_t s) {
 
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s) {
   if (a.n_chunks <= 0) return cudaSuccess;
-  dispatch_count<<<a.n_chunks, kThreads, 0, s>>>(a);
-  dispatch_scan<<<1, kThreads, 0, s>>>(a);
-  dispatch_scatter<<<a.n_chunks, kThreads, 0, s>>>(a);
+  if (static_cast<int64_t>(a.T) * a.k <= kSmallM) {
+    dispatch_small<<<1, kSmallThreads, 0, s>>>(a);
+  } else {
+    dispatch_count<<<a.n_chunks, kThreads, 0, s>>>(a);
+    dispatch_scan<<<1, kThreads, 0, s>>>(a);
+    dispatch_scatter<<<a.n_chunks, kThreads, 0, s>>>(a);
+  }
   dispatch_gather<<<a.gather_blocks, kThreads, 0, s>>>(a);
   return cudaGetLastError();
 }

@@ -74,6 +74,43 @@ __device__ __forceinline__ TileCoord decode_tile(int tile, const GemmArgs& p) {
   return c;
 }
 
+// The down kernel splits the last, partial wave of tiles along N: with G
+// CTAs and R = tiles mod G leftover tiles, each leftover tile becomes S
+// sub-tiles of BN / S columns (S = the largest of 1, 2, 4 with R S <= G), so
+// the tail takes 1/S of a tile's time.  Work unit u < F = tiles - R is tile
+// u; unit F + i is part i % S of tile F + i / S.
+struct Work {
+  TileCoord c;
+  int nsub;  // columns (and weight rows) of this unit
+  int col0;  // first output column within the expert
+};
+
+__device__ __forceinline__ void tail_split(int total_tiles, int grid, int& full, int& split) {
+  const int r = total_tiles % grid;
+  full = total_tiles - r;
+  split = 1;
+  if (r > 0) {
+    if (4 * r <= grid)
+      split = 4;
+    else if (2 * r <= grid)
+      split = 2;
+  }
+}
+
+__device__ __forceinline__ Work decode_work(int u, const GemmArgs& p, int full, int split) {
+  Work w;
+  int tile = u, part = 0;
+  w.nsub = BN;
+  if (u >= full) {
+    tile = full + (u - full) / split;
+    part = (u - full) % split;
+    w.nsub = BN / split;
+  }
+  w.c = decode_tile(tile, p);
+  w.col0 = w.c.n * BN + part * w.nsub;
+  return w;
+}
+
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -84,7 +121,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 template <int KIND>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                        const __grid_constant__ CUtensorMap tm_out, const GemmArgs p) {
+                        const __grid_constant__ CUtensorMap tm_out, const __grid_constant__ CUtensorMap tm_b64,
+                        const GemmArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sa = smem;
@@ -109,7 +147,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     fence_barrier_init();
     prefetch_tensormap(&tm_a);
     prefetch_tensormap(&tm_b);
-    if (KIND == kDownF32) prefetch_tensormap(&tm_out);
+    if (KIND == kDownF32) {
+      prefetch_tensormap(&tm_out);
+      prefetch_tensormap(&tm_b64);
+    }
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, TMEM_COLS);
@@ -120,6 +161,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int total_tiles = p.mtile_off[p.E] * p.n_tiles;
+  int full_tiles = total_tiles, split = 1;
+  if (KIND == kDownF32) tail_split(total_tiles, gridDim.x, full_tiles, split);
+  const int total_units = full_tiles + (total_tiles - full_tiles) * split;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -128,19 +172,24 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t phase = 0;
       int64_t issued = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-        const TileCoord c = decode_tile(tile, p);
-        const int a_row = c.m_tile * BM;
-        const int b_row = c.e * p.b_rows_per_expert + c.n * BN;
+      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+        const Work w = decode_work(u, p, full_tiles, split);
+        const int a_row = w.c.m_tile * BM;
+        const int b_row = w.c.e * p.b_rows_per_expert + w.col0;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, p.wait_limit_ns)) {
             set_error(p.err, kErrTimeout);
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+          mbar_arrive_expect_tx(&full[stage], A_BYTES + w.nsub * BK * 2);
           tma_load_2d(sa + stage * A_BYTES, &tm_a, &full[stage], kb * BK, a_row);
-          tma_load_2d(sb + stage * B_BYTES, &tm_b, &full[stage], kb * BK, b_row);
+          if (w.nsub == BN) {
+            tma_load_2d(sb + stage * B_BYTES, &tm_b, &full[stage], kb * BK, b_row);
+          } else {
+            for (int i = 0; i < w.nsub / 64; ++i)
+              tma_load_2d(sb + stage * B_BYTES + i * 64 * BK * 2, &tm_b64, &full[stage], kb * BK, b_row + 64 * i);
+          }
           ++issued;
           if (++stage == STAGES) {
             stage = 0;
@@ -163,7 +212,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+        const int nsub = (u < full_tiles) ? BN : BN / split;
+        const uint32_t idesc = (nsub == BN) ? IDESC : idesc_bf16_f32(BM, nsub);
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, p.wait_limit_ns)) {
           set_error(p.err, kErrTimeout);
           break;
@@ -181,7 +232,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint64_t bdesc = sw128_desc(smem_u32(sb + stage * B_BYTES));
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
-            tc_mma_f16(d_tmem, adesc + 2 * k, bdesc + 2 * k, IDESC, (kb | k) != 0 ? 1u : 0u);
+            tc_mma_f16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
           tc_commit(&empty[stage]);
           if (++stage == STAGES) {
             stage = 0;
@@ -202,8 +253,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     int n_stores = 0;  // bulk stores issued by this warp (down only)
-    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
-      const TileCoord c = decode_tile(tile, p);
+    for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+      const Work w = decode_work(u, p, full_tiles, split);
+      const TileCoord c = w.c;
       if (!mbar_wait(&tfull[acc], acc_phase, p.wait_limit_ns)) {
         set_error(p.err, kErrTimeout);
         break;
@@ -235,7 +287,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // one bulk tensor store writes whole 128-byte row segments.
         const int row0 = c.m_tile * BM + q * 32;
 #pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 32, ++n_stores) {
+        for (int c0 = 0; c0 < w.nsub; c0 += 32, ++n_stores) {
           uint32_t r[32];
           tmem_load32(tbase + c0, r);
           uint8_t* buf = staging + (q * 2 + (n_stores & 1)) * 4096;
@@ -250,7 +302,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(&tm_out, buf, c.n * BN + c0, row0);
+            tma_store_2d(&tm_out, buf, w.col0 + c0, row0);
             bulk_commit_group();
           }
         }
@@ -287,12 +339,14 @@ cudaError_t grouped_gemm_prepare() {
 }
 
 cudaError_t launch_grouped_gemm(GemmKind kind, bool int8_weights, const CUtensorMap& tm_a, const CUtensorMap& tm_b,
-                                const CUtensorMap& tm_out, const GemmArgs& a, cudaStream_t s) {
+                                const CUtensorMap& tm_out, const CUtensorMap& tm_b64, const GemmArgs& a,
+                                cudaStream_t s) {
   if (int8_weights) return cudaErrorNotSupported;
   if (kind == kGateUpSwiGLU)
-    grouped_gemm_kernel<kGateUpSwiGLU><<<a.grid, THREADS, Smem<kGateUpSwiGLU>::BYTES, s>>>(tm_a, tm_b, tm_out, a);
+    grouped_gemm_kernel<kGateUpSwiGLU>
+        <<<a.grid, THREADS, Smem<kGateUpSwiGLU>::BYTES, s>>>(tm_a, tm_b, tm_out, tm_b64, a);
   else
-    grouped_gemm_kernel<kDownF32><<<a.grid, THREADS, Smem<kDownF32>::BYTES, s>>>(tm_a, tm_b, tm_out, a);
+    grouped_gemm_kernel<kDownF32><<<a.grid, THREADS, Smem<kDownF32>::BYTES, s>>>(tm_a, tm_b, tm_out, tm_b64, a);
   return cudaGetLastError();
 }
 
