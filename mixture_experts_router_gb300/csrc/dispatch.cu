@@ -22,7 +22,7 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kPerWarp = kDispatchChunk / kWarps;  // 256 pairs, 8 rounds of 32
-constexpr int64_t kSmallM = 65536;  // T*k handled by the one-block kernel
+constexpr int64_t kSmallM = 16384;  // T*k handled by the one-block kernel
 
 __global__ void __launch_bounds__(kThreads) dispatch_count(DispatchArgs a) {
   __shared__ int hist[256];
@@ -100,6 +100,9 @@ __global__ void __launch_bounds__(kThreads) dispatch_scan(DispatchArgs a) {
     }
     for (int b = 0; b < a.n_chunks; ++b) a.chunk[static_cast<int64_t>(b) * a.E + e] += off;
     for (int i = moff; i < moff + mt && i < a.max_mtiles; ++i) a.mtile_expert[i] = e;
+    if (a.rowsrc != nullptr && moff + mt <= a.max_mtiles)
+      for (int64_t r = static_cast<int64_t>(moff) * kTileM + total; r < static_cast<int64_t>(moff + mt) * kTileM; ++r)
+        a.rowsrc[r] = -1;
     if (a.ptile_off != nullptr) {
       a.ptile_off[e] = poff;
       if (e == a.E - 1) a.ptile_off[a.E] = poff + pt;
@@ -153,6 +156,9 @@ __global__ void __launch_bounds__(kThreads) dispatch_scatter(DispatchArgs a) {
       } else {
         a.tok[rank] = static_cast<int32_t>(p / a.k);
         a.inv[p] = rank;
+        if (a.rowsrc != nullptr)
+          a.rowsrc[static_cast<int64_t>(a.mtile_off[e]) * kTileM + (rank - a.offsets[e])] =
+              static_cast<int32_t>(p / a.k);
       }
     }
   }
@@ -168,6 +174,8 @@ constexpr int kSmallWarps = kSmallThreads / 32;
 __global__ void __launch_bounds__(kSmallThreads) dispatch_small(DispatchArgs a) {
   __shared__ int wh[kSmallWarps][256];
   __shared__ int tmp[kSmallWarps];
+  __shared__ int smoff[256];   // tile offset of each expert
+  __shared__ int soff[256];    // row offset of each expert
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   for (int i = threadIdx.x; i < kSmallWarps * 256; i += kSmallThreads) (&wh[0][0])[i] = 0;
   __syncthreads();
@@ -213,6 +221,11 @@ __global__ void __launch_bounds__(kSmallThreads) dispatch_small(DispatchArgs a) 
       if (e == a.E - 1) a.ptile_off[a.E] = poff + pt;
       for (int i = poff; i < poff + pt && i < a.max_mtiles; ++i) a.ptile_expert[i] = e;
     }
+    if (a.rowsrc != nullptr && moff + mt <= a.max_mtiles)
+      for (int64_t r = static_cast<int64_t>(moff) * kTileM + total; r < static_cast<int64_t>(moff + mt) * kTileM; ++r)
+        a.rowsrc[r] = -1;
+    smoff[e] = moff;
+    soff[e] = off;
     for (int w = 0; w < kSmallWarps; ++w) wh[w][e] += off;
   }
   __syncthreads();
@@ -232,42 +245,46 @@ __global__ void __launch_bounds__(kSmallThreads) dispatch_small(DispatchArgs a) 
       } else {
         a.tok[rank] = static_cast<int32_t>(p / a.k);
         a.inv[p] = rank;
+        if (a.rowsrc != nullptr)
+          a.rowsrc[static_cast<int64_t>(smoff[e2]) * kTileM + (rank - soff[e2])] = static_cast<int32_t>(p / a.k);
       }
     }
   }
 }
 
-// One warp per padded row: copy x[tok] into Xp with 16-byte vectors, up to
-// eight loads in flight per lane before the stores (d <= 2048: one round).
+// Row gather Xp[row] = x[rowsrc[row]] (rows with rowsrc < 0 are padding).
+// A warp takes 32 consecutive padded rows: one coalesced load of their 32
+// source tokens, then it copies them one after the other with 16-byte
+// vectors, eight loads in flight per lane.
 __global__ void __launch_bounds__(kThreads) dispatch_gather(DispatchArgs a) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int total_tiles = min(a.mtile_off[a.E], a.max_mtiles);
   const int64_t rows = static_cast<int64_t>(total_tiles) * kTileM;
   const int vec_per_row = a.d / 8;
-  for (int64_t row = static_cast<int64_t>(blockIdx.x) * kWarps + warp; row < rows;
-       row += static_cast<int64_t>(gridDim.x) * kWarps) {
-    const int mt = static_cast<int>(row / kTileM);
-    const int e = a.mtile_expert[mt];
-    const int local = static_cast<int>(row - static_cast<int64_t>(a.mtile_off[e]) * kTileM);
-    if (local >= a.counts[e]) continue;  // padding row of the expert's last tile
-    const int t = a.tok[a.offsets[e] + local];
-    if (t < 0 || t >= a.T) {
-      if (lane == 0) set_error(a.err, kErrDevice);
-      continue;
+  for (int64_t r0 = (static_cast<int64_t>(blockIdx.x) * kWarps + warp) * 32; r0 < rows;
+       r0 += static_cast<int64_t>(gridDim.x) * kWarps * 32) {
+    int my_t = (r0 + lane < rows) ? a.rowsrc[r0 + lane] : -1;
+    if (my_t >= a.T) {
+      set_error(a.err, kErrDevice);
+      my_t = -1;
     }
-    const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<int64_t>(t) * a.d);
-    uint4* dst = reinterpret_cast<uint4*>(a.xp + row * a.d);
-    for (int v0 = 0; v0 < vec_per_row; v0 += 32 * 8) {
-      uint4 buf[8];
+    for (int j = 0; j < 32; ++j) {
+      const int t = __shfl_sync(0xffffffffu, my_t, j);
+      if (t < 0) continue;
+      const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<int64_t>(t) * a.d);
+      uint4* dst = reinterpret_cast<uint4*>(a.xp + (r0 + j) * a.d);
+      for (int v0 = 0; v0 < vec_per_row; v0 += 32 * 8) {
+        uint4 buf[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int v = v0 + u * 32 + lane;
-        if (v < vec_per_row) buf[u] = __ldg(src + v);
-      }
+        for (int u = 0; u < 8; ++u) {
+          const int v = v0 + u * 32 + lane;
+          if (v < vec_per_row) buf[u] = __ldg(src + v);
+        }
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int v = v0 + u * 32 + lane;
-        if (v < vec_per_row) dst[v] = buf[u];
+        for (int u = 0; u < 8; ++u) {
+          const int v = v0 + u * 32 + lane;
+          if (v < vec_per_row) dst[v] = buf[u];
+        }
       }
     }
   }
