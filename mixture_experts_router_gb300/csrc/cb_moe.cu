@@ -222,7 +222,7 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
   da.rowsrc = h->rowsrc;
   da.xp = h->xp;
   da.gather_blocks = static_cast<int32_t>(
-      std::min<int64_t>(h->num_sms * 4, (static_cast<int64_t>(h->max_mtiles) * kTileM + 255) / 256));
+      std::min<int64_t>(h->num_sms * 8, (static_cast<int64_t>(h->max_mtiles) * kTileM + 7) / 8));
   da.err = h->err;
   if (launch_dispatch(da, s) != cudaSuccess || !mark(2)) return CB_ERR_CUDA;
 

@@ -253,26 +253,23 @@ __global__ void __launch_bounds__(kSmallThreads) dispatch_small(DispatchArgs a) 
 }
 
 // Row gather Xp[row] = x[rowsrc[row]] (rows with rowsrc < 0 are padding).
-// A warp takes 32 consecutive padded rows: one coalesced load of their 32
-// source tokens, then it copies them one after the other with 16-byte
-// vectors, eight loads in flight per lane.
+// One warp per row, the next row's source index loaded while this row is
+// copied with 16-byte vectors, eight loads in flight per lane.
 __global__ void __launch_bounds__(kThreads) dispatch_gather(DispatchArgs a) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int total_tiles = min(a.mtile_off[a.E], a.max_mtiles);
   const int64_t rows = static_cast<int64_t>(total_tiles) * kTileM;
   const int vec_per_row = a.d / 8;
-  for (int64_t r0 = (static_cast<int64_t>(blockIdx.x) * kWarps + warp) * 32; r0 < rows;
-       r0 += static_cast<int64_t>(gridDim.x) * kWarps * 32) {
-    int my_t = (r0 + lane < rows) ? a.rowsrc[r0 + lane] : -1;
-    if (my_t >= a.T) {
-      set_error(a.err, kErrDevice);
-      my_t = -1;
-    }
-    for (int j = 0; j < 32; ++j) {
-      const int t = __shfl_sync(0xffffffffu, my_t, j);
-      if (t < 0) continue;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kWarps;
+  int64_t row = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
+  int t = (row < rows) ? a.rowsrc[row] : -1;
+  for (; row < rows; row += stride) {
+    const int t_next = (row + stride < rows) ? a.rowsrc[row + stride] : -1;
+    if (t >= a.T) {
+      if (lane == 0) set_error(a.err, kErrDevice);
+    } else if (t >= 0) {
       const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<int64_t>(t) * a.d);
-      uint4* dst = reinterpret_cast<uint4*>(a.xp + (r0 + j) * a.d);
+      uint4* dst = reinterpret_cast<uint4*>(a.xp + row * a.d);
       for (int v0 = 0; v0 < vec_per_row; v0 += 32 * 8) {
         uint4 buf[8];
 #pragma unroll
@@ -287,6 +284,7 @@ __global__ void __launch_bounds__(kThreads) dispatch_gather(DispatchArgs a) {
         }
       }
     }
+    t = t_next;
   }
 }
 
