@@ -71,6 +71,13 @@ typedef enum { CB_W_BF16 = 0, CB_W_INT8 = 1 } cb_wdtype_t;
 #define CB_FLAG_KEEP_LOGITS 0x1u   /* also store the fp32 router logits [T][E] */
 #define CB_FLAG_STAGE_TIMING 0x2u  /* record CUDA events between the stages of each
                                       forward (see cb_moe_stage_times)          */
+#define CB_FLAG_TEST_STALL 0x4u    /* test only: in every forward the gate/up GEMM
+                                      waits on a barrier phase that nothing
+                                      completes, with all its waits bounded to
+                                      1 ms, so the device timeout path runs: the
+                                      forward finishes (its output is garbage)
+                                      and cb_moe_last_error returns
+                                      CB_ERR_TIMEOUT                            */
 
 typedef struct {
   int32_t n_tokens;   /* T: tokens in every forward on this handle (>= 0)         */

@@ -18,6 +18,7 @@ CB_ERR_OOM, CB_ERR_CUDA, CB_ERR_TIMEOUT, CB_ERR_DEVICE = 4, 5, 6, 7
 CB_W_BF16, CB_W_INT8 = 0, 1
 CB_FLAG_KEEP_LOGITS = 0x1
 CB_FLAG_STAGE_TIMING = 0x2
+CB_FLAG_TEST_STALL = 0x4
 CB_N_STAGES = 5
 STAGE_NAMES = ("router", "dispatch", "gateup_gemm", "down_gemm", "combine")
 
@@ -186,8 +187,9 @@ class MoELayer:
     int8 as torch.int8).  Raises CbMoeError on any non-zero status."""
 
     def __init__(self, T, d, f, E, k, w_router, w_gate, w_up, w_down, router_bias=None,
-                 s_gate=None, s_up=None, s_down=None, device=0, keep_logits=False, stage_timing=False):
-        flags = (CB_FLAG_KEEP_LOGITS if keep_logits else 0) | (CB_FLAG_STAGE_TIMING if stage_timing else 0)
+                 s_gate=None, s_up=None, s_down=None, device=0, keep_logits=False, stage_timing=False,
+                 flags=0):
+        flags |= (CB_FLAG_KEEP_LOGITS if keep_logits else 0) | (CB_FLAG_STAGE_TIMING if stage_timing else 0)
         self.cfg = cb_moe_config_t(T, d, f, E, k, CB_W_INT8 if s_gate is not None else CB_W_BF16,
                                    device, flags)
         w = cb_moe_weights_t(_ptr(w_router), _ptr(router_bias), _ptr(w_gate), _ptr(w_up), _ptr(w_down),

@@ -114,7 +114,8 @@ cb_status_t validate_config(const cb_moe_config_t* c) {
   if (c->wdtype != CB_W_BF16 && c->wdtype != CB_W_INT8) return CB_ERR_INVALID_ARG;
   if (c->d_model % 256 != 0 || c->d_ff % 256 != 0) return CB_ERR_UNSUPPORTED;
   if (c->n_experts > 256 || c->top_k > 16) return CB_ERR_UNSUPPORTED;
-  if ((c->flags & ~(CB_FLAG_KEEP_LOGITS | CB_FLAG_STAGE_TIMING)) != 0) return CB_ERR_INVALID_ARG;
+  if ((c->flags & ~(CB_FLAG_KEEP_LOGITS | CB_FLAG_STAGE_TIMING | CB_FLAG_TEST_STALL)) != 0)
+    return CB_ERR_INVALID_ARG;
   // 32-bit row and tile indices everywhere
   const uint64_t M = static_cast<uint64_t>(c->n_tokens) * c->top_k;
   const uint64_t rows = M + static_cast<uint64_t>(c->n_experts) * kTileM;
@@ -243,12 +244,18 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
   ga.err = h->err;
   ga.wait_limit_ns = kWaitLimitNs;
   ga.grid = h->num_sms;
+  if (c.flags & CB_FLAG_TEST_STALL) {
+    ga.test_stall = 1;
+    ga.wait_limit_ns = 1000000ull;  // 1 ms
+  }
   const cudaError_t e1 = int8w ? launch_grouped_gemm_int8(kGateUpSwiGLU, h->tm_a_gu, h->tm_b_gu, h->tm_y, ga, s)
                                : launch_grouped_gemm(kGateUpSwiGLU, false, h->tm_a_gu, h->tm_b_gu, h->tm_y,
                                                      h->tm_b_dn64, ga, s);
   if (e1 != cudaSuccess || !mark(3)) return CB_ERR_CUDA;
 
   GemmArgs gd = ga;
+  gd.test_stall = 0;
+  gd.wait_limit_ns = kWaitLimitNs;
   gd.n_tiles = c.d_model / (int8w ? grouped_gemm_int8_tile_n(kDownF32) : grouped_gemm_tile_n(kDownF32));
   gd.k_blocks = c.d_ff / 64;
   gd.b_rows_per_expert = c.d_model;

@@ -215,7 +215,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
         const int nsub = (u < full_tiles) ? BN : BN / split;
         const uint32_t idesc = (nsub == BN) ? IDESC : idesc_bf16_f32(BM, nsub);
-        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, p.wait_limit_ns)) {
+        // (test_stall waits on the phase in progress, which no thread completes)
+        if (!mbar_wait(&tempty[acc], p.test_stall ? acc_phase : acc_phase ^ 1u, p.wait_limit_ns)) {
           set_error(p.err, kErrTimeout);
           break;
         }

@@ -183,7 +183,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, p.wait_limit_ns)) {
+        // (test_stall waits on the phase in progress, which no thread completes)
+        if (!mbar_wait(&tempty[acc], p.test_stall ? acc_phase : acc_phase ^ 1u, p.wait_limit_ns)) {
           set_error(p.err, kErrTimeout);
           break;
         }

@@ -98,6 +98,7 @@ struct GemmArgs {
   int* err;
   uint64_t wait_limit_ns;
   int32_t grid;                 // persistent CTAs
+  int32_t test_stall;           // test only: MMA warp waits on a phase nothing completes
 };
 enum GemmKind { kGateUpSwiGLU = 0, kDownF32 = 1 };
 // tm_out: the fp32 output Y [rows][d] with a 32 x 32 box and the 128-byte

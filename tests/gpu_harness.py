@@ -36,14 +36,15 @@ def to_dev(a, device="cuda"):
 
 
 class GpuLayer:
-    def __init__(self, layer: synth.Layer, keep_logits=True, device=0):
+    def __init__(self, layer: synth.Layer, keep_logits=True, device=0, flags=0):
         s = layer.shape
         self.layer = layer
         self.T = layer.x.shape[0]
         self.dev = f"cuda:{device}"
         w = {n: to_dev(getattr(layer, n), self.dev) for n in ("wr", "bias", "wg", "wu", "wd", "sg", "su", "sd")}
         self.m = cb.MoELayer(self.T, s.d, s.f, s.E, s.k, w["wr"], w["wg"], w["wu"], w["wd"], router_bias=w["bias"],
-                             s_gate=w["sg"], s_up=w["su"], s_down=w["sd"], device=device, keep_logits=keep_logits)
+                             s_gate=w["sg"], s_up=w["su"], s_down=w["sd"], device=device, keep_logits=keep_logits,
+                             flags=flags)
         del w
         self.x = to_dev(layer.x, self.dev)
         self.out = torch.empty((self.T, s.d), dtype=torch.bfloat16, device=self.dev)

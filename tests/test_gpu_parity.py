@@ -141,3 +141,23 @@ def test_both_routers(name, router, monkeypatch):
     rep = gh.full_check(synth.make_layer(ROUTER_CASES[name]))
     print(name, router, rep)
     assert rep.get("logit_max_err", 0.0) <= 5e-6
+
+
+@pytest.mark.parametrize("wdtype", ["bf16", "int8"])
+def test_device_wait_timeout_is_reported_and_context_survives(wdtype):
+    """A bounded device wait that nothing satisfies (CB_FLAG_TEST_STALL) ends the
+    kernel with CB_ERR_TIMEOUT in the status word instead of a hang or a fault;
+    the context stays usable: a normal handle afterwards still matches the oracle."""
+    import mixture_experts_router_gb300 as cb
+    shape = synth.custom_shape("stall", T=300, d=512, f=512, E=8, k=2, wdtype=wdtype, seed=51)
+    layer = synth.make_layer(shape)
+    gl = gh.GpuLayer(layer, flags=cb.CB_FLAG_TEST_STALL)
+    try:
+        gl.m.forward(gl.x, gl.out)
+        torch.cuda.synchronize()
+        assert gl.m.last_error() == cb.CB_ERR_TIMEOUT
+        assert gl.m.last_error() == cb.CB_OK     # reading the word clears it
+    finally:
+        gl.close()
+    rep = gh.full_check(layer)
+    assert rep["f32_max_abs"] <= gh.MAX_ABS
