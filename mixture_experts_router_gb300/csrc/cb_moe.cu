@@ -39,7 +39,7 @@ struct cb_moe {
   int32_t* ids;
   float* w;
   float* logits;
-  int32_t *chunk, *counts, *offsets, *mtile_off, *mtile_expert, *ptile_off, *ptile_expert, *tok, *inv, *rowsrc;
+  int32_t *chunk, *counts, *offsets, *mtile_off, *mtile_expert, *ptile_off, *ptile_expert, *tok, *inv;
   int* err;
   uint16_t *x_stage, *out_stage;
   int32_t max_mtiles, n_chunks;
@@ -55,7 +55,7 @@ namespace {
 struct Layout {
   uint64_t off_wr, off_bias, off_wgu, off_wd, off_sg, off_su, off_sd;
   uint64_t off_xp, off_hb, off_y, off_ids, off_w, off_logits, off_chunk, off_counts, off_offsets, off_mtile_off,
-      off_mtile_expert, off_ptile_off, off_ptile_expert, off_tok, off_inv, off_rowsrc, off_err, off_xs, off_os;
+      off_mtile_expert, off_ptile_off, off_ptile_expert, off_tok, off_inv, off_err, off_xs, off_os;
   uint64_t total;
   int32_t max_mtiles, n_chunks;
 };
@@ -98,7 +98,6 @@ Layout plan(const cb_moe_config_t& c) {
   L.off_ptile_expert = take(static_cast<uint64_t>(L.max_mtiles) * 4);
   L.off_tok = take(M * 4);
   L.off_inv = take(M * 4);
-  L.off_rowsrc = take(mpad * 4);
   L.off_err = take(64);
   L.off_xs = take(T * d * 2);
   L.off_os = take(T * d * 2);
@@ -220,10 +219,8 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
   da.ptile_expert = h->ptile_expert;
   da.tok = h->tok;
   da.inv = h->inv;
-  da.rowsrc = h->rowsrc;
   da.xp = h->xp;
-  da.gather_blocks = static_cast<int32_t>(
-      std::min<int64_t>(h->num_sms * 8, (static_cast<int64_t>(h->max_mtiles) * kTileM + 7) / 8));
+  da.gather_blocks = static_cast<int32_t>(std::min<int64_t>(h->num_sms * 8, (c.n_tokens + 7) / 8));
   da.err = h->err;
   if (launch_dispatch(da, s) != cudaSuccess || !mark(2)) return CB_ERR_CUDA;
 
@@ -378,7 +375,6 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
   h->ptile_expert = reinterpret_cast<int32_t*>(b + L.off_ptile_expert);
   h->tok = reinterpret_cast<int32_t*>(b + L.off_tok);
   h->inv = reinterpret_cast<int32_t*>(b + L.off_inv);
-  h->rowsrc = reinterpret_cast<int32_t*>(b + L.off_rowsrc);
   h->err = reinterpret_cast<int*>(b + L.off_err);
   h->x_stage = reinterpret_cast<uint16_t*>(b + L.off_xs);
   h->out_stage = reinterpret_cast<uint16_t*>(b + L.off_os);

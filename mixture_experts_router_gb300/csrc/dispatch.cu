@@ -13,7 +13,8 @@
 //                      bases, the expert-aligned 128-row tile prefix and the
 //                      tile -> expert map used by the grouped GEMMs
 //   dispatch_scatter : per chunk: warp-aggregated ranks -> tok[], inv[]
-//   dispatch_gather  : Xp[row] = x[tok[row]] over the padded row space
+//   dispatch_small   : the three above in one block, for small T*k
+//   dispatch_copy    : each token's row of x into its k rows of Xp
 #include "internal.h"
 
 namespace cbmoe {
@@ -100,9 +101,6 @@ __global__ void __launch_bounds__(kThreads) dispatch_scan(DispatchArgs a) {
     }
     for (int b = 0; b < a.n_chunks; ++b) a.chunk[static_cast<int64_t>(b) * a.E + e] += off;
     for (int i = moff; i < moff + mt && i < a.max_mtiles; ++i) a.mtile_expert[i] = e;
-    if (a.rowsrc != nullptr && moff + mt <= a.max_mtiles)
-      for (int64_t r = static_cast<int64_t>(moff) * kTileM + total; r < static_cast<int64_t>(moff + mt) * kTileM; ++r)
-        a.rowsrc[r] = -1;
     if (a.ptile_off != nullptr) {
       a.ptile_off[e] = poff;
       if (e == a.E - 1) a.ptile_off[a.E] = poff + pt;
@@ -156,9 +154,6 @@ __global__ void __launch_bounds__(kThreads) dispatch_scatter(DispatchArgs a) {
       } else {
         a.tok[rank] = static_cast<int32_t>(p / a.k);
         a.inv[p] = rank;
-        if (a.rowsrc != nullptr)
-          a.rowsrc[static_cast<int64_t>(a.mtile_off[e]) * kTileM + (rank - a.offsets[e])] =
-              static_cast<int32_t>(p / a.k);
       }
     }
   }
@@ -174,8 +169,6 @@ constexpr int kSmallWarps = kSmallThreads / 32;
 __global__ void __launch_bounds__(kSmallThreads) dispatch_small(DispatchArgs a) {
   __shared__ int wh[kSmallWarps][256];
   __shared__ int tmp[kSmallWarps];
-  __shared__ int smoff[256];   // tile offset of each expert
-  __shared__ int soff[256];    // row offset of each expert
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   for (int i = threadIdx.x; i < kSmallWarps * 256; i += kSmallThreads) (&wh[0][0])[i] = 0;
   __syncthreads();
@@ -221,11 +214,6 @@ __global__ void __launch_bounds__(kSmallThreads) dispatch_small(DispatchArgs a) 
       if (e == a.E - 1) a.ptile_off[a.E] = poff + pt;
       for (int i = poff; i < poff + pt && i < a.max_mtiles; ++i) a.ptile_expert[i] = e;
     }
-    if (a.rowsrc != nullptr && moff + mt <= a.max_mtiles)
-      for (int64_t r = static_cast<int64_t>(moff) * kTileM + total; r < static_cast<int64_t>(moff + mt) * kTileM; ++r)
-        a.rowsrc[r] = -1;
-    smoff[e] = moff;
-    soff[e] = off;
     for (int w = 0; w < kSmallWarps; ++w) wh[w][e] += off;
   }
   __syncthreads();
@@ -245,38 +233,43 @@ __global__ void __launch_bounds__(kSmallThreads) dispatch_small(DispatchArgs a) 
       } else {
         a.tok[rank] = static_cast<int32_t>(p / a.k);
         a.inv[p] = rank;
-        if (a.rowsrc != nullptr)
-          a.rowsrc[static_cast<int64_t>(smoff[e2]) * kTileM + (rank - soff[e2])] = static_cast<int32_t>(p / a.k);
       }
     }
   }
 }
 
-// Row gather Xp[row] = x[rowsrc[row]] (rows with rowsrc < 0 are padding).
-// One warp per row, the next row's source index loaded while this row is
-// copied with 16-byte vectors, eight loads in flight per lane.
-__global__ void __launch_bounds__(kThreads) dispatch_gather(DispatchArgs a) {
+// Row copy into the expert-grouped layout, token-major: one warp per token
+// reads its row of x once (16-byte vectors, eight in flight per lane) and
+// writes it to its k padded rows, row(t, s) = 128 tile_off[e] + inv - off[e].
+// Padding rows of each expert's last tile are left as they are: no GEMM
+// output row depends on another row.
+__global__ void __launch_bounds__(kThreads) dispatch_copy(DispatchArgs a) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int total_tiles = min(a.mtile_off[a.E], a.max_mtiles);
-  const int64_t rows = static_cast<int64_t>(total_tiles) * kTileM;
   const int vec_per_row = a.d / 8;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * kWarps;
-  int64_t row = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
-  int t = (row < rows) ? a.rowsrc[row] : -1;
-  for (; row < rows; row += stride) {
-    const int t_next = (row + stride < rows) ? a.rowsrc[row + stride] : -1;
-    if (t >= a.T) {
-      if (lane == 0) set_error(a.err, kErrDevice);
-    } else if (t >= 0) {
-      const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<int64_t>(t) * a.d);
-      uint4* dst = reinterpret_cast<uint4*>(a.xp + row * a.d);
-      for (int v0 = 0; v0 < vec_per_row; v0 += 32 * 8) {
-        uint4 buf[8];
+  const int64_t rows = static_cast<int64_t>(a.max_mtiles) * kTileM;
+  for (int t = blockIdx.x * kWarps + warp; t < a.T; t += gridDim.x * kWarps) {
+    int64_t dst_row = -1;
+    if (lane < a.k) {
+      const int e = a.ids[static_cast<int64_t>(t) * a.k + lane];
+      const int r = a.inv[static_cast<int64_t>(t) * a.k + lane];
+      if (e >= 0 && e < a.E) dst_row = static_cast<int64_t>(a.mtile_off[e]) * kTileM + (r - a.offsets[e]);
+      if (dst_row < 0 || dst_row >= rows) {
+        set_error(a.err, kErrDevice);
+        dst_row = -1;
+      }
+    }
+    const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<int64_t>(t) * a.d);
+    for (int v0 = 0; v0 < vec_per_row; v0 += 32 * 8) {
+      uint4 buf[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int v = v0 + u * 32 + lane;
-          if (v < vec_per_row) buf[u] = __ldg(src + v);
-        }
+      for (int u = 0; u < 8; ++u) {
+        const int v = v0 + u * 32 + lane;
+        if (v < vec_per_row) buf[u] = __ldg(src + v);
+      }
+      for (int s = 0; s < a.k; ++s) {
+        const int64_t row = __shfl_sync(0xffffffffu, dst_row, s);
+        if (row < 0) continue;
+        uint4* dst = reinterpret_cast<uint4*>(a.xp + row * a.d);
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
           const int v = v0 + u * 32 + lane;
@@ -284,7 +277,6 @@ __global__ void __launch_bounds__(kThreads) dispatch_gather(DispatchArgs a) {
         }
       }
     }
-    t = t_next;
   }
 }
 
@@ -307,7 +299,7 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s) {
     dispatch_scan<<<1, kThreads, 0, s>>>(a);
     dispatch_scatter<<<a.n_chunks, kThreads, 0, s>>>(a);
   }
-  dispatch_gather<<<a.gather_blocks, kThreads, 0, s>>>(a);
+  dispatch_copy<<<a.gather_blocks, kThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -57,9 +57,8 @@ struct DispatchArgs {
   int32_t* ptile_expert; // [max_mtiles] expert owning each pair (or nullptr)
   int32_t* tok;          // [T*k]
   int32_t* inv;          // [T*k]
-  int32_t* rowsrc;       // [max_mtiles*kTileM] token of each padded row, -1 on padding (or nullptr)
   uint16_t* xp;          // bf16 [max_mtiles*kTileM][d]
-  int32_t gather_blocks;
+  int32_t gather_blocks;  // blocks of the row copy
   int* err;
 };
 constexpr int kDispatchChunk = 2048;
