@@ -20,10 +20,10 @@
 //   warp 1      : TMEM owner (512 columns = 2 buffers x 2 m-tiles x 128) and
 //                 MMA issuer
 //   warps 2..5  : epilogue (tcgen05.ld, scales, SwiGLU or fp32, 16-B stores)
-//   warps 6..9  : int8 -> bf16 transform of each staged weight tile into the
+//   warps 6..13 : int8 -> bf16 transform of each staged weight tile into the
 //                 stage's 128-byte-swizzled B buffer, then fence to the async
 //                 proxy and arrive on the stage barrier
-//   warp 10     : TMA producer of the int8 weight tiles (128x64) into a
+//   warp 14     : TMA producer of the int8 weight tiles (128x64) into a
 //                 6-slot ring, running up to 6 k-blocks ahead
 // The down kernel's epilogue stages each warp's 32x32 fp32 blocks in
 // 128-byte-swizzled shared memory and writes them with bulk tensor stores.
@@ -45,7 +45,7 @@ constexpr int B_BYTES = BN * BK * 2;  // 16 KB bf16
 constexpr int STAGE_BYTES = 2 * A_BYTES + B_BYTES;
 constexpr int I8_SLOTS = 6;
 constexpr int I8_BYTES = BN * BK;     // 8 KB int8
-constexpr int N_XFORM_WARPS = 4;
+constexpr int N_XFORM_WARPS = 8;
 constexpr int XFORM_WARP0 = 6;
 constexpr int BPROD_WARP = XFORM_WARP0 + N_XFORM_WARPS;
 constexpr int THREADS = 32 * (BPROD_WARP + 1);
