@@ -46,8 +46,10 @@ struct cb_moe {
   cudaEvent_t ev[CB_N_STAGES + 1];
   bool timing;
   bool router_tc;          // tcgen05 router (else the mma.sync router)
+  bool gather_a;           // gate/up GEMM gathers its rows from x (no Xp copy)
   const void* tm_x_src;    // x pointer tm_x was encoded for
-  CUtensorMap tm_a_gu, tm_b_gu, tm_a_dn, tm_b_dn, tm_b_dn64, tm_y, tm_x, tm_wr;
+  const void* tm_xg_src;   // x pointer tm_xg was encoded for
+  CUtensorMap tm_a_gu, tm_b_gu, tm_a_dn, tm_b_dn, tm_b_dn64, tm_y, tm_x, tm_xg, tm_wr;
 };
 
 namespace {
@@ -221,6 +223,7 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
   da.inv = h->inv;
   da.xp = h->xp;
   da.gather_blocks = static_cast<int32_t>(std::min<int64_t>(h->num_sms * 8, (c.n_tokens + 7) / 8));
+  da.copy_rows = h->gather_a ? 0 : 1;
   da.err = h->err;
   if (launch_dispatch(da, s) != cudaSuccess || !mark(2)) return CB_ERR_CUDA;
 
@@ -241,16 +244,30 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
   ga.err = h->err;
   ga.wait_limit_ns = kWaitLimitNs;
   ga.grid = h->num_sms;
+  const CUtensorMap* tm_a_gu = &h->tm_a_gu;
+  if (h->gather_a) {
+    if (h->tm_xg_src != x) {
+      if (!make_tmap(&h->tm_xg, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c.d_model, c.n_tokens, 64, 1))
+        return CB_ERR_CUDA;
+      h->tm_xg_src = x;
+    }
+    tm_a_gu = &h->tm_xg;
+    ga.gather = 1;
+    ga.tok = h->tok;
+    ga.offsets = h->offsets;
+    ga.counts = h->counts;
+  }
   if (c.flags & CB_FLAG_TEST_STALL) {
     ga.test_stall = 1;
     ga.wait_limit_ns = 1000000ull;  // 1 ms
   }
   const cudaError_t e1 = int8w ? launch_grouped_gemm_int8(kGateUpSwiGLU, h->tm_a_gu, h->tm_b_gu, h->tm_y, ga, s)
-                               : launch_grouped_gemm(kGateUpSwiGLU, false, h->tm_a_gu, h->tm_b_gu, h->tm_y,
+                               : launch_grouped_gemm(kGateUpSwiGLU, false, *tm_a_gu, h->tm_b_gu, h->tm_y,
                                                      h->tm_b_dn64, ga, s);
   if (e1 != cudaSuccess || !mark(3)) return CB_ERR_CUDA;
 
   GemmArgs gd = ga;
+  gd.gather = 0;
   gd.test_stall = 0;
   gd.wait_limit_ns = kWaitLimitNs;
   gd.n_tiles = c.d_model / (int8w ? grouped_gemm_int8_tile_n(kDownF32) : grouped_gemm_tile_n(kDownF32));
@@ -418,6 +435,10 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
     h->router_tc = cfg->n_experts > 16;
     if (rv != nullptr && std::strcmp(rv, "tc") == 0) h->router_tc = true;
     if (rv != nullptr && std::strcmp(rv, "mma") == 0) h->router_tc = false;
+    // bf16 layers gather the gate/up rows straight from x; CB_MOE_GATHER=0
+    // copies them into the grouped activations first instead
+    const char* gv = std::getenv("CB_MOE_GATHER");
+    h->gather_a = !int8w && !(gv != nullptr && std::strcmp(gv, "0") == 0);
   }
   ok = ok && make_tmap(&h->tm_wr, h->wr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, E, 64,
                        static_cast<uint32_t>(router_tc_rows(cfg->n_experts)));

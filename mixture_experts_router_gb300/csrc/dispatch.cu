@@ -299,7 +299,7 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s) {
     dispatch_scan<<<1, kThreads, 0, s>>>(a);
     dispatch_scatter<<<a.n_chunks, kThreads, 0, s>>>(a);
   }
-  dispatch_copy<<<a.gather_blocks, kThreads, 0, s>>>(a);
+  if (a.copy_rows) dispatch_copy<<<a.gather_blocks, kThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 

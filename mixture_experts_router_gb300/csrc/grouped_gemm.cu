@@ -165,7 +165,52 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (KIND == kDownF32) tail_split(total_tiles, gridDim.x, full_tiles, split);
   const int total_units = full_tiles + (total_tiles - full_tiles) * split;
 
-  if (warp == 0) {
+  if (KIND == kGateUpSwiGLU && warp == 0 && p.gather) {
+    // ---------------------------- TMA producer, A rows gathered from x
+    // Each lane owns 4 of the m-tile's 128 rows: their tokens, then one
+    // tile::gather4 of those 4 rows per k-block (512 bytes at lane*512).
+    // Padding rows of an expert's last tile repeat its first token; their
+    // outputs land in padding rows of H that nothing reads.
+    int64_t issued = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+      const Work w = decode_work(u, p, full_tiles, split);
+      const int e = w.c.e;
+      const int row0 = p.offsets[e] + (w.c.m_tile - p.mtile_off[e]) * BM;
+      const int row_end = p.offsets[e] + p.counts[e];
+      const int first = p.tok[row0];
+      int tk[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int r = row0 + 4 * lane + j;
+        tk[j] = r < row_end ? p.tok[r] : first;
+      }
+      const int b_row = e * p.b_rows_per_expert + w.col0;
+      for (int kb = 0; kb < p.k_blocks; ++kb) {
+        const int stage = static_cast<int>(issued % STAGES);
+        const uint32_t phase = static_cast<uint32_t>((issued / STAGES) & 1);
+        int got = 1;
+        if (lane == 0) got = mbar_wait(&empty[stage], phase ^ 1u, p.wait_limit_ns) ? 1 : 0;
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (!got) {
+          if (lane == 0) set_error(p.err, kErrTimeout);
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+          tma_load_2d(sb + stage * B_BYTES, &tm_b, &full[stage], kb * BK, b_row);
+        }
+        __syncwarp();
+        tma_gather4(sa + stage * A_BYTES + lane * 4 * 128, &tm_a, &full[stage], kb * BK, tk[0], tk[1], tk[2], tk[3]);
+        ++issued;
+      }
+    }
+    if (lane == 0)
+      for (int64_t i = (issued > STAGES ? issued - STAGES : 0); i < issued; ++i)
+        if (!mbar_wait(&full[i % STAGES], static_cast<uint32_t>((i / STAGES) & 1), p.wait_limit_ns))
+          set_error(p.err, kErrTimeout);
+  } else if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------ TMA producer
       int stage = 0;

@@ -59,6 +59,7 @@ struct DispatchArgs {
   int32_t* inv;          // [T*k]
   uint16_t* xp;          // bf16 [max_mtiles*kTileM][d]
   int32_t gather_blocks;  // blocks of the row copy
+  int32_t copy_rows;      // 0: the GEMM gathers its rows from x itself, skip the copy
   int* err;
 };
 constexpr int kDispatchChunk = 2048;
@@ -98,6 +99,12 @@ struct GemmArgs {
   uint64_t wait_limit_ns;
   int32_t grid;                 // persistent CTAs
   int32_t test_stall;           // test only: MMA warp waits on a phase nothing completes
+  // gate/up with gathered A: tm_a is x [T][d] with a 64 x 1 box; rows of
+  // m-tile mt of expert e are tokens tok[offsets[e] + 128 (mt - mtile_off[e]) + i]
+  int32_t gather;
+  const int32_t* tok;
+  const int32_t* offsets;
+  const int32_t* counts;
 };
 enum GemmKind { kGateUpSwiGLU = 0, kDownF32 = 1 };
 // tm_out: the fp32 output Y [rows][d] with a 32 x 32 box and the 128-byte
