@@ -435,10 +435,14 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
     h->router_tc = cfg->n_experts > 16;
     if (rv != nullptr && std::strcmp(rv, "tc") == 0) h->router_tc = true;
     if (rv != nullptr && std::strcmp(rv, "mma") == 0) h->router_tc = false;
-    // bf16 layers gather the gate/up rows straight from x; CB_MOE_GATHER=0
-    // copies them into the grouped activations first instead
+    // The gate/up rows are copied into the grouped activations by the
+    // dispatch and loaded as 128-row TMA tiles.  CB_MOE_GATHER=1 (bf16
+    // layers) instead gathers them straight from x with TMA tile::gather4,
+    // which skips the copy but measured 3.3x slower in the GEMM on GB300
+    // (32 four-row gathers per k-block); it is kept for callers short of
+    // memory.
     const char* gv = std::getenv("CB_MOE_GATHER");
-    h->gather_a = !int8w && !(gv != nullptr && std::strcmp(gv, "0") == 0);
+    h->gather_a = !int8w && gv != nullptr && std::strcmp(gv, "1") == 0;
   }
   ok = ok && make_tmap(&h->tm_wr, h->wr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, E, 64,
                        static_cast<uint32_t>(router_tc_rows(cfg->n_experts)));

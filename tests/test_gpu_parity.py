@@ -161,3 +161,12 @@ def test_device_wait_timeout_is_reported_and_context_survives(wdtype):
         gl.close()
     rep = gh.full_check(layer)
     assert rep["f32_max_abs"] <= gh.MAX_ABS
+
+
+@pytest.mark.parametrize("name", ["ragged_mid", "skewed_small", "tiny"])
+def test_gathered_rows_path(name, monkeypatch):
+    """CB_MOE_GATHER=1: the gate/up GEMM loads its rows from x with TMA
+    tile::gather4 instead of the dispatch's row copy; same results."""
+    monkeypatch.setenv("CB_MOE_GATHER", "1")
+    rep = gh.full_check(synth.make_layer(SMALL[name]))
+    print(name, "gather", rep)
