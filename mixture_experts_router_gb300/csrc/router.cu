@@ -15,7 +15,7 @@
 // Wr per 32-element step and feeds two MMAs from them.
 //
 // Each warp computes a 16-token m-tile against NTW n-tiles of 8 experts over
-// a slice of d.  A block of 8 warps splits d KS ways (memory parallelism for
+// a slice of d.  A block of up to 16 warps splits d KS ways (memory parallelism for
 // small E, where the kernel is bound by reading x) and the experts NS ways
 // (register budget for E > 128).  Partial logits are summed in a fixed order
 // in shared memory, the bias is added, and one warp per token takes k rounds
@@ -28,8 +28,7 @@
 namespace cbmoe {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
+constexpr int kMaxWarps = 16;
 
 struct Cand {
   float v;
@@ -53,10 +52,13 @@ __device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1
 }
 
 // NT: n-tiles of 8 experts in total (E padded to 8 NT); KS: d split; NS:
-// expert split; MTB: 16-token m-tiles per block.  KS * NS * MTB == 8 warps.
+// expert split; MTB: 16-token m-tiles per block; the block has KS NS MTB
+// warps.
 template <int NT, int KS, int NS, int MTB>
 struct RCfg {
-  static_assert(KS * NS * MTB == kWarps, "8 warps per block");
+  static constexpr int WARPS = KS * NS * MTB;
+  static constexpr int THREADS = 32 * WARPS;
+  static_assert(WARPS <= kMaxWarps, "at most 16 warps per block");
   static constexpr int NTW = NT / NS;      // n-tiles per warp
   static constexpr int EP = NT * 8;        // padded experts
   static constexpr int TB = 16 * MTB;      // tokens per block
@@ -64,9 +66,10 @@ struct RCfg {
 };
 
 template <int NT, int KS, int NS, int MTB>
-__global__ void __launch_bounds__(kThreads) router_mma_kernel(RouterArgs a) {
+__global__ void __launch_bounds__(RCfg<NT, KS, NS, MTB>::THREADS) router_mma_kernel(RouterArgs a) {
   using C = RCfg<NT, KS, NS, MTB>;
   constexpr int NTW = C::NTW, EP = C::EP, TB = C::TB;
+  constexpr int kThreads = C::THREADS, kWarps = C::WARPS;
   extern __shared__ float part[];  // [KS][TB][EP], then part[0] holds the logits
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int g = lane >> 2, q = lane & 3;
@@ -96,7 +99,7 @@ __global__ void __launch_bounds__(kThreads) router_mma_kernel(RouterArgs a) {
 
   // UNR 32-element steps per iteration: all their loads are issued before
   // any MMA, so each thread keeps several 16-byte loads in flight.
-  constexpr int UNR = NTW <= 2 ? 4 : (NTW <= 4 ? 2 : 1);
+  constexpr int UNR = NTW <= 2 ? 8 : (NTW <= 4 ? 2 : 1);
   const uint4 zero = make_uint4(0, 0, 0, 0);
   for (int c = 0; c < dslice; c += 32 * UNR) {
     uint4 xa[UNR], xb[UNR], wr[UNR][NTW];
@@ -206,7 +209,7 @@ cudaError_t launch_cfg(const RouterArgs& a, cudaStream_t s) {
   using C = RCfg<NT, KS, NS, MTB>;
   const int blocks = (a.T + C::TB - 1) / C::TB;
   if (blocks == 0) return cudaSuccess;
-  router_mma_kernel<NT, KS, NS, MTB><<<blocks, kThreads, C::SMEM, s>>>(a);
+  router_mma_kernel<NT, KS, NS, MTB><<<blocks, C::THREADS, C::SMEM, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -222,6 +225,8 @@ cudaError_t prepare_cfg() {
 // Configurations by expert count: small E splits d 8 ways over 16 tokens
 // per block; large E keeps up to 16 n-tiles (128 experts) per warp.
 #define CBMOE_ROUTER_CONFIGS(X) \
+  X(1, 16, 1, 1)                \
+  X(2, 16, 1, 1)                \
   X(1, 8, 1, 1)                 \
   X(2, 8, 1, 1)                 \
   X(4, 4, 1, 2)                 \
@@ -240,8 +245,9 @@ cudaError_t router_prepare() {
 
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t s) {
   const int nt = (a.E + 7) / 8;
-  if (nt <= 1) return launch_cfg<1, 8, 1, 1>(a, s);
-  if (nt <= 2) return launch_cfg<2, 8, 1, 1>(a, s);
+  // small E is bound by reading x: 16 warps split d 16 ways when d allows
+  if (nt <= 1) return a.d % 512 == 0 ? launch_cfg<1, 16, 1, 1>(a, s) : launch_cfg<1, 8, 1, 1>(a, s);
+  if (nt <= 2) return a.d % 512 == 0 ? launch_cfg<2, 16, 1, 1>(a, s) : launch_cfg<2, 8, 1, 1>(a, s);
   if (nt <= 4) return launch_cfg<4, 4, 1, 2>(a, s);
   if (nt <= 8) return launch_cfg<8, 2, 1, 4>(a, s);
   if (nt <= 16) return launch_cfg<16, 2, 1, 4>(a, s);
