@@ -196,15 +196,19 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
           for (int j = 0; j < CW; ++j) sum[j] += __uint_as_float(r[j]);
         }
+        if (a.bias != nullptr) {
+#pragma unroll
+          for (int j = 0; j < CW; ++j)
+            if (c0 + j < a.E) sum[j] += __ldg(a.bias + c0 + j);
+        }
 #pragma unroll
         for (int j = 0; j < CW; ++j) my[j] = sum[j];
         __syncwarp();
         const int nj = a.E - c0 < CW ? a.E - c0 : CW;
-#pragma unroll 1
+#pragma unroll 4
         for (int j = 0; j < nj; ++j) {
           const int e = c0 + j;
-          float v = my[j];
-          if (a.bias != nullptr) v += __ldg(a.bias + e);
+          const float v = my[j];
           if (a.logits != nullptr && t < a.T) a.logits[static_cast<int64_t>(t) * a.E + e] = v;
           uint64_t key = rank_key(v, e);
           if (key > thr) {
