@@ -46,6 +46,12 @@ struct cb_moe {
   cudaEvent_t ev[CB_N_STAGES + 1];
   bool timing;
   bool router_tc;          // tcgen05 router (else the mma.sync router)
+  bool use_graphs;         // replay each forward variant from a captured CUDA graph
+  struct GraphSlot {
+    const void* a;
+    const void* b;
+    cudaGraphExec_t exec;
+  } graphs[3];             // bf16 forward, fp32-out forward, host-buffer forward
   bool gather_a;           // gate/up GEMM gathers its rows from x (no Xp copy)
   const void* tm_x_src;    // x pointer tm_x was encoded for
   const void* tm_xg_src;   // x pointer tm_xg was encoded for
@@ -177,7 +183,10 @@ struct DeviceGuard {
 cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, cudaStream_t s) {
   const cb_moe_config_t& c = h->cfg;
   if (fault_injected("launch")) return CB_ERR_CUDA;
-  auto mark = [&](int i) { return !h->timing || cudaEventRecord(h->ev[i], s) == cudaSuccess; };
+  // external event nodes when captured, so stage timing works through a graph
+  auto mark = [&](int i) {
+    return !h->timing || cudaEventRecordWithFlags(h->ev[i], s, cudaEventRecordExternal) == cudaSuccess;
+  };
   if (!mark(0)) return CB_ERR_CUDA;
 
   RouterArgs ra{};
@@ -296,6 +305,49 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
   ca.out_f32 = f32out ? 1 : 0;
   if (launch_combine(ca, s) != cudaSuccess || !mark(5)) return CB_ERR_CUDA;
   return CB_OK;
+}
+
+// Enqueue body(s) through a CUDA graph cached per forward variant and keyed
+// by its buffer pointers (a, b): the first call for a key captures the
+// kernel launches into a graph and instantiates it, later calls replay it,
+// which removes the launch gaps between the layer's kernels.  Without graphs
+// (the legacy default stream, a stream the caller is already capturing, or
+// a capture that fails) the launches are enqueued directly.
+template <class Body>
+cb_status_t run_graphed(cb_moe_t* h, int slot, const void* a, const void* b, cudaStream_t s, Body body) {
+  if (!h->use_graphs || s == nullptr) return body(s);
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
+    cudaGetLastError();
+    return body(s);
+  }
+  if (cs != cudaStreamCaptureStatusNone) return body(s);
+  cb_moe::GraphSlot& g = h->graphs[slot];
+  if (g.exec == nullptr || g.a != a || g.b != b) {
+    if (g.exec != nullptr) {
+      cudaGraphExecDestroy(g.exec);
+      g.exec = nullptr;
+    }
+    if (cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+      cudaGetLastError();
+      return body(s);
+    }
+    const cb_status_t st = body(s);
+    cudaGraph_t graph = nullptr;
+    const cudaError_t ec = cudaStreamEndCapture(s, &graph);
+    cudaGraphExec_t exec = nullptr;
+    const bool ok = st == CB_OK && ec == cudaSuccess && graph != nullptr &&
+                    cudaGraphInstantiate(&exec, graph, 0) == cudaSuccess;
+    if (graph != nullptr) cudaGraphDestroy(graph);
+    if (!ok) {
+      cudaGetLastError();
+      return body(s);
+    }
+    g.exec = exec;
+    g.a = a;
+    g.b = b;
+  }
+  return cudaGraphLaunch(g.exec, s) == cudaSuccess ? CB_OK : CB_ERR_CUDA;
 }
 
 cb_status_t check_forward_args(const cb_moe_t* h, const void* x, const void* out, uint64_t out_elem_bytes) {
@@ -443,6 +495,9 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
     // memory.
     const char* gv = std::getenv("CB_MOE_GATHER");
     h->gather_a = !int8w && gv != nullptr && std::strcmp(gv, "1") == 0;
+    // forwards replay captured CUDA graphs unless CB_MOE_GRAPHS=0
+    const char* grv = std::getenv("CB_MOE_GRAPHS");
+    h->use_graphs = !(grv != nullptr && std::strcmp(grv, "0") == 0);
   }
   ok = ok && make_tmap(&h->tm_wr, h->wr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, E, 64,
                        static_cast<uint32_t>(router_tc_rows(cfg->n_experts)));
@@ -463,32 +518,38 @@ cb_status_t cb_moe_forward(cb_moe_t* h, const void* x, void* out, void* stream) 
   const cb_status_t st = check_forward_args(h, x, out, 2);
   if (st != CB_OK) return st;
   if (h->cfg.n_tokens == 0) return CB_OK;
+  if (fault_injected("launch")) return CB_ERR_CUDA;
   DeviceGuard guard(h->cfg.device);
   if (!guard.ok) return CB_ERR_CUDA;
-  return enqueue_forward(h, x, out, false, static_cast<cudaStream_t>(stream));
+  return run_graphed(h, 0, x, out, static_cast<cudaStream_t>(stream),
+                     [&](cudaStream_t s) { return enqueue_forward(h, x, out, false, s); });
 }
 
 cb_status_t cb_moe_forward_f32out(cb_moe_t* h, const void* x, float* out, void* stream) {
   const cb_status_t st = check_forward_args(h, x, out, 4);
   if (st != CB_OK) return st;
   if (h->cfg.n_tokens == 0) return CB_OK;
+  if (fault_injected("launch")) return CB_ERR_CUDA;
   DeviceGuard guard(h->cfg.device);
   if (!guard.ok) return CB_ERR_CUDA;
-  return enqueue_forward(h, x, out, true, static_cast<cudaStream_t>(stream));
+  return run_graphed(h, 1, x, out, static_cast<cudaStream_t>(stream),
+                     [&](cudaStream_t s) { return enqueue_forward(h, x, out, true, s); });
 }
 
 cb_status_t cb_moe_forward_host(cb_moe_t* h, const void* x_host, void* out_host, void* stream) {
   if (h == nullptr || x_host == nullptr || out_host == nullptr) return CB_ERR_INVALID_ARG;
   if (h->cfg.n_tokens == 0) return CB_OK;
+  if (fault_injected("launch")) return CB_ERR_CUDA;
   DeviceGuard guard(h->cfg.device);
   if (!guard.ok) return CB_ERR_CUDA;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   const uint64_t bytes = static_cast<uint64_t>(h->cfg.n_tokens) * h->cfg.d_model * 2;
-  if (cudaMemcpyAsync(h->x_stage, x_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return CB_ERR_CUDA;
-  const cb_status_t st = enqueue_forward(h, h->x_stage, h->out_stage, false, s);
-  if (st != CB_OK) return st;
-  if (cudaMemcpyAsync(out_host, h->out_stage, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) return CB_ERR_CUDA;
-  return CB_OK;
+  return run_graphed(h, 2, x_host, out_host, static_cast<cudaStream_t>(stream), [&](cudaStream_t s) {
+    if (cudaMemcpyAsync(h->x_stage, x_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return CB_ERR_CUDA;
+    const cb_status_t st2 = enqueue_forward(h, h->x_stage, h->out_stage, false, s);
+    if (st2 != CB_OK) return st2;
+    if (cudaMemcpyAsync(out_host, h->out_stage, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) return CB_ERR_CUDA;
+    return CB_OK;
+  });
 }
 
 cb_status_t cb_moe_routing(const cb_moe_t* h, cb_routing_view_t* v) {
@@ -533,6 +594,8 @@ cb_status_t cb_moe_free(cb_moe_t* h) {
     if (!guard.ok || cudaDeviceSynchronize() != cudaSuccess) st = CB_ERR_CUDA;
     for (int i = 0; h->timing && i <= CB_N_STAGES; ++i)
       if (h->ev[i] != nullptr) cudaEventDestroy(h->ev[i]);
+    for (auto& g : h->graphs)
+      if (g.exec != nullptr) cudaGraphExecDestroy(g.exec);
     if (cudaFree(h->block) != cudaSuccess) st = CB_ERR_CUDA;
   }
   delete h;

@@ -170,3 +170,53 @@ def test_gathered_rows_path(name, monkeypatch):
     monkeypatch.setenv("CB_MOE_GATHER", "1")
     rep = gh.full_check(synth.make_layer(SMALL[name]))
     print(name, "gather", rep)
+
+
+def test_graph_replay_matches_direct_launches():
+    """On a non-default stream each forward variant is captured once into a CUDA
+    graph and replayed; replays, re-captures after a pointer change, and the
+    stage-timing events all give the same bits as direct launches."""
+    import mixture_experts_router_gb300 as cb
+    layer = synth.make_layer(SMALL["ragged_mid"])
+    gl = gh.GpuLayer(layer)
+    timed = None
+    try:
+        gl.run()                                   # legacy stream: direct launches
+        ref16 = gl.out.clone()
+        ref32 = gl.out32.clone()
+        s = torch.cuda.Stream()
+        outs = [torch.empty_like(gl.out) for _ in range(2)]
+        for it in range(3):                        # capture, replay, replay
+            for o in outs:                         # alternate pointers: re-capture
+                o.zero_()
+                gl.m.forward(gl.x, o, stream=s)
+                s.synchronize()
+                assert torch.equal(o.view(torch.int16), ref16.view(torch.int16)), it
+        o32 = torch.empty_like(gl.out32)
+        for _ in range(2):
+            gl.m.forward(gl.x, o32, stream=s, f32out=True)
+            s.synchronize()
+            assert torch.equal(o32, ref32)
+        xh = torch.from_numpy(layer.x.view(np.int16)).pin_memory()
+        oh = torch.empty_like(xh).pin_memory()
+        for _ in range(2):
+            oh.zero_()
+            gl.m.forward_host(xh, oh, stream=s)
+            s.synchronize()
+            assert torch.equal(oh, ref16.view(torch.int16).cpu())
+        assert gl.m.last_error() == cb.CB_OK
+        # stage timing through a replayed graph
+        w = {n: gh.to_dev(getattr(layer, n)) for n in ("wr", "wg", "wu", "wd")}
+        shp = layer.shape
+        timed = cb.MoELayer(gl.T, shp.d, shp.f, shp.E, shp.k, w["wr"], w["wg"], w["wu"], w["wd"], stage_timing=True)
+        ot = torch.empty_like(gl.out)
+        for _ in range(3):
+            timed.forward(gl.x, ot, stream=s)
+            ms = timed.stage_times()
+            assert all(v > 0 for v in ms) and sum(ms) < 1000
+        s.synchronize()
+        assert torch.equal(ot.view(torch.int16), ref16.view(torch.int16))
+    finally:
+        if timed is not None:
+            timed.close()
+        gl.close()
