@@ -47,6 +47,8 @@ struct cb_moe {
   bool timing;
   bool router_tc;          // tcgen05 router (else the mma.sync router)
   bool use_graphs;         // replay each forward variant from a captured CUDA graph
+  bool use_mc;             // bf16 GEMMs on multicast CTA pairs
+  int mc_grid_gu, mc_grid_dn;
   struct GraphSlot {
     const void* a;
     const void* b;
@@ -55,7 +57,7 @@ struct cb_moe {
   bool gather_a;           // gate/up GEMM gathers its rows from x (no Xp copy)
   const void* tm_x_src;    // x pointer tm_x was encoded for
   const void* tm_xg_src;   // x pointer tm_xg was encoded for
-  CUtensorMap tm_a_gu, tm_b_gu, tm_a_dn, tm_b_dn, tm_b_dn64, tm_y, tm_x, tm_xg, tm_wr;
+  CUtensorMap tm_a_gu, tm_b_gu, tm_a_dn, tm_b_dn, tm_b_dn64, tm_b_gu128, tm_b_dn128, tm_y, tm_x, tm_xg, tm_wr;
 };
 
 namespace {
@@ -270,9 +272,17 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
     ga.test_stall = 1;
     ga.wait_limit_ns = 1000000ull;  // 1 ms
   }
-  const cudaError_t e1 = int8w ? launch_grouped_gemm_int8(kGateUpSwiGLU, h->tm_a_gu, h->tm_b_gu, h->tm_y, ga, s)
-                               : launch_grouped_gemm(kGateUpSwiGLU, false, *tm_a_gu, h->tm_b_gu, h->tm_y,
-                                                     h->tm_b_dn64, ga, s);
+  const bool mc = !int8w && h->use_mc && !h->gather_a;
+  cudaError_t e1;
+  if (int8w) {
+    e1 = launch_grouped_gemm_int8(kGateUpSwiGLU, h->tm_a_gu, h->tm_b_gu, h->tm_y, ga, s);
+  } else if (mc) {
+    GemmArgs gm = ga;
+    gm.grid = h->mc_grid_gu;
+    e1 = launch_grouped_gemm_mc(kGateUpSwiGLU, h->tm_a_gu, h->tm_b_gu128, h->tm_y, gm, s);
+  } else {
+    e1 = launch_grouped_gemm(kGateUpSwiGLU, false, *tm_a_gu, h->tm_b_gu, h->tm_y, h->tm_b_dn64, ga, s);
+  }
   if (e1 != cudaSuccess || !mark(3)) return CB_ERR_CUDA;
 
   GemmArgs gd = ga;
@@ -286,9 +296,16 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
   gd.ld_out = c.d_model;
   gd.scale0 = h->sd;
   gd.scale1 = nullptr;
-  const cudaError_t e2 = int8w ? launch_grouped_gemm_int8(kDownF32, h->tm_a_dn, h->tm_b_dn, h->tm_y, gd, s)
-                               : launch_grouped_gemm(kDownF32, false, h->tm_a_dn, h->tm_b_dn, h->tm_y, h->tm_b_dn64,
-                                                     gd, s);
+  cudaError_t e2;
+  if (int8w) {
+    e2 = launch_grouped_gemm_int8(kDownF32, h->tm_a_dn, h->tm_b_dn, h->tm_y, gd, s);
+  } else if (mc) {
+    GemmArgs gm = gd;
+    gm.grid = h->mc_grid_dn;
+    e2 = launch_grouped_gemm_mc(kDownF32, h->tm_a_dn, h->tm_b_dn128, h->tm_y, gm, s);
+  } else {
+    e2 = launch_grouped_gemm(kDownF32, false, h->tm_a_dn, h->tm_b_dn, h->tm_y, h->tm_b_dn64, gd, s);
+  }
   if (e2 != cudaSuccess || !mark(4)) return CB_ERR_CUDA;
 
   CombineArgs ca{};
@@ -477,6 +494,10 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
   ok = ok && make_tmap(&h->tm_b_dn, h->wd, wdt, eb, f, E * d, 64, brows_box, wsw);
   ok = ok && make_tmap(&h->tm_y, h->y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, mpad, 32, 32);
   ok = ok && make_tmap(&h->tm_b_dn64, h->wd, wdt, eb, f, E * d, 64, 64, wsw);
+  if (!int8w) {
+    ok = ok && make_tmap(&h->tm_b_gu128, h->wgu, wdt, eb, d, E * 2 * f, 64, 128, wsw);
+    ok = ok && make_tmap(&h->tm_b_dn128, h->wd, wdt, eb, f, E * d, 64, 128, wsw);
+  }
   ok = ok && grouped_gemm_prepare() == cudaSuccess && grouped_gemm_int8_prepare() == cudaSuccess &&
        router_prepare() == cudaSuccess && router_tc_prepare() == cudaSuccess;
   // router: tcgen05 for wide expert counts, the mma.sync split-K router for
@@ -495,6 +516,13 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
     // memory.
     const char* gv = std::getenv("CB_MOE_GATHER");
     h->gather_a = !int8w && gv != nullptr && std::strcmp(gv, "1") == 0;
+    // bf16 GEMMs on multicast CTA pairs when CB_MOE_MULTICAST=1
+    const char* mv = std::getenv("CB_MOE_MULTICAST");
+    h->use_mc = !int8w && mv != nullptr && std::strcmp(mv, "1") == 0;
+    if (h->use_mc) {
+      ok = ok && grouped_gemm_mc_prepare(h->num_sms, &h->mc_grid_gu, &h->mc_grid_dn) == cudaSuccess;
+      if (h->mc_grid_gu < 2 || h->mc_grid_dn < 2) h->use_mc = false;
+    }
     // forwards replay captured CUDA graphs unless CB_MOE_GRAPHS=0
     const char* grv = std::getenv("CB_MOE_GRAPHS");
     h->use_graphs = !(grv != nullptr && std::strcmp(grv, "0") == 0);

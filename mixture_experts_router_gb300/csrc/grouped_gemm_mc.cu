@@ -1,0 +1,328 @@
+// Grouped expert GEMMs (bf16) on CTA pairs that share each weight tile by
+// TMA multicast.
+//
+// Same math and epilogues as grouped_gemm.cu (gate/up with SwiGLU into bf16
+// H, down into fp32 Y with bulk tensor stores), run by clusters of two CTAs:
+// both CTAs of a cluster take the same (expert, N tile) and the two m-tiles
+// of one pair (2p, 2p+1) of that expert.  Each CTA TMA-loads its own A tile
+// (128 x 64) and ONE HALF of the shared 256 x 64 weight tile, multicast into
+// the same offset of both CTAs' shared memory, so every SM moves 32 KB per
+// k-block from L2 instead of 48 KB.  The MMA stays per CTA
+// (tcgen05.mma.cta_group::1, M=128 N=256); a stage is released only when
+// both CTAs' MMAs have read it: each MMA commit arrives on the stage's empty
+// barrier of both CTAs (count 2).  In a pair whose second m-tile does not
+// exist (an expert with an odd number of m-tiles), the second CTA computes on
+// a repeat of the first tile and stores nothing.
+//
+// Roles per CTA as in grouped_gemm.cu: warp 0 TMA producer, warp 1 TMEM owner
+// and MMA issuer, warps 2..5 epilogue; bounded waits throughout.  A cluster
+// barrier after set-up makes every barrier of the pair exist before any
+// multicast or remote arrive, and one before exit keeps a CTA alive until
+// its peer can no longer write into it.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace cbmoe {
+namespace {
+
+constexpr int BM = kTileM;
+constexpr int BK = 64;
+constexpr int BN = 256;
+constexpr int HALF_ROWS = BN / 2;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = BN * BK * 2;
+constexpr int HALF_B_BYTES = B_BYTES / 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int THREADS = 192;
+constexpr uint32_t TMEM_COLS = 2 * BN;
+constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+constexpr uint16_t PAIR_MASK = 0x3;
+constexpr int STG_BYTES = 4 * 2 * 32 * 128;
+
+template <int KIND>
+struct Smem {
+  static constexpr int RING = STAGES * STAGE_BYTES;
+  static constexpr int STAGING = KIND == kDownF32 ? STG_BYTES : 0;
+  static constexpr int BYTES = RING + STAGING + 1024 + 256;
+};
+
+struct MyTile {
+  int m_tile;  // this CTA's m-tile (a repeat of the pair's first when !valid)
+  bool valid;
+  int e;
+  int n;
+};
+
+__device__ __forceinline__ MyTile decode_pair_tile(int tile, const GemmArgs& p, int rank) {
+  const int e = p.ptile_expert[tile / p.n_tiles];
+  const int base = p.ptile_off[e];
+  const int np = p.ptile_off[e + 1] - base;
+  const int local = tile - base * p.n_tiles;
+  const int pair = local % np;
+  MyTile t;
+  t.e = e;
+  t.n = local / np;
+  const int mt_e = p.mtile_off[e + 1] - p.mtile_off[e];
+  const int idx = 2 * pair + rank;
+  t.valid = idx < mt_e;
+  t.m_tile = p.mtile_off[e] + (t.valid ? idx : 2 * pair);
+  return t;
+}
+
+__device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&b);
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(THREADS, 1)
+    grouped_gemm_mc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_bh,
+                           const __grid_constant__ CUtensorMap tm_out, const GemmArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sa = smem;
+  uint8_t* sb = smem + STAGES * A_BYTES;
+  uint8_t* staging = smem + Smem<KIND>::RING;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Smem<KIND>::RING + Smem<KIND>::STAGING);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int cluster = blockIdx.x / 2, n_clusters = gridDim.x / 2;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 2);  // both CTAs' MMAs release a stage
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 128);
+    }
+    fence_barrier_init();
+    prefetch_tensormap(&tm_a);
+    prefetch_tensormap(&tm_bh);
+    if (KIND == kDownF32) prefetch_tensormap(&tm_out);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total_tiles = p.ptile_off[p.E] * p.n_tiles;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int64_t issued = 0;
+      bool ok = true;
+      for (int tile = cluster; ok && tile < total_tiles; tile += n_clusters) {
+        const MyTile t = decode_pair_tile(tile, p, rank);
+        const int a_row = t.m_tile * BM;
+        const int b_row = t.e * p.b_rows_per_expert + t.n * BN + rank * HALF_ROWS;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          const int stage = static_cast<int>(issued % STAGES);
+          const uint32_t phase = static_cast<uint32_t>((issued / STAGES) & 1);
+          if (!mbar_wait(&empty[stage], phase ^ 1u, p.wait_limit_ns)) {
+            set_error(p.err, kErrTimeout);
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+          tma_load_2d(sa + stage * A_BYTES, &tm_a, &full[stage], kb * BK, a_row);
+          tma_load_2d_multicast(sb + stage * B_BYTES + rank * HALF_B_BYTES, &tm_bh, &full[stage], kb * BK, b_row,
+                                PAIR_MASK);
+          ++issued;
+        }
+      }
+      for (int64_t i = (issued > STAGES ? issued - STAGES : 0); i < issued; ++i)
+        if (!mbar_wait(&full[i % STAGES], static_cast<uint32_t>((i / STAGES) & 1), p.wait_limit_ns))
+          set_error(p.err, kErrTimeout);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = cluster; ok && tile < total_tiles; tile += n_clusters) {
+        if (!mbar_wait(&tempty[acc], p.test_stall ? acc_phase : acc_phase ^ 1u, p.wait_limit_ns)) {
+          set_error(p.err, kErrTimeout);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait(&full[stage], phase, p.wait_limit_ns)) {
+            set_error(p.err, kErrTimeout);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t adesc = sw128_desc(smem_u32(sa + stage * A_BYTES));
+          const uint64_t bdesc = sw128_desc(smem_u32(sb + stage * B_BYTES));
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            tc_mma_f16(d_tmem, adesc + 2 * k, bdesc + 2 * k, IDESC, (kb | k) != 0 ? 1u : 0u);
+          tc_commit_multicast(&empty[stage], PAIR_MASK);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(&tfull[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+    }
+  } else {
+    const int q = warp & 3;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    int n_stores = 0;
+    for (int tile = cluster; tile < total_tiles; tile += n_clusters) {
+      const MyTile t = decode_pair_tile(tile, p, rank);
+      if (!mbar_wait(&tfull[acc], acc_phase, p.wait_limit_ns)) {
+        set_error(p.err, kErrTimeout);
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      if (t.valid) {
+        if constexpr (KIND == kGateUpSwiGLU) {
+          const int64_t row = static_cast<int64_t>(t.m_tile) * BM + q * 32 + lane;
+          uint16_t* out_row = static_cast<uint16_t*>(p.out) + row * p.ld_out + t.n * (BN / 2);
+#pragma unroll 1
+          for (int c0 = 0; c0 < BN / 2; c0 += 32) {
+            uint32_t g[32], u[32];
+            tmem_load32(tbase + c0, g);
+            tmem_load32(tbase + BN / 2 + c0, u);
+            uint32_t h[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float h0 = silu(__uint_as_float(g[2 * j])) * __uint_as_float(u[2 * j]);
+              const float h1 = silu(__uint_as_float(g[2 * j + 1])) * __uint_as_float(u[2 * j + 1]);
+              h[j] = pack_bf16x2(h0, h1);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(out_row + c0);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) dst[j] = make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
+          }
+        } else {
+          const int row0 = t.m_tile * BM + q * 32;
+#pragma unroll 1
+          for (int c0 = 0; c0 < BN; c0 += 32, ++n_stores) {
+            uint32_t r[32];
+            tmem_load32(tbase + c0, r);
+            uint8_t* buf = staging + (q * 2 + (n_stores & 1)) * 4096;
+            if (n_stores >= 2) {
+              if (lane == 0) bulk_wait_group_read<1>();
+              __syncwarp();
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              *reinterpret_cast<uint4*>(buf + lane * 128 + 16 * (j ^ (lane & 7))) =
+                  make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tm_out, buf, t.n * BN + c0, row0);
+              bulk_commit_group();
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    if (KIND == kDownF32 && lane == 0) bulk_wait_group<0>();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+  cluster_sync();
+}
+
+template <int KIND>
+cudaError_t launch_kind(const CUtensorMap& tm_a, const CUtensorMap& tm_bh, const CUtensorMap& tm_out,
+                        const GemmArgs& a, int grid, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.dynamicSmemBytes = Smem<KIND>::BYTES;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_mc_kernel<KIND>, tm_a, tm_bh, tm_out, a);
+}
+
+template <int KIND>
+int max_pairs(int num_sms) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.dynamicSmemBytes = Smem<KIND>::BYTES;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_mc_kernel<KIND>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+}  // namespace
+
+cudaError_t grouped_gemm_mc_prepare(int num_sms, int* grid_gateup, int* grid_down) {
+  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_mc_kernel<kGateUpSwiGLU>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<kGateUpSwiGLU>::BYTES);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(grouped_gemm_mc_kernel<kDownF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Smem<kDownF32>::BYTES);
+  if (e != cudaSuccess) return e;
+  *grid_gateup = 2 * max_pairs<kGateUpSwiGLU>(num_sms);
+  *grid_down = 2 * max_pairs<kDownF32>(num_sms);
+  return cudaSuccess;
+}
+
+cudaError_t launch_grouped_gemm_mc(GemmKind kind, const CUtensorMap& tm_a, const CUtensorMap& tm_bh,
+                                   const CUtensorMap& tm_out, const GemmArgs& a, cudaStream_t s) {
+  if (a.grid < 2) return cudaErrorInvalidConfiguration;
+  if (kind == kGateUpSwiGLU) return launch_kind<kGateUpSwiGLU>(tm_a, tm_bh, tm_out, a, a.grid, s);
+  return launch_kind<kDownF32>(tm_a, tm_bh, tm_out, a, a.grid, s);
+}
+
+}  // namespace cbmoe

@@ -116,6 +116,12 @@ cudaError_t launch_grouped_gemm(GemmKind kind, bool int8_weights, const CUtensor
                                 const GemmArgs& a, cudaStream_t s);
 cudaError_t grouped_gemm_prepare();  // one-time function attributes
 int grouped_gemm_tile_n(GemmKind kind);  // output columns per tile
+// bf16 on CTA pairs sharing each weight tile by TMA multicast: tm_bh is the
+// weight tensor with a 128-row box (half a tile); tiles are m-tile pairs.
+// prepare returns the persistent grids (2 x co-resident clusters, 0 if none)
+cudaError_t launch_grouped_gemm_mc(GemmKind kind, const CUtensorMap& tm_a, const CUtensorMap& tm_bh,
+                                   const CUtensorMap& tm_out, const GemmArgs& a, cudaStream_t s);
+cudaError_t grouped_gemm_mc_prepare(int num_sms, int* grid_gateup, int* grid_down);
 // int8 weights: tiles are pairs of m-tiles against 128 weight rows
 cudaError_t launch_grouped_gemm_int8(GemmKind kind, const CUtensorMap& tm_a, const CUtensorMap& tm_b,
                                      const CUtensorMap& tm_out, const GemmArgs& a, cudaStream_t s);
