@@ -34,9 +34,17 @@ sys.path.insert(0, ROOT)
 
 METRIC = "MoE-layer tokens/s; grouped-GEMM % of bf16 TC peak; decode weight GB/s % HBM"
 DEFAULT_WORKLOAD = "mixtral_prefill"
-KERNELS_PER_FORWARD = 8   # router, 4 dispatch kernels, 2 grouped GEMMs, combine
+SMALL_DISPATCH_PAIRS = 16384   # up to this many (token, slot) pairs the dispatch is one fused block
+
+
+def kernels_per_forward(shape) -> int:
+    """Kernels one forward launches: router, dispatch (fused block + row copy,
+    or count/scan/scatter + row copy), the two grouped GEMMs, combine."""
+    dispatch = 2 if shape.T * shape.k <= SMALL_DISPATCH_PAIRS else 4
+    return 1 + dispatch + 2 + 1
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
-GEMM_SOURCE = os.path.join(ROOT, "mixture_experts_router_gb300", "csrc", "grouped_gemm.cu")
+GEMM_SOURCES = [os.path.join(ROOT, "mixture_experts_router_gb300", "csrc", n)
+                for n in ("grouped_gemm.cu", "grouped_gemm_pair.cu")]
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -141,6 +149,15 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(inside)}
 
 
+def gemm_source_digest() -> str:
+    """First 16 hex digits of the sha256 over the bf16 grouped-GEMM sources."""
+    h = hashlib.sha256()
+    for path in GEMM_SOURCES:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def measured_traffic(kernel_key):
     """DRAM bytes per launch of a kernel from the committed ncu summary, or None
     when the kernel's source changed since the counters were taken."""
@@ -151,8 +168,7 @@ def measured_traffic(kernel_key):
     entry = data.get(kernel_key)
     if not entry:
         return None
-    with open(GEMM_SOURCE, "rb") as f:
-        digest = hashlib.sha256(f.read()).hexdigest()[:16]
+    digest = gemm_source_digest()
     if entry.get("source_sha256_16") != digest:
         return None
     return entry.get("dram_bytes_per_launch")
@@ -412,7 +428,7 @@ def run_ours(args):
         "e2e": {"value": shape.T * world * k2 / (e2e_ms / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": shape.T * shape.d * 2, "d2h_bytes_per_step": shape.T * shape.d * 2,
                 "steps": k2, "api": "cb_moe_forward_host (pinned host x and out, copies on the stream)"},
-        "gpu_launches": KERNELS_PER_FORWARD * args.steps,
+        "gpu_launches": kernels_per_forward(shape) * args.steps,
         "roofline": roof,
         "stages": stages,
         "expert_rows": {"active_experts": sum(1 for c in counts if c > 0), "max_rows": max(counts),

@@ -47,8 +47,8 @@ struct cb_moe {
   bool timing;
   bool router_tc;          // tcgen05 router (else the mma.sync router)
   bool use_graphs;         // replay each forward variant from a captured CUDA graph
-  bool use_mc;             // bf16 GEMMs on multicast CTA pairs
-  int mc_grid_gu, mc_grid_dn;
+  bool pair_gu, pair_dn;   // bf16 gate/up, down GEMMs on CTA pairs (2-SM MMA)
+  int pair_grid_gu, pair_grid_dn;
   struct GraphSlot {
     const void* a;
     const void* b;
@@ -272,14 +272,15 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
     ga.test_stall = 1;
     ga.wait_limit_ns = 1000000ull;  // 1 ms
   }
-  const bool mc = !int8w && h->use_mc && !h->gather_a;
+  const bool pair_gu = !int8w && h->pair_gu && !h->gather_a;
+  const bool pair_dn = !int8w && h->pair_dn;
   cudaError_t e1;
   if (int8w) {
     e1 = launch_grouped_gemm_int8(kGateUpSwiGLU, h->tm_a_gu, h->tm_b_gu, h->tm_y, ga, s);
-  } else if (mc) {
-    GemmArgs gm = ga;
-    gm.grid = h->mc_grid_gu;
-    e1 = launch_grouped_gemm_mc(kGateUpSwiGLU, h->tm_a_gu, h->tm_b_gu128, h->tm_y, gm, s);
+  } else if (pair_gu) {
+    GemmArgs gp = ga;
+    gp.grid = h->pair_grid_gu;
+    e1 = launch_grouped_gemm_pair(kGateUpSwiGLU, h->tm_a_gu, h->tm_b_gu128, h->tm_y, gp, s);
   } else {
     e1 = launch_grouped_gemm(kGateUpSwiGLU, false, *tm_a_gu, h->tm_b_gu, h->tm_y, h->tm_b_dn64, ga, s);
   }
@@ -299,10 +300,10 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
   cudaError_t e2;
   if (int8w) {
     e2 = launch_grouped_gemm_int8(kDownF32, h->tm_a_dn, h->tm_b_dn, h->tm_y, gd, s);
-  } else if (mc) {
-    GemmArgs gm = gd;
-    gm.grid = h->mc_grid_dn;
-    e2 = launch_grouped_gemm_mc(kDownF32, h->tm_a_dn, h->tm_b_dn128, h->tm_y, gm, s);
+  } else if (pair_dn) {
+    GemmArgs gp = gd;
+    gp.grid = h->pair_grid_dn;
+    e2 = launch_grouped_gemm_pair(kDownF32, h->tm_a_dn, h->tm_b_dn128, h->tm_y, gp, s);
   } else {
     e2 = launch_grouped_gemm(kDownF32, false, h->tm_a_dn, h->tm_b_dn, h->tm_y, h->tm_b_dn64, gd, s);
   }
@@ -516,12 +517,22 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
     // memory.
     const char* gv = std::getenv("CB_MOE_GATHER");
     h->gather_a = !int8w && gv != nullptr && std::strcmp(gv, "1") == 0;
-    // bf16 GEMMs on multicast CTA pairs when CB_MOE_MULTICAST=1
-    const char* mv = std::getenv("CB_MOE_MULTICAST");
-    h->use_mc = !int8w && mv != nullptr && std::strcmp(mv, "1") == 0;
-    if (h->use_mc) {
-      ok = ok && grouped_gemm_mc_prepare(h->num_sms, &h->mc_grid_gu, &h->mc_grid_dn) == cudaSuccess;
-      if (h->mc_grid_gu < 2 || h->mc_grid_dn < 2) h->use_mc = false;
+    // bf16 GEMMs on CTA pairs (2-SM MMA).  Measured on GB300: the down GEMM
+    // gains 4-9 % once experts average two or more m-tiles (T k >= 256 E);
+    // the gate/up GEMM loses 4-10 %, and so does a decode-size layer, whose
+    // experts have one m-tile each.  CB_MOE_PAIR=1|0|gateup|down overrides.
+    const char* pv = std::getenv("CB_MOE_PAIR");
+    const int64_t routed = static_cast<int64_t>(cfg->n_tokens) * cfg->top_k;
+    h->pair_gu = false;
+    h->pair_dn = routed >= 256ll * cfg->n_experts;
+    if (pv != nullptr) {
+      h->pair_gu = std::strcmp(pv, "1") == 0 || std::strcmp(pv, "gateup") == 0;
+      h->pair_dn = std::strcmp(pv, "1") == 0 || std::strcmp(pv, "down") == 0;
+    }
+    if (int8w) h->pair_gu = h->pair_dn = false;
+    if (h->pair_gu || h->pair_dn) {
+      ok = ok && grouped_gemm_pair_prepare(h->num_sms, &h->pair_grid_gu, &h->pair_grid_dn) == cudaSuccess;
+      if (h->pair_grid_gu < 2 || h->pair_grid_dn < 2) h->pair_gu = h->pair_dn = false;
     }
     // forwards replay captured CUDA graphs unless CB_MOE_GRAPHS=0
     const char* grv = std::getenv("CB_MOE_GRAPHS");

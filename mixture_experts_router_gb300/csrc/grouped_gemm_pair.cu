@@ -1,24 +1,29 @@
-// Grouped expert GEMMs (bf16) on CTA pairs that share each weight tile by
-// TMA multicast.
+// Grouped expert GEMMs (bf16) on CTA pairs with the 2-SM tensor-core MMA.
 //
 // Same math and epilogues as grouped_gemm.cu (gate/up with SwiGLU into bf16
-// H, down into fp32 Y with bulk tensor stores), run by clusters of two CTAs:
-// both CTAs of a cluster take the same (expert, N tile) and the two m-tiles
-// of one pair (2p, 2p+1) of that expert.  Each CTA TMA-loads its own A tile
-// (128 x 64) and ONE HALF of the shared 256 x 64 weight tile, multicast into
-// the same offset of both CTAs' shared memory, so every SM moves 32 KB per
-// k-block from L2 instead of 48 KB.  The MMA stays per CTA
-// (tcgen05.mma.cta_group::1, M=128 N=256); a stage is released only when
-// both CTAs' MMAs have read it: each MMA commit arrives on the stage's empty
-// barrier of both CTAs (count 2).  In a pair whose second m-tile does not
-// exist (an expert with an odd number of m-tiles), the second CTA computes on
-// a repeat of the first tile and stores nothing.
+// H, down into fp32 Y with bulk tensor stores), run by clusters of two CTAs
+// on two SMs.  The pair computes the two m-tiles (2p, 2p+1) of one expert
+// against one 256-row weight tile with tcgen05.mma.cta_group::2 (M = 256,
+// N = 256, K = 16), issued by one thread of the even CTA:
 //
-// Roles per CTA as in grouped_gemm.cu: warp 0 TMA producer, warp 1 TMEM owner
-// and MMA issuer, warps 2..5 epilogue; bounded waits throughout.  A cluster
-// barrier after set-up makes every barrier of the pair exist before any
-// multicast or remote arrive, and one before exit keeps a CTA alive until
-// its peer can no longer write into it.
+//   CTA r stages the A rows of m-tile 2p+r (128 x 64 per k-block) and
+//   weight rows [128 r, 128 r + 128) of the tile (128 x 64); the two tensor
+//   cores read each other's weight half, so each SM stages 32 KB per k-block
+//   instead of 48 KB and the same shared memory holds a 6-deep ring;
+//   each CTA's tensor memory receives its own 128 rows x 256 fp32 columns.
+//
+// Barriers: the TMA loads of both CTAs signal the even CTA's `full` barrier
+// (whose producer expects both CTAs' bytes); the MMA thread's commits arrive
+// on `empty` (stage free) and `tfull` (accumulator ready) in both CTAs; the
+// epilogue warps of both CTAs arrive on the even CTA's `tempty`.  In a pair
+// whose second m-tile does not exist (an expert with an odd number of
+// m-tiles), the odd CTA loads a repeat of the first tile and stores nothing.
+//
+// Roles per CTA: warp 0 TMA producer, warp 1 TMEM allocation for the pair
+// (and, in the even CTA, the MMA issuer), warps 2..5 epilogue.  All waits
+// are bounded.  Cluster barriers after set-up (every barrier of the pair
+// exists before any remote signal) and before the TMEM release (no remote
+// arrive or tensor-memory read is still outstanding).
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -27,42 +32,49 @@
 namespace cbmoe {
 namespace {
 
-constexpr int BM = kTileM;
+constexpr int BM = kTileM;  // rows per CTA
 constexpr int BK = 64;
 constexpr int BN = 256;
 constexpr int HALF_ROWS = BN / 2;
-constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;
-constexpr int B_BYTES = BN * BK * 2;
-constexpr int HALF_B_BYTES = B_BYTES / 2;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int BH_BYTES = HALF_ROWS * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + BH_BYTES;  // per CTA
 constexpr int THREADS = 192;
+constexpr int EPI_WARPS = 4;
 constexpr uint32_t TMEM_COLS = 2 * BN;
-constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+constexpr uint32_t IDESC = idesc_bf16_f32(2 * BM, BN);
 constexpr uint16_t PAIR_MASK = 0x3;
-constexpr int STG_BYTES = 4 * 2 * 32 * 128;
+constexpr int STG_BYTES = EPI_WARPS * 2 * 32 * 128;
 
+// Ring of A stages then weight-half stages; behind the ring the down
+// kernel's store staging, or for gate/up an unused tile, so that an operand
+// read of a full 256-row tile at the last stage would still fall inside the
+// CTA's shared memory.
 template <int KIND>
-struct Smem {
+struct Cfg {
+  static constexpr int STAGES = 6;
   static constexpr int RING = STAGES * STAGE_BYTES;
-  static constexpr int STAGING = KIND == kDownF32 ? STG_BYTES : 0;
+  static constexpr int STAGING = KIND == kDownF32 ? STG_BYTES : BH_BYTES;
   static constexpr int BYTES = RING + STAGING + 1024 + 256;
 };
+static_assert(Cfg<kGateUpSwiGLU>::BYTES <= 232448 && Cfg<kDownF32>::BYTES <= 232448, "shared memory per CTA");
 
-struct MyTile {
+struct PairTile {
   int m_tile;  // this CTA's m-tile (a repeat of the pair's first when !valid)
   bool valid;
   int e;
   int n;
 };
 
-__device__ __forceinline__ MyTile decode_pair_tile(int tile, const GemmArgs& p, int rank) {
+// Tile index -> (expert, N tile, pair); consecutive clusters take the pairs
+// of one expert against the same weight tile.
+__device__ __forceinline__ PairTile decode_pair_tile(int tile, const GemmArgs& p, int rank) {
   const int e = p.ptile_expert[tile / p.n_tiles];
   const int base = p.ptile_off[e];
   const int np = p.ptile_off[e + 1] - base;
   const int local = tile - base * p.n_tiles;
   const int pair = local % np;
-  MyTile t;
+  PairTile t;
   t.e = e;
   t.n = local / np;
   const int mt_e = p.mtile_off[e + 1] - p.mtile_off[e];
@@ -81,14 +93,16 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 template <int KIND>
 __global__ void __launch_bounds__(THREADS, 1)
-    grouped_gemm_mc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_bh,
-                           const __grid_constant__ CUtensorMap tm_out, const GemmArgs p) {
+    grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_bh,
+                             const __grid_constant__ CUtensorMap tm_out, const GemmArgs p) {
+  using C = Cfg<KIND>;
+  constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sa = smem;
   uint8_t* sb = smem + STAGES * A_BYTES;
-  uint8_t* staging = smem + Smem<KIND>::RING;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Smem<KIND>::RING + Smem<KIND>::STAGING);
+  uint8_t* staging = smem + C::RING;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::RING + C::STAGING);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
@@ -96,15 +110,16 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int rank = static_cast<int>(cluster_ctarank());
+  const bool even = rank == 0;
   const int cluster = blockIdx.x / 2, n_clusters = gridDim.x / 2;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 2);  // both CTAs' MMAs release a stage
+      mbar_init(&full[s], 1);  // used in the even CTA: its producer's arrive + both CTAs' bytes
+      mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 128);
+      mbar_init(&tempty[a], 2 * EPI_WARPS);  // used in the even CTA
     }
     fence_barrier_init();
     prefetch_tensormap(&tm_a);
@@ -112,8 +127,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (KIND == kDownF32) prefetch_tensormap(&tm_out);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc_pair(tmem_slot, TMEM_COLS);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
   __syncthreads();
@@ -124,10 +139,11 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (warp == 0) {
     if (lane == 0) {
+      const uint32_t full_even = mapa_shared(smem_u32(full), 0);
       int64_t issued = 0;
       bool ok = true;
       for (int tile = cluster; ok && tile < total_tiles; tile += n_clusters) {
-        const MyTile t = decode_pair_tile(tile, p, rank);
+        const PairTile t = decode_pair_tile(tile, p, rank);
         const int a_row = t.m_tile * BM;
         const int b_row = t.e * p.b_rows_per_expert + t.n * BN + rank * HALF_ROWS;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
@@ -138,26 +154,31 @@ __global__ void __launch_bounds__(THREADS, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
-          tma_load_2d(sa + stage * A_BYTES, &tm_a, &full[stage], kb * BK, a_row);
-          tma_load_2d_multicast(sb + stage * B_BYTES + rank * HALF_B_BYTES, &tm_bh, &full[stage], kb * BK, b_row,
-                                PAIR_MASK);
+          if (even) mbar_arrive_expect_tx(&full[stage], 2 * STAGE_BYTES);
+          const uint32_t bar = full_even + static_cast<uint32_t>(stage * 8);
+          tma_load_2d_pair(sa + stage * A_BYTES, &tm_a, bar, kb * BK, a_row);
+          tma_load_2d_pair(sb + stage * BH_BYTES, &tm_bh, bar, kb * BK, b_row);
           ++issued;
         }
       }
-      for (int64_t i = (issued > STAGES ? issued - STAGES : 0); i < issued; ++i)
-        if (!mbar_wait(&full[i % STAGES], static_cast<uint32_t>((i / STAGES) & 1), p.wait_limit_ns))
-          set_error(p.err, kErrTimeout);
+      // The even CTA's full barriers count both CTAs' bytes, so waiting on
+      // its last phases covers the odd CTA's loads in flight too.
+      if (even)
+        for (int64_t i = (issued > STAGES ? issued - STAGES : 0); i < issued; ++i)
+          if (!mbar_wait(&full[i % STAGES], static_cast<uint32_t>((i / STAGES) & 1), p.wait_limit_ns)) {
+            set_error(p.err, kErrTimeout);
+            break;
+          }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (even && lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int tile = cluster; ok && tile < total_tiles; tile += n_clusters) {
-        if (!mbar_wait(&tempty[acc], p.test_stall ? acc_phase : acc_phase ^ 1u, p.wait_limit_ns)) {
+        if (!mbar_wait_cluster(&tempty[acc], p.test_stall ? acc_phase : acc_phase ^ 1u, p.wait_limit_ns)) {
           set_error(p.err, kErrTimeout);
           break;
         }
@@ -171,18 +192,18 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           tc_fence_after();
           const uint64_t adesc = sw128_desc(smem_u32(sa + stage * A_BYTES));
-          const uint64_t bdesc = sw128_desc(smem_u32(sb + stage * B_BYTES));
+          const uint64_t bdesc = sw128_desc(smem_u32(sb + stage * BH_BYTES));
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
-            tc_mma_f16(d_tmem, adesc + 2 * k, bdesc + 2 * k, IDESC, (kb | k) != 0 ? 1u : 0u);
-          tc_commit_multicast(&empty[stage], PAIR_MASK);
+            tc_mma_f16_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, IDESC, (kb | k) != 0 ? 1u : 0u);
+          tc_commit_pair_multicast(&empty[stage], PAIR_MASK);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        tc_commit(&tfull[acc]);
+        tc_commit_pair_multicast(&tfull[acc], PAIR_MASK);
         if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1u;
@@ -191,11 +212,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else {
     const int q = warp & 3;
+    const uint32_t tempty_even = mapa_shared(smem_u32(tempty), 0);
     int acc = 0;
     uint32_t acc_phase = 0;
     int n_stores = 0;
     for (int tile = cluster; tile < total_tiles; tile += n_clusters) {
-      const MyTile t = decode_pair_tile(tile, p, rank);
+      const PairTile t = decode_pair_tile(tile, p, rank);
       if (!mbar_wait(&tfull[acc], acc_phase, p.wait_limit_ns)) {
         set_error(p.err, kErrTimeout);
         break;
@@ -247,7 +269,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(&tempty[acc]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(tempty_even + static_cast<uint32_t>(acc * 8));
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;
@@ -256,48 +279,45 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (KIND == kDownF32 && lane == 0) bulk_wait_group<0>();
   }
 
+  __syncwarp();
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
   }
-  cluster_sync();
+}
+
+template <int KIND>
+cudaLaunchConfig_t pair_config(int grid, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.dynamicSmemBytes = Cfg<KIND>::BYTES;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
 }
 
 template <int KIND>
 cudaError_t launch_kind(const CUtensorMap& tm_a, const CUtensorMap& tm_bh, const CUtensorMap& tm_out,
-                        const GemmArgs& a, int grid, cudaStream_t s) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid, 1, 1);
-  cfg.blockDim = dim3(THREADS, 1, 1);
-  cfg.dynamicSmemBytes = Smem<KIND>::BYTES;
-  cfg.stream = s;
+                        const GemmArgs& a, cudaStream_t s) {
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, grouped_gemm_mc_kernel<KIND>, tm_a, tm_bh, tm_out, a);
+  cudaLaunchConfig_t cfg = pair_config<KIND>(a.grid, attr);
+  cfg.stream = s;
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<KIND>, tm_a, tm_bh, tm_out, a);
 }
 
 template <int KIND>
 int max_pairs(int num_sms) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
-  cfg.blockDim = dim3(THREADS, 1, 1);
-  cfg.dynamicSmemBytes = Smem<KIND>::BYTES;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cudaLaunchConfig_t cfg = pair_config<KIND>(2 * (num_sms / 2), attr);
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_mc_kernel<KIND>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_pair_kernel<KIND>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -306,23 +326,23 @@ int max_pairs(int num_sms) {
 
 }  // namespace
 
-cudaError_t grouped_gemm_mc_prepare(int num_sms, int* grid_gateup, int* grid_down) {
-  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_mc_kernel<kGateUpSwiGLU>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<kGateUpSwiGLU>::BYTES);
+cudaError_t grouped_gemm_pair_prepare(int num_sms, int* grid_gateup, int* grid_down) {
+  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_pair_kernel<kGateUpSwiGLU>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<kGateUpSwiGLU>::BYTES);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(grouped_gemm_mc_kernel<kDownF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Smem<kDownF32>::BYTES);
+    e = cudaFuncSetAttribute(grouped_gemm_pair_kernel<kDownF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg<kDownF32>::BYTES);
   if (e != cudaSuccess) return e;
   *grid_gateup = 2 * max_pairs<kGateUpSwiGLU>(num_sms);
   *grid_down = 2 * max_pairs<kDownF32>(num_sms);
   return cudaSuccess;
 }
 
-cudaError_t launch_grouped_gemm_mc(GemmKind kind, const CUtensorMap& tm_a, const CUtensorMap& tm_bh,
-                                   const CUtensorMap& tm_out, const GemmArgs& a, cudaStream_t s) {
-  if (a.grid < 2) return cudaErrorInvalidConfiguration;
-  if (kind == kGateUpSwiGLU) return launch_kind<kGateUpSwiGLU>(tm_a, tm_bh, tm_out, a, a.grid, s);
-  return launch_kind<kDownF32>(tm_a, tm_bh, tm_out, a, a.grid, s);
+cudaError_t launch_grouped_gemm_pair(GemmKind kind, const CUtensorMap& tm_a, const CUtensorMap& tm_bh,
+                                     const CUtensorMap& tm_out, const GemmArgs& a, cudaStream_t s) {
+  if (a.grid < 2 || (a.grid & 1)) return cudaErrorInvalidConfiguration;
+  if (kind == kGateUpSwiGLU) return launch_kind<kGateUpSwiGLU>(tm_a, tm_bh, tm_out, a, s);
+  return launch_kind<kDownF32>(tm_a, tm_bh, tm_out, a, s);
 }
 
 }  // namespace cbmoe

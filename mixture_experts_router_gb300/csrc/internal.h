@@ -85,7 +85,7 @@ cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s);
 struct GemmArgs {
   const int32_t* mtile_off;     // [E+1]
   const int32_t* mtile_expert;  // [max_mtiles]
-  const int32_t* ptile_off;     // [E+1] m-tile pairs (int8 kernels)
+  const int32_t* ptile_off;     // [E+1] m-tile pairs (int8 and pair kernels)
   const int32_t* ptile_expert;  // [max_mtiles]
   int32_t E;
   int32_t n_tiles;              // N tiles per expert
@@ -116,12 +116,13 @@ cudaError_t launch_grouped_gemm(GemmKind kind, bool int8_weights, const CUtensor
                                 const GemmArgs& a, cudaStream_t s);
 cudaError_t grouped_gemm_prepare();  // one-time function attributes
 int grouped_gemm_tile_n(GemmKind kind);  // output columns per tile
-// bf16 on CTA pairs sharing each weight tile by TMA multicast: tm_bh is the
-// weight tensor with a 128-row box (half a tile); tiles are m-tile pairs.
-// prepare returns the persistent grids (2 x co-resident clusters, 0 if none)
-cudaError_t launch_grouped_gemm_mc(GemmKind kind, const CUtensorMap& tm_a, const CUtensorMap& tm_bh,
-                                   const CUtensorMap& tm_out, const GemmArgs& a, cudaStream_t s);
-cudaError_t grouped_gemm_mc_prepare(int num_sms, int* grid_gateup, int* grid_down);
+// bf16 on CTA pairs with the 2-SM MMA (M = 256 over m-tiles 2p, 2p+1 of one
+// expert): tm_bh is the weight tensor with a 128-row box (each CTA's half of
+// a 256-row tile); prepare returns the persistent grids (2 x co-resident
+// clusters, 0 if none)
+cudaError_t launch_grouped_gemm_pair(GemmKind kind, const CUtensorMap& tm_a, const CUtensorMap& tm_bh,
+                                     const CUtensorMap& tm_out, const GemmArgs& a, cudaStream_t s);
+cudaError_t grouped_gemm_pair_prepare(int num_sms, int* grid_gateup, int* grid_down);
 // int8 weights: tiles are pairs of m-tiles against 128 weight rows
 cudaError_t launch_grouped_gemm_int8(GemmKind kind, const CUtensorMap& tm_a, const CUtensorMap& tm_b,
                                      const CUtensorMap& tm_out, const GemmArgs& a, cudaStream_t s);

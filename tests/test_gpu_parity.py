@@ -220,3 +220,39 @@ def test_graph_replay_matches_direct_launches():
         if timed is not None:
             timed.close()
         gl.close()
+
+
+PAIR_SMALL = ["tiny", "ragged_mid", "one_expert", "k_equals_E", "skewed_small", "e256_k16", "odd_T"]
+
+
+@pytest.mark.parametrize("name", PAIR_SMALL)
+def test_pair_mma_path_small(name, monkeypatch):
+    """CB_MOE_PAIR=1: bf16 expert GEMMs on CTA pairs with the 2-SM MMA
+    (M = 256 over two m-tiles of one expert); odd m-tile counts leave the
+    second CTA of a pair without rows to store."""
+    monkeypatch.setenv("CB_MOE_PAIR", "1")
+    rep = gh.full_check(synth.make_layer(SMALL[name]))
+    print(name, "pair", rep)
+
+
+@pytest.mark.parametrize("name", ["mixtral_prefill", "skewed", "mixtral_decode"])
+def test_pair_mma_path_full_size(name, monkeypatch):
+    monkeypatch.setenv("CB_MOE_PAIR", "1")
+    rep = gh.full_check(synth.make_layer(synth.WORKLOADS[name]), sample=FULL[name])
+    print(name, "pair", rep)
+
+
+def test_pair_mma_path_timeout(monkeypatch):
+    import mixture_experts_router_gb300 as cb
+    monkeypatch.setenv("CB_MOE_PAIR", "1")
+    shape = synth.custom_shape("stall_pair", T=300, d=512, f=512, E=8, k=2, seed=52)
+    layer = synth.make_layer(shape)
+    gl = gh.GpuLayer(layer, flags=cb.CB_FLAG_TEST_STALL)
+    try:
+        gl.m.forward(gl.x, gl.out)
+        torch.cuda.synchronize()
+        assert gl.m.last_error() == cb.CB_ERR_TIMEOUT
+    finally:
+        gl.close()
+    rep = gh.full_check(layer)
+    assert rep["f32_max_abs"] <= gh.MAX_ABS
