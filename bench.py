@@ -34,14 +34,6 @@ sys.path.insert(0, ROOT)
 
 METRIC = "MoE-layer tokens/s; grouped-GEMM % of bf16 TC peak; decode weight GB/s % HBM"
 DEFAULT_WORKLOAD = "mixtral_prefill"
-SMALL_DISPATCH_PAIRS = 16384   # up to this many (token, slot) pairs the dispatch is one fused block
-
-
-def kernels_per_forward(shape) -> int:
-    """Kernels one forward launches: router, dispatch (fused block + row copy,
-    or count/scan/scatter + row copy), the two grouped GEMMs, combine."""
-    dispatch = 2 if shape.T * shape.k <= SMALL_DISPATCH_PAIRS else 4
-    return 1 + dispatch + 2 + 1
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 GEMM_SOURCES = [os.path.join(ROOT, "mixture_experts_router_gb300", "csrc", n)
                 for n in ("grouped_gemm.cu", "grouped_gemm_pair.cu")]
@@ -293,6 +285,7 @@ def run_ours(args):
     m = cb.MoELayer(shape.T, shape.d, shape.f, shape.E, shape.k, w["wr"], w["wg"], w["wu"], w["wd"],
                     router_bias=w["bias"], s_gate=w["sg"], s_up=w["su"], s_down=w["sd"], device=local,
                     stage_timing=True)
+    launches_per_forward = m.kernels_per_forward()
     del w
     torch.cuda.empty_cache()
     x = dev(layer.x)
@@ -428,7 +421,7 @@ def run_ours(args):
         "e2e": {"value": shape.T * world * k2 / (e2e_ms / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": shape.T * shape.d * 2, "d2h_bytes_per_step": shape.T * shape.d * 2,
                 "steps": k2, "api": "cb_moe_forward_host (pinned host x and out, copies on the stream)"},
-        "gpu_launches": kernels_per_forward(shape) * args.steps,
+        "gpu_launches": launches_per_forward * args.steps,
         "roofline": roof,
         "stages": stages,
         "expert_rows": {"active_experts": sum(1 for c in counts if c > 0), "max_rows": max(counts),

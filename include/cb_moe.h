@@ -195,6 +195,11 @@ CB_API cb_status_t cb_moe_dispatch_noalloc(const int32_t *ids, int32_t n_tokens,
                                            int32_t *counts, int32_t *offsets, int32_t *tok, int32_t *inv,
                                            int32_t *status, void *stream);
 
+/* Number of kernels one forward of this handle launches (router, dispatch
+ * kernels, the two grouped GEMMs, combine), fixed at init by the shapes and
+ * the kernel choices made there.  Returns CB_ERR_INVALID_ARG on NULL. */
+CB_API cb_status_t cb_moe_kernels_per_forward(const cb_moe_t *h, int32_t *n);
+
 /* Bytes of device memory a handle with this config holds (weights + workspace). */
 CB_API cb_status_t cb_moe_device_bytes(const cb_moe_config_t *cfg, uint64_t *bytes);
 

@@ -25,7 +25,7 @@ STAGE_NAMES = ("router", "dispatch", "gateup_gemm", "down_gemm", "combine")
 # every symbol include/cb_moe.h declares
 ABI_SYMBOLS = ("cb_moe_init", "cb_moe_forward", "cb_moe_forward_f32out", "cb_moe_forward_host",
                "cb_moe_routing", "cb_moe_stage_times", "cb_moe_last_error", "cb_moe_device_bytes",
-               "cb_moe_free", "cb_status_string", "cb_moe_dispatch_noalloc")
+               "cb_moe_free", "cb_status_string", "cb_moe_dispatch_noalloc", "cb_moe_kernels_per_forward")
 
 
 class cb_moe_config_t(ctypes.Structure):
@@ -74,12 +74,13 @@ def load_library(path: str = LIB_PATH):
     lib.cb_moe_last_error.argtypes = [vp]
     lib.cb_moe_device_bytes.argtypes = [ctypes.POINTER(cb_moe_config_t), ctypes.POINTER(ctypes.c_uint64)]
     lib.cb_moe_free.argtypes = [vp]
+    lib.cb_moe_kernels_per_forward.argtypes = [vp, ctypes.POINTER(i32)]
     lib.cb_moe_dispatch_noalloc.argtypes = [vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, vp, vp, vp, vp,
                                             vp, vp]
     lib.cb_moe_dispatch_noalloc.restype = i32
     for name in ("cb_moe_init", "cb_moe_forward", "cb_moe_forward_f32out", "cb_moe_forward_host",
                  "cb_moe_routing", "cb_moe_stage_times", "cb_moe_last_error", "cb_moe_device_bytes",
-                 "cb_moe_free"):
+                 "cb_moe_free", "cb_moe_kernels_per_forward"):
         getattr(lib, name).restype = i32
     lib.cb_status_string.argtypes = [i32]
     lib.cb_status_string.restype = ctypes.c_char_p
@@ -132,6 +133,12 @@ def cb_moe_device_bytes(cfg: cb_moe_config_t):
     b = ctypes.c_uint64()
     st = load_library().cb_moe_device_bytes(ctypes.byref(cfg), ctypes.byref(b))
     return st, b.value
+
+
+def cb_moe_kernels_per_forward(handle):
+    n = ctypes.c_int32()
+    st = load_library().cb_moe_kernels_per_forward(handle, ctypes.byref(n))
+    return st, n.value
 
 
 def cb_moe_free(handle) -> int:
@@ -228,6 +235,12 @@ class MoELayer:
 
     def last_error(self) -> int:
         return cb_moe_last_error(self.handle)
+
+    def kernels_per_forward(self) -> int:
+        st, n = cb_moe_kernels_per_forward(self.handle)
+        if st != CB_OK:
+            raise CbMoeError(st, "cb_moe_kernels_per_forward")
+        return n
 
     def close(self):
         if getattr(self, "handle", None) is not None:

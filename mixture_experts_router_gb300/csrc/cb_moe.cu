@@ -48,6 +48,8 @@ struct cb_moe {
   bool router_tc;          // tcgen05 router (else the mma.sync router)
   bool use_graphs;         // replay each forward variant from a captured CUDA graph
   bool pair_gu, pair_dn;   // bf16 gate/up, down GEMMs on CTA pairs (2-SM MMA)
+  int32_t rank_block;      // > 0: the router ranks pairs in blocks of this many tokens
+  int32_t n_rank_blocks;
   int pair_grid_gu, pair_grid_dn;
   struct GraphSlot {
     const void* a;
@@ -99,7 +101,9 @@ Layout plan(const cb_moe_config_t& c) {
   L.off_ids = take(M * 4);
   L.off_w = take(M * 4);
   L.off_logits = take((c.flags & CB_FLAG_KEEP_LOGITS) ? T * E * 4 : 0);
-  L.off_chunk = take(static_cast<uint64_t>(L.n_chunks) * E * 4);
+  // per-chunk counts of the dispatch's own ranking, or the router's per-block
+  // counts of the fused ranking (at most kFusedScanWords)
+  L.off_chunk = take(std::max<uint64_t>(static_cast<uint64_t>(L.n_chunks) * E, kFusedScanWords) * 4);
   L.off_counts = take(E * 4);
   L.off_offsets = take((E + 1) * 4);
   L.off_mtile_off = take((E + 1) * 4);
@@ -203,6 +207,10 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
   ra.w = h->w;
   ra.logits = h->logits;
   ra.err = h->err;
+  if (h->rank_block > 0) {
+    ra.blk_counts = h->chunk;
+    ra.local_rank = h->inv;
+  }
   if (h->router_tc) {
     if (h->tm_x_src != x) {
       if (!make_tmap(&h->tm_x, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c.d_model, c.n_tokens, 64, 128))
@@ -236,6 +244,8 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
   da.gather_blocks = static_cast<int32_t>(std::min<int64_t>(h->num_sms * 8, (c.n_tokens + 7) / 8));
   da.copy_rows = h->gather_a ? 0 : 1;
   da.err = h->err;
+  da.rank_block = h->rank_block;
+  da.n_rank_blocks = h->n_rank_blocks;
   if (launch_dispatch(da, s) != cudaSuccess || !mark(2)) return CB_ERR_CUDA;
 
   const bool int8w = c.wdtype == CB_W_INT8;
@@ -396,6 +406,22 @@ const char* cb_status_string(cb_status_t s) {
   return "unknown status";
 }
 
+cb_status_t cb_moe_kernels_per_forward(const cb_moe_t* h, int32_t* n) {
+  if (h == nullptr || n == nullptr) return CB_ERR_INVALID_ARG;
+  const cb_moe_config_t& c = h->cfg;
+  if (c.n_tokens == 0) {  // a forward of no tokens launches nothing
+    *n = 0;
+    return CB_OK;
+  }
+  int32_t dispatch;
+  if (h->rank_block > 0)
+    dispatch = 2;  // block-count scan + row copy (which also finalises the ranks)
+  else
+    dispatch = (static_cast<int64_t>(c.n_tokens) * c.top_k <= kDispatchSmallPairs ? 1 : 3) + (h->gather_a ? 0 : 1);
+  *n = 1 + dispatch + 2 + 1;
+  return CB_OK;
+}
+
 cb_status_t cb_moe_device_bytes(const cb_moe_config_t* cfg, uint64_t* bytes) {
   if (bytes == nullptr) return CB_ERR_INVALID_ARG;
   const cb_status_t st = validate_config(cfg);
@@ -500,7 +526,7 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
     ok = ok && make_tmap(&h->tm_b_dn128, h->wd, wdt, eb, f, E * d, 64, 128, wsw);
   }
   ok = ok && grouped_gemm_prepare() == cudaSuccess && grouped_gemm_int8_prepare() == cudaSuccess &&
-       router_prepare() == cudaSuccess && router_tc_prepare() == cudaSuccess;
+       router_prepare() == cudaSuccess && router_tc_prepare() == cudaSuccess && dispatch_prepare() == cudaSuccess;
   // router: tcgen05 for wide expert counts, the mma.sync split-K router for
   // E <= 16 (bound by reading x, where more CTAs help); CB_MOE_ROUTER=tc|mma
   // overrides the choice
@@ -537,6 +563,23 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
     // forwards replay captured CUDA graphs unless CB_MOE_GRAPHS=0
     const char* grv = std::getenv("CB_MOE_GRAPHS");
     h->use_graphs = !(grv != nullptr && std::strcmp(grv, "0") == 0);
+    // With the mma router, each router block ranks its routed pairs while the
+    // ids are at hand, and one small scan of the per-block counts replaces the
+    // dispatch's own counting passes, when those counts fit the scan's shared
+    // memory.  (Measured on GB300: router + dispatch 44.6 vs 47.9 us at the
+    // Mixtral prefill layer.  In the tcgen05 router the per-expert ballots
+    // cost more than they save: +10 us on the 128-expert layer, so it is not
+    // built there.)  CB_MOE_FUSED_RANKS=0 keeps the dispatch's ranking.
+    const char* fv = std::getenv("CB_MOE_FUSED_RANKS");
+    const int rb = router_rank_block(cfg->n_experts);
+    const int64_t nb = (static_cast<int64_t>(cfg->n_tokens) + rb - 1) / rb;
+    h->rank_block = 0;
+    h->n_rank_blocks = 0;
+    if (!h->router_tc && (nb + 1) * (cfg->n_experts + 1) <= kFusedScanWords &&
+        !(fv != nullptr && std::strcmp(fv, "0") == 0)) {
+      h->rank_block = rb;
+      h->n_rank_blocks = static_cast<int32_t>(nb);
+    }
   }
   ok = ok && make_tmap(&h->tm_wr, h->wr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, E, 64,
                        static_cast<uint32_t>(router_tc_rows(cfg->n_experts)));

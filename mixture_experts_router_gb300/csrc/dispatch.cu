@@ -14,7 +14,12 @@
 //                      tile -> expert map used by the grouped GEMMs
 //   dispatch_scatter : per chunk: warp-aggregated ranks -> tok[], inv[]
 //   dispatch_small   : the three above in one block, for small T*k
-//   dispatch_copy    : each token's row of x into its k rows of Xp
+//   dispatch_scan_blocks : when the router already ranked each pair inside
+//                      its block of tokens: one block scans the per-block
+//                      counts (all of them staged in shared memory at once)
+//                      into per-block row bases, totals, offsets and tiles
+//   dispatch_copy    : each token's row of x into its k rows of Xp (and,
+//                      after dispatch_scan_blocks, the global ranks: inv, tok)
 #include "internal.h"
 
 namespace cbmoe {
@@ -23,7 +28,6 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kPerWarp = kDispatchChunk / kWarps;  // 256 pairs, 8 rounds of 32
-constexpr int64_t kSmallM = 16384;  // T*k handled by the one-block kernel
 
 __global__ void __launch_bounds__(kThreads) dispatch_count(DispatchArgs a) {
   __shared__ int hist[256];
@@ -159,7 +163,7 @@ __global__ void __launch_bounds__(kThreads) dispatch_scatter(DispatchArgs a) {
   }
 }
 
-// Count, scan and ranks in one 1024-thread block, for T*k <= kSmallM: the
+// Count, scan and ranks in one 1024-thread block, for T*k <= kDispatchSmallPairs: the
 // 32 warps take consecutive runs of the flat (token, slot) pairs, so the
 // warp-aggregated ranks come out in token order exactly as in the chunked
 // kernels above.
@@ -238,6 +242,75 @@ __global__ void __launch_bounds__(kSmallThreads) dispatch_small(DispatchArgs a) 
   }
 }
 
+constexpr int kScanThreads = 1024;
+constexpr int kScanWarps = kScanThreads / 32;
+
+// Per-expert totals -> counts, offsets, the 128-row tile prefix (and pairs)
+// with their tile -> expert maps; thread e of the block handles expert e.
+// Returns offsets[e] (0 for threads past E).  All threads must call it.
+__device__ int publish_totals(const DispatchArgs& a, int total, int* tmp) {
+  const int e = threadIdx.x;
+  const int mt = (total + kTileM - 1) / kTileM;
+  const int pt = (mt + 1) / 2;
+  const int off = block_exclusive_scan<kScanWarps>(e < a.E ? total : 0, tmp);
+  const int moff = block_exclusive_scan<kScanWarps>(e < a.E ? mt : 0, tmp);
+  const int poff = block_exclusive_scan<kScanWarps>(e < a.E ? pt : 0, tmp);
+  if (e < a.E) {
+    a.counts[e] = total;
+    a.offsets[e] = off;
+    a.mtile_off[e] = moff;
+    if (e == a.E - 1) {
+      a.offsets[a.E] = off + total;
+      a.mtile_off[a.E] = moff + mt;
+      if (moff + mt > a.max_mtiles) set_error(a.err, kErrDevice);
+    }
+    for (int i = moff; i < moff + mt && i < a.max_mtiles; ++i) a.mtile_expert[i] = e;
+    if (a.ptile_off != nullptr) {
+      a.ptile_off[e] = poff;
+      if (e == a.E - 1) a.ptile_off[a.E] = poff + pt;
+      for (int i = poff; i < poff + pt && i < a.max_mtiles; ++i) a.ptile_expert[i] = e;
+    }
+  }
+  return e < a.E ? off : 0;
+}
+
+// chunk[b][e] holds rank block b's count of expert e; it becomes the global
+// rank of the block's first pair of e: offsets[e] + sum_{b' < b} chunk[b'][e].
+// Shared memory: (n_rank_blocks + 1) rows of E + 1 counts (the odd row
+// length keeps the per-expert column walk free of bank conflicts; the last
+// row holds the totals).
+__global__ void __launch_bounds__(kScanThreads) dispatch_scan_blocks(DispatchArgs a) {
+  extern __shared__ int sc[];
+  __shared__ int tmp[kScanWarps];
+  __shared__ int s_off[256];
+  const int nb = a.n_rank_blocks, E = a.E, ld = E + 1;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  for (int i = threadIdx.x; i < nb * E; i += kScanThreads) sc[(i / E) * ld + i % E] = a.chunk[i];
+  __syncthreads();
+  for (int e = warp; e < E; e += kScanWarps) {
+    int carry = 0;
+    for (int b0 = 0; b0 < nb; b0 += 32) {
+      const int b = b0 + lane;
+      const int v = b < nb ? sc[b * ld + e] : 0;
+      int x = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (b < nb) sc[b * ld + e] = carry + x - v;
+      carry += __shfl_sync(0xffffffffu, x, 31);
+    }
+    if (lane == 0) sc[nb * ld + e] = carry;
+  }
+  __syncthreads();
+  const int total = threadIdx.x < E ? sc[nb * ld + threadIdx.x] : 0;
+  const int off = publish_totals(a, total, tmp);
+  if (threadIdx.x < E) s_off[threadIdx.x] = off;
+  __syncthreads();
+  for (int i = threadIdx.x; i < nb * E; i += kScanThreads) a.chunk[i] = sc[(i / E) * ld + i % E] + s_off[i % E];
+}
+
 // Row copy into the expert-grouped layout, token-major: one warp per token
 // reads its row of x once (16-byte vectors, eight in flight per lane) and
 // writes it to its k padded rows, row(t, s) = 128 tile_off[e] + inv - off[e].
@@ -247,17 +320,28 @@ __global__ void __launch_bounds__(kThreads) dispatch_copy(DispatchArgs a) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int vec_per_row = a.d / 8;
   const int64_t rows = static_cast<int64_t>(a.max_mtiles) * kTileM;
+  const int64_t M = static_cast<int64_t>(a.T) * a.k;
   for (int t = blockIdx.x * kWarps + warp; t < a.T; t += gridDim.x * kWarps) {
     int64_t dst_row = -1;
     if (lane < a.k) {
-      const int e = a.ids[static_cast<int64_t>(t) * a.k + lane];
-      const int r = a.inv[static_cast<int64_t>(t) * a.k + lane];
+      const int64_t p = static_cast<int64_t>(t) * a.k + lane;
+      const int e = a.ids[p];
+      int r = a.inv[p];
+      if (a.rank_block > 0 && e >= 0 && e < a.E) {
+        r += a.chunk[static_cast<int64_t>(t / a.rank_block) * a.E + e];
+        a.inv[p] = r;
+        if (r >= 0 && r < M)
+          a.tok[r] = t;
+        else
+          set_error(a.err, kErrDevice);
+      }
       if (e >= 0 && e < a.E) dst_row = static_cast<int64_t>(a.mtile_off[e]) * kTileM + (r - a.offsets[e]);
       if (dst_row < 0 || dst_row >= rows) {
         set_error(a.err, kErrDevice);
         dst_row = -1;
       }
     }
+    if (!a.copy_rows) continue;
     const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<int64_t>(t) * a.d);
     for (int v0 = 0; v0 < vec_per_row; v0 += 32 * 8) {
       uint4 buf[8];
@@ -290,9 +374,21 @@ cudaError_t launch_dispatch_ranks(const DispatchArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+cudaError_t dispatch_prepare() {
+  return cudaFuncSetAttribute(dispatch_scan_blocks, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kFusedScanWords * 4);
+}
+
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s) {
   if (a.n_chunks <= 0) return cudaSuccess;
-  if (static_cast<int64_t>(a.T) * a.k <= kSmallM) {
+  if (a.rank_block > 0) {
+    const int words = (a.n_rank_blocks + 1) * (a.E + 1);
+    if (words > kFusedScanWords || a.E > 256) return cudaErrorInvalidValue;
+    dispatch_scan_blocks<<<1, kScanThreads, words * 4, s>>>(a);
+    dispatch_copy<<<a.gather_blocks, kThreads, 0, s>>>(a);
+    return cudaGetLastError();
+  }
+  if (static_cast<int64_t>(a.T) * a.k <= kDispatchSmallPairs) {
     dispatch_small<<<1, kSmallThreads, 0, s>>>(a);
   } else {
     dispatch_count<<<a.n_chunks, kThreads, 0, s>>>(a);

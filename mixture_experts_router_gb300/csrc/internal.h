@@ -31,7 +31,17 @@ struct RouterArgs {
   float* w;              // [T][k]
   float* logits;         // [T][E] or nullptr
   int* err;
+  // fused dispatch ranks (mma router; or nullptr): per block b of
+  // router_rank_block(E) tokens and
+  // expert e, blk_counts[b E + e] = the block's pairs routed to e, and per
+  // pair local_rank[t k + s] = its rank among the block's pairs of its expert
+  // in (token, slot) order
+  int32_t* blk_counts;
+  int32_t* local_rank;
 };
+// tokens per block of the mma router, each one rank block of the fused
+// dispatch ranks (the tcgen05 router leaves the ranking to the dispatch)
+int router_rank_block(int E);
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t s);
 cudaError_t router_prepare();  // one-time function attributes
 // tcgen05 router: x and Wr through TMA (tm_x: [T][d] box 64x128; tm_w: [E][d]
@@ -61,8 +71,17 @@ struct DispatchArgs {
   int32_t gather_blocks;  // blocks of the row copy
   int32_t copy_rows;      // 0: the GEMM gathers its rows from x itself, skip the copy
   int* err;
+  // > 0: the router already wrote per-block counts into chunk ([n_rank_blocks][E])
+  // and in-block ranks into inv; the dispatch scans the block counts and the
+  // row-copy kernel turns the ranks into global ones
+  int32_t rank_block;     // tokens per rank block
+  int32_t n_rank_blocks;
 };
 constexpr int kDispatchChunk = 2048;
+constexpr int64_t kDispatchSmallPairs = 16384;  // T*k ranked by the one-block kernel
+// the fused-rank scan holds (n_rank_blocks + 1) x (E + 1) counts in shared memory
+constexpr int kFusedScanWords = 49152;
+cudaError_t dispatch_prepare();  // one-time function attributes
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s);
 // histogram, prefix sums and ranks only (no row gather; x and xp unused)
 cudaError_t launch_dispatch_ranks(const DispatchArgs& a, cudaStream_t s);

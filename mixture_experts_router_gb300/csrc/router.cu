@@ -24,6 +24,7 @@
 #include <cuda_bf16.h>
 
 #include "internal.h"
+#include "route_ranks.cuh"
 
 namespace cbmoe {
 namespace {
@@ -71,6 +72,8 @@ __global__ void __launch_bounds__(RCfg<NT, KS, NS, MTB>::THREADS) router_mma_ker
   constexpr int NTW = C::NTW, EP = C::EP, TB = C::TB;
   constexpr int kThreads = C::THREADS, kWarps = C::WARPS;
   extern __shared__ float part[];  // [KS][TB][EP], then part[0] holds the logits
+  __shared__ int s_ids[TB * 16];   // the block's routing ids, for the fused dispatch ranks
+  __shared__ int s_cnt[256];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int g = lane >> 2, q = lane & 3;
   const int ks = warp % KS;
@@ -200,6 +203,32 @@ __global__ void __launch_bounds__(RCfg<NT, KS, NS, MTB>::THREADS) router_mma_ker
     if (lane < a.k) {
       a.ids[static_cast<int64_t>(t) * a.k + lane] = my_i;
       a.w[static_cast<int64_t>(t) * a.k + lane] = ex / sum;
+      s_ids[r * 16 + lane] = my_i;
+    }
+  }
+
+  // Fused dispatch ranks: this block is one rank block of TB tokens.  Warp 0
+  // takes its tokens 32 at a time in token order.
+  if (a.blk_counts != nullptr) {
+    __syncthreads();
+    if (warp == 0) {
+      for (int e = lane; e < a.E; e += 32) s_cnt[e] = 0;
+      __syncwarp();
+      for (int r0 = 0; r0 < TB; r0 += 32) {
+        const int r = r0 + lane, t = t_base + r;
+        const bool valid = r < TB && t < a.T;
+        int ids_l[16], rank[16];
+#pragma unroll
+        for (int s2 = 0; s2 < 16; ++s2) ids_l[s2] = (valid && s2 < a.k) ? s_ids[r * 16 + s2] : -1;
+        warp_expert_ranks<16>(ids_l, a.k, valid, a.E, s_cnt, rank);
+        if (valid) {
+#pragma unroll
+          for (int s2 = 0; s2 < 16; ++s2)
+            if (s2 < a.k) a.local_rank[static_cast<int64_t>(t) * a.k + s2] = rank[s2];
+        }
+      }
+      __syncwarp();
+      for (int e = lane; e < a.E; e += 32) a.blk_counts[static_cast<int64_t>(blockIdx.x) * a.E + e] = s_cnt[e];
     }
   }
 }
@@ -241,6 +270,14 @@ cudaError_t router_prepare() {
   CBMOE_ROUTER_CONFIGS(X)
 #undef X
   return e;
+}
+
+// tokens per block (16 MTB) of the configuration launch_router picks
+int router_rank_block(int E) {
+  const int nt = (E + 7) / 8;
+  if (nt <= 2) return 16;
+  if (nt <= 4) return 32;
+  return 64;
 }
 
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t s) {

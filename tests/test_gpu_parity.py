@@ -256,3 +256,37 @@ def test_pair_mma_path_timeout(monkeypatch):
         gl.close()
     rep = gh.full_check(layer)
     assert rep["f32_max_abs"] <= gh.MAX_ABS
+
+
+@pytest.mark.parametrize("name", ["tiny", "ragged_mid", "odd_T", "int8_mid"])
+def test_dispatch_own_ranking_small(name, monkeypatch):
+    """CB_MOE_FUSED_RANKS=0: the dispatch ranks the routed pairs itself
+    (one-block or count/scan/scatter kernels) instead of scanning the
+    router's per-block counts; same routing views and outputs."""
+    monkeypatch.setenv("CB_MOE_FUSED_RANKS", "0")
+    rep = gh.full_check(synth.make_layer(SMALL[name]))
+    print(name, "own ranking", rep)
+
+
+@pytest.mark.parametrize("name", ["mixtral_prefill", "mixtral_decode"])
+def test_dispatch_own_ranking_full_size(name, monkeypatch):
+    monkeypatch.setenv("CB_MOE_FUSED_RANKS", "0")
+    rep = gh.full_check(synth.make_layer(synth.WORKLOADS[name]), sample=FULL[name])
+    print(name, "own ranking", rep)
+
+
+@pytest.mark.parametrize("fused,name,expect", [
+    ("1", "mixtral_prefill", 6), ("1", "skewed", 8), ("0", "mixtral_prefill", 6), ("0", "skewed", 8)])
+def test_kernels_per_forward(fused, name, expect, monkeypatch):
+    """The launch count the library reports: router, dispatch kernels (block
+    scan + row copy after the mma router's ranks; or one-block /
+    count-scan-scatter ranking + row copy), two grouped GEMMs, combine."""
+    if fused == "0":
+        monkeypatch.setenv("CB_MOE_FUSED_RANKS", fused)
+    shp = synth.WORKLOADS[name]
+    gl = gh.GpuLayer(synth.make_layer(synth.custom_shape(name + "_n", T=shp.T, d=256, f=256, E=shp.E, k=shp.k,
+                                                         seed=61)))
+    try:
+        assert gl.m.kernels_per_forward() == expect
+    finally:
+        gl.close()
