@@ -34,6 +34,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "swiglu.cuh"
 
 namespace cbmoe {
 namespace {
@@ -109,13 +110,6 @@ __device__ __forceinline__ Work decode_work(int u, const GemmArgs& p, int full, 
   w.c = decode_tile(tile, p);
   w.col0 = w.c.n * BN + part * w.nsub;
   return w;
-}
-
-__device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&b);
 }
 
 template <int KIND>

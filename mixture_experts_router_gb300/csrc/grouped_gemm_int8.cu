@@ -32,6 +32,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "swiglu.cuh"
 
 namespace cbmoe {
 namespace {
@@ -79,13 +80,6 @@ __device__ __forceinline__ PairCoord decode_pair(int tile, const GemmArgs& p) {
   c.m0 = p.mtile_off[e] + 2 * pair;
   c.two = 2 * pair + 1 < mt_e;
   return c;
-}
-
-__device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&b);
 }
 
 // Four int8 codes (one 32-bit word) -> four bf16, exactly.  With m = q & 0x7F

@@ -28,6 +28,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "swiglu.cuh"
 
 namespace cbmoe {
 namespace {
@@ -82,13 +83,6 @@ __device__ __forceinline__ PairTile decode_pair_tile(int tile, const GemmArgs& p
   t.valid = idx < mt_e;
   t.m_tile = p.mtile_off[e] + (t.valid ? idx : 2 * pair);
   return t;
-}
-
-__device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&b);
 }
 
 template <int KIND>
