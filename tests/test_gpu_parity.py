@@ -290,3 +290,12 @@ def test_kernels_per_forward(fused, name, expect, monkeypatch):
         assert gl.m.kernels_per_forward() == expect
     finally:
         gl.close()
+
+
+@pytest.mark.parametrize("name", ["mixtral_prefill", "skewed"])
+def test_single_cta_gemms_full_size(name, monkeypatch):
+    """CB_MOE_PAIR=0: the 1-CTA grouped GEMMs (the default only for layers
+    whose experts average under two m-tiles) at the full prefill sizes."""
+    monkeypatch.setenv("CB_MOE_PAIR", "0")
+    rep = gh.full_check(synth.make_layer(synth.WORKLOADS[name]), sample=FULL[name])
+    print(name, "single CTA", rep)
