@@ -32,6 +32,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "int8_bf16.cuh"
 #include "swiglu.cuh"
 
 namespace cbmoe {
@@ -80,18 +81,6 @@ __device__ __forceinline__ PairCoord decode_pair(int tile, const GemmArgs& p) {
   c.m0 = p.mtile_off[e] + 2 * pair;
   c.two = 2 * pair + 1 < mt_e;
   return c;
-}
-
-// Four int8 codes (one 32-bit word) -> four bf16, exactly.  With m = q & 0x7F
-// and s = q & 0x80, the bf16 words 0x4300|m and 0x4300|s are 128 + m and
-// 128 (s = 0) or 256 (s = 0x80); their difference is m or m - 128, i.e. q,
-// an integer below 2^8 in magnitude, so the bf16 subtraction is exact.
-__device__ __forceinline__ void int8x4_to_bf16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  const uint32_t m = w & 0x7F7F7F7Fu, s = w & 0x80808080u;
-  const uint32_t m01 = __byte_perm(m, 0x43434343u, 0x4140), m23 = __byte_perm(m, 0x43434343u, 0x4342);
-  const uint32_t s01 = __byte_perm(s, 0x43434343u, 0x4140), s23 = __byte_perm(s, 0x43434343u, 0x4342);
-  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(lo) : "r"(m01), "r"(s01));
-  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(hi) : "r"(m23), "r"(s23));
 }
 
 template <int KIND>
@@ -341,18 +330,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint8_t* src = s8 + slot * I8_BYTES;
         uint8_t* dst = smem + stage * STAGE_BYTES + 2 * A_BYTES;
 #pragma unroll
-        for (int ch = xt; ch < BN * 4; ch += 32 * N_XFORM_WARPS) {
-          const int r = ch >> 2, c2 = 2 * (ch & 3);
-          const uint4 w = *reinterpret_cast<const uint4*>(src + ch * 16);
-          uint4 o0, o1;
-          int8x4_to_bf16x4(w.x, o0.x, o0.y);
-          int8x4_to_bf16x4(w.y, o0.z, o0.w);
-          int8x4_to_bf16x4(w.z, o1.x, o1.y);
-          int8x4_to_bf16x4(w.w, o1.z, o1.w);
-          uint8_t* row = dst + r * 128;
-          *reinterpret_cast<uint4*>(row + 16 * (c2 ^ (r & 7))) = o0;
-          *reinterpret_cast<uint4*>(row + 16 * ((c2 + 1) ^ (r & 7))) = o1;
-        }
+        for (int ch = xt; ch < BN * 4; ch += 32 * N_XFORM_WARPS) convert_chunk16(src + ch * 16, dst, ch >> 2, ch & 3);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {

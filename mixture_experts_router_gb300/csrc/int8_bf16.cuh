@@ -1,0 +1,35 @@
+// Exact int8 -> bf16 conversion of staged weight codes, shared by the int8
+// grouped GEMM kernels.
+#pragma once
+#include <cstdint>
+
+namespace cbmoe {
+
+// Four int8 codes (one 32-bit word) -> four bf16, exactly.  With m = q & 0x7F
+// and s = q & 0x80, the bf16 words 0x4300|m and 0x4300|s are 128 + m and
+// 128 (s = 0) or 256 (s = 0x80); their difference is m or m - 128, i.e. q,
+// an integer below 2^8 in magnitude, so the bf16 subtraction is exact.
+__device__ __forceinline__ void int8x4_to_bf16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t m = w & 0x7F7F7F7Fu, s = w & 0x80808080u;
+  const uint32_t m01 = __byte_perm(m, 0x43434343u, 0x4140), m23 = __byte_perm(m, 0x43434343u, 0x4342);
+  const uint32_t s01 = __byte_perm(s, 0x43434343u, 0x4140), s23 = __byte_perm(s, 0x43434343u, 0x4342);
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(lo) : "r"(m01), "r"(s01));
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(hi) : "r"(m23), "r"(s23));
+}
+
+// 16 staged int8 codes (K elements 16c..16c+15 of a weight row) -> the two
+// 16-byte bf16 chunks 2c and 2c+1 of that row in a 128-byte-swizzled K-major
+// tile (row r at r * 128, chunk i at 16 * (i ^ (r & 7))).
+__device__ __forceinline__ void convert_chunk16(const uint8_t* src, uint8_t* tile, int r, int c) {
+  const uint4 w = *reinterpret_cast<const uint4*>(src);
+  uint4 o0, o1;
+  int8x4_to_bf16x4(w.x, o0.x, o0.y);
+  int8x4_to_bf16x4(w.y, o0.z, o0.w);
+  int8x4_to_bf16x4(w.z, o1.x, o1.y);
+  int8x4_to_bf16x4(w.w, o1.z, o1.w);
+  uint8_t* row = tile + r * 128;
+  *reinterpret_cast<uint4*>(row + 16 * ((2 * c) ^ (r & 7))) = o0;
+  *reinterpret_cast<uint4*>(row + 16 * ((2 * c + 1) ^ (r & 7))) = o1;
+}
+
+}  // namespace cbmoe
