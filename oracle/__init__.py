@@ -24,7 +24,10 @@ class _Layer(ctypes.Structure):
                 ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("wdtype", ctypes.c_int32),
                 ("x", ctypes.c_void_p), ("wr", ctypes.c_void_p), ("bias", ctypes.c_void_p),
                 ("wg", ctypes.c_void_p), ("wu", ctypes.c_void_p), ("wd", ctypes.c_void_p),
-                ("sg", ctypes.c_void_p), ("su", ctypes.c_void_p), ("sd", ctypes.c_void_p)]
+                ("sg", ctypes.c_void_p), ("su", ctypes.c_void_p), ("sd", ctypes.c_void_p),
+                ("router_mode", ctypes.c_int32), ("hash_dims", ctypes.c_int32), ("wh", ctypes.c_void_p)]
+
+ROUTER_MODES = {"softmax": 0, "raw": 1, "hash": 2}
 
 
 def build(force: bool = False, extra_flags=()) -> str:
@@ -45,6 +48,10 @@ def _bind(lib):
     lib.moe_oracle_route.restype = i32
     lib.moe_oracle_gate.argtypes = [i32, i32, vp, vp, vp, vp, vp]
     lib.moe_oracle_gate.restype = i32
+    lib.moe_oracle_gate_raw.argtypes = [i32, i32, vp, vp, vp, vp, vp]
+    lib.moe_oracle_gate_raw.restype = i32
+    lib.moe_oracle_hash_expert.argtypes = [vp, vp, i32, i32, i32]
+    lib.moe_oracle_hash_expert.restype = ctypes.c_int32
     lib.moe_oracle_dispatch.argtypes = [i64, i32, i32, vp, vp, vp, vp, vp]
     lib.moe_oracle_dispatch.restype = i32
     lib.moe_oracle_expert.argtypes = [vp, i32, vp, i32, vp]
@@ -87,11 +94,13 @@ class Oracle:
         T = layer.x.shape[0]
         self._keep = [np.ascontiguousarray(a) if a is not None else None
                       for a in (layer.x, layer.wr, layer.bias, layer.wg, layer.wu, layer.wd,
-                                layer.sg, layer.su, layer.sd)]
-        x, wr, b, wg, wu, wd, sg, su, sd = self._keep
+                                layer.sg, layer.su, layer.sd, getattr(layer, "wh", None))]
+        x, wr, b, wg, wu, wd, sg, su, sd, wh = self._keep
         self.T, self.d, self.f, self.E, self.k = T, s.d, s.f, s.E, s.k
+        router = getattr(s, "router", "softmax")
         self.c = _Layer(T, s.d, s.f, s.E, s.k, 1 if s.wdtype == "int8" else 0,
-                        _p(x), _p(wr), _p(b), _p(wg), _p(wu), _p(wd), _p(sg), _p(su), _p(sd))
+                        _p(x), _p(wr), _p(b), _p(wg), _p(wu), _p(wd), _p(sg), _p(su), _p(sd),
+                        ROUTER_MODES[router], getattr(s, "hash_dims", 0), _p(wh))
 
     def route(self, tokens=None, want_logits=False):
         """Gate for the listed tokens (all when None): ids, w, gap_k, gap_slot[, logits]."""
@@ -127,18 +136,30 @@ class Oracle:
         return y
 
 
-def gate(logits, k, lib=None):
-    """Gate of one token from its E logits (double): ids, w, gap_k, gap_slot."""
+def gate(logits, k, lib=None, raw=False):
+    """Gate of one token from its E logits (double): ids, w, gap_k, gap_slot
+    (raw=True: the raw-logit gate, whose weights are the selected logits)."""
     lib = lib or load()
     l = np.ascontiguousarray(logits, dtype=np.float64)
     ids = np.empty(k, np.int32)
     w = np.empty(k, np.float64)
     gk = ctypes.c_double()
     gs = ctypes.c_double()
-    if lib.moe_oracle_gate(len(l), k, l.ctypes.data, ids.ctypes.data, w.ctypes.data,
-                           ctypes.addressof(gk), ctypes.addressof(gs)):
+    fn = lib.moe_oracle_gate_raw if raw else lib.moe_oracle_gate
+    if fn(len(l), k, l.ctypes.data, ids.ctypes.data, w.ctypes.data, ctypes.addressof(gk), ctypes.addressof(gs)):
         raise ValueError("bad gate sizes")
     return ids, w, gk.value, gs.value
+
+
+def hash_expert(xrow_bits, wh_bits, E, lib=None):
+    """The hash router's expert of one bf16 row under W_h [hash_dims][d] (bits)."""
+    lib = lib or load()
+    x = np.ascontiguousarray(xrow_bits, dtype=np.uint16)
+    wh = np.ascontiguousarray(wh_bits, dtype=np.uint16)
+    e = lib.moe_oracle_hash_expert(x.ctypes.data, wh.ctypes.data, x.shape[0], wh.shape[0], int(E))
+    if e < 0:
+        raise ValueError("bad hash sizes")
+    return int(e)
 
 
 def dispatch(ids, E, lib=None):

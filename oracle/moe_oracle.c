@@ -19,6 +19,18 @@
  *     softmax is monotone and its full denominator cancels after the
  *     renormalisation, w[t][s] = exp(l_s - l_0) / sum_{j<k} exp(l_j - l_0).
  *     A NaN logit ranks below every number; among NaNs the lower index wins.
+ *     Router variants (step 2 replaced; the rest of the layer unchanged):
+ *     - raw-logit gate (the first page's §3.2: top-k straight on the raw
+ *       logits, no softmax): the same expert order, and slot s carries the
+ *       selected logit itself as its weight, w[t][s] = l_s;
+ *     - hash routing ("lshu.cn/news/53496" §2): a light projection
+ *       r = x W_h to hash_dims values (W_h stored [hash_dims][d]; each r_i a
+ *       left-to-right sum in double of the exact bf16 products), each mapped
+ *       to a 20-bit integer h_i = (int32)(r_i * 1e6) & 0xFFFFF, and the expert
+ *       (h_0 ^ h_1 ^ ...) mod E, with k = 1 and weight 1.  The int32
+ *       conversion truncates toward zero and saturates at the int32 range
+ *       (NaN gives 0); the page does not say, and that is what the GPU's
+ *       conversion does.
  *  3. dispatch (the dispatch kernel of the first page's §2.3): per-expert
  *     counts, exclusive prefix-sum offsets, and the canonical permutation:
  *     rows of expert e hold its tokens in ascending token order.
@@ -56,9 +68,13 @@ typedef struct {
   const void *wd;                 /* [E][d][f]                           */
   const float *sg, *su;           /* [E][f] (int8 only)                  */
   const float *sd;                /* [E][d] (int8 only)                  */
+  int32_t router_mode;            /* 0 softmax top-k, 1 raw logits, 2 hash */
+  int32_t hash_dims;              /* hash router: rows of wh             */
+  const uint16_t *wh;             /* [hash_dims][d] bf16 bits, or NULL   */
 } moe_oracle_layer_t;
 
 enum { ORACLE_EXACT = 0, ORACLE_BF16H = 1 };
+enum { ROUTER_SOFTMAX = 0, ROUTER_RAW = 1, ROUTER_HASH = 2 };
 
 /* ---------------------------------------------------------------- threads */
 void moe_oracle_set_threads(int n) {
@@ -155,9 +171,10 @@ static void order_experts(int E, const double *l, int *order) {
 
 /* One token's gate: ids[k], w[k]; gap_k = l(k-1) - l(k) in the sorted order
  * (+inf when k == E), gap_slot = smallest adjacent gap among the k chosen
- * (+inf when k == 1).  Returns 0, or -1 on bad sizes. */
-int moe_oracle_gate(int E, int k, const double *l, int32_t *ids, double *w,
-                    double *gap_k, double *gap_slot) {
+ * (+inf when k == 1).  raw != 0: the raw-logit gate (w = the logits).
+ * Returns 0, or -1 on bad sizes. */
+static int gate_common(int E, int k, const double *l, int32_t *ids, double *w,
+                       double *gap_k, double *gap_slot, int raw) {
   if (E <= 0 || k <= 0 || k > E) return -1;
   int *order = (int *)malloc(sizeof(int) * (size_t)E);
   if (!order) return -1;
@@ -167,7 +184,7 @@ int moe_oracle_gate(int E, int k, const double *l, int32_t *ids, double *w,
   for (int s = 0; s < k; ++s) den += exp(l[order[s]] - l0);
   for (int s = 0; s < k; ++s) {
     ids[s] = order[s];
-    w[s] = exp(l[order[s]] - l0) / den;
+    w[s] = raw ? l[order[s]] : exp(l[order[s]] - l0) / den;
   }
   if (gap_k) *gap_k = (k < E) ? l[order[k - 1]] - l[order[k]] : INFINITY;
   if (gap_slot) {
@@ -182,6 +199,56 @@ int moe_oracle_gate(int E, int k, const double *l, int32_t *ids, double *w,
   return 0;
 }
 
+int moe_oracle_gate(int E, int k, const double *l, int32_t *ids, double *w,
+                    double *gap_k, double *gap_slot) {
+  return gate_common(E, k, l, ids, w, gap_k, gap_slot, 0);
+}
+
+int moe_oracle_gate_raw(int E, int k, const double *l, int32_t *ids, double *w,
+                        double *gap_k, double *gap_slot) {
+  return gate_common(E, k, l, ids, w, gap_k, gap_slot, 1);
+}
+
+/* int32 conversion of a double: truncation toward zero, saturating at the
+ * int32 range, NaN -> 0 */
+static int32_t trunc_sat_i32(double v) {
+  if (isnan(v)) return 0;
+  if (v >= 2147483647.0) return INT32_MAX;
+  if (v <= -2147483648.0) return INT32_MIN;
+  return (int32_t)v;
+}
+
+/* The hash router's expert of one bf16 row (d elements) under W_h
+ * [hd][d]: see the header.  Returns -1 on bad sizes. */
+int32_t moe_oracle_hash_expert(const uint16_t *xrow, const uint16_t *wh, int d, int hd, int E) {
+  if (d <= 0 || hd <= 0 || E <= 0) return -1;
+  uint32_t acc = 0;
+  for (int i = 0; i < hd; ++i) {
+    double r = 0.0;
+    for (int j = 0; j < d; ++j) r += bf16_value(xrow[j]) * bf16_value(wh[(int64_t)i * d + j]);
+    acc ^= (uint32_t)trunc_sat_i32(r * 1e6) & 0xFFFFFu;
+  }
+  return (int32_t)(acc % (uint32_t)E);
+}
+
+/* The gate of token t under the layer's router; l is scratch of E doubles
+ * (left holding the logits, or NaN under the hash router). */
+static int gate_token(const moe_oracle_layer_t *L, int64_t t, double *l, int32_t *ids, double *w,
+                      double *gap_k, double *gap_slot) {
+  if (L->router_mode == ROUTER_HASH) {
+    if (L->k != 1 || L->wh == NULL || L->hash_dims <= 0) return -1;
+    for (int e = 0; e < L->E; ++e) l[e] = NAN;
+    ids[0] = moe_oracle_hash_expert(L->x + t * (int64_t)L->d, L->wh, L->d, L->hash_dims, L->E);
+    w[0] = 1.0;
+    if (gap_k) *gap_k = INFINITY;
+    if (gap_slot) *gap_slot = INFINITY;
+    return ids[0] < 0 ? -1 : 0;
+  }
+  if (L->router_mode != ROUTER_SOFTMAX && L->router_mode != ROUTER_RAW) return -1;
+  router_logits_row(L, t, l);
+  return gate_common(L->E, L->k, l, ids, w, gap_k, gap_slot, L->router_mode == ROUTER_RAW);
+}
+
 /* Route tokens tokens[0..n) (or 0..n when tokens == NULL).  Outputs are
  * indexed by position in the list; logits may be NULL. */
 int moe_oracle_route(const moe_oracle_layer_t *L, const int32_t *tokens, int64_t n,
@@ -194,11 +261,10 @@ int moe_oracle_route(const moe_oracle_layer_t *L, const int32_t *tokens, int64_t
     for (int64_t p = 0; p < n; ++p) {
       int64_t t = tokens ? tokens[p] : p;
       if (!l || t < 0 || t >= L->T) { bad = 1; continue; }
-      router_logits_row(L, t, l);
-      if (logits) memcpy(logits + p * L->E, l, sizeof(double) * (size_t)L->E);
-      if (moe_oracle_gate(L->E, L->k, l, ids + p * L->k, w + p * L->k,
-                          gap_k ? gap_k + p : NULL, gap_slot ? gap_slot + p : NULL))
+      if (gate_token(L, t, l, ids + p * L->k, w + p * L->k, gap_k ? gap_k + p : NULL,
+                     gap_slot ? gap_slot + p : NULL))
         bad = 1;
+      if (logits) memcpy(logits + p * L->E, l, sizeof(double) * (size_t)L->E);
     }
     free(l);
   }
@@ -293,8 +359,7 @@ int moe_oracle_forward(const moe_oracle_layer_t *L, const int32_t *tokens, int64
     for (int64_t p = 0; p < n; ++p) {
       int64_t t = tokens ? tokens[p] : p;
       if (!l || !xv || !h || !y || !ids || !w || t < 0 || t >= L->T) { bad = 1; continue; }
-      router_logits_row(L, t, l);
-      if (moe_oracle_gate(E, k, l, ids, w, NULL, NULL)) { bad = 1; continue; }
+      if (gate_token(L, t, l, ids, w, NULL, NULL)) { bad = 1; continue; }
       for (int i = 0; i < d; ++i) xv[i] = bf16_value(L->x[t * (int64_t)d + i]);
       double *o = out + p * d;
       for (int c = 0; c < d; ++c) o[c] = 0.0;

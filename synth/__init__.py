@@ -2,8 +2,8 @@
 
 This module is shared by the fp64 oracle's tests and by the CUDA library's
 tests and benchmark.  It holds no part of the layer's arithmetic: it only
-draws the inputs (activations, router weights, expert weights, int8 codes and
-scales, the skewed router bias) in the shapes and distributions of the five
+draws the inputs (activations, router weights, the hash router's projection,
+expert weights, int8 codes and scales, the skewed router bias) in the shapes and distributions of the five
 workloads below, from a counter-based stream defined in ``synth.c``.
 
 The workloads follow the layer shapes the Colibri pages discuss: a Mixtral-8x7B
@@ -28,7 +28,7 @@ _SO = os.path.join(_HERE, "libsynth.so")
 _lib = None
 
 # tensor ids of the counter streams
-TID_X, TID_WR, TID_WG, TID_WU, TID_WD, TID_SG, TID_SU, TID_SD = 1, 2, 3, 4, 5, 6, 7, 8
+TID_X, TID_WR, TID_WG, TID_WU, TID_WD, TID_SG, TID_SU, TID_SD, TID_WH = 1, 2, 3, 4, 5, 6, 7, 8, 9
 
 WEIGHT_STD = 0.02      # bf16 weights ~ N(0, 0.02^2)
 INT8_SCALE = 40.0      # int8 codes round(40 N(0,1)) clipped to [-127, 127]
@@ -116,6 +116,8 @@ class Shape:
     wdtype: str = "bf16"       # "bf16" or "int8"
     bias: bool = False         # skewed router bias b_e = 2 ln(1/(e+1))
     seed: int = 0
+    router: str = "softmax"    # "softmax" (top-k, renormalised), "raw" (raw-logit weights), "hash"
+    hash_dims: int = 0         # hash router: columns of the d x hash_dims projection
 
 
 # The five workloads (sizes and distributions of the layer shapes above).
@@ -146,6 +148,7 @@ class Layer:
     sg: np.ndarray | None = None  # [E][f] float32 (int8 only)
     su: np.ndarray | None = None  # [E][f]
     sd: np.ndarray | None = None  # [E][d]
+    wh: np.ndarray | None = None  # [hash_dims][d] bf16 bits (hash router only)
     extra: dict = field(default_factory=dict)
 
 
@@ -157,19 +160,35 @@ def make_layer(shape: Shape, seed: int | None = None, T: int | None = None) -> L
     x = normal_bf16(s, TID_X, 1.0, (T, d))
     wr = normal_bf16(s, TID_WR, WEIGHT_STD, (E, d))
     bias = skew_bias(E) if shape.bias else None
+    wh = normal_bf16(s, TID_WH, WEIGHT_STD, (shape.hash_dims, d)) if shape.router == "hash" else None
     if shape.wdtype == "bf16":
         wg = normal_bf16(s, TID_WG, WEIGHT_STD, (E, f, d))
         wu = normal_bf16(s, TID_WU, WEIGHT_STD, (E, f, d))
         wd = normal_bf16(s, TID_WD, WEIGHT_STD, (E, d, f))
-        return Layer(shape, x, wr, bias, wg, wu, wd)
+        return Layer(shape, x, wr, bias, wg, wu, wd, wh=wh)
     wg = int8_codes(s, TID_WG, INT8_SCALE, (E, f, d))
     wu = int8_codes(s, TID_WU, INT8_SCALE, (E, f, d))
     wd = int8_codes(s, TID_WD, INT8_SCALE, (E, d, f))
     sg = uniform_f32(s, TID_SG, SCALE_LO, SCALE_HI, (E, f))
     su = uniform_f32(s, TID_SU, SCALE_LO, SCALE_HI, (E, f))
     sd = uniform_f32(s, TID_SD, SCALE_LO, SCALE_HI, (E, d))
-    return Layer(shape, x, wr, bias, wg, wu, wd, sg, su, sd)
+    return Layer(shape, x, wr, bias, wg, wu, wd, sg, su, sd, wh=wh)
 
 
-def custom_shape(name, T, d, f, E, k, wdtype="bf16", bias=False, seed=7) -> Shape:
-    return Shape(name, T=T, d=d, f=f, E=E, k=k, wdtype=wdtype, bias=bias, seed=seed)
+def custom_shape(name, T, d, f, E, k, wdtype="bf16", bias=False, seed=7, router="softmax", hash_dims=0) -> Shape:
+    return Shape(name, T=T, d=d, f=f, E=E, k=k, wdtype=wdtype, bias=bias, seed=seed, router=router,
+                 hash_dims=hash_dims)
+
+
+def with_router(shape: Shape, router: str, hash_dims: int = 8) -> Shape:
+    """The same layer with another router: "raw" keeps k; "hash" routes each
+    token to one expert (k = 1) through a d x hash_dims projection."""
+    if router == "softmax":
+        return shape
+    if router == "raw":
+        return Shape(shape.name + "_raw", shape.T, shape.d, shape.f, shape.E, shape.k, shape.wdtype, shape.bias,
+                     shape.seed, router="raw")
+    if router == "hash":
+        return Shape(shape.name + "_hash", shape.T, shape.d, shape.f, shape.E, 1, shape.wdtype, shape.bias,
+                     shape.seed, router="hash", hash_dims=hash_dims)
+    raise ValueError(f"unknown router {router!r}")

@@ -22,6 +22,7 @@ import oracle
 import synth
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "tiny_layer.json")
+GOLDEN_ROUTERS = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "router_variants.json")
 
 
 # ----------------------------------------------------------------- helpers
@@ -37,7 +38,8 @@ def bf16_bits_to_f64(b):
     return synth.bf16_bits_to_f32(np.asarray(b, dtype=np.uint16)).astype(np.float64)
 
 
-def make_layer_from_values(x, wr, wg, wu, wd, k, bias=None, wdtype="bf16", sg=None, su=None, sd=None):
+def make_layer_from_values(x, wr, wg, wu, wd, k, bias=None, wdtype="bf16", sg=None, su=None, sd=None,
+                           router="softmax", wh=None):
     """A synth.Layer from explicit values (bf16-exact floats or int8 codes)."""
     x = np.asarray(x, np.float64)
     wr = np.asarray(wr, np.float64)
@@ -45,7 +47,9 @@ def make_layer_from_values(x, wr, wg, wu, wd, k, bias=None, wdtype="bf16", sg=No
     E = wr.shape[0]
     wg_a = np.asarray(wg)
     f = wg_a.shape[1]
-    shape = synth.Shape("custom", T=T, d=d, f=f, E=E, k=k, wdtype=wdtype, bias=bias is not None)
+    hd = 0 if wh is None else np.asarray(wh).shape[0]
+    shape = synth.Shape("custom", T=T, d=d, f=f, E=E, k=k, wdtype=wdtype, bias=bias is not None, router=router,
+                        hash_dims=hd)
     conv = f32_to_bf16_bits
     if wdtype == "bf16":
         wgb, wub, wdb = conv(wg), conv(wu), conv(wd)
@@ -57,7 +61,8 @@ def make_layer_from_values(x, wr, wg, wu, wd, k, bias=None, wdtype="bf16", sg=No
     return synth.Layer(shape, conv(x), conv(wr), b, wgb, wub, wdb,
                        None if sg is None else np.asarray(sg, np.float32),
                        None if su is None else np.asarray(su, np.float32),
-                       None if sd is None else np.asarray(sd, np.float32))
+                       None if sd is None else np.asarray(sd, np.float32),
+                       wh=None if wh is None else conv(wh))
 
 
 def dense_swiglu(xv, wg, wu, wd):
@@ -350,6 +355,73 @@ def pin_routing_invariants(lib):
         assert np.all(np.diff(seg) > 0)
 
 
+# ---------------------------------------------------------- router variants
+def pin_raw_gate(lib):
+    """Raw-logit gate: the worked example of router_variants.json, and on random
+    logits (with exact ties) the same ids as the softmax gate with w = the
+    selected logits."""
+    g = json.load(open(GOLDEN))
+    gr = json.load(open(GOLDEN_ROUTERS))["raw"]
+    L = make_layer_from_values(g["x"], g["wr"], g["wg"], g["wu"], g["wd"], 2, router="raw")
+    out, ids, w = oracle.Oracle(L, lib).forward(mode=oracle.EXACT)
+    env = {"silu": lambda z: z * float(expit(z))}
+    want = np.array([[eval(e, {"__builtins__": {}}, env) for e in row] for row in gr["expected_out"]])
+    assert np.array_equal(ids, np.array(gr["expected_ids"]))
+    assert np.array_equal(w, np.array(gr["expected_w"]))
+    assert np.allclose(out, want, rtol=1e-13, atol=1e-15), (out, want)
+    rng = np.random.default_rng(21)
+    for _ in range(200):
+        E = int(rng.integers(2, 9))
+        k = int(rng.integers(1, E + 1))
+        l = np.round(rng.standard_normal(E) * 4) / 4      # quarter steps: exact ties happen
+        ids_s, _, gk_s, gs_s = oracle.gate(l, k, lib)
+        ids_r, w_r, gk_r, gs_r = oracle.gate(l, k, lib, raw=True)
+        assert np.array_equal(ids_r, ids_s) and gk_r == gk_s and gs_r == gs_s
+        assert np.array_equal(w_r, l[ids_r])
+
+
+def pin_hash_golden(lib):
+    """Hash router: the hand-derived ids of router_variants.json (truncation toward
+    zero, negative values, saturation), one token at a time and through a layer."""
+    gh = json.load(open(GOLDEN_ROUTERS))["hash"]
+    E = gh["E"]
+    xb = f32_to_bf16_bits(gh["x"])
+    whb = f32_to_bf16_bits(gh["wh"])
+    got = [oracle.hash_expert(xb[t], whb, E, lib) for t in range(xb.shape[0])]
+    assert got == gh["expected_ids"], got
+    T, d = xb.shape
+    zeros = np.zeros((E, d))
+    L = make_layer_from_values(gh["x"], zeros, np.zeros((E, 2, d)), np.zeros((E, 2, d)), np.zeros((E, d, 2)), 1,
+                               router="hash", wh=gh["wh"])
+    ids, w, gk, gs = oracle.Oracle(L, lib).route()
+    assert ids.ravel().tolist() == gh["expected_ids"] and np.all(w == 1.0)
+
+
+def pin_hash_invariants(lib):
+    """Hash router on a random layer: the expert does not depend on the router
+    weights, bias or experts; permuting the projection's rows leaves it
+    unchanged (XOR is symmetric); zero input goes to expert 0; k = 1 with
+    weight 1, and the layer's output is that expert's FFN."""
+    rng = np.random.default_rng(22)
+    T, d, f, E = 24, 32, 8, 5
+    L, (x, wr, wg, wu, wd) = _random_layer(rng, T, d, f, E, 1)
+    wh = rng_bf16(rng, (4, d), 0.5)
+    La = make_layer_from_values(x, wr, wg, wu, wd, 1, router="hash", wh=wh)
+    Lb = make_layer_from_values(x, rng_bf16(rng, wr.shape, 1.0), wg, wu, wd, 1,
+                                bias=rng.standard_normal(E).astype(np.float32), router="hash", wh=wh[::-1])
+    oa, ia, wa = oracle.Oracle(La, lib).forward(mode=oracle.EXACT)
+    ob, ib, wb = oracle.Oracle(Lb, lib).forward(mode=oracle.EXACT)
+    assert np.array_equal(ia, ib) and np.all(wa == 1.0) and np.all(wb == 1.0)
+    assert len(set(ia.ravel().tolist())) > 1
+    o = oracle.Oracle(La, lib)
+    for t in range(T):
+        assert np.array_equal(oa[t], o.expert(ia[t, 0], La.x[t], mode=oracle.EXACT))
+    Lz = make_layer_from_values(np.zeros((3, d)), wr, wg, wu, wd, 1, router="hash", wh=wh)
+    iz, _, _, _ = oracle.Oracle(Lz, lib).route()
+    assert np.all(iz == 0)
+
+
 ALL_PINS = [pin_round_bf16, pin_gate_bruteforce, pin_gate_weights, pin_dispatch, pin_identical_experts,
             pin_one_hot_router, pin_two_expert_mix, pin_zero_input, pin_bf16_h_mode, pin_int8_equals_bf16,
-            pin_token_permutation, pin_expert_relabel, pin_golden_tiny, pin_routing_invariants]
+            pin_token_permutation, pin_expert_relabel, pin_golden_tiny, pin_routing_invariants,
+            pin_raw_gate, pin_hash_golden, pin_hash_invariants]

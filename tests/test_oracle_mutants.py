@@ -20,7 +20,20 @@ MUTANTS = {
     "nan_ranks_first": ("if (na != nb) return nb;", "if (na != nb) return na;"),
     "not_renormalised": ("for (int s = 0; s < k; ++s) den += exp(l[order[s]] - l0);",
                          "for (int s = 0; s < E; ++s) den += exp(l[order[s]] - l0);"),
-    "weights_reversed": ("w[s] = exp(l[order[s]] - l0) / den;", "w[s] = exp(l[order[k - 1 - s]] - l0) / den;"),
+    "weights_reversed": ("w[s] = raw ? l[order[s]] : exp(l[order[s]] - l0) / den;",
+                         "w[s] = raw ? l[order[s]] : exp(l[order[k - 1 - s]] - l0) / den;"),
+    "raw_weight_is_softmax": ("w[s] = raw ? l[order[s]] : exp(l[order[s]] - l0) / den;",
+                              "w[s] = exp(l[order[s]] - l0) / den;"),
+    "hash_or_for_xor": ("acc ^= (uint32_t)trunc_sat_i32(r * 1e6) & 0xFFFFFu;",
+                        "acc |= (uint32_t)trunc_sat_i32(r * 1e6) & 0xFFFFFu;"),
+    "hash_rounds": ("  return (int32_t)v;\n}", "  return (int32_t)nearbyint(v);\n}"),
+    "hash_floor": ("  return (int32_t)v;\n}", "  return (int32_t)floor(v);\n}"),
+    "hash_mask_16_bits": ("acc ^= (uint32_t)trunc_sat_i32(r * 1e6) & 0xFFFFFu;",
+                          "acc ^= (uint32_t)trunc_sat_i32(r * 1e6) & 0xFFFFu;"),
+    "hash_no_saturation": ("  if (v >= 2147483647.0) return INT32_MAX;\n", ""),
+    "hash_scale_1e5": ("acc ^= (uint32_t)trunc_sat_i32(r * 1e6) & 0xFFFFFu;",
+                       "acc ^= (uint32_t)trunc_sat_i32(r * 1e5) & 0xFFFFFu;"),
+    "hash_first_dim_only": ("for (int i = 0; i < hd; ++i) {", "for (int i = 0; i < 1; ++i) {"),
     "gate_transposed": ("g += xv[i] * weight_elem(L, L->wg, gbase + (int64_t)j * d + i);",
                         "g += xv[i] * weight_elem(L, L->wg, gbase + (int64_t)i * f + j);"),
     "down_transposed": ("weight_elem(L, L->wd, dbase + (int64_t)c * f + j)",
