@@ -24,13 +24,14 @@
  *       logits, no softmax): the same expert order, and slot s carries the
  *       selected logit itself as its weight, w[t][s] = l_s;
  *     - hash routing ("lshu.cn/news/53496" §2): a light projection
- *       r = x W_h to hash_dims values (W_h stored [hash_dims][d]; each r_i a
- *       left-to-right sum in double of the exact bf16 products), each mapped
- *       to a 20-bit integer h_i = (int32)(r_i * 1e6) & 0xFFFFF, and the expert
- *       (h_0 ^ h_1 ^ ...) mod E, with k = 1 and weight 1.  The int32
- *       conversion truncates toward zero and saturates at the int32 range
- *       (NaN gives 0); the page does not say, and that is what the GPU's
- *       conversion does.
+ *       r = x W_h to hash_dims values (W_h stored [hash_dims][d]), each
+ *       mapped to a 20-bit integer h_i = (int32)(r_i * 1e6) & 0xFFFFF, and
+ *       the expert (h_0 ^ h_1 ^ ...) mod E, with k = 1 and weight 1.  The
+ *       page's expression is C on a float routing vector, so r_i is a float
+ *       sum, taken left to right, of the exact bf16 products; r_i * 1e6 is
+ *       evaluated in double (the literal is a double), which is exact; the
+ *       int32 conversion truncates toward zero and saturates at the int32
+ *       range (NaN gives 0), which the page leaves open.
  *  3. dispatch (the dispatch kernel of the first page's §2.3): per-expert
  *     counts, exclusive prefix-sum offsets, and the canonical permutation:
  *     rows of expert e hold its tokens in ascending token order.
@@ -224,9 +225,9 @@ int32_t moe_oracle_hash_expert(const uint16_t *xrow, const uint16_t *wh, int d, 
   if (d <= 0 || hd <= 0 || E <= 0) return -1;
   uint32_t acc = 0;
   for (int i = 0; i < hd; ++i) {
-    double r = 0.0;
-    for (int j = 0; j < d; ++j) r += bf16_value(xrow[j]) * bf16_value(wh[(int64_t)i * d + j]);
-    acc ^= (uint32_t)trunc_sat_i32(r * 1e6) & 0xFFFFFu;
+    float r = 0.0f;
+    for (int j = 0; j < d; ++j) r += (float)bf16_value(xrow[j]) * (float)bf16_value(wh[(int64_t)i * d + j]);
+    acc ^= (uint32_t)trunc_sat_i32((double)r * 1e6) & 0xFFFFFu;
   }
   return (int32_t)(acc % (uint32_t)E);
 }

@@ -382,7 +382,8 @@ def pin_raw_gate(lib):
 
 def pin_hash_golden(lib):
     """Hash router: the hand-derived ids of router_variants.json (truncation toward
-    zero, negative values, saturation), one token at a time and through a layer."""
+    zero, negative values, saturation; a float sum that rounds, in both
+    orders), one token at a time and through a layer."""
     gh = json.load(open(GOLDEN_ROUTERS))["hash"]
     E = gh["E"]
     xb = f32_to_bf16_bits(gh["x"])
@@ -395,6 +396,10 @@ def pin_hash_golden(lib):
                                router="hash", wh=gh["wh"])
     ids, w, gk, gs = oracle.Oracle(L, lib).route()
     assert ids.ravel().tolist() == gh["expected_ids"] and np.all(w == 1.0)
+    go = json.load(open(GOLDEN_ROUTERS))["hash_order"]
+    xo, who = f32_to_bf16_bits(go["x"]), f32_to_bf16_bits(go["wh"])
+    got = [oracle.hash_expert(xo[t], who, go["E"], lib) for t in range(xo.shape[0])]
+    assert got == go["expected_ids"], got
 
 
 def pin_hash_invariants(lib):

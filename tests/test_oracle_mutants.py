@@ -24,16 +24,19 @@ MUTANTS = {
                          "w[s] = raw ? l[order[s]] : exp(l[order[k - 1 - s]] - l0) / den;"),
     "raw_weight_is_softmax": ("w[s] = raw ? l[order[s]] : exp(l[order[s]] - l0) / den;",
                               "w[s] = exp(l[order[s]] - l0) / den;"),
-    "hash_or_for_xor": ("acc ^= (uint32_t)trunc_sat_i32(r * 1e6) & 0xFFFFFu;",
-                        "acc |= (uint32_t)trunc_sat_i32(r * 1e6) & 0xFFFFFu;"),
+    "hash_or_for_xor": ("acc ^= (uint32_t)trunc_sat_i32((double)r * 1e6) & 0xFFFFFu;",
+                        "acc |= (uint32_t)trunc_sat_i32((double)r * 1e6) & 0xFFFFFu;"),
     "hash_rounds": ("  return (int32_t)v;\n}", "  return (int32_t)nearbyint(v);\n}"),
     "hash_floor": ("  return (int32_t)v;\n}", "  return (int32_t)floor(v);\n}"),
-    "hash_mask_16_bits": ("acc ^= (uint32_t)trunc_sat_i32(r * 1e6) & 0xFFFFFu;",
-                          "acc ^= (uint32_t)trunc_sat_i32(r * 1e6) & 0xFFFFu;"),
+    "hash_mask_16_bits": ("acc ^= (uint32_t)trunc_sat_i32((double)r * 1e6) & 0xFFFFFu;",
+                          "acc ^= (uint32_t)trunc_sat_i32((double)r * 1e6) & 0xFFFFu;"),
     "hash_no_saturation": ("  if (v >= 2147483647.0) return INT32_MAX;\n", ""),
-    "hash_scale_1e5": ("acc ^= (uint32_t)trunc_sat_i32(r * 1e6) & 0xFFFFFu;",
-                       "acc ^= (uint32_t)trunc_sat_i32(r * 1e5) & 0xFFFFFu;"),
+    "hash_scale_1e5": ("acc ^= (uint32_t)trunc_sat_i32((double)r * 1e6) & 0xFFFFFu;",
+                       "acc ^= (uint32_t)trunc_sat_i32((double)r * 1e5) & 0xFFFFFu;"),
     "hash_first_dim_only": ("for (int i = 0; i < hd; ++i) {", "for (int i = 0; i < 1; ++i) {"),
+    "hash_sums_in_double": ("    float r = 0.0f;\n", "    double r = 0.0;\n"),
+    "hash_sums_backward": ("for (int j = 0; j < d; ++j) r += (float)bf16_value(xrow[j])",
+                           "for (int j = d - 1; j >= 0; --j) r += (float)bf16_value(xrow[j])"),
     "gate_transposed": ("g += xv[i] * weight_elem(L, L->wg, gbase + (int64_t)j * d + i);",
                         "g += xv[i] * weight_elem(L, L->wg, gbase + (int64_t)i * f + j);"),
     "down_transposed": ("weight_elem(L, L->wd, dbase + (int64_t)c * f + j)",
