@@ -49,6 +49,8 @@ def parse_args(argv=None):
     p.add_argument("--shape", default=None, help="T,d,f,E,k of a custom layer (profiling cases)")
     p.add_argument("--wdtype", default="bf16", choices=["bf16", "int8"], help="expert weights of a --shape layer")
     p.add_argument("--bias", action="store_true", help="skewed router bias on a --shape layer")
+    p.add_argument("--router", default="softmax", choices=["softmax", "raw", "hash"],
+                   help="router variant: softmax top-k (default), raw-logit weights, or the hash router (k = 1)")
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--l2-flush-mb", type=int, default=512)
     p.add_argument("--e2e-steps", type=int, default=50)
@@ -83,7 +85,7 @@ def algorithmic_work(shape, counts):
     active = sum(1 for c in counts if c > 0)
     wbytes = active * 3 * d * f * eb + (active * (2 * f + d) * 4 if eb == 1 else 0)
     return {
-        "router_bytes": T * d * 2 + E * d * 2 + T * k * 8,
+        "router_bytes": T * d * 2 + (shape.hash_dims if shape.router == "hash" else E) * d * 2 + T * k * 8,
         "dispatch_bytes": T * d * 2 + M * d * 2 + 16 * M,
         "gateup_flops": 4 * d * f * M,
         "down_flops": 2 * d * f * M,
@@ -188,6 +190,7 @@ def max_over_ranks(value: float, world: int) -> float:
 def config_block(shape, l2_mb):
     return {"workload": shape.name, "T": shape.T, "d_model": shape.d, "d_ff": shape.f, "n_experts": shape.E,
             "top_k": shape.k, "expert_weights": shape.wdtype, "router_bias": shape.bias,
+            "router": shape.router + (f" ({shape.hash_dims} hash dims)" if shape.router == "hash" else ""),
             "l2": f"flushed between timed steps ({l2_mb} MB write, outside the timed events)",
             "parallelism": "replicas (token-sharded, no collective)"}
 
@@ -281,10 +284,10 @@ def run_ours(args):
             return torch.from_numpy(a.view(np.int16)).to(device).view(torch.bfloat16)
         return torch.from_numpy(a).to(device)
 
-    w = {n: dev(getattr(layer, n)) for n in ("wr", "bias", "wg", "wu", "wd", "sg", "su", "sd")}
+    w = {n: dev(getattr(layer, n)) for n in ("wr", "bias", "wg", "wu", "wd", "sg", "su", "sd", "wh")}
     m = cb.MoELayer(shape.T, shape.d, shape.f, shape.E, shape.k, w["wr"], w["wg"], w["wu"], w["wd"],
                     router_bias=w["bias"], s_gate=w["sg"], s_up=w["su"], s_down=w["sd"], device=local,
-                    stage_timing=True)
+                    stage_timing=True, router=shape.router, w_hash=w["wh"])
     launches_per_forward = m.kernels_per_forward()
     del w
     torch.cuda.empty_cache()
@@ -443,8 +446,9 @@ def workload_shape(args):
         T, d, f, E, k = (int(v) for v in args.shape.split(","))
         name = f"custom_T{T}_d{d}_f{f}_E{E}_k{k}" + ("_int8" if args.wdtype == "int8" else "") + \
             ("_bias" if args.bias else "")
-        return synth.custom_shape(name, T=T, d=d, f=f, E=E, k=k, wdtype=args.wdtype, bias=args.bias, seed=1100)
-    return synth.WORKLOADS[args.workload]
+        return synth.with_router(synth.custom_shape(name, T=T, d=d, f=f, E=E, k=k, wdtype=args.wdtype,
+                                                    bias=args.bias, seed=1100), args.router)
+    return synth.with_router(synth.WORKLOADS[args.workload], args.router)
 
 
 def main(argv=None):

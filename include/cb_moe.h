@@ -54,7 +54,9 @@ extern "C" {
 
 typedef enum {
   CB_OK = 0,
-  CB_ERR_INVALID_ARG = 1,  /* NULL pointer, negative size, k > E, x aliasing out        */
+  CB_ERR_INVALID_ARG = 1,  /* NULL pointer, negative size, k > E, x aliasing out, unknown
+                              router_mode, hash router with top_k != 1, hash_dims
+                              outside 1..CB_MAX_HASH_DIMS or no w_hash          */
   CB_ERR_UNSUPPORTED = 2,  /* d_model or d_ff not a multiple of 256, E > 256, k > 16,
                               wrong GPU (not compute capability 10.3), missing scales     */
   CB_ERR_ALIGNMENT = 3,    /* a pointer not 16-byte aligned                               */
@@ -66,6 +68,26 @@ typedef enum {
 } cb_status_t;
 
 typedef enum { CB_W_BF16 = 0, CB_W_INT8 = 1 } cb_wdtype_t;
+
+/*
+ * config.router_mode: how each token picks its experts and their weights.
+ *  CB_ROUTER_SOFTMAX_TOPK: logits l = x Wr^T + b; the k largest (ties to the
+ *    lower index); softmax renormalised over the k,
+ *    w_s = exp(l_s - l_0) / sum_j exp(l_j - l_0) ("Colibri：面向MoE模型的高性能C语言
+ *    推理引擎" §1, §2.1).  The default.
+ *  CB_ROUTER_RAW_LOGITS: the same k experts, and each weight is the raw logit
+ *    itself, w_s = l_s: top-k on the raw logits without a softmax
+ *    ("Colibri：面向MoE架构的C语言级高效推理引擎" §3.2).
+ *  CB_ROUTER_HASH: one expert per token (top_k must be 1, weight 1) from a
+ *    d x hash_dims projection r = x W_h ("lshu.cn/news/53496" §2): each r_i a
+ *    float sum, left to right over d, of the exact bf16 products; h_i =
+ *    (int32)((double)r_i * 1e6) & 0xFFFFF with the int32 conversion
+ *    truncating toward zero and saturating (NaN -> 0); expert =
+ *    (h_0 ^ h_1 ^ ...) mod E.  No logits are computed (w_router and
+ *    router_bias are ignored).
+ */
+typedef enum { CB_ROUTER_SOFTMAX_TOPK = 0, CB_ROUTER_RAW_LOGITS = 1, CB_ROUTER_HASH = 2 } cb_router_mode_t;
+#define CB_MAX_HASH_DIMS 8
 
 /* config.flags */
 #define CB_FLAG_KEEP_LOGITS 0x1u   /* also store the fp32 router logits [T][E] */
@@ -88,6 +110,8 @@ typedef struct {
   int32_t wdtype;     /* cb_wdtype_t of the expert weights                       */
   int32_t device;     /* CUDA device ordinal                                     */
   uint32_t flags;     /* CB_FLAG_*                                               */
+  int32_t router_mode; /* cb_router_mode_t (0 = softmax top-k)                    */
+  int32_t hash_dims;  /* CB_ROUTER_HASH: 1..CB_MAX_HASH_DIMS columns of W_h; else 0 */
 } cb_moe_config_t;
 
 /* Expert and router weights: device pointers, read only during cb_moe_init. */
@@ -100,6 +124,7 @@ typedef struct {
   const float *s_gate;      /* fp32 [E][f]  int8 only, else NULL                  */
   const float *s_up;        /* fp32 [E][f]  int8 only, else NULL                  */
   const float *s_down;      /* fp32 [E][d]  int8 only, else NULL                  */
+  const void *w_hash;       /* bf16 [hash_dims][d], CB_ROUTER_HASH only, else NULL */
 } cb_moe_weights_t;
 
 typedef struct cb_moe cb_moe_t;   /* opaque handle */
@@ -138,13 +163,15 @@ CB_API cb_status_t cb_moe_forward_host(cb_moe_t *h, const void *x_host, void *ou
  * forward or cb_moe_free; read after synchronising its stream). */
 typedef struct {
   const int32_t *ids;       /* [T][k] expert ids, slot order                       */
-  const float *w;           /* [T][k] renormalised gate weights                    */
+  const float *w;           /* [T][k] gate weights (renormalised softmax, raw
+                               logits, or 1 under the hash router)              */
   const int32_t *counts;    /* [E]   rows per expert                               */
   const int32_t *offsets;   /* [E+1] exclusive prefix sum of counts                */
   const int32_t *tok;       /* [T*k] token of each row (expert-major, stable)      */
   const int32_t *inv;       /* [T][k] row of each (token, slot)                    */
   const float *logits;      /* [T][E] fp32 logits with bias, or NULL unless
-                               CB_FLAG_KEEP_LOGITS                                */
+                               CB_FLAG_KEEP_LOGITS (not written by the hash
+                               router)                                          */
   const int32_t *tile_offsets; /* [E+1] prefix sum of ceil(counts/128): the
                                expert-aligned 128-row tiles of the GEMM layout   */
 } cb_routing_view_t;

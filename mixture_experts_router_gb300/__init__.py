@@ -28,16 +28,23 @@ ABI_SYMBOLS = ("cb_moe_init", "cb_moe_forward", "cb_moe_forward_f32out", "cb_moe
                "cb_moe_free", "cb_status_string", "cb_moe_dispatch_noalloc", "cb_moe_kernels_per_forward")
 
 
+CB_ROUTER_SOFTMAX_TOPK, CB_ROUTER_RAW_LOGITS, CB_ROUTER_HASH = 0, 1, 2
+CB_MAX_HASH_DIMS = 8
+ROUTER_MODES = {"softmax": CB_ROUTER_SOFTMAX_TOPK, "raw": CB_ROUTER_RAW_LOGITS, "hash": CB_ROUTER_HASH}
+
+
 class cb_moe_config_t(ctypes.Structure):
     _fields_ = [("n_tokens", ctypes.c_int32), ("d_model", ctypes.c_int32), ("d_ff", ctypes.c_int32),
                 ("n_experts", ctypes.c_int32), ("top_k", ctypes.c_int32), ("wdtype", ctypes.c_int32),
-                ("device", ctypes.c_int32), ("flags", ctypes.c_uint32)]
+                ("device", ctypes.c_int32), ("flags", ctypes.c_uint32), ("router_mode", ctypes.c_int32),
+                ("hash_dims", ctypes.c_int32)]
 
 
 class cb_moe_weights_t(ctypes.Structure):
     _fields_ = [("w_router", ctypes.c_void_p), ("router_bias", ctypes.c_void_p),
                 ("w_gate", ctypes.c_void_p), ("w_up", ctypes.c_void_p), ("w_down", ctypes.c_void_p),
-                ("s_gate", ctypes.c_void_p), ("s_up", ctypes.c_void_p), ("s_down", ctypes.c_void_p)]
+                ("s_gate", ctypes.c_void_p), ("s_up", ctypes.c_void_p), ("s_down", ctypes.c_void_p),
+                ("w_hash", ctypes.c_void_p)]
 
 
 class cb_routing_view_t(ctypes.Structure):
@@ -195,12 +202,14 @@ class MoELayer:
 
     def __init__(self, T, d, f, E, k, w_router, w_gate, w_up, w_down, router_bias=None,
                  s_gate=None, s_up=None, s_down=None, device=0, keep_logits=False, stage_timing=False,
-                 flags=0):
+                 flags=0, router="softmax", w_hash=None):
         flags |= (CB_FLAG_KEEP_LOGITS if keep_logits else 0) | (CB_FLAG_STAGE_TIMING if stage_timing else 0)
+        mode = ROUTER_MODES[router]
+        hash_dims = 0 if w_hash is None else int(w_hash.shape[0])
         self.cfg = cb_moe_config_t(T, d, f, E, k, CB_W_INT8 if s_gate is not None else CB_W_BF16,
-                                   device, flags)
+                                   device, flags, mode, hash_dims)
         w = cb_moe_weights_t(_ptr(w_router), _ptr(router_bias), _ptr(w_gate), _ptr(w_up), _ptr(w_down),
-                             _ptr(s_gate), _ptr(s_up), _ptr(s_down))
+                             _ptr(s_gate), _ptr(s_up), _ptr(s_down), _ptr(w_hash))
         st, h = cb_moe_init(self.cfg, w)
         if st != CB_OK:
             raise CbMoeError(st, "cb_moe_init")

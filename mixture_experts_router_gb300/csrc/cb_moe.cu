@@ -28,6 +28,7 @@ struct cb_moe {
   uint64_t block_bytes;
   // weights (handle-owned copies)
   uint16_t* wr;
+  uint16_t* wh;  // hash router projection [hash_dims][d], or nullptr
   float* bias;
   void* wgu;  // [E][f/B][2][B][d]: gate rows then up rows per B-row block (B = 128 bf16, 64 int8)
   void* wd;   // [E][d][f]
@@ -65,7 +66,7 @@ struct cb_moe {
 namespace {
 
 struct Layout {
-  uint64_t off_wr, off_bias, off_wgu, off_wd, off_sg, off_su, off_sd;
+  uint64_t off_wr, off_bias, off_wgu, off_wd, off_sg, off_su, off_sd, off_wh;
   uint64_t off_xp, off_hb, off_y, off_ids, off_w, off_logits, off_chunk, off_counts, off_offsets, off_mtile_off,
       off_mtile_expert, off_ptile_off, off_ptile_expert, off_tok, off_inv, off_err, off_xs, off_os;
   uint64_t total;
@@ -95,6 +96,7 @@ Layout plan(const cb_moe_config_t& c) {
   L.off_sg = take(c.wdtype == CB_W_INT8 ? E * f * 4 : 0);
   L.off_su = take(c.wdtype == CB_W_INT8 ? E * f * 4 : 0);
   L.off_sd = take(c.wdtype == CB_W_INT8 ? E * d * 4 : 0);
+  L.off_wh = take(c.router_mode == CB_ROUTER_HASH ? static_cast<uint64_t>(c.hash_dims) * d * 2 : 0);
   L.off_xp = take(mpad * d * 2);
   L.off_hb = take(mpad * f * 2);
   L.off_y = take(mpad * d * 4);
@@ -127,6 +129,10 @@ cb_status_t validate_config(const cb_moe_config_t* c) {
   if (c->wdtype != CB_W_BF16 && c->wdtype != CB_W_INT8) return CB_ERR_INVALID_ARG;
   if (c->d_model % 256 != 0 || c->d_ff % 256 != 0) return CB_ERR_UNSUPPORTED;
   if (c->n_experts > 256 || c->top_k > 16) return CB_ERR_UNSUPPORTED;
+  if (c->router_mode < CB_ROUTER_SOFTMAX_TOPK || c->router_mode > CB_ROUTER_HASH) return CB_ERR_INVALID_ARG;
+  if (c->router_mode == CB_ROUTER_HASH &&
+      (c->top_k != 1 || c->hash_dims < 1 || c->hash_dims > CB_MAX_HASH_DIMS))
+    return CB_ERR_INVALID_ARG;
   if ((c->flags & ~(CB_FLAG_KEEP_LOGITS | CB_FLAG_STAGE_TIMING | CB_FLAG_TEST_STALL)) != 0)
     return CB_ERR_INVALID_ARG;
   // 32-bit row and tile indices everywhere
@@ -211,7 +217,19 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
     ra.blk_counts = h->chunk;
     ra.local_rank = h->inv;
   }
-  if (h->router_tc) {
+  ra.raw_weights = c.router_mode == CB_ROUTER_RAW_LOGITS ? 1 : 0;
+  if (c.router_mode == CB_ROUTER_HASH) {
+    HashRouterArgs ha{};
+    ha.x = static_cast<const uint16_t*>(x);
+    ha.wh = h->wh;
+    ha.T = c.n_tokens;
+    ha.d = c.d_model;
+    ha.E = c.n_experts;
+    ha.hash_dims = c.hash_dims;
+    ha.ids = h->ids;
+    ha.w = h->w;
+    if (launch_router_hash(ha, s) != cudaSuccess || !mark(1)) return CB_ERR_CUDA;
+  } else if (h->router_tc) {
     if (h->tm_x_src != x) {
       if (!make_tmap(&h->tm_x, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c.d_model, c.n_tokens, 64, 128))
         return CB_ERR_CUDA;
@@ -435,14 +453,15 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
   *out = nullptr;
   cb_status_t st = validate_config(cfg);
   if (st != CB_OK) return st;
-  if (wts == nullptr || wts->w_router == nullptr || wts->w_gate == nullptr || wts->w_up == nullptr ||
-      wts->w_down == nullptr)
+  const bool hashr = cfg->router_mode == CB_ROUTER_HASH;
+  if (wts == nullptr || (wts->w_router == nullptr && !hashr) || wts->w_gate == nullptr || wts->w_up == nullptr ||
+      wts->w_down == nullptr || (hashr && wts->w_hash == nullptr))
     return CB_ERR_INVALID_ARG;
   const bool int8w = cfg->wdtype == CB_W_INT8;
   if (int8w && (wts->s_gate == nullptr || wts->s_up == nullptr || wts->s_down == nullptr))
     return CB_ERR_UNSUPPORTED;
   const void* ptrs[] = {wts->w_router, wts->router_bias, wts->w_gate, wts->w_up, wts->w_down,
-                        wts->s_gate,   wts->s_up,        wts->s_down};
+                        wts->s_gate,   wts->s_up,        wts->s_down, wts->w_hash};
   for (const void* p : ptrs)
     if (p != nullptr && !aligned16(p)) return CB_ERR_ALIGNMENT;
 
@@ -467,6 +486,7 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
   }
   char* b = h->block;
   h->wr = reinterpret_cast<uint16_t*>(b + L.off_wr);
+  h->wh = hashr ? reinterpret_cast<uint16_t*>(b + L.off_wh) : nullptr;
   h->bias = wts->router_bias ? reinterpret_cast<float*>(b + L.off_bias) : nullptr;
   h->wgu = b + L.off_wgu;
   h->wd = b + L.off_wd;
@@ -496,7 +516,13 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
   const uint64_t eb = int8w ? 1 : 2;
   bool ok = cudaMemset(h->block + L.off_xp, 0, L.off_ids - L.off_xp) == cudaSuccess &&
             cudaMemset(h->block + L.off_ids, 0, L.total - L.off_ids) == cudaSuccess;
-  ok = ok && cudaMemcpy(h->wr, wts->w_router, E * d * 2, cudaMemcpyDeviceToDevice) == cudaSuccess;
+  if (wts->w_router != nullptr)
+    ok = ok && cudaMemcpy(h->wr, wts->w_router, E * d * 2, cudaMemcpyDeviceToDevice) == cudaSuccess;
+  else
+    ok = ok && cudaMemset(h->wr, 0, E * d * 2) == cudaSuccess;
+  if (hashr)
+    ok = ok && cudaMemcpy(h->wh, wts->w_hash, static_cast<uint64_t>(cfg->hash_dims) * d * 2,
+                          cudaMemcpyDeviceToDevice) == cudaSuccess;
   if (ok && h->bias) ok = cudaMemcpy(h->bias, wts->router_bias, E * 4, cudaMemcpyDeviceToDevice) == cudaSuccess;
   ok = ok && cudaMemcpy(h->wd, wts->w_down, E * d * f * eb, cudaMemcpyDeviceToDevice) == cudaSuccess;
   if (ok && int8w) {
@@ -576,7 +602,7 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
     const int64_t nb = (static_cast<int64_t>(cfg->n_tokens) + rb - 1) / rb;
     h->rank_block = 0;
     h->n_rank_blocks = 0;
-    if (!h->router_tc && (nb + 1) * (cfg->n_experts + 1) <= kFusedScanWords &&
+    if (!h->router_tc && !hashr && (nb + 1) * (cfg->n_experts + 1) <= kFusedScanWords &&
         !(fv != nullptr && std::strcmp(fv, "0") == 0)) {
       h->rank_block = rb;
       h->n_rank_blocks = static_cast<int32_t>(nb);

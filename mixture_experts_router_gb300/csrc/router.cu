@@ -4,6 +4,8 @@
 // "discosf.com/news/4774337" §5.1).  Softmax is applied and renormalised
 // over the k ("Colibri：面向MoE模型的高性能C语言推理引擎" §2.1); since its full
 // denominator cancels, w_s = exp(l_s - l_0) / sum_{j<k} exp(l_j - l_0).
+// With raw_weights the weights are the selected logits themselves (top-k
+// straight on the raw logits, no softmax: the first page's §3.2).
 //
 // The logit GEMM [T x d] x [d x E] runs on the tensor cores with
 // mma.sync m16n8k16 (bf16 products are exact, fp32 accumulation).  It is a
@@ -202,7 +204,7 @@ __global__ void __launch_bounds__(RCfg<NT, KS, NS, MTB>::THREADS) router_mma_ker
     for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
     if (lane < a.k) {
       a.ids[static_cast<int64_t>(t) * a.k + lane] = my_i;
-      a.w[static_cast<int64_t>(t) * a.k + lane] = ex / sum;
+      a.w[static_cast<int64_t>(t) * a.k + lane] = a.raw_weights ? my_v : ex / sum;
       s_ids[r * 16 + lane] = my_i;
     }
   }

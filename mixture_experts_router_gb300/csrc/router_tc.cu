@@ -2,7 +2,8 @@
 // the top-k gate (the router kernel of "Colibri：面向MoE架构的C语言级高效推理引擎"
 // §3.2, routing decided on the device: "discosf.com/news/4774337" §5.1), with
 // softmax renormalised over the k ("Colibri：面向MoE模型的高性能C语言推理引擎"
-// §2.1): w_s = exp(l_s - l_0) / sum_{j<k} exp(l_j - l_0).
+// §2.1): w_s = exp(l_s - l_0) / sum_{j<k} exp(l_j - l_0); with raw_weights,
+// w_s = l_s (no softmax, the first page's §3.2).
 //
 // A tile is 128 tokens; the whole expert dimension (E padded to NP, a power of
 // two >= 16) is one UMMA N.  x is streamed by TMA (rows past T read as zeros),
@@ -243,7 +244,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int s2 = 0; s2 < KMAX; ++s2) {
           if (s2 < a.k) {
             a.ids[static_cast<int64_t>(t) * a.k + s2] = static_cast<int>(~static_cast<uint32_t>(top[s2]));
-            a.w[static_cast<int64_t>(t) * a.k + s2] = ex[s2] / den;
+            a.w[static_cast<int64_t>(t) * a.k + s2] = a.raw_weights ? topv[s2] : ex[s2] / den;
           }
         }
       }

@@ -58,6 +58,13 @@ def cfg(**kw):
     (dict(n_experts=32, top_k=17), cb.CB_ERR_UNSUPPORTED),
     (dict(wdtype=5), cb.CB_ERR_INVALID_ARG),
     (dict(flags=0x80), cb.CB_ERR_INVALID_ARG),
+    (dict(router_mode=1), cb.CB_OK),
+    (dict(router_mode=2, top_k=1, hash_dims=8), cb.CB_OK),
+    (dict(router_mode=3), cb.CB_ERR_INVALID_ARG),
+    (dict(router_mode=-1), cb.CB_ERR_INVALID_ARG),
+    (dict(router_mode=2, top_k=2, hash_dims=4), cb.CB_ERR_INVALID_ARG),
+    (dict(router_mode=2, top_k=1, hash_dims=0), cb.CB_ERR_INVALID_ARG),
+    (dict(router_mode=2, top_k=1, hash_dims=9), cb.CB_ERR_INVALID_ARG),
 ])
 def test_config_validation(lib, kw, status):
     st, nbytes = cb.cb_moe_device_bytes(cfg(**kw))
@@ -74,6 +81,13 @@ def test_device_bytes_cover_the_workspace(lib):
     assert weights < nbytes < weights + 2 * 10**9
 
 
+def test_device_bytes_hold_the_hash_projection(lib):
+    st, plain = cb.cb_moe_device_bytes(cfg(top_k=1))
+    st2, hashed = cb.cb_moe_device_bytes(cfg(top_k=1, router_mode=2, hash_dims=8))
+    assert st == st2 == cb.CB_OK
+    assert 8 * 256 * 2 <= hashed - plain <= 8 * 256 * 2 + 256
+
+
 def test_init_rejects_bad_arguments_before_cuda(lib):
     w = cb.cb_moe_weights_t()
     st, h = cb.cb_moe_init(cfg(d_model=300), w)
@@ -86,5 +100,10 @@ def test_init_rejects_bad_arguments_before_cuda(lib):
     w = cb.cb_moe_weights_t(w_router=16, w_gate=32, w_up=48, w_down=64)
     st, h = cb.cb_moe_init(cfg(wdtype=1), w)         # int8 without scales
     assert st == cb.CB_ERR_UNSUPPORTED
+    st, h = cb.cb_moe_init(cfg(top_k=1, router_mode=2, hash_dims=4), w)   # hash router without W_h
+    assert st == cb.CB_ERR_INVALID_ARG and h is None
+    w = cb.cb_moe_weights_t(w_router=16, w_gate=32, w_up=48, w_down=64, w_hash=72)
+    st, h = cb.cb_moe_init(cfg(top_k=1, router_mode=2, hash_dims=4), w)   # misaligned W_h
+    assert st == cb.CB_ERR_ALIGNMENT
     assert cb.cb_moe_forward(None, 16, 32, 0) == cb.CB_ERR_INVALID_ARG
     assert cb.cb_moe_free(None) == cb.CB_OK

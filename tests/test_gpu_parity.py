@@ -299,3 +299,63 @@ def test_single_cta_gemms_full_size(name, monkeypatch):
     monkeypatch.setenv("CB_MOE_PAIR", "0")
     rep = gh.full_check(synth.make_layer(synth.WORKLOADS[name]), sample=FULL[name])
     print(name, "single CTA", rep)
+
+
+RAW_SMALL = ["ragged_mid", "skewed_small", "e256_k16", "int8_k6"]
+
+
+@pytest.mark.parametrize("name", RAW_SMALL)
+def test_raw_logit_router_small(name):
+    """CB_ROUTER_RAW_LOGITS: the same experts as the softmax gate, weighted by the
+    raw logits (mma.sync router for E <= 16, tcgen05 router above)."""
+    rep = gh.full_check(synth.make_layer(synth.with_router(SMALL[name], "raw")))
+    print(name, "raw", rep)
+
+
+HASH_SMALL = {
+    "h_ragged": synth.custom_shape("h_ragged", T=300, d=512, f=768, E=8, k=1, seed=71, router="hash", hash_dims=8),
+    "h_e128_d3": synth.custom_shape("h_e128", T=1000, d=256, f=256, E=128, k=1, seed=72, router="hash",
+                                    hash_dims=3),
+    "h_one_dim": synth.custom_shape("h_one", T=33, d=768, f=256, E=5, k=1, seed=73, router="hash", hash_dims=1),
+    "h_int8": synth.custom_shape("h_int8", T=700, d=256, f=512, E=64, k=1, wdtype="int8", seed=74, router="hash",
+                                 hash_dims=8),
+}
+
+
+@pytest.mark.parametrize("name", list(HASH_SMALL))
+def test_hash_router_small(name):
+    """CB_ROUTER_HASH: one expert per token from the hashed projection, bit for bit."""
+    rep = gh.full_check(synth.make_layer(HASH_SMALL[name]))
+    print(name, "hash", rep)
+
+
+@pytest.mark.parametrize("router", ["raw", "hash"])
+def test_router_variants_full_size(router):
+    shape = synth.with_router(synth.WORKLOADS["mixtral_prefill"], router)
+    rep = gh.full_check(synth.make_layer(shape), sample=24)
+    print(router, rep)
+
+
+@pytest.mark.parametrize("case", ["hash", "hash_order"])
+def test_hash_router_golden_cases(case):
+    """The hand-derived cases of tests/golden/router_variants.json (truncation,
+    negative values, saturation, a float sum that rounds), in the first four
+    columns of a d = 256 layer."""
+    import json
+    import os
+    import oracle_pins
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "router_variants.json")))[case]
+    T, d, E = len(g["x"]), 256, g["E"]
+    x = np.zeros((T, d))
+    x[:, :4] = g["x"]
+    wh = np.zeros((len(g["wh"]), d))
+    wh[:, :4] = g["wh"]
+    zeros = np.zeros((E, d))
+    layer = oracle_pins.make_layer_from_values(x, zeros, np.zeros((E, 256, d)), np.zeros((E, 256, d)),
+                                               np.zeros((E, d, 256)), 1, router="hash", wh=wh)
+    gl = gh.GpuLayer(layer, keep_logits=False)
+    try:
+        gl.run()
+        assert gl.routing()["ids"].ravel().tolist() == g["expected_ids"]
+    finally:
+        gl.close()
