@@ -28,7 +28,7 @@ struct cb_moe {
   uint64_t block_bytes;
   // weights (handle-owned copies)
   uint16_t* wr;
-  uint16_t* wh;  // hash router projection [hash_dims][d], or nullptr
+  float* wh;  // hash router projection [hash_dims][d] widened to fp32, or nullptr
   float* bias;
   void* wgu;  // [E][f/B][2][B][d]: gate rows then up rows per B-row block (B = 128 bf16, 64 int8)
   void* wd;   // [E][d][f]
@@ -96,7 +96,7 @@ Layout plan(const cb_moe_config_t& c) {
   L.off_sg = take(c.wdtype == CB_W_INT8 ? E * f * 4 : 0);
   L.off_su = take(c.wdtype == CB_W_INT8 ? E * f * 4 : 0);
   L.off_sd = take(c.wdtype == CB_W_INT8 ? E * d * 4 : 0);
-  L.off_wh = take(c.router_mode == CB_ROUTER_HASH ? static_cast<uint64_t>(c.hash_dims) * d * 2 : 0);
+  L.off_wh = take(c.router_mode == CB_ROUTER_HASH ? static_cast<uint64_t>(c.hash_dims) * d * 4 : 0);  // fp32
   L.off_xp = take(mpad * d * 2);
   L.off_hb = take(mpad * f * 2);
   L.off_y = take(mpad * d * 4);
@@ -486,7 +486,7 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
   }
   char* b = h->block;
   h->wr = reinterpret_cast<uint16_t*>(b + L.off_wr);
-  h->wh = hashr ? reinterpret_cast<uint16_t*>(b + L.off_wh) : nullptr;
+  h->wh = hashr ? reinterpret_cast<float*>(b + L.off_wh) : nullptr;
   h->bias = wts->router_bias ? reinterpret_cast<float*>(b + L.off_bias) : nullptr;
   h->wgu = b + L.off_wgu;
   h->wd = b + L.off_wd;
@@ -521,8 +521,8 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
   else
     ok = ok && cudaMemset(h->wr, 0, E * d * 2) == cudaSuccess;
   if (hashr)
-    ok = ok && cudaMemcpy(h->wh, wts->w_hash, static_cast<uint64_t>(cfg->hash_dims) * d * 2,
-                          cudaMemcpyDeviceToDevice) == cudaSuccess;
+    ok = ok && prepare_hash_weights(static_cast<const uint16_t*>(wts->w_hash), cfg->hash_dims, static_cast<int>(d),
+                                    h->wh, nullptr) == cudaSuccess;
   if (ok && h->bias) ok = cudaMemcpy(h->bias, wts->router_bias, E * 4, cudaMemcpyDeviceToDevice) == cudaSuccess;
   ok = ok && cudaMemcpy(h->wd, wts->w_down, E * d * f * eb, cudaMemcpyDeviceToDevice) == cudaSuccess;
   if (ok && int8w) {

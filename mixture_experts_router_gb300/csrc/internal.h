@@ -40,15 +40,18 @@ struct RouterArgs {
   int32_t* local_rank;
   int32_t raw_weights;   // 1: w = the selected raw logits (no softmax)
 };
-// hash router: x [T][d] and W_h [hash_dims][d] (bf16) -> ids [T], w [T] = 1
+// hash router: x [T][d] (bf16) and W_h [hash_dims][d] widened to fp32 ->
+// ids [T], w [T] = 1
 struct HashRouterArgs {
   const uint16_t* x;
-  const uint16_t* wh;
+  const float* wh;
   int32_t T, d, E, hash_dims;
   int32_t* ids;
   float* w;
 };
 cudaError_t launch_router_hash(const HashRouterArgs& a, cudaStream_t s);
+// W_h bf16 [hash_dims][d] -> fp32 (exact) for HashRouterArgs::wh
+cudaError_t prepare_hash_weights(const uint16_t* wh, int hash_dims, int d, float* wh_f32, cudaStream_t s);
 // tokens per block of the mma router, each one rank block of the fused
 // dispatch ranks (the tcgen05 router leaves the ranking to the dispatch)
 int router_rank_block(int E);
