@@ -645,6 +645,21 @@ cb_status_t cb_moe_forward_f32out(cb_moe_t* h, const void* x, float* out, void* 
                      [&](cudaStream_t s) { return enqueue_forward(h, x, out, true, s); });
 }
 
+namespace {
+// Device address of host memory that CUDA maps into the device's address
+// space (pinned by cudaHostAlloc / cudaHostRegister), or nullptr (pageable
+// memory, or a pointer CUDA does not know).
+void* mapped_host_ptr(void* host) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, host) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (a.type != cudaMemoryTypeHost || a.devicePointer == nullptr || !aligned16(a.devicePointer)) return nullptr;
+  return a.devicePointer;
+}
+}  // namespace
+
 cb_status_t cb_moe_forward_host(cb_moe_t* h, const void* x_host, void* out_host, void* stream) {
   if (h == nullptr || x_host == nullptr || out_host == nullptr) return CB_ERR_INVALID_ARG;
   if (h->cfg.n_tokens == 0) return CB_OK;
@@ -652,10 +667,13 @@ cb_status_t cb_moe_forward_host(cb_moe_t* h, const void* x_host, void* out_host,
   DeviceGuard guard(h->cfg.device);
   if (!guard.ok) return CB_ERR_CUDA;
   const uint64_t bytes = static_cast<uint64_t>(h->cfg.n_tokens) * h->cfg.d_model * 2;
+  // A mapped output buffer receives the combine's rows directly over the
+  // host link, in place of a staging copy back after the combine.
+  void* out_mapped = mapped_host_ptr(out_host);
   return run_graphed(h, 2, x_host, out_host, static_cast<cudaStream_t>(stream), [&](cudaStream_t s) {
     if (cudaMemcpyAsync(h->x_stage, x_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return CB_ERR_CUDA;
-    const cb_status_t st2 = enqueue_forward(h, h->x_stage, h->out_stage, false, s);
-    if (st2 != CB_OK) return st2;
+    const cb_status_t st2 = enqueue_forward(h, h->x_stage, out_mapped ? out_mapped : h->out_stage, false, s);
+    if (st2 != CB_OK || out_mapped != nullptr) return st2;
     if (cudaMemcpyAsync(out_host, h->out_stage, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) return CB_ERR_CUDA;
     return CB_OK;
   });
