@@ -30,7 +30,7 @@ struct cb_moe {
   uint16_t* wr;
   float* wh;  // hash router projection [hash_dims][d] widened to fp32, or nullptr
   float* bias;
-  void* wgu;  // [E][f/B][2][B][d]: gate rows then up rows per B-row block (B = 128 bf16, 64 int8)
+  void* wgu;  // [E][f/B][2][B][d]: gate rows then up rows per B-row block (B = 128 bf16; int8: 16 or 64)
   void* wd;   // [E][d][f]
   float *sg, *su, *sd;
   // workspace
@@ -58,9 +58,11 @@ struct cb_moe {
     cudaGraphExec_t exec;
   } graphs[3];             // bf16 forward, fp32-out forward, host-buffer forward
   bool gather_a;           // gate/up GEMM gathers its rows from x (no Xp copy)
+  bool int8_tm;            // int8 GEMMs convert their weights into tensor memory
   const void* tm_x_src;    // x pointer tm_x was encoded for
   const void* tm_xg_src;   // x pointer tm_xg was encoded for
-  CUtensorMap tm_a_gu, tm_b_gu, tm_a_dn, tm_b_dn, tm_b_dn64, tm_b_gu128, tm_b_dn128, tm_y, tm_x, tm_xg, tm_wr;
+  CUtensorMap tm_a_gu, tm_b_gu, tm_a_dn, tm_b_dn, tm_b_dn64, tm_b_gu128, tm_b_dn128, tm_y, tm_x, tm_xg, tm_wr,
+      tm_w_gu8, tm_w_dn8;
 };
 
 namespace {
@@ -273,7 +275,9 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
   ga.ptile_off = h->ptile_off;
   ga.ptile_expert = h->ptile_expert;
   ga.E = c.n_experts;
-  ga.n_tiles = c.d_ff / (int8w ? grouped_gemm_int8_tile_n(kGateUpSwiGLU) : grouped_gemm_tile_n(kGateUpSwiGLU));
+  ga.n_tiles = c.d_ff / (int8w ? (h->int8_tm ? grouped_gemm_int8_tm_tile_n(kGateUpSwiGLU)
+                                              : grouped_gemm_int8_tile_n(kGateUpSwiGLU))
+                                : grouped_gemm_tile_n(kGateUpSwiGLU));
   ga.k_blocks = c.d_model / 64;
   ga.b_rows_per_expert = 2 * c.d_ff;
   ga.out = h->hb;
@@ -303,7 +307,9 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
   const bool pair_gu = !int8w && h->pair_gu && !h->gather_a;
   const bool pair_dn = !int8w && h->pair_dn;
   cudaError_t e1;
-  if (int8w) {
+  if (int8w && h->int8_tm) {
+    e1 = launch_grouped_gemm_int8_tm(kGateUpSwiGLU, h->tm_a_gu, h->tm_w_gu8, ga, s);
+  } else if (int8w) {
     e1 = launch_grouped_gemm_int8(kGateUpSwiGLU, h->tm_a_gu, h->tm_b_gu, h->tm_y, ga, s);
   } else if (pair_gu) {
     GemmArgs gp = ga;
@@ -318,7 +324,8 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
   gd.gather = 0;
   gd.test_stall = 0;
   gd.wait_limit_ns = kWaitLimitNs;
-  gd.n_tiles = c.d_model / (int8w ? grouped_gemm_int8_tile_n(kDownF32) : grouped_gemm_tile_n(kDownF32));
+  gd.n_tiles = c.d_model / (int8w ? (h->int8_tm ? grouped_gemm_int8_tm_tile_n(kDownF32) : grouped_gemm_int8_tile_n(kDownF32))
+                                   : grouped_gemm_tile_n(kDownF32));
   gd.k_blocks = c.d_ff / 64;
   gd.b_rows_per_expert = c.d_model;
   gd.out = h->y;
@@ -326,7 +333,9 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
   gd.scale0 = h->sd;
   gd.scale1 = nullptr;
   cudaError_t e2;
-  if (int8w) {
+  if (int8w && h->int8_tm) {
+    e2 = launch_grouped_gemm_int8_tm(kDownF32, h->tm_a_dn, h->tm_w_dn8, gd, s);
+  } else if (int8w) {
     e2 = launch_grouped_gemm_int8(kDownF32, h->tm_a_dn, h->tm_b_dn, h->tm_y, gd, s);
   } else if (pair_dn) {
     GemmArgs gp = gd;
@@ -531,7 +540,16 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
          cudaMemcpy(h->sd, wts->s_down, E * d * 4, cudaMemcpyDeviceToDevice) == cudaSuccess;
   }
   // gate/up interleave: block n of expert e = gate rows [Bn, Bn+B) then the same up rows
-  const uint64_t brows = int8w ? grouped_gemm_int8_gateup_block() : 128;
+  // int8 expert GEMMs: weights converted into tensor memory as the MMA's A
+  // operand (default), or CB_MOE_INT8=smem for the kernel that converts them
+  // into shared memory as the B operand; the two interleave gate and up rows
+  // in blocks of different sizes
+  {
+    const char* iv = std::getenv("CB_MOE_INT8");
+    h->int8_tm = !(iv != nullptr && std::strcmp(iv, "smem") == 0);
+  }
+  const uint64_t brows =
+      int8w ? (h->int8_tm ? grouped_gemm_int8_tm_gateup_block() : grouped_gemm_int8_gateup_block()) : 128;
   const uint64_t blk = brows * d * eb;  // bytes of one block of weight rows
   const uint64_t nblk = E * (f / brows);
   ok = ok && cudaMemcpy2D(h->wgu, 2 * blk, wts->w_gate, blk, blk, nblk, cudaMemcpyDeviceToDevice) == cudaSuccess;
@@ -547,11 +565,16 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
   ok = ok && make_tmap(&h->tm_b_dn, h->wd, wdt, eb, f, E * d, 64, brows_box, wsw);
   ok = ok && make_tmap(&h->tm_y, h->y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, mpad, 32, 32);
   ok = ok && make_tmap(&h->tm_b_dn64, h->wd, wdt, eb, f, E * d, 64, 64, wsw);
+  if (int8w) {
+    ok = ok && make_tmap(&h->tm_w_gu8, h->wgu, wdt, 1, d, E * 2 * f, 128, 128);
+    ok = ok && make_tmap(&h->tm_w_dn8, h->wd, wdt, 1, f, E * d, 128, 128);
+  }
   if (!int8w) {
     ok = ok && make_tmap(&h->tm_b_gu128, h->wgu, wdt, eb, d, E * 2 * f, 64, 128, wsw);
     ok = ok && make_tmap(&h->tm_b_dn128, h->wd, wdt, eb, f, E * d, 64, 128, wsw);
   }
   ok = ok && grouped_gemm_prepare() == cudaSuccess && grouped_gemm_int8_prepare() == cudaSuccess &&
+       grouped_gemm_int8_tm_prepare() == cudaSuccess &&
        router_prepare() == cudaSuccess && router_tc_prepare() == cudaSuccess && dispatch_prepare() == cudaSuccess;
   // router: tcgen05 for wide expert counts, the mma.sync split-K router for
   // E <= 16 (bound by reading x, where more CTAs help); CB_MOE_ROUTER=tc|mma

@@ -161,5 +161,13 @@ cudaError_t launch_grouped_gemm_int8(GemmKind kind, const CUtensorMap& tm_a, con
 cudaError_t grouped_gemm_int8_prepare();
 int grouped_gemm_int8_tile_n(GemmKind kind);
 int grouped_gemm_int8_gateup_block();  // gate/up rows interleaved in blocks of this size
+// int8 weights converted into tensor memory (the MMA's A operand): tiles are
+// 128 weight rows against a pair of m-tiles; tm_x: the activations (128 x 64
+// boxes), tm_w: the int8 weights with a 128 x 128 box and the 128-byte swizzle
+cudaError_t launch_grouped_gemm_int8_tm(GemmKind kind, const CUtensorMap& tm_x, const CUtensorMap& tm_w,
+                                        const GemmArgs& a, cudaStream_t s);
+cudaError_t grouped_gemm_int8_tm_prepare();
+int grouped_gemm_int8_tm_tile_n(GemmKind kind);
+int grouped_gemm_int8_tm_gateup_block();  // gate/up rows interleaved in blocks of this size
 
 }  // namespace cbmoe

@@ -22,6 +22,8 @@ SMALL = {
     # int8 experts with per-channel scales: several tiles, ragged tails
     "int8_mid": synth.custom_shape("int8_mid", T=300, d=512, f=768, E=8, k=2, wdtype="int8", seed=27),
     "int8_k6": synth.custom_shape("int8_k6", T=700, d=256, f=512, E=64, k=6, wdtype="int8", seed=28),
+    # int8 experts of about five m-tiles each: full and half-empty m-tile pairs
+    "int8_pairs": synth.custom_shape("int8_pairs", T=1100, d=512, f=768, E=4, k=2, wdtype="int8", seed=29),
 }
 
 FULL = {  # workload: tokens sampled for the output check
@@ -290,6 +292,21 @@ def test_kernels_per_forward(fused, name, expect, monkeypatch):
         assert gl.m.kernels_per_forward() == expect
     finally:
         gl.close()
+
+
+@pytest.mark.parametrize("name", ["int8_mid", "int8_k6", "int8_pairs"])
+def test_int8_smem_kernel_small(name, monkeypatch):
+    """CB_MOE_INT8=smem: the int8 GEMMs that convert the weights into shared
+    memory (the MMA's B operand) instead of tensor memory; same results."""
+    monkeypatch.setenv("CB_MOE_INT8", "smem")
+    rep = gh.full_check(synth.make_layer(SMALL[name]))
+    print(name, "int8 smem", rep)
+
+
+def test_int8_smem_kernel_full_size(monkeypatch):
+    monkeypatch.setenv("CB_MOE_INT8", "smem")
+    rep = gh.full_check(synth.make_layer(synth.WORKLOADS["int8"]), sample=FULL["int8"])
+    print("int8 smem", rep)
 
 
 @pytest.mark.parametrize("name", ["mixtral_prefill", "skewed"])
