@@ -143,10 +143,14 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(inside)}
 
 
-def gemm_source_digest() -> str:
-    """First 16 hex digits of the sha256 over the bf16 grouped-GEMM sources."""
+def gemm_source_digest(sources=None) -> str:
+    """First 16 hex digits of the sha256 over grouped-GEMM sources (default: the
+    bf16 kernels'; a traffic entry may name its own, relative to the package's
+    csrc/)."""
     h = hashlib.sha256()
-    for path in GEMM_SOURCES:
+    paths = GEMM_SOURCES if sources is None else [os.path.join(ROOT, "mixture_experts_router_gb300", "csrc", s)
+                                                  for s in sources]
+    for path in paths:
         with open(path, "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -162,7 +166,7 @@ def measured_traffic(kernel_key):
     entry = data.get(kernel_key)
     if not entry:
         return None
-    digest = gemm_source_digest()
+    digest = gemm_source_digest(entry.get("sources"))
     if entry.get("source_sha256_16") != digest:
         return None
     return entry.get("dram_bytes_per_launch")
@@ -423,7 +427,7 @@ def run_ours(args):
         "config": config_block(shape, args.l2_flush_mb),
         "e2e": {"value": shape.T * world * k2 / (e2e_ms / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": shape.T * shape.d * 2, "d2h_bytes_per_step": shape.T * shape.d * 2,
-                "steps": k2, "api": "cb_moe_forward_host (pinned host x and out, copies on the stream)"},
+                "steps": k2, "api": "cb_moe_forward_host (pinned host x and out: x copied on the stream, out written by the combine through the host mapping)"},
         "gpu_launches": launches_per_forward * args.steps,
         "roofline": roof,
         "stages": stages,

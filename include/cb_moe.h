@@ -153,9 +153,13 @@ CB_API cb_status_t cb_moe_forward_f32out(cb_moe_t *h, const void *x, float *out,
 
 /*
  * Same pass from host memory: copies x_host (bf16 [T][d]) to a handle-owned
- * device buffer, runs cb_moe_forward, and copies the bf16 result back to
- * out_host, all on `stream`.  Asynchronous when both host buffers are pinned;
- * the caller synchronises the stream before reading out_host.
+ * device buffer and runs cb_moe_forward, all on `stream`.  When out_host is
+ * page-locked memory that CUDA maps into the device's address space
+ * (cudaHostAlloc / cudaHostRegister, as torch's pin_memory does), the combine
+ * writes the bf16 result straight into it; otherwise the result goes to a
+ * handle-owned device buffer and is copied back.  Asynchronous when both host
+ * buffers are pinned; the caller synchronises the stream before reading
+ * out_host.
  */
 CB_API cb_status_t cb_moe_forward_host(cb_moe_t *h, const void *x_host, void *out_host, void *stream);
 
