@@ -40,6 +40,7 @@ struct cb_moe {
   int32_t* ids;
   float* w;
   float* logits;
+  float* rpart;  // tcgen05 router's partial logits
   int32_t *chunk, *counts, *offsets, *mtile_off, *mtile_expert, *ptile_off, *ptile_expert, *tok, *inv;
   int* err;
   uint16_t *x_stage, *out_stage;
@@ -69,7 +70,7 @@ namespace {
 
 struct Layout {
   uint64_t off_wr, off_bias, off_wgu, off_wd, off_sg, off_su, off_sd, off_wh;
-  uint64_t off_xp, off_hb, off_y, off_ids, off_w, off_logits, off_chunk, off_counts, off_offsets, off_mtile_off,
+  uint64_t off_xp, off_hb, off_y, off_ids, off_w, off_logits, off_rpart, off_chunk, off_counts, off_offsets, off_mtile_off,
       off_mtile_expert, off_ptile_off, off_ptile_expert, off_tok, off_inv, off_err, off_xs, off_os;
   uint64_t total;
   int32_t max_mtiles, n_chunks;
@@ -105,6 +106,9 @@ Layout plan(const cb_moe_config_t& c) {
   L.off_ids = take(M * 4);
   L.off_w = take(M * 4);
   L.off_logits = take((c.flags & CB_FLAG_KEEP_LOGITS) ? T * E * 4 : 0);
+  // partial logits of the tcgen05 router: slices x 128-token tiles x E padded
+  L.off_rpart = take(static_cast<uint64_t>(kRouterMaxSlices) * ((T + 127) / 128) * 128 *
+                     static_cast<uint64_t>(router_tc_rows(static_cast<int>(E))) * 4);
   // per-chunk counts of the dispatch's own ranking, or the router's per-block
   // counts of the fused ranking (at most kFusedScanWords)
   L.off_chunk = take(std::max<uint64_t>(static_cast<uint64_t>(L.n_chunks) * E, kFusedScanWords) * 4);
@@ -237,7 +241,8 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
         return CB_ERR_CUDA;
       h->tm_x_src = x;
     }
-    if (launch_router_tc(h->tm_x, h->tm_wr, ra, h->num_sms, s) != cudaSuccess || !mark(1)) return CB_ERR_CUDA;
+    if (launch_router_tc(h->tm_x, h->tm_wr, ra, h->rpart, h->num_sms, s) != cudaSuccess || !mark(1))
+      return CB_ERR_CUDA;
   } else {
     if (launch_router(ra, s) != cudaSuccess || !mark(1)) return CB_ERR_CUDA;
   }
@@ -445,7 +450,8 @@ cb_status_t cb_moe_kernels_per_forward(const cb_moe_t* h, int32_t* n) {
     dispatch = 2;  // block-count scan + row copy (which also finalises the ranks)
   else
     dispatch = (static_cast<int64_t>(c.n_tokens) * c.top_k <= kDispatchSmallPairs ? 1 : 3) + (h->gather_a ? 0 : 1);
-  *n = 1 + dispatch + 2 + 1;
+  const int32_t router = (h->router_tc && c.router_mode != CB_ROUTER_HASH) ? 2 : 1;  // tcgen05: partials + top-k
+  *n = router + dispatch + 2 + 1;
   return CB_OK;
 }
 
@@ -508,6 +514,7 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
   h->ids = reinterpret_cast<int32_t*>(b + L.off_ids);
   h->w = reinterpret_cast<float*>(b + L.off_w);
   h->logits = (cfg->flags & CB_FLAG_KEEP_LOGITS) ? reinterpret_cast<float*>(b + L.off_logits) : nullptr;
+  h->rpart = reinterpret_cast<float*>(b + L.off_rpart);
   h->chunk = reinterpret_cast<int32_t*>(b + L.off_chunk);
   h->counts = reinterpret_cast<int32_t*>(b + L.off_counts);
   h->offsets = reinterpret_cast<int32_t*>(b + L.off_offsets);

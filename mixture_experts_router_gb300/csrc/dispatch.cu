@@ -366,10 +366,26 @@ __global__ void __launch_bounds__(kThreads) dispatch_copy(DispatchArgs a) {
 
 }  // namespace
 
+// The per-chunk counts of dispatch_count have the layout of the router's
+// per-block counts ([chunk][E]), so the shared-memory block scan turns them
+// into per-chunk row bases when they fit in max_words (kFusedScanWords after
+// dispatch_prepare, else the 48 KB a launch gets without it); its columns are
+// scanned by whole warps, where dispatch_scan walks each expert's chunks with
+// one thread.
+static void launch_chunk_scan(const DispatchArgs& a, int max_words, cudaStream_t s) {
+  if ((a.n_chunks + 1) * (a.E + 1) <= max_words && a.E <= 256) {
+    DispatchArgs b = a;
+    b.n_rank_blocks = a.n_chunks;
+    dispatch_scan_blocks<<<1, kScanThreads, (b.n_rank_blocks + 1) * (b.E + 1) * 4, s>>>(b);
+  } else {
+    dispatch_scan<<<1, kThreads, 0, s>>>(a);
+  }
+}
+
 cudaError_t launch_dispatch_ranks(const DispatchArgs& a, cudaStream_t s) {
   if (a.n_chunks <= 0) return cudaSuccess;
   dispatch_count<<<a.n_chunks, kThreads, 0, s>>>(a);
-  dispatch_scan<<<1, kThreads, 0, s>>>(a);
+  launch_chunk_scan(a, 12 * 1024, s);
   dispatch_scatter<<<a.n_chunks, kThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
@@ -392,7 +408,7 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s) {
     dispatch_small<<<1, kSmallThreads, 0, s>>>(a);
   } else {
     dispatch_count<<<a.n_chunks, kThreads, 0, s>>>(a);
-    dispatch_scan<<<1, kThreads, 0, s>>>(a);
+    launch_chunk_scan(a, kFusedScanWords, s);
     dispatch_scatter<<<a.n_chunks, kThreads, 0, s>>>(a);
   }
   if (a.copy_rows) dispatch_copy<<<a.gather_blocks, kThreads, 0, s>>>(a);

@@ -58,11 +58,16 @@ int router_rank_block(int E);
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t s);
 cudaError_t router_prepare();  // one-time function attributes
 // tcgen05 router: x and Wr through TMA (tm_x: [T][d] box 64x128; tm_w: [E][d]
-// box 64 x router_tc_rows(E)), one CTA per 128-token tile, persistent
-cudaError_t launch_router_tc(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const RouterArgs& a, int num_sms,
-                             cudaStream_t s);
+// box 64 x router_tc_rows(E)); units of 128 tokens x one of
+// router_tc_slices(..) slices of d write partial logits to `part`
+// ([slices][128 ceil(T/128)][router_tc_rows(E)] fp32, at most
+// kRouterMaxSlices slices), then one warp per token takes the top k
+constexpr int kRouterMaxSlices = 4;
+cudaError_t launch_router_tc(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const RouterArgs& a, float* part,
+                             int num_sms, cudaStream_t s);
 cudaError_t router_tc_prepare();
 int router_tc_rows(int E);
+int router_tc_slices(int T, int d, int E, int num_sms);
 
 // ---------------------------------------------------------------- dispatch
 struct DispatchArgs {

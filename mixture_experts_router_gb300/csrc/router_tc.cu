@@ -1,22 +1,29 @@
-// Router on the tcgen05 tensor cores: fp32 logits l = x Wr^T + b fused with
-// the top-k gate (the router kernel of "Colibri：面向MoE架构的C语言级高效推理引擎"
-// §3.2, routing decided on the device: "discosf.com/news/4774337" §5.1), with
-// softmax renormalised over the k ("Colibri：面向MoE模型的高性能C语言推理引擎"
-// §2.1): w_s = exp(l_s - l_0) / sum_{j<k} exp(l_j - l_0); with raw_weights,
-// w_s = l_s (no softmax, the first page's §3.2).
+// Router on the tcgen05 tensor cores for wide expert counts: fp32 logits
+// l = x Wr^T + b and the top-k gate (the router kernel of
+// "Colibri：面向MoE架构的C语言级高效推理引擎" §3.2, routing decided on the device:
+// "discosf.com/news/4774337" §5.1), with softmax renormalised over the k
+// ("Colibri：面向MoE模型的高性能C语言推理引擎" §2.1):
+// w_s = exp(l_s - l_0) / sum_{j<k} exp(l_j - l_0); with raw_weights, w_s = l_s
+// (no softmax, the first page's §3.2).
 //
-// A tile is 128 tokens; the whole expert dimension (E padded to NP, a power of
-// two >= 16) is one UMMA N.  x is streamed by TMA (rows past T read as zeros),
-// the router weights come by TMA too (rows past E read as zeros), and the
-// K loop rotates over NACC = 512 / NP accumulators in TMEM (k-block kb adds
-// into accumulator kb % NACC), so no fp32 accumulation chain in the tensor
-// core is longer than ceil(d / (64 NACC)) k-blocks; the epilogue sums the
-// NACC partials in a fixed order in fp32.  One epilogue thread owns one
-// token: it adds the bias, keeps a sorted top-k in registers (order: number
-// before NaN, larger first, lower index on ties) and writes ids and weights.
+// Two kernels:
 //
-// Per CTA (persistent over 128-token tiles): warp 0 TMA producer, warp 1
-// TMEM owner + MMA issuer, warps 2..5 epilogue.  Bounded waits as elsewhere.
+// router_tc_part_kernel: a unit is 128 tokens x one of KS slices of the
+// model dimension, so a layer of few 128-token tiles still fills the GPU
+// (KS units per tile).  The expert dimension (E padded to
+// NP, a power of two >= 16) is one UMMA N.  x and the router weights are
+// streamed by TMA (rows past T or E read as zeros); the K loop rotates over
+// NACC = 256 / NP accumulators in TMEM, so no fp32 accumulation chain in
+// the tensor core is longer than ceil(d / (64 KS NACC)) k-blocks.  The
+// epilogue sums the NACC accumulators in a fixed order and writes the
+// unit's partial logits part[ks][t][0..NP) with coalesced stores.
+//
+// router_topk_kernel: one warp per token sums the KS partials in slice order,
+// adds the bias, optionally writes the logits, and takes the top k by k
+// rounds of a warp-wide maximum (number before NaN, larger first, lower
+// index on ties), then the weights.
+//
+// Bounded waits as elsewhere.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -29,35 +36,27 @@ constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int THREADS = 192;
-constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t TMEM_COLS = 256;
 
+// Two CTAs share an SM (256 TMEM columns and at most 113 KB of shared memory
+// each) for NP <= 64; from NP = 128 a stage is 32 KB or more and one CTA per
+// SM with up to six stages in flight measured faster (skewed 128-expert
+// layer: 25.6 vs 26.6 us for the router stage).
 template <int NP>
 struct RtCfg {
-  static constexpr int NACC = 512 / NP > 32 ? 32 : 512 / NP;
+  static constexpr int NACC = 256 / NP;
+  static constexpr int CTAS_PER_SM = NP >= 128 ? 1 : 2;
   static constexpr int B_BYTES = NP * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES_RAW = (200 * 1024) / STAGE_BYTES;
-  static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
-  static constexpr int CW = NP < 32 ? NP : 32;  // epilogue column chunk
-  static constexpr int STG_FLOATS = 128 * (CW + 1);  // per-row logit staging, padded
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STG_FLOATS * 4 + 1024 + 256;
+  static constexpr int CW = NP < 32 ? NP : 32;     // epilogue column chunk
+  static constexpr int STG_FLOATS = 4 * 32 * 33;   // per-warp 32 x 32 transpose buffer, padded
+  static constexpr int FIXED = STG_FLOATS * 4 + 1024 + 256;
+  static constexpr int BUDGET = (CTAS_PER_SM == 2 ? 113 * 1024 : 200 * 1024) - FIXED;
+  static constexpr int STAGES_RAW = BUDGET / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_RAW > 6 ? 6 : STAGES_RAW;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + FIXED;
+  static_assert(STAGES >= 2, "router stages");
 };
-
-// A candidate (logit v, expert e) as one 64-bit key whose unsigned order is
-// the routing order: numbers by value (larger first; -0 folded into +0 so
-// the two zeros tie), then NaN, then an empty slot (key 0); on equal values
-// the lower expert index has the larger key.
-__device__ __forceinline__ uint64_t rank_key(float v, int e) {
-  uint32_t hi;
-  if (isnan(v)) {
-    hi = 1u;
-  } else {
-    const uint32_t b = __float_as_uint(v + 0.0f);
-    hi = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-    hi = hi < 2u ? 2u : hi;  // stay above NaN and empty (only -inf maps below)
-  }
-  return (static_cast<uint64_t>(hi) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(e));
-}
 
 template <int CW>
 __device__ __forceinline__ void tmem_load_cols(uint32_t taddr, uint32_t (&r)[CW]) {
@@ -67,16 +66,24 @@ __device__ __forceinline__ void tmem_load_cols(uint32_t taddr, uint32_t (&r)[CW]
     tmem_load16(taddr, r);
 }
 
-template <int NP, int KMAX>
-__global__ void __launch_bounds__(THREADS, 1)
-    router_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
-                     const RouterArgs a, const uint64_t wait_limit_ns) {
+struct PartArgs {
+  int32_t T, d, E;
+  int32_t ks;          // slices of the model dimension
+  int32_t t_pad;       // rows of each slice's partial block (tiles * 128)
+  float* part;         // [ks][t_pad][NP]
+  int* err;
+};
+
+template <int NP>
+__global__ void __launch_bounds__(THREADS, 2)
+    router_tc_part_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+                          const PartArgs a, const uint64_t wait_limit_ns) {
   using C = RtCfg<NP>;
   constexpr int STAGES = C::STAGES, NACC = C::NACC, CW = C::CW;
   constexpr uint32_t IDESC = idesc_bf16_f32(BM, NP);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float* stg = reinterpret_cast<float*>(smem + STAGES * C::STAGE_BYTES);  // [128][CW + 1]
+  float* stg = reinterpret_cast<float*>(smem + STAGES * C::STAGE_BYTES);  // [4 warps][32][33]
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES + C::STG_FLOATS * 4);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
@@ -90,7 +97,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&empty[s], 1);
     }
     mbar_init(tfull, 1);
-    mbar_init(tempty, 128);
+    mbar_init(tempty, 4);
     fence_barrier_init();
     prefetch_tensormap(&tm_x);
     prefetch_tensormap(&tm_w);
@@ -104,15 +111,24 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int n_tiles = (a.T + BM - 1) / BM;
+  const int n_units = n_tiles * a.ks;
   const int kblocks = a.d / BK;
-  const int nacc = kblocks < NACC ? kblocks : NACC;
+  // unit u: tile u / ks, k-blocks [kb_lo, kb_hi) of slice u % ks
+  auto k_range = [&](int u, int& lo, int& hi) {
+    const int sl = u % a.ks;
+    lo = sl * kblocks / a.ks;
+    hi = (sl + 1) * kblocks / a.ks;
+  };
 
   if (warp == 0) {
     if (lane == 0) {
       int64_t issued = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
-        for (int kb = 0; kb < kblocks; ++kb) {
+      for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
+        int lo, hi;
+        k_range(u, lo, hi);
+        const int tile = u / a.ks;
+        for (int kb = lo; kb < hi; ++kb) {
           const int stage = static_cast<int>(issued % STAGES);
           const uint32_t phase = static_cast<uint32_t>((issued / STAGES) & 1);
           if (!mbar_wait(&empty[stage], phase ^ 1u, wait_limit_ns)) {
@@ -136,13 +152,15 @@ __global__ void __launch_bounds__(THREADS, 1)
       int stage = 0;
       uint32_t phase = 0, tphase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
+      for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
+        int lo, hi;
+        k_range(u, lo, hi);
         if (!mbar_wait(tempty, tphase ^ 1u, wait_limit_ns)) {
           set_error(a.err, kErrTimeout);
           break;
         }
         tc_fence_after();
-        for (int kb = 0; kb < kblocks; ++kb) {
+        for (int kb = lo; kb < hi; ++kb) {
           if (!mbar_wait(&full[stage], phase, wait_limit_ns)) {
             set_error(a.err, kErrTimeout);
             ok = false;
@@ -151,10 +169,11 @@ __global__ void __launch_bounds__(THREADS, 1)
           tc_fence_after();
           const uint32_t st = smem_u32(smem + stage * C::STAGE_BYTES);
           const uint64_t adesc = sw128_desc(st), bdesc = sw128_desc(st + A_BYTES);
-          const uint32_t d = tmem_base + static_cast<uint32_t>((kb % NACC) * NP);
+          const int j = kb - lo;
+          const uint32_t d = tmem_base + static_cast<uint32_t>((j % NACC) * NP);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
-            tc_mma_f16(d, adesc + 2 * k, bdesc + 2 * k, IDESC, (kb >= NACC || k > 0) ? 1u : 0u);
+            tc_mma_f16(d, adesc + 2 * k, bdesc + 2 * k, IDESC, (j >= NACC || k > 0) ? 1u : 0u);
           tc_commit(&empty[stage]);
           if (++stage == STAGES) {
             stage = 0;
@@ -167,27 +186,26 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
     }
   } else {
+    // epilogue: warp q reads TMEM lanes 32q.. (tokens), sums the accumulators
+    // of each 32-column chunk in a fixed order, transposes the 32 x 32 block
+    // through shared memory and writes each token's 32 logits as one
+    // 128-byte row segment
     const int q = warp & 3;
+    float* tb32 = stg + q * 32 * 33;
     uint32_t tphase = 0;
-    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+      int lo, hi;
+      k_range(u, lo, hi);
+      const int nacc = hi - lo < NACC ? hi - lo : NACC;
       if (!mbar_wait(tfull, tphase, wait_limit_ns)) {
         set_error(a.err, kErrTimeout);
         break;
       }
       tc_fence_after();
-      const int t = tile * BM + q * 32 + lane;
+      const int tile = u / a.ks, sl = u % a.ks;
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-      uint64_t top[KMAX];   // sorted, best first
-      float topv[KMAX];
-#pragma unroll
-      for (int j = 0; j < KMAX; ++j) {
-        top[j] = 0;
-        topv[j] = 0.f;
-      }
-      uint64_t thr = 0;  // key of the k-th best so far
-      float* my = stg + (q * 32 + lane) * (CW + 1);
+      float* dst = a.part + (static_cast<int64_t>(sl) * a.t_pad + tile * BM + q * 32) * NP;
       for (int c0 = 0; c0 < NP; c0 += CW) {
-        if (c0 >= a.E) break;  // uniform across the warp
         float sum[CW];
 #pragma unroll
         for (int j = 0; j < CW; ++j) sum[j] = 0.f;
@@ -197,59 +215,18 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
           for (int j = 0; j < CW; ++j) sum[j] += __uint_as_float(r[j]);
         }
-        if (a.bias != nullptr) {
 #pragma unroll
-          for (int j = 0; j < CW; ++j)
-            if (c0 + j < a.E) sum[j] += __ldg(a.bias + c0 + j);
-        }
-#pragma unroll
-        for (int j = 0; j < CW; ++j) my[j] = sum[j];
+        for (int j = 0; j < CW; ++j) tb32[lane * 33 + j] = sum[j];
         __syncwarp();
-        const int nj = a.E - c0 < CW ? a.E - c0 : CW;
+        if (lane < CW) {
 #pragma unroll 4
-        for (int j = 0; j < nj; ++j) {
-          const int e = c0 + j;
-          const float v = my[j];
-          if (a.logits != nullptr && t < a.T) a.logits[static_cast<int64_t>(t) * a.E + e] = v;
-          uint64_t key = rank_key(v, e);
-          if (key > thr) {
-            float kv = v;
-#pragma unroll
-            for (int s2 = 0; s2 < KMAX; ++s2) {
-              const bool better = s2 < a.k && key > top[s2];
-              const uint64_t tk = top[s2];
-              const float tv = topv[s2];
-              top[s2] = better ? key : tk;
-              topv[s2] = better ? kv : tv;
-              key = better ? tk : key;
-              kv = better ? tv : kv;
-            }
-#pragma unroll
-            for (int s2 = 0; s2 < KMAX; ++s2)
-              if (s2 == a.k - 1) thr = top[s2];
-          }
+          for (int i = 0; i < 32; ++i) dst[static_cast<int64_t>(i) * NP + c0 + lane] = tb32[i * 33 + lane];
         }
         __syncwarp();
-      }
-      if (t < a.T) {
-        const float l0 = topv[0];
-        float ex[KMAX];
-        float den = 0.f;
-#pragma unroll
-        for (int s2 = 0; s2 < KMAX; ++s2) {
-          ex[s2] = (s2 < a.k) ? expf(topv[s2] - l0) : 0.f;
-          den += ex[s2];
-        }
-#pragma unroll
-        for (int s2 = 0; s2 < KMAX; ++s2) {
-          if (s2 < a.k) {
-            a.ids[static_cast<int64_t>(t) * a.k + s2] = static_cast<int>(~static_cast<uint32_t>(top[s2]));
-            a.w[static_cast<int64_t>(t) * a.k + s2] = a.raw_weights ? topv[s2] : ex[s2] / den;
-          }
-        }
       }
       tc_fence_before();
-      mbar_arrive(tempty);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty);
       tphase ^= 1u;
     }
   }
@@ -262,33 +239,121 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-template <int NP, int KMAX>
-cudaError_t launch_np(const CUtensorMap& tx, const CUtensorMap& tw, const RouterArgs& a, int grid,
-                      cudaStream_t s) {
-  router_tc_kernel<NP, KMAX><<<grid, THREADS, RtCfg<NP>::SMEM_BYTES, s>>>(tx, tw, a, kWaitLimitNs);
+// Order of a logit as an unsigned key: numbers by value (larger first; -0
+// folded into +0 so the two zeros tie), then NaN; 0 marks an empty or taken
+// candidate.  Ties between experts go to the lower index.
+__device__ __forceinline__ uint32_t order_key(float v) {
+  if (isnan(v)) return 1u;
+  const uint32_t b = __float_as_uint(v + 0.0f);
+  const uint32_t h = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  return h < 2u ? 2u : h;  // stay above NaN and empty (only -inf maps below)
+}
+
+// One warp per token: lane l owns experts l, l + 32, ... (NPL of them).  Each
+// of the k rounds takes the warp's largest order key (a hardware warp
+// reduction), then the lowest expert index among the lanes holding it.
+template <int NPL, int KMAX>
+__global__ void __launch_bounds__(256) router_topk_kernel(const float* __restrict__ part, int ks, int t_pad, int np,
+                                                          const RouterArgs a) {
+  const int lane = threadIdx.x % 32;
+  const int t = blockIdx.x * 8 + threadIdx.x / 32;
+  if (t >= a.T) return;
+  float p[NPL][kRouterMaxSlices];
+#pragma unroll
+  for (int j = 0; j < NPL; ++j) {
+    const int e = lane + 32 * j;
+    const float* src = part + static_cast<int64_t>(t) * np + e;
+#pragma unroll
+    for (int sl = 0; sl < kRouterMaxSlices; ++sl)
+      p[j][sl] = (e < a.E && sl < ks) ? __ldg(src + static_cast<int64_t>(sl) * t_pad * np) : 0.f;
+  }
+  float v[NPL];
+  uint32_t key[NPL];
+#pragma unroll
+  for (int j = 0; j < NPL; ++j) {
+    const int e = lane + 32 * j;
+    float l = p[j][0];
+#pragma unroll
+    for (int sl = 1; sl < kRouterMaxSlices; ++sl)
+      if (sl < ks) l += p[j][sl];
+    if (e < a.E) {
+      if (a.bias != nullptr) l += __ldg(a.bias + e);
+      if (a.logits != nullptr) a.logits[static_cast<int64_t>(t) * a.E + e] = l;
+    }
+    v[j] = l;
+    key[j] = e < a.E ? order_key(l) : 0u;
+  }
+  float topv[KMAX];
+  int topi[KMAX];
+#pragma unroll
+  for (int s = 0; s < KMAX; ++s) {
+    topv[s] = 0.f;
+    topi[s] = 0;
+    if (s < a.k) {
+      uint32_t bk = key[0];
+      int bj = 0;
+      float bv = v[0];
+#pragma unroll
+      for (int j = 1; j < NPL; ++j)
+        if (key[j] > bk) {  // strictly larger: the lower index keeps a tie
+          bk = key[j];
+          bj = j;
+          bv = v[j];
+        }
+      const uint32_t wk = __reduce_max_sync(0xffffffffu, bk);
+      const uint32_t we = __reduce_min_sync(0xffffffffu, bk == wk ? static_cast<uint32_t>(lane + 32 * bj) : ~0u);
+      const int owner = static_cast<int>(we & 31u);
+      topv[s] = __shfl_sync(0xffffffffu, bv, owner);
+      topi[s] = static_cast<int>(we);
+      if (lane == owner) {
+#pragma unroll
+        for (int j = 0; j < NPL; ++j)
+          if (j == bj) key[j] = 0u;
+      }
+    }
+  }
+  const float l0 = topv[0];
+  float ex[KMAX];
+  float den = 0.f;
+#pragma unroll
+  for (int s = 0; s < KMAX; ++s) {
+    ex[s] = (s < a.k) ? expf(topv[s] - l0) : 0.f;
+    den += ex[s];
+  }
+#pragma unroll
+  for (int s = 0; s < KMAX; ++s) {
+    if (s < a.k && lane == s) {
+      a.ids[static_cast<int64_t>(t) * a.k + s] = topi[s];
+      a.w[static_cast<int64_t>(t) * a.k + s] = a.raw_weights ? topv[s] : ex[s] / den;
+    }
+  }
+}
+
+template <int NP>
+cudaError_t launch_np(const CUtensorMap& tx, const CUtensorMap& tw, const RouterArgs& a, int ks, int t_pad,
+                      float* part, int num_sms, cudaStream_t s) {
+  PartArgs pa{a.T, a.d, a.E, ks, t_pad, part, a.err};
+  const int units = (a.T + BM - 1) / BM * ks;
+  const int slots = RtCfg<NP>::CTAS_PER_SM * num_sms;
+  const int grid = units < slots ? units : slots;
+  router_tc_part_kernel<NP><<<grid, THREADS, RtCfg<NP>::SMEM_BYTES, s>>>(tx, tw, pa, kWaitLimitNs);
+  constexpr int NPL = NP < 32 ? 1 : NP / 32;
+  const int blocks = (a.T + 7) / 8;
+  if (a.k <= 2)
+    router_topk_kernel<NPL, 2><<<blocks, 256, 0, s>>>(part, ks, t_pad, NP, a);
+  else if (a.k <= 4)
+    router_topk_kernel<NPL, 4><<<blocks, 256, 0, s>>>(part, ks, t_pad, NP, a);
+  else if (a.k <= 8)
+    router_topk_kernel<NPL, 8><<<blocks, 256, 0, s>>>(part, ks, t_pad, NP, a);
+  else
+    router_topk_kernel<NPL, 16><<<blocks, 256, 0, s>>>(part, ks, t_pad, NP, a);
   return cudaGetLastError();
 }
 
 template <int NP>
-cudaError_t launch_k(const CUtensorMap& tx, const CUtensorMap& tw, const RouterArgs& a, int grid, cudaStream_t s) {
-  if (a.k <= 2) return launch_np<NP, 2>(tx, tw, a, grid, s);
-  if (a.k <= 4) return launch_np<NP, 4>(tx, tw, a, grid, s);
-  if (a.k <= 8) return launch_np<NP, 8>(tx, tw, a, grid, s);
-  return launch_np<NP, 16>(tx, tw, a, grid, s);
-}
-
-template <int NP>
 cudaError_t prepare_np() {
-  cudaError_t e = cudaSuccess;
-  auto set = [&](auto fn) {
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, RtCfg<NP>::SMEM_BYTES);
-  };
-  set(router_tc_kernel<NP, 2>);
-  set(router_tc_kernel<NP, 4>);
-  set(router_tc_kernel<NP, 8>);
-  set(router_tc_kernel<NP, 16>);
-  return e;
+  return cudaFuncSetAttribute(router_tc_part_kernel<NP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              RtCfg<NP>::SMEM_BYTES);
 }
 
 }  // namespace
@@ -297,6 +362,17 @@ int router_tc_rows(int E) {
   int np = 16;
   while (np < E) np *= 2;
   return np;
+}
+
+int router_tc_slices(int T, int d, int E, int num_sms) {
+  const int tiles = (T + BM - 1) / BM;
+  if (tiles == 0) return 1;
+  const int slots = (router_tc_rows(E) >= 128 ? 1 : 2) * num_sms;
+  int ks = (slots + tiles / 2) / tiles;
+  const int kblocks = d / BK;
+  if (ks > kRouterMaxSlices) ks = kRouterMaxSlices;
+  if (ks > kblocks) ks = kblocks;
+  return ks < 1 ? 1 : ks;
 }
 
 cudaError_t router_tc_prepare() {
@@ -308,17 +384,18 @@ cudaError_t router_tc_prepare() {
   return e;
 }
 
-cudaError_t launch_router_tc(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const RouterArgs& a, int num_sms,
-                             cudaStream_t s) {
+cudaError_t launch_router_tc(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const RouterArgs& a, float* part,
+                             int num_sms, cudaStream_t s) {
   const int tiles = (a.T + BM - 1) / BM;
   if (tiles == 0) return cudaSuccess;
-  const int grid = tiles < num_sms ? tiles : num_sms;
+  const int ks = router_tc_slices(a.T, a.d, a.E, num_sms);
+  const int t_pad = tiles * BM;
   switch (router_tc_rows(a.E)) {
-    case 16: return launch_k<16>(tm_x, tm_w, a, grid, s);
-    case 32: return launch_k<32>(tm_x, tm_w, a, grid, s);
-    case 64: return launch_k<64>(tm_x, tm_w, a, grid, s);
-    case 128: return launch_k<128>(tm_x, tm_w, a, grid, s);
-    default: return launch_k<256>(tm_x, tm_w, a, grid, s);
+    case 16: return launch_np<16>(tm_x, tm_w, a, ks, t_pad, part, num_sms, s);
+    case 32: return launch_np<32>(tm_x, tm_w, a, ks, t_pad, part, num_sms, s);
+    case 64: return launch_np<64>(tm_x, tm_w, a, ks, t_pad, part, num_sms, s);
+    case 128: return launch_np<128>(tm_x, tm_w, a, ks, t_pad, part, num_sms, s);
+    default: return launch_np<256>(tm_x, tm_w, a, ks, t_pad, part, num_sms, s);
   }
 }
 

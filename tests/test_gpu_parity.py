@@ -278,11 +278,12 @@ def test_dispatch_own_ranking_full_size(name, monkeypatch):
 
 
 @pytest.mark.parametrize("fused,name,expect", [
-    ("1", "mixtral_prefill", 6), ("1", "skewed", 8), ("0", "mixtral_prefill", 6), ("0", "skewed", 8)])
+    ("1", "mixtral_prefill", 6), ("1", "skewed", 9), ("0", "mixtral_prefill", 6), ("0", "skewed", 9)])
 def test_kernels_per_forward(fused, name, expect, monkeypatch):
-    """The launch count the library reports: router, dispatch kernels (block
-    scan + row copy after the mma router's ranks; or one-block /
-    count-scan-scatter ranking + row copy), two grouped GEMMs, combine."""
+    """The launch count the library reports: router (the tcgen05 router of wide
+    layers: partial logits + top-k), dispatch kernels (block scan + row copy
+    after the mma router's ranks; or one-block / count-scan-scatter ranking +
+    row copy), two grouped GEMMs, combine."""
     if fused == "0":
         monkeypatch.setenv("CB_MOE_FUSED_RANKS", fused)
     shp = synth.WORKLOADS[name]
