@@ -192,6 +192,17 @@ CB_API cb_status_t cb_moe_routing(const cb_moe_t *h, cb_routing_view_t *view);
 #define CB_N_STAGES 5
 CB_API cb_status_t cb_moe_stage_times(cb_moe_t *h, float *ms, int32_t n);
 
+/*
+ * Turns the stage events on (on != 0) or off for the forwards enqueued after
+ * this call, on a handle created with CB_FLAG_STAGE_TIMING (its events exist);
+ * CB_ERR_INVALID_ARG for any other handle.  The events are nodes between the
+ * stages' kernels, so forwards without them run a little faster: a caller can
+ * time its steps with the events off and take stage times from other steps.
+ * cb_moe_stage_times reports the last forward that recorded them.  Host-side
+ * only; the handle's captured graphs are keyed on the setting.
+ */
+CB_API cb_status_t cb_moe_set_stage_timing(cb_moe_t *h, int32_t on);
+
 /* Synchronise the device, return the handle's device status word (CB_OK,
  * CB_ERR_TIMEOUT or CB_ERR_DEVICE) and clear it. */
 CB_API cb_status_t cb_moe_last_error(cb_moe_t *h);

@@ -25,7 +25,8 @@ STAGE_NAMES = ("router", "dispatch", "gateup_gemm", "down_gemm", "combine")
 # every symbol include/cb_moe.h declares
 ABI_SYMBOLS = ("cb_moe_init", "cb_moe_forward", "cb_moe_forward_f32out", "cb_moe_forward_host",
                "cb_moe_routing", "cb_moe_stage_times", "cb_moe_last_error", "cb_moe_device_bytes",
-               "cb_moe_free", "cb_status_string", "cb_moe_dispatch_noalloc", "cb_moe_kernels_per_forward")
+               "cb_moe_free", "cb_status_string", "cb_moe_dispatch_noalloc", "cb_moe_kernels_per_forward",
+               "cb_moe_set_stage_timing")
 
 
 CB_ROUTER_SOFTMAX_TOPK, CB_ROUTER_RAW_LOGITS, CB_ROUTER_HASH = 0, 1, 2
@@ -82,12 +83,13 @@ def load_library(path: str = LIB_PATH):
     lib.cb_moe_device_bytes.argtypes = [ctypes.POINTER(cb_moe_config_t), ctypes.POINTER(ctypes.c_uint64)]
     lib.cb_moe_free.argtypes = [vp]
     lib.cb_moe_kernels_per_forward.argtypes = [vp, ctypes.POINTER(i32)]
+    lib.cb_moe_set_stage_timing.argtypes = [vp, i32]
     lib.cb_moe_dispatch_noalloc.argtypes = [vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, vp, vp, vp, vp,
                                             vp, vp]
     lib.cb_moe_dispatch_noalloc.restype = i32
     for name in ("cb_moe_init", "cb_moe_forward", "cb_moe_forward_f32out", "cb_moe_forward_host",
                  "cb_moe_routing", "cb_moe_stage_times", "cb_moe_last_error", "cb_moe_device_bytes",
-                 "cb_moe_free", "cb_moe_kernels_per_forward"):
+                 "cb_moe_free", "cb_moe_kernels_per_forward", "cb_moe_set_stage_timing"):
         getattr(lib, name).restype = i32
     lib.cb_status_string.argtypes = [i32]
     lib.cb_status_string.restype = ctypes.c_char_p
@@ -241,6 +243,12 @@ class MoELayer:
         if st != CB_OK:
             raise CbMoeError(st, "cb_moe_stage_times")
         return ms
+
+    def set_stage_timing(self, on: bool):
+        """Stage events on or off for later forwards (handle made with stage_timing=True)."""
+        st = load_library().cb_moe_set_stage_timing(self.handle, 1 if on else 0)
+        if st != CB_OK:
+            raise CbMoeError(st, "cb_moe_set_stage_timing")
 
     def last_error(self) -> int:
         return cb_moe_last_error(self.handle)

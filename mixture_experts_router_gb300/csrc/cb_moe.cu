@@ -46,7 +46,8 @@ struct cb_moe {
   uint16_t *x_stage, *out_stage;
   int32_t max_mtiles, n_chunks;
   cudaEvent_t ev[CB_N_STAGES + 1];
-  bool timing;
+  bool timing;             // record the stage events in forwards now
+  bool timing_events;      // the events exist (CB_FLAG_STAGE_TIMING at init)
   bool router_tc;          // tcgen05 router (else the mma.sync router)
   bool use_graphs;         // replay each forward variant from a captured CUDA graph
   bool pair_gu, pair_dn;   // bf16 gate/up, down GEMMs on CTA pairs (2-SM MMA)
@@ -56,6 +57,7 @@ struct cb_moe {
   struct GraphSlot {
     const void* a;
     const void* b;
+    bool timing;           // captured with the stage events
     cudaGraphExec_t exec;
   } graphs[3];             // bf16 forward, fp32-out forward, host-buffer forward
   bool gather_a;           // gate/up GEMM gathers its rows from x (no Xp copy)
@@ -201,9 +203,13 @@ struct DeviceGuard {
 cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, cudaStream_t s) {
   const cb_moe_config_t& c = h->cfg;
   if (fault_injected("launch")) return CB_ERR_CUDA;
-  // external event nodes when captured, so stage timing works through a graph
+  // external event nodes when captured, so stage timing works through a
+  // graph; plain records otherwise
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (h->timing && cudaStreamIsCapturing(s, &cap) != cudaSuccess) return CB_ERR_CUDA;
+  const unsigned int ev_flags = cap == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault;
   auto mark = [&](int i) {
-    return !h->timing || cudaEventRecordWithFlags(h->ev[i], s, cudaEventRecordExternal) == cudaSuccess;
+    return !h->timing || cudaEventRecordWithFlags(h->ev[i], s, ev_flags) == cudaSuccess;
   };
   if (!mark(0)) return CB_ERR_CUDA;
 
@@ -383,7 +389,7 @@ cb_status_t run_graphed(cb_moe_t* h, int slot, const void* a, const void* b, cud
   }
   if (cs != cudaStreamCaptureStatusNone) return body(s);
   cb_moe::GraphSlot& g = h->graphs[slot];
-  if (g.exec == nullptr || g.a != a || g.b != b) {
+  if (g.exec == nullptr || g.a != a || g.b != b || g.timing != h->timing) {
     if (g.exec != nullptr) {
       cudaGraphExecDestroy(g.exec);
       g.exec = nullptr;
@@ -406,6 +412,7 @@ cb_status_t run_graphed(cb_moe_t* h, int slot, const void* a, const void* b, cud
     g.exec = exec;
     g.a = a;
     g.b = b;
+    g.timing = h->timing;
   }
   return cudaGraphLaunch(g.exec, s) == cudaSuccess ? CB_OK : CB_ERR_CUDA;
 }
@@ -641,6 +648,7 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
   ok = ok && make_tmap(&h->tm_wr, h->wr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, E, 64,
                        static_cast<uint32_t>(router_tc_rows(cfg->n_experts)));
   h->timing = (cfg->flags & CB_FLAG_STAGE_TIMING) != 0;
+  h->timing_events = h->timing;
   for (int i = 0; ok && h->timing && i <= CB_N_STAGES; ++i) ok = cudaEventCreate(&h->ev[i]) == cudaSuccess;
   ok = ok && cudaDeviceSynchronize() == cudaSuccess;
   if (!ok) {
@@ -732,6 +740,12 @@ cb_status_t cb_moe_stage_times(cb_moe_t* h, float* ms, int32_t n) {
   return CB_OK;
 }
 
+cb_status_t cb_moe_set_stage_timing(cb_moe_t* h, int32_t on) {
+  if (h == nullptr || !h->timing_events) return CB_ERR_INVALID_ARG;
+  h->timing = on != 0;
+  return CB_OK;
+}
+
 cb_status_t cb_moe_last_error(cb_moe_t* h) {
   if (h == nullptr) return CB_ERR_INVALID_ARG;
   DeviceGuard guard(h->cfg.device);
@@ -749,7 +763,7 @@ cb_status_t cb_moe_free(cb_moe_t* h) {
   {
     DeviceGuard guard(h->cfg.device);
     if (!guard.ok || cudaDeviceSynchronize() != cudaSuccess) st = CB_ERR_CUDA;
-    for (int i = 0; h->timing && i <= CB_N_STAGES; ++i)
+    for (int i = 0; h->timing_events && i <= CB_N_STAGES; ++i)
       if (h->ev[i] != nullptr) cudaEventDestroy(h->ev[i]);
     for (auto& g : h->graphs)
       if (g.exec != nullptr) cudaGraphExecDestroy(g.exec);

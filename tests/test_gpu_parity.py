@@ -260,7 +260,7 @@ def test_pair_mma_path_timeout(monkeypatch):
     assert rep["f32_max_abs"] <= gh.MAX_ABS
 
 
-@pytest.mark.parametrize("name", ["tiny", "ragged_mid", "odd_T", "int8_mid"])
+@pytest.mark.parametrize("name", ["tiny", "ragged_mid", "odd_T", "int8_mid", "skewed_small", "e256_k16", "int8_k6"])
 def test_dispatch_own_ranking_small(name, monkeypatch):
     """CB_MOE_FUSED_RANKS=0: the dispatch ranks the routed pairs itself
     (one-block or count/scan/scatter kernels) instead of scanning the
@@ -270,7 +270,7 @@ def test_dispatch_own_ranking_small(name, monkeypatch):
     print(name, "own ranking", rep)
 
 
-@pytest.mark.parametrize("name", ["mixtral_prefill", "mixtral_decode"])
+@pytest.mark.parametrize("name", ["mixtral_prefill", "mixtral_decode", "skewed"])
 def test_dispatch_own_ranking_full_size(name, monkeypatch):
     monkeypatch.setenv("CB_MOE_FUSED_RANKS", "0")
     rep = gh.full_check(synth.make_layer(synth.WORKLOADS[name]), sample=FULL[name])
@@ -282,8 +282,8 @@ def test_dispatch_own_ranking_full_size(name, monkeypatch):
 def test_kernels_per_forward(fused, name, expect, monkeypatch):
     """The launch count the library reports: router (the tcgen05 router of wide
     layers: partial logits + top-k), dispatch kernels (block scan + row copy
-    after the mma router's ranks; or one-block / count-scan-scatter ranking +
-    row copy), two grouped GEMMs, combine."""
+    after the mma router's per-block ranks; or one-block / count-scan-scatter
+    ranking + row copy), two grouped GEMMs, combine."""
     if fused == "0":
         monkeypatch.setenv("CB_MOE_FUSED_RANKS", fused)
     shp = synth.WORKLOADS[name]
@@ -377,3 +377,36 @@ def test_hash_router_golden_cases(case):
         assert gl.routing()["ids"].ravel().tolist() == g["expected_ids"]
     finally:
         gl.close()
+
+
+def test_stage_timing_switch():
+    """cb_moe_set_stage_timing: forwards with and without the stage events give
+    the same bytes; stage times need the events; handles made without
+    CB_FLAG_STAGE_TIMING refuse the switch."""
+    import mixture_experts_router_gb300 as cb
+    layer = synth.make_layer(SMALL["ragged_mid"])
+    s = layer.shape
+    w = {n: gh.to_dev(getattr(layer, n), "cuda:0") for n in ("wr", "bias", "wg", "wu", "wd")}
+    m = cb.MoELayer(layer.x.shape[0], s.d, s.f, s.E, s.k, w["wr"], w["wg"], w["wu"], w["wd"],
+                    router_bias=w["bias"], stage_timing=True)
+    x = gh.to_dev(layer.x, "cuda:0")
+    out_a = torch.empty((layer.x.shape[0], s.d), dtype=torch.bfloat16, device="cuda:0")
+    out_b = torch.empty_like(out_a)
+    m.forward(x, out_a)
+    ms = m.stage_times()
+    assert len(ms) == cb.CB_N_STAGES and all(v >= 0 for v in ms)
+    m.set_stage_timing(False)
+    m.forward(x, out_b)
+    torch.cuda.synchronize()
+    assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
+    with pytest.raises(cb.CbMoeError):
+        m.stage_times()
+    m.set_stage_timing(True)
+    m.forward(x, out_b)
+    assert len(m.stage_times()) == cb.CB_N_STAGES
+    assert m.last_error() == cb.CB_OK
+    m2 = cb.MoELayer(layer.x.shape[0], s.d, s.f, s.E, s.k, w["wr"], w["wg"], w["wu"], w["wd"],
+                     router_bias=w["bias"])
+    with pytest.raises(cb.CbMoeError):
+        m2.set_stage_timing(True)
+    del m, m2
