@@ -9,6 +9,7 @@
 #include <cuda_bf16.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace cbmoe {
 namespace {
@@ -18,6 +19,8 @@ constexpr int kMaxK = 16;
 
 template <bool F32OUT>
 __global__ void __launch_bounds__(kThreads) combine_kernel(CombineArgs a) {
+  grid_dep_wait();    // what earlier kernels in the stream wrote is visible from here
+  grid_dep_launch();
   __shared__ int64_t rows[kMaxK];
   __shared__ float ws[kMaxK];
   const int t = blockIdx.x;
@@ -71,9 +74,9 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(CombineArgs a) {
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s) {
   if (a.T <= 0) return cudaSuccess;
   if (a.out_f32)
-    combine_kernel<true><<<a.T, kThreads, 0, s>>>(a);
+    launch_kernel(combine_kernel<true>, a.T, kThreads, 0, s, a);
   else
-    combine_kernel<false><<<a.T, kThreads, 0, s>>>(a);
+    launch_kernel(combine_kernel<false>, a.T, kThreads, 0, s, a);
   return cudaGetLastError();
 }
 

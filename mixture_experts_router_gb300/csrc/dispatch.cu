@@ -21,6 +21,7 @@
 //   dispatch_copy    : each token's row of x into its k rows of Xp (and,
 //                      after dispatch_scan_blocks, the global ranks: inv, tok)
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace cbmoe {
 namespace {
@@ -30,6 +31,8 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kPerWarp = kDispatchChunk / kWarps;  // 256 pairs, 8 rounds of 32
 
 __global__ void __launch_bounds__(kThreads) dispatch_count(DispatchArgs a) {
+  grid_dep_wait();    // what earlier kernels in the stream wrote is visible from here
+  grid_dep_launch();
   __shared__ int hist[256];
   for (int e = threadIdx.x; e < a.E; e += kThreads) hist[e] = 0;
   __syncthreads();
@@ -78,6 +81,8 @@ __device__ int block_exclusive_scan(int v, int* tmp) {
 }
 
 __global__ void __launch_bounds__(kThreads) dispatch_scan(DispatchArgs a) {
+  grid_dep_wait();    // what earlier kernels in the stream wrote is visible from here
+  grid_dep_launch();
   __shared__ int tmp[kWarps];
   const int e = threadIdx.x;
   int total = 0;
@@ -114,6 +119,8 @@ __global__ void __launch_bounds__(kThreads) dispatch_scan(DispatchArgs a) {
 }
 
 __global__ void __launch_bounds__(kThreads) dispatch_scatter(DispatchArgs a) {
+  grid_dep_wait();    // what earlier kernels in the stream wrote is visible from here
+  grid_dep_launch();
   __shared__ int wh[kWarps][256];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   for (int i = threadIdx.x; i < kWarps * 256; i += kThreads) (&wh[0][0])[i] = 0;
@@ -171,6 +178,8 @@ constexpr int kSmallThreads = 1024;
 constexpr int kSmallWarps = kSmallThreads / 32;
 
 __global__ void __launch_bounds__(kSmallThreads) dispatch_small(DispatchArgs a) {
+  grid_dep_wait();    // what earlier kernels in the stream wrote is visible from here
+  grid_dep_launch();
   __shared__ int wh[kSmallWarps][256];
   __shared__ int tmp[kSmallWarps];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -280,6 +289,8 @@ __device__ int publish_totals(const DispatchArgs& a, int total, int* tmp) {
 // length keeps the per-expert column walk free of bank conflicts; the last
 // row holds the totals).
 __global__ void __launch_bounds__(kScanThreads) dispatch_scan_blocks(DispatchArgs a) {
+  grid_dep_wait();    // what earlier kernels in the stream wrote is visible from here
+  grid_dep_launch();
   extern __shared__ int sc[];
   __shared__ int tmp[kScanWarps];
   __shared__ int s_off[256];
@@ -317,6 +328,8 @@ __global__ void __launch_bounds__(kScanThreads) dispatch_scan_blocks(DispatchArg
 // Padding rows of each expert's last tile are left as they are: no GEMM
 // output row depends on another row.
 __global__ void __launch_bounds__(kThreads) dispatch_copy(DispatchArgs a) {
+  grid_dep_wait();    // what earlier kernels in the stream wrote is visible from here
+  grid_dep_launch();
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int vec_per_row = a.d / 8;
   const int64_t rows = static_cast<int64_t>(a.max_mtiles) * kTileM;
@@ -376,17 +389,17 @@ static void launch_chunk_scan(const DispatchArgs& a, int max_words, cudaStream_t
   if ((a.n_chunks + 1) * (a.E + 1) <= max_words && a.E <= 256) {
     DispatchArgs b = a;
     b.n_rank_blocks = a.n_chunks;
-    dispatch_scan_blocks<<<1, kScanThreads, (b.n_rank_blocks + 1) * (b.E + 1) * 4, s>>>(b);
+    launch_kernel(dispatch_scan_blocks, 1, kScanThreads, (b.n_rank_blocks + 1) * (b.E + 1) * 4, s, b);
   } else {
-    dispatch_scan<<<1, kThreads, 0, s>>>(a);
+    launch_kernel(dispatch_scan, 1, kThreads, 0, s, a);
   }
 }
 
 cudaError_t launch_dispatch_ranks(const DispatchArgs& a, cudaStream_t s) {
   if (a.n_chunks <= 0) return cudaSuccess;
-  dispatch_count<<<a.n_chunks, kThreads, 0, s>>>(a);
+  launch_kernel(dispatch_count, a.n_chunks, kThreads, 0, s, a);
   launch_chunk_scan(a, 12 * 1024, s);
-  dispatch_scatter<<<a.n_chunks, kThreads, 0, s>>>(a);
+  launch_kernel(dispatch_scatter, a.n_chunks, kThreads, 0, s, a);
   return cudaGetLastError();
 }
 
@@ -400,18 +413,18 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s) {
   if (a.rank_block > 0) {
     const int words = (a.n_rank_blocks + 1) * (a.E + 1);
     if (words > kFusedScanWords || a.E > 256) return cudaErrorInvalidValue;
-    dispatch_scan_blocks<<<1, kScanThreads, words * 4, s>>>(a);
-    dispatch_copy<<<a.gather_blocks, kThreads, 0, s>>>(a);
+    launch_kernel(dispatch_scan_blocks, 1, kScanThreads, words * 4, s, a);
+    launch_kernel(dispatch_copy, a.gather_blocks, kThreads, 0, s, a);
     return cudaGetLastError();
   }
   if (static_cast<int64_t>(a.T) * a.k <= kDispatchSmallPairs) {
-    dispatch_small<<<1, kSmallThreads, 0, s>>>(a);
+    launch_kernel(dispatch_small, 1, kSmallThreads, 0, s, a);
   } else {
-    dispatch_count<<<a.n_chunks, kThreads, 0, s>>>(a);
+    launch_kernel(dispatch_count, a.n_chunks, kThreads, 0, s, a);
     launch_chunk_scan(a, kFusedScanWords, s);
-    dispatch_scatter<<<a.n_chunks, kThreads, 0, s>>>(a);
+    launch_kernel(dispatch_scatter, a.n_chunks, kThreads, 0, s, a);
   }
-  if (a.copy_rows) dispatch_copy<<<a.gather_blocks, kThreads, 0, s>>>(a);
+  if (a.copy_rows) launch_kernel(dispatch_copy, a.gather_blocks, kThreads, 0, s, a);
   return cudaGetLastError();
 }
 

@@ -154,6 +154,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  grid_dep_wait();    // what earlier kernels in the stream wrote is visible from here
+  grid_dep_launch();
   const int total_tiles = p.mtile_off[p.E] * p.n_tiles;
   int full_tiles = total_tiles, split = 1;
   if (KIND == kDownF32) tail_split(total_tiles, gridDim.x, full_tiles, split);
@@ -383,10 +385,9 @@ cudaError_t launch_grouped_gemm(GemmKind kind, bool int8_weights, const CUtensor
                                 cudaStream_t s) {
   if (int8_weights) return cudaErrorNotSupported;
   if (kind == kGateUpSwiGLU)
-    grouped_gemm_kernel<kGateUpSwiGLU>
-        <<<a.grid, THREADS, Smem<kGateUpSwiGLU>::BYTES, s>>>(tm_a, tm_b, tm_out, tm_b64, a);
+    launch_kernel(grouped_gemm_kernel<kGateUpSwiGLU>, a.grid, THREADS, Smem<kGateUpSwiGLU>::BYTES, s, tm_a, tm_b, tm_out, tm_b64, a);
   else
-    grouped_gemm_kernel<kDownF32><<<a.grid, THREADS, Smem<kDownF32>::BYTES, s>>>(tm_a, tm_b, tm_out, tm_b64, a);
+    launch_kernel(grouped_gemm_kernel<kDownF32>, a.grid, THREADS, Smem<kDownF32>::BYTES, s, tm_a, tm_b, tm_out, tm_b64, a);
   return cudaGetLastError();
 }
 

@@ -127,6 +127,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  grid_dep_wait();    // what earlier kernels in the stream wrote is visible from here
+  grid_dep_launch();
   const int total_tiles = p.ptile_off[p.E] * p.n_tiles;
 
   if (warp == 0) {
@@ -365,10 +367,9 @@ cudaError_t grouped_gemm_int8_prepare() {
 cudaError_t launch_grouped_gemm_int8(GemmKind kind, const CUtensorMap& tm_a, const CUtensorMap& tm_b,
                                      const CUtensorMap& tm_out, const GemmArgs& a, cudaStream_t s) {
   if (kind == kGateUpSwiGLU)
-    grouped_gemm_int8_kernel<kGateUpSwiGLU>
-        <<<a.grid, THREADS, Smem<kGateUpSwiGLU>::BYTES, s>>>(tm_a, tm_b, tm_out, a);
+    launch_kernel(grouped_gemm_int8_kernel<kGateUpSwiGLU>, a.grid, THREADS, Smem<kGateUpSwiGLU>::BYTES, s, tm_a, tm_b, tm_out, a);
   else
-    grouped_gemm_int8_kernel<kDownF32><<<a.grid, THREADS, Smem<kDownF32>::BYTES, s>>>(tm_a, tm_b, tm_out, a);
+    launch_kernel(grouped_gemm_int8_kernel<kDownF32>, a.grid, THREADS, Smem<kDownF32>::BYTES, s, tm_a, tm_b, tm_out, a);
   return cudaGetLastError();
 }
 

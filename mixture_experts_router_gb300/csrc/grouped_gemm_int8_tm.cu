@@ -132,6 +132,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  grid_dep_wait();    // what earlier kernels in the stream wrote is visible from here
+  grid_dep_launch();
   const int total_tiles = p.ptile_off[p.E] * p.n_tiles;
 
   if (warp == 0) {
@@ -384,9 +386,9 @@ cudaError_t launch_grouped_gemm_int8_tm(GemmKind kind, const CUtensorMap& tm_x, 
                                         const GemmArgs& a, cudaStream_t s) {
   if (a.k_blocks % 2 != 0) return cudaErrorInvalidValue;
   if (kind == kGateUpSwiGLU)
-    grouped_gemm_int8_tm_kernel<kGateUpSwiGLU><<<a.grid, THREADS, SMEM_BYTES, s>>>(tm_x, tm_w, a);
+    launch_kernel(grouped_gemm_int8_tm_kernel<kGateUpSwiGLU>, a.grid, THREADS, SMEM_BYTES, s, tm_x, tm_w, a);
   else
-    grouped_gemm_int8_tm_kernel<kDownF32><<<a.grid, THREADS, SMEM_BYTES, s>>>(tm_x, tm_w, a);
+    launch_kernel(grouped_gemm_int8_tm_kernel<kDownF32>, a.grid, THREADS, SMEM_BYTES, s, tm_x, tm_w, a);
   return cudaGetLastError();
 }
 

@@ -129,6 +129,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  grid_dep_wait();    // what earlier kernels in the stream wrote is visible from here
+  grid_dep_launch();
   const int total_tiles = p.ptile_off[p.E] * p.n_tiles;
 
   if (warp == 0) {
@@ -300,9 +302,14 @@ cudaLaunchConfig_t pair_config(int grid, cudaLaunchAttribute* attr) {
 template <int KIND>
 cudaError_t launch_kind(const CUtensorMap& tm_a, const CUtensorMap& tm_bh, const CUtensorMap& tm_out,
                         const GemmArgs& a, cudaStream_t s) {
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = pair_config<KIND>(a.grid, attr);
   cfg.stream = s;
+  if (PdlScope::next()) {  // see launch_kernel
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 2;
+  }
   return cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<KIND>, tm_a, tm_bh, tm_out, a);
 }
 

@@ -4,6 +4,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <utility>
 
 namespace cbmoe {
 
@@ -15,6 +16,58 @@ constexpr int kErrTimeout = 6;
 constexpr int kErrDevice = 7;
 // Default bound on any device-side wait.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+// Kernel launches of this library go through launch_kernel.  Inside a
+// PdlScope that is on, every launch after the first `plain_first` ones
+// carries programmatic stream serialization: the kernel may start (and run
+// its prologue) while the previous one in the stream finishes.  Every kernel
+// of the library calls grid_dep_wait before it reads what an earlier kernel
+// wrote, so the results do not depend on it.
+struct PdlScope {
+  static bool& flag() {
+    static thread_local bool on = false;
+    return on;
+  }
+  static int& plain() {
+    static thread_local int n = 0;
+    return n;
+  }
+  bool prev_on;
+  int prev_plain;
+  PdlScope(bool on, int plain_first) : prev_on(flag()), prev_plain(plain()) {
+    flag() = on;
+    plain() = plain_first;
+  }
+  ~PdlScope() {
+    flag() = prev_on;
+    plain() = prev_plain;
+  }
+  // whether the launch being made carries the attribute
+  static bool next() {
+    if (!flag()) return false;
+    if (plain() > 0) {
+      --plain();
+      return false;
+    }
+    return true;
+  }
+};
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                          Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = PdlScope::next() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Record a device-side error: the first one wins.
 __device__ __forceinline__ void set_error(int* err, int code) {

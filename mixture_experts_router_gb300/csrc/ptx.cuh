@@ -366,4 +366,14 @@ __device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t n, bool pred
   return r != 0;
 }
 
+// ------------------------------------------ programmatic dependent launch
+// Wait until the grid this one was launched after (with programmatic stream
+// serialization) has completed and its memory is visible; returns at once
+// when the launch had no such dependency.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Let the next grid in the stream begin launching (its CTAs run their
+// prologue and then wait in grid_dep_wait for this grid to complete).
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 }  // namespace cbmoe

@@ -26,6 +26,7 @@
 #include <cuda_bf16.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 #include "route_ranks.cuh"
 
 namespace cbmoe {
@@ -70,6 +71,8 @@ struct RCfg {
 
 template <int NT, int KS, int NS, int MTB>
 __global__ void __launch_bounds__(RCfg<NT, KS, NS, MTB>::THREADS) router_mma_kernel(RouterArgs a) {
+  grid_dep_wait();    // what earlier kernels in the stream wrote is visible from here
+  grid_dep_launch();
   using C = RCfg<NT, KS, NS, MTB>;
   constexpr int NTW = C::NTW, EP = C::EP, TB = C::TB;
   constexpr int kThreads = C::THREADS, kWarps = C::WARPS;
@@ -240,7 +243,7 @@ cudaError_t launch_cfg(const RouterArgs& a, cudaStream_t s) {
   using C = RCfg<NT, KS, NS, MTB>;
   const int blocks = (a.T + C::TB - 1) / C::TB;
   if (blocks == 0) return cudaSuccess;
-  router_mma_kernel<NT, KS, NS, MTB><<<blocks, C::THREADS, C::SMEM, s>>>(a);
+  launch_kernel(router_mma_kernel<NT, KS, NS, MTB>, blocks, C::THREADS, C::SMEM, s, a);
   return cudaGetLastError();
 }
 

@@ -22,6 +22,7 @@
 #include <cuda_bf16.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace cbmoe {
 namespace {
@@ -67,6 +68,8 @@ __device__ __forceinline__ void stage_chunk(const HashRouterArgs& a, int t0, int
 }
 
 __global__ void __launch_bounds__(kHashThreads) router_hash_kernel(HashRouterArgs a) {
+  grid_dep_wait();    // what earlier kernels in the stream wrote is visible from here
+  grid_dep_launch();
   __shared__ __align__(16) float ws[kStages][kWBuf];
   __shared__ __align__(16) uint16_t xs[kStages][kXBuf];
   const int tl = threadIdx.x / kLanesPerToken;
@@ -152,14 +155,14 @@ __global__ void widen_bf16(const uint16_t* src, int64_t n, float* dst) {
 
 cudaError_t prepare_hash_weights(const uint16_t* wh, int hash_dims, int d, float* wh_f32, cudaStream_t s) {
   if (hash_dims < 1 || hash_dims > kHashDimsMax) return cudaErrorInvalidValue;
-  widen_bf16<<<64, 256, 0, s>>>(wh, static_cast<int64_t>(hash_dims) * d, wh_f32);
+  launch_kernel(widen_bf16, 64, 256, 0, s, wh, static_cast<int64_t>(hash_dims) * d, wh_f32);
   return cudaGetLastError();
 }
 
 cudaError_t launch_router_hash(const HashRouterArgs& a, cudaStream_t s) {
   if (a.T <= 0) return cudaSuccess;
   if (a.hash_dims < 1 || a.hash_dims > kHashDimsMax || a.d % kChunk != 0) return cudaErrorInvalidValue;
-  router_hash_kernel<<<(a.T + kHashTokens - 1) / kHashTokens, kHashThreads, 0, s>>>(a);
+  launch_kernel(router_hash_kernel, (a.T + kHashTokens - 1) / kHashTokens, kHashThreads, 0, s, a);
   return cudaGetLastError();
 }
 

@@ -110,6 +110,8 @@ __global__ void __launch_bounds__(THREADS, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  grid_dep_wait();    // what earlier kernels in the stream wrote is visible from here
+  grid_dep_launch();
   const int n_tiles = (a.T + BM - 1) / BM;
   const int n_units = n_tiles * a.ks;
   const int kblocks = a.d / BK;
@@ -255,6 +257,8 @@ __device__ __forceinline__ uint32_t order_key(float v) {
 template <int NPL, int KMAX>
 __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restrict__ part, int ks, int t_pad, int np,
                                                           const RouterArgs a) {
+  grid_dep_wait();    // what earlier kernels in the stream wrote is visible from here
+  grid_dep_launch();
   const int lane = threadIdx.x % 32;
   const int t = blockIdx.x * 8 + threadIdx.x / 32;
   if (t >= a.T) return;
@@ -336,17 +340,17 @@ cudaError_t launch_np(const CUtensorMap& tx, const CUtensorMap& tw, const Router
   const int units = (a.T + BM - 1) / BM * ks;
   const int slots = RtCfg<NP>::CTAS_PER_SM * num_sms;
   const int grid = units < slots ? units : slots;
-  router_tc_part_kernel<NP><<<grid, THREADS, RtCfg<NP>::SMEM_BYTES, s>>>(tx, tw, pa, kWaitLimitNs);
+  launch_kernel(router_tc_part_kernel<NP>, grid, THREADS, RtCfg<NP>::SMEM_BYTES, s, tx, tw, pa, kWaitLimitNs);
   constexpr int NPL = NP < 32 ? 1 : NP / 32;
   const int blocks = (a.T + 7) / 8;
   if (a.k <= 2)
-    router_topk_kernel<NPL, 2><<<blocks, 256, 0, s>>>(part, ks, t_pad, NP, a);
+    launch_kernel(router_topk_kernel<NPL, 2>, blocks, 256, 0, s, part, ks, t_pad, NP, a);
   else if (a.k <= 4)
-    router_topk_kernel<NPL, 4><<<blocks, 256, 0, s>>>(part, ks, t_pad, NP, a);
+    launch_kernel(router_topk_kernel<NPL, 4>, blocks, 256, 0, s, part, ks, t_pad, NP, a);
   else if (a.k <= 8)
-    router_topk_kernel<NPL, 8><<<blocks, 256, 0, s>>>(part, ks, t_pad, NP, a);
+    launch_kernel(router_topk_kernel<NPL, 8>, blocks, 256, 0, s, part, ks, t_pad, NP, a);
   else
-    router_topk_kernel<NPL, 16><<<blocks, 256, 0, s>>>(part, ks, t_pad, NP, a);
+    launch_kernel(router_topk_kernel<NPL, 16>, blocks, 256, 0, s, part, ks, t_pad, NP, a);
   return cudaGetLastError();
 }
 

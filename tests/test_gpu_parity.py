@@ -410,3 +410,30 @@ def test_stage_timing_switch():
     with pytest.raises(cb.CbMoeError):
         m2.set_stage_timing(True)
     del m, m2
+
+
+@pytest.mark.parametrize("name", ["tiny", "skewed_small", "int8_pairs", "ragged_mid"])
+def test_programmatic_dependent_launch(name, monkeypatch):
+    """CB_MOE_PDL=1: the forward's kernels after the first are launched with
+    programmatic stream serialization on a stream (each waits for its
+    predecessor's grid before reading its output); same results."""
+    monkeypatch.setenv("CB_MOE_PDL", "1")
+    layer = synth.make_layer(SMALL[name])
+    gl = gh.GpuLayer(layer)
+    try:
+        # on the legacy default stream the launches are plain: the reference
+        gl.m.forward(gl.x, gl.out)
+        torch.cuda.synchronize()
+        plain = gl.out.clone()
+        stream = torch.cuda.Stream()
+        with torch.cuda.stream(stream):
+            for _ in range(4):
+                gl.out.zero_()
+                gl.m.forward(gl.x, gl.out, stream=stream)
+        stream.synchronize()
+        assert gl.m.last_error() == 0
+        assert torch.equal(plain.view(torch.int16), gl.out.view(torch.int16))
+    finally:
+        gl.close()
+    rep = gh.full_check(layer)
+    print(name, "pdl", rep)
