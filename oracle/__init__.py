@@ -25,7 +25,10 @@ class _Layer(ctypes.Structure):
                 ("x", ctypes.c_void_p), ("wr", ctypes.c_void_p), ("bias", ctypes.c_void_p),
                 ("wg", ctypes.c_void_p), ("wu", ctypes.c_void_p), ("wd", ctypes.c_void_p),
                 ("sg", ctypes.c_void_p), ("su", ctypes.c_void_p), ("sd", ctypes.c_void_p),
-                ("router_mode", ctypes.c_int32), ("hash_dims", ctypes.c_int32), ("wh", ctypes.c_void_p)]
+                ("router_mode", ctypes.c_int32), ("hash_dims", ctypes.c_int32), ("wh", ctypes.c_void_p),
+                ("zg", ctypes.c_void_p), ("zu", ctypes.c_void_p), ("zd", ctypes.c_void_p)]
+
+WDTYPES = {"bf16": 0, "int8": 1, "int4": 2}
 
 ROUTER_MODES = {"softmax": 0, "raw": 1, "hash": 2}
 
@@ -94,13 +97,14 @@ class Oracle:
         T = layer.x.shape[0]
         self._keep = [np.ascontiguousarray(a) if a is not None else None
                       for a in (layer.x, layer.wr, layer.bias, layer.wg, layer.wu, layer.wd,
-                                layer.sg, layer.su, layer.sd, getattr(layer, "wh", None))]
-        x, wr, b, wg, wu, wd, sg, su, sd, wh = self._keep
+                                layer.sg, layer.su, layer.sd, getattr(layer, "wh", None),
+                                getattr(layer, "zg", None), getattr(layer, "zu", None), getattr(layer, "zd", None))]
+        x, wr, b, wg, wu, wd, sg, su, sd, wh, zg, zu, zd = self._keep
         self.T, self.d, self.f, self.E, self.k = T, s.d, s.f, s.E, s.k
         router = getattr(s, "router", "softmax")
-        self.c = _Layer(T, s.d, s.f, s.E, s.k, 1 if s.wdtype == "int8" else 0,
+        self.c = _Layer(T, s.d, s.f, s.E, s.k, WDTYPES[s.wdtype],
                         _p(x), _p(wr), _p(b), _p(wg), _p(wu), _p(wd), _p(sg), _p(su), _p(sd),
-                        ROUTER_MODES[router], getattr(s, "hash_dims", 0), _p(wh))
+                        ROUTER_MODES[router], getattr(s, "hash_dims", 0), _p(wh), _p(zg), _p(zu), _p(zd))
 
     def route(self, tokens=None, want_logits=False):
         """Gate for the listed tokens (all when None): ids, w, gap_k, gap_slot[, logits]."""

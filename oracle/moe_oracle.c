@@ -42,6 +42,11 @@
  *     SiLU(z) = z / (1 + exp(-z)), y_c = sum_j h_j Wd[e][c][j].
  *     int8 experts (symmetric per-output-channel, "lshu.cn/news/53496" §4.3):
  *     W[e][j][i] = s[e][j] * Q[e][j][i], so g_j = s_g[e][j] * sum_i x_i Q_g.
+ *     int4 experts (4-bit codes with a scale and a zero point per channel,
+ *     "m.nxbn.cn/news/47706" §3.2; a channel is read as an output row):
+ *     W[e][j][i] = s[e][j] * (q[e][j][i] - z[e][j]) with q in 0..15 packed two
+ *     to a byte along i (element 2m in the low nibble of byte m) and an
+ *     integer zero point z, so g_j = s_g[e][j] * sum_i x_i (q_g - z_g).
  *     Mode EXACT keeps h in double; mode BF16H rounds each h_j to bf16
  *     (round to nearest even) before the down projection, which is the
  *     precision the layer's bf16 down-projection operand holds.
@@ -49,7 +54,8 @@
  *     o[t] = sum_s w[t][s] * y(t, s).
  *
  * Every sum is a plain sequential loop in double.  Inputs are bf16 bit
- * patterns (uint16) or int8 codes with float scales.
+ * patterns (uint16), or int8 or packed int4 codes with float scales (and
+ * uint8 zero points for int4).
  */
 #include <math.h>
 #include <stdint.h>
@@ -61,7 +67,8 @@
 
 typedef struct {
   int32_t T, d, f, E, k;
-  int32_t wdtype;                 /* 0 = bf16 weights, 1 = int8 + scales */
+  int32_t wdtype;                 /* 0 = bf16 weights, 1 = int8 + scales,
+                                     2 = int4 + scales + zero points      */
   const uint16_t *x;              /* [T][d] bf16 bits                    */
   const uint16_t *wr;             /* [E][d] bf16 bits                    */
   const float *bias;              /* [E] or NULL                         */
@@ -72,6 +79,8 @@ typedef struct {
   int32_t router_mode;            /* 0 softmax top-k, 1 raw logits, 2 hash */
   int32_t hash_dims;              /* hash router: rows of wh             */
   const uint16_t *wh;             /* [hash_dims][d] bf16 bits, or NULL   */
+  const uint8_t *zg, *zu;         /* [E][f] zero points (int4 only)      */
+  const uint8_t *zd;              /* [E][d] (int4 only)                  */
 } moe_oracle_layer_t;
 
 enum { ORACLE_EXACT = 0, ORACLE_BF16H = 1 };
@@ -130,9 +139,14 @@ uint16_t moe_oracle_bf16_bits(double v) {
   return (uint16_t)(u >> 16);
 }
 
-static double weight_elem(const moe_oracle_layer_t *L, const void *w, int64_t idx) {
+/* Element idx of a weight tensor before its channel scale: the bf16 value,
+ * the int8 code, or the int4 code minus the row's zero point `zero`. */
+static double weight_elem(const moe_oracle_layer_t *L, const void *w, int64_t idx, int zero) {
   if (L->wdtype == 0) return bf16_value(((const uint16_t *)w)[idx]);
-  return (double)((const int8_t *)w)[idx];
+  if (L->wdtype == 1) return (double)((const int8_t *)w)[idx];
+  const uint8_t byte = ((const uint8_t *)w)[idx / 2];
+  const int q = (idx % 2 == 0) ? (byte & 0x0F) : (byte >> 4);
+  return (double)(q - zero);
 }
 
 /* ---------------------------------------------------------- 1. the router */
@@ -309,13 +323,15 @@ static void expert_row(const moe_oracle_layer_t *L, int e, const double *xv, int
                        double *h, double *y) {
   const int d = L->d, f = L->f;
   const int64_t gbase = (int64_t)e * f * d, dbase = (int64_t)e * d * f;
+  const int int4 = L->wdtype == 2;
   for (int j = 0; j < f; ++j) {
     double g = 0.0, u = 0.0;
+    const int zg = int4 ? L->zg[(int64_t)e * f + j] : 0, zu = int4 ? L->zu[(int64_t)e * f + j] : 0;
     for (int i = 0; i < d; ++i) {
-      g += xv[i] * weight_elem(L, L->wg, gbase + (int64_t)j * d + i);
-      u += xv[i] * weight_elem(L, L->wu, gbase + (int64_t)j * d + i);
+      g += xv[i] * weight_elem(L, L->wg, gbase + (int64_t)j * d + i, zg);
+      u += xv[i] * weight_elem(L, L->wu, gbase + (int64_t)j * d + i, zu);
     }
-    if (L->wdtype == 1) {
+    if (L->wdtype != 0) {
       g *= (double)L->sg[(int64_t)e * f + j];
       u *= (double)L->su[(int64_t)e * f + j];
     }
@@ -325,8 +341,9 @@ static void expert_row(const moe_oracle_layer_t *L, int e, const double *xv, int
   }
   for (int c = 0; c < d; ++c) {
     double acc = 0.0;
-    for (int j = 0; j < f; ++j) acc += h[j] * weight_elem(L, L->wd, dbase + (int64_t)c * f + j);
-    if (L->wdtype == 1) acc *= (double)L->sd[(int64_t)e * d + c];
+    const int zd = int4 ? L->zd[(int64_t)e * d + c] : 0;
+    for (int j = 0; j < f; ++j) acc += h[j] * weight_elem(L, L->wd, dbase + (int64_t)c * f + j, zd);
+    if (L->wdtype != 0) acc *= (double)L->sd[(int64_t)e * d + c];
     y[c] = acc;
   }
 }

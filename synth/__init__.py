@@ -29,10 +29,18 @@ _lib = None
 
 # tensor ids of the counter streams
 TID_X, TID_WR, TID_WG, TID_WU, TID_WD, TID_SG, TID_SU, TID_SD, TID_WH = 1, 2, 3, 4, 5, 6, 7, 8, 9
+TID_ZG, TID_ZU, TID_ZD = 10, 11, 12
 
 WEIGHT_STD = 0.02      # bf16 weights ~ N(0, 0.02^2)
 INT8_SCALE = 40.0      # int8 codes round(40 N(0,1)) clipped to [-127, 127]
 SCALE_LO, SCALE_HI = 0.5e-3, 1.0e-3   # per-output-channel fp32 scales ~ U
+# int4 weights, asymmetric per output channel: W = s (q - z) with 4-bit codes
+# q = z + clip(rint(2.5 N(0,1)), -6, 6), integer zero points z = 7 +
+# clip(rint(1.2 N(0,1)), -1, 2) in 6..9 (so q stays in 0..15) and scales
+# s ~ U(0.006, 0.010): weights of about the bf16 layers' N(0, 0.02^2) spread
+INT4_CODE_SCALE, INT4_CODE_LO, INT4_CODE_HI = 2.5, -6, 6
+INT4_ZERO_SCALE, INT4_ZERO_LO, INT4_ZERO_HI, INT4_ZERO_MID = 1.2, -1, 2, 7
+INT4_SCALE_LO, INT4_SCALE_HI = 0.006, 0.010
 
 
 def build(force: bool = False) -> str:
@@ -93,6 +101,30 @@ def uniform_f32(seed, tid, lo, hi, shape, offset=0) -> np.ndarray:
     return out.reshape(shape)
 
 
+def pack_int4(q: np.ndarray) -> np.ndarray:
+    """4-bit codes 0..15 [..., n] (n even) -> bytes [..., n/2]: element 2i in the
+    low nibble of byte i, element 2i + 1 in its high nibble."""
+    q = q.astype(np.uint8)
+    return (q[..., 0::2] | (q[..., 1::2] << 4)).astype(np.uint8)
+
+
+def unpack_int4(b: np.ndarray) -> np.ndarray:
+    """Inverse of pack_int4."""
+    out = np.empty(b.shape[:-1] + (2 * b.shape[-1],), dtype=np.uint8)
+    out[..., 0::2] = b & 0x0F
+    out[..., 1::2] = b >> 4
+    return out
+
+
+def int4_weights(seed, tid_w, tid_z, rows_shape, cols):
+    """Packed int4 codes [..., cols/2] and their zero points [...] (uint8)."""
+    z = (int8_codes(seed, tid_z, INT4_ZERO_SCALE, rows_shape, INT4_ZERO_LO, INT4_ZERO_HI).astype(np.int32)
+         + INT4_ZERO_MID)
+    c = int8_codes(seed, tid_w, INT4_CODE_SCALE, rows_shape + (cols,), INT4_CODE_LO, INT4_CODE_HI).astype(np.int32)
+    q = c + z[..., None]
+    return pack_int4(q), z.astype(np.uint8)
+
+
 def raw_bits(seed, tid, n, offset=0) -> np.ndarray:
     out = np.empty(n, dtype=np.uint64)
     _load().synth_bits(seed, tid, out.ctypes.data, offset, n)
@@ -113,7 +145,7 @@ class Shape:
     f: int
     E: int
     k: int
-    wdtype: str = "bf16"       # "bf16" or "int8"
+    wdtype: str = "bf16"       # "bf16", "int8" or "int4"
     bias: bool = False         # skewed router bias b_e = 2 ln(1/(e+1))
     seed: int = 0
     router: str = "softmax"    # "softmax" (top-k, renormalised), "raw" (raw-logit weights), "hash"
@@ -127,6 +159,8 @@ WORKLOADS = {
     "mixtral_decode": Shape("mixtral_decode", T=64, d=4096, f=14336, E=8, k=2, seed=1003),
     "skewed": Shape("skewed", T=8192, d=2048, f=768, E=128, k=4, bias=True, seed=1004),
     "int8": Shape("int8", T=16384, d=4096, f=1536, E=64, k=6, wdtype="int8", seed=1005),
+    # the int8 layer's shape with 4-bit weights (scale and zero point per channel)
+    "int4": Shape("int4", T=16384, d=4096, f=1536, E=64, k=6, wdtype="int4", seed=1006),
 }
 
 
@@ -142,13 +176,16 @@ class Layer:
     x: np.ndarray                 # [T][d] bf16 bits
     wr: np.ndarray                # [E][d] bf16 bits
     bias: np.ndarray | None       # [E] float32
-    wg: np.ndarray                # [E][f][d] bf16 bits or int8
+    wg: np.ndarray                # [E][f][d] bf16 bits or int8; int4: [E][f][d/2] packed
     wu: np.ndarray                # [E][f][d]
     wd: np.ndarray                # [E][d][f]
-    sg: np.ndarray | None = None  # [E][f] float32 (int8 only)
+    sg: np.ndarray | None = None  # [E][f] float32 (int8 and int4)
     su: np.ndarray | None = None  # [E][f]
     sd: np.ndarray | None = None  # [E][d]
     wh: np.ndarray | None = None  # [hash_dims][d] bf16 bits (hash router only)
+    zg: np.ndarray | None = None  # [E][f] uint8 zero points (int4 only)
+    zu: np.ndarray | None = None  # [E][f]
+    zd: np.ndarray | None = None  # [E][d]
     extra: dict = field(default_factory=dict)
 
 
@@ -166,6 +203,14 @@ def make_layer(shape: Shape, seed: int | None = None, T: int | None = None) -> L
         wu = normal_bf16(s, TID_WU, WEIGHT_STD, (E, f, d))
         wd = normal_bf16(s, TID_WD, WEIGHT_STD, (E, d, f))
         return Layer(shape, x, wr, bias, wg, wu, wd, wh=wh)
+    if shape.wdtype == "int4":
+        wg, zg = int4_weights(s, TID_WG, TID_ZG, (E, f), d)
+        wu, zu = int4_weights(s, TID_WU, TID_ZU, (E, f), d)
+        wd, zd = int4_weights(s, TID_WD, TID_ZD, (E, d), f)
+        sg = uniform_f32(s, TID_SG, INT4_SCALE_LO, INT4_SCALE_HI, (E, f))
+        su = uniform_f32(s, TID_SU, INT4_SCALE_LO, INT4_SCALE_HI, (E, f))
+        sd = uniform_f32(s, TID_SD, INT4_SCALE_LO, INT4_SCALE_HI, (E, d))
+        return Layer(shape, x, wr, bias, wg, wu, wd, sg, su, sd, wh=wh, zg=zg, zu=zu, zd=zd)
     wg = int8_codes(s, TID_WG, INT8_SCALE, (E, f, d))
     wu = int8_codes(s, TID_WU, INT8_SCALE, (E, f, d))
     wd = int8_codes(s, TID_WD, INT8_SCALE, (E, d, f))

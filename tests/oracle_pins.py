@@ -39,20 +39,25 @@ def bf16_bits_to_f64(b):
 
 
 def make_layer_from_values(x, wr, wg, wu, wd, k, bias=None, wdtype="bf16", sg=None, su=None, sd=None,
-                           router="softmax", wh=None):
-    """A synth.Layer from explicit values (bf16-exact floats or int8 codes)."""
+                           router="softmax", wh=None, zg=None, zu=None, zd=None):
+    """A synth.Layer from explicit values (bf16-exact floats, int8 codes, or packed int4
+    bytes with uint8 zero points)."""
     x = np.asarray(x, np.float64)
     wr = np.asarray(wr, np.float64)
     T, d = x.shape
     E = wr.shape[0]
     wg_a = np.asarray(wg)
     f = wg_a.shape[1]
+    if wdtype == "int4":
+        d = 2 * wg_a.shape[2]
     hd = 0 if wh is None else np.asarray(wh).shape[0]
     shape = synth.Shape("custom", T=T, d=d, f=f, E=E, k=k, wdtype=wdtype, bias=bias is not None, router=router,
                         hash_dims=hd)
     conv = f32_to_bf16_bits
     if wdtype == "bf16":
         wgb, wub, wdb = conv(wg), conv(wu), conv(wd)
+    elif wdtype == "int4":
+        wgb, wub, wdb = (np.asarray(a, np.uint8) for a in (wg, wu, wd))
     else:
         wgb = np.asarray(wg, np.int8)
         wub = np.asarray(wu, np.int8)
@@ -62,7 +67,10 @@ def make_layer_from_values(x, wr, wg, wu, wd, k, bias=None, wdtype="bf16", sg=No
                        None if sg is None else np.asarray(sg, np.float32),
                        None if su is None else np.asarray(su, np.float32),
                        None if sd is None else np.asarray(sd, np.float32),
-                       wh=None if wh is None else conv(wh))
+                       wh=None if wh is None else conv(wh),
+                       zg=None if zg is None else np.asarray(zg, np.uint8),
+                       zu=None if zu is None else np.asarray(zu, np.uint8),
+                       zd=None if zd is None else np.asarray(zd, np.uint8))
 
 
 def dense_swiglu(xv, wg, wu, wd):
@@ -290,6 +298,40 @@ def pin_int8_equals_bf16(lib):
         assert np.allclose(oi, ob, rtol=1e-13, atol=1e-15), np.abs(oi - ob).max()
 
 
+def _pack_nibbles(q):
+    """The ABI's int4 layout written out: byte m of a row = q[2m] + 16 q[2m + 1]."""
+    q = np.asarray(q, np.int64)
+    return (q[..., 0::2] + 16 * q[..., 1::2]).astype(np.uint8)
+
+
+def pin_int4_equals_bf16(lib):
+    """4-bit codes q with per-output-channel zero points z and power-of-two scales s equal the
+    bf16 layer whose weights are s[j] * (q[j][i] - z[j]) (exact in both), for gate/up (channel
+    j) and down (channel c); a hand-packed byte 0x21 holds elements (1, 2)."""
+    rng = np.random.default_rng(12)
+    T, d, f, E, k = 6, 16, 24, 4, 2
+    x = rng_bf16(rng, (T, d), 1.0)
+    wr = rng_bf16(rng, (E, d), 0.3)
+    qg, qu, qd = rng.integers(0, 16, (E, f, d)), rng.integers(0, 16, (E, f, d)), rng.integers(0, 16, (E, d, f))
+    zg, zu, zd = rng.integers(0, 16, (E, f)), rng.integers(0, 16, (E, f)), rng.integers(0, 16, (E, d))
+    sg = 2.0 ** -rng.integers(5, 10, (E, f)); su = 2.0 ** -rng.integers(5, 10, (E, f))
+    sd = 2.0 ** -rng.integers(5, 10, (E, d))
+    Li = make_layer_from_values(x, wr, _pack_nibbles(qg), _pack_nibbles(qu), _pack_nibbles(qd), k, wdtype="int4",
+                                sg=sg, su=su, sd=sd, zg=zg, zu=zu, zd=zd)
+    Lb = make_layer_from_values(x, wr, (qg - zg[:, :, None]) * sg[:, :, None], (qu - zu[:, :, None]) * su[:, :, None],
+                                (qd - zd[:, :, None]) * sd[:, :, None], k)
+    for mode in (oracle.EXACT, oracle.BF16H):
+        oi, ii, _ = oracle.Oracle(Li, lib).forward(mode=mode)
+        ob, ib, _ = oracle.Oracle(Lb, lib).forward(mode=mode)
+        assert np.array_equal(ii, ib)
+        assert np.allclose(oi, ob, rtol=1e-13, atol=1e-15), np.abs(oi - ob).max()
+    assert _pack_nibbles([[1, 2]])[0, 0] == 0x21
+    # the generator's packing is the same layout
+    q = rng.integers(0, 16, (3, 8))
+    assert np.array_equal(synth.pack_int4(q), _pack_nibbles(q))
+    assert np.array_equal(synth.unpack_int4(_pack_nibbles(q)), q)
+
+
 def pin_token_permutation(lib):
     rng = np.random.default_rng(10)
     L, (x, wr, wg, wu, wd) = _random_layer(rng, 9, 16, 8, 5, 2)
@@ -428,5 +470,6 @@ def pin_hash_invariants(lib):
 
 ALL_PINS = [pin_round_bf16, pin_gate_bruteforce, pin_gate_weights, pin_dispatch, pin_identical_experts,
             pin_one_hot_router, pin_two_expert_mix, pin_zero_input, pin_bf16_h_mode, pin_int8_equals_bf16,
+            pin_int4_equals_bf16,
             pin_token_permutation, pin_expert_relabel, pin_golden_tiny, pin_routing_invariants,
             pin_raw_gate, pin_hash_golden, pin_hash_invariants]

@@ -37,10 +37,18 @@ MUTANTS = {
     "hash_sums_in_double": ("    float r = 0.0f;\n", "    double r = 0.0;\n"),
     "hash_sums_backward": ("for (int j = 0; j < d; ++j) r += (float)bf16_value(xrow[j])",
                            "for (int j = d - 1; j >= 0; --j) r += (float)bf16_value(xrow[j])"),
-    "gate_transposed": ("g += xv[i] * weight_elem(L, L->wg, gbase + (int64_t)j * d + i);",
-                        "g += xv[i] * weight_elem(L, L->wg, gbase + (int64_t)i * f + j);"),
-    "down_transposed": ("weight_elem(L, L->wd, dbase + (int64_t)c * f + j)",
-                        "weight_elem(L, L->wd, dbase + (int64_t)j * d + c)"),
+    "gate_transposed": ("g += xv[i] * weight_elem(L, L->wg, gbase + (int64_t)j * d + i, zg);",
+                        "g += xv[i] * weight_elem(L, L->wg, gbase + (int64_t)i * f + j, zg);"),
+    "down_transposed": ("weight_elem(L, L->wd, dbase + (int64_t)c * f + j, zd)",
+                        "weight_elem(L, L->wd, dbase + (int64_t)j * d + c, zd)"),
+    "int4_nibbles_swapped": ("const int q = (idx % 2 == 0) ? (byte & 0x0F) : (byte >> 4);",
+                             "const int q = (idx % 2 == 0) ? (byte >> 4) : (byte & 0x0F);"),
+    "int4_zero_added": ("return (double)(q - zero);", "return (double)(q + zero);"),
+    "int4_zero_dropped": ("return (double)(q - zero);", "return (double)q;"),
+    "int4_gate_uses_up_zero": ("const int zg = int4 ? L->zg[(int64_t)e * f + j] : 0,",
+                               "const int zg = int4 ? L->zu[(int64_t)e * f + j] : 0,"),
+    "int4_down_zero_index": ("const int zd = int4 ? L->zd[(int64_t)e * d + c] : 0;",
+                             "const int zd = int4 ? L->zd[(int64_t)e * d] : 0;"),
     "bf16_truncates": ("b += ((uint64_t)1 << 44) - 1u + lsb;", ""),
     "bf16_ties_away": ("b += ((uint64_t)1 << 44) - 1u + lsb;", "b += ((uint64_t)1 << 44);"),
     "int8_gate_uses_up_scale": ("g *= (double)L->sg[(int64_t)e * f + j];", "g *= (double)L->su[(int64_t)e * f + j];"),

@@ -65,3 +65,20 @@ def test_workload_shapes():
     assert b[0] == 0.0 and math.isclose(b[127], 2 * math.log(1 / 128), rel_tol=1e-7)
     L = synth.make_layer(w["tiny"])
     assert L.x.shape == (64, 256) and L.wg.shape == (8, 512, 256) and L.wd.shape == (8, 256, 512)
+
+
+def test_int4_weights_ranges_and_packing():
+    """int4 layers: codes 0..15 packed two to a byte (element 2m low nibble), zero
+    points 6..9, q - z within +-6, scales in [0.006, 0.010)."""
+    shape = synth.custom_shape("i4", T=4, d=64, f=32, E=3, k=2, wdtype="int4", seed=5)
+    L = synth.make_layer(shape)
+    assert L.wg.shape == (3, 32, 32) and L.wd.shape == (3, 64, 16) and L.wg.dtype == np.uint8
+    for w, z in ((L.wg, L.zg), (L.wu, L.zu), (L.wd, L.zd)):
+        q = synth.unpack_int4(w).astype(int)
+        assert q.min() >= 0 and q.max() <= 15
+        assert z.min() >= 6 and z.max() <= 9
+        c = q - z.astype(int)[..., None]
+        assert np.abs(c).max() <= 6 and 2.0 < c.std() < 3.0
+        assert np.array_equal(synth.pack_int4(q), w)
+    for s in (L.sg, L.su, L.sd):
+        assert s.dtype == np.float32 and s.min() >= 0.006 and s.max() < 0.010
