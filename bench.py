@@ -47,7 +47,7 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--shape", default=None, help="T,d,f,E,k of a custom layer (profiling cases)")
-    p.add_argument("--wdtype", default="bf16", choices=["bf16", "int8"], help="expert weights of a --shape layer")
+    p.add_argument("--wdtype", default="bf16", choices=["bf16", "int8", "int4"], help="expert weights of a --shape layer")
     p.add_argument("--bias", action="store_true", help="skewed router bias on a --shape layer")
     p.add_argument("--router", default="softmax", choices=["softmax", "raw", "hash"],
                    help="router variant: softmax top-k (default), raw-logit weights, or the hash router (k = 1)")
@@ -81,9 +81,11 @@ def algorithmic_work(shape, counts):
     count routed rows only (padding rows of the 128-row tiles are waste)."""
     T, d, f, E, k = shape.T, shape.d, shape.f, shape.E, shape.k
     M = T * k
-    eb = 1 if shape.wdtype == "int8" else 2
+    eb = {"bf16": 2.0, "int8": 1.0, "int4": 0.5}[shape.wdtype]   # bytes per expert weight
     active = sum(1 for c in counts if c > 0)
-    wbytes = active * 3 * d * f * eb + (active * (2 * f + d) * 4 if eb == 1 else 0)
+    # + per-channel scales (int8, int4) and zero points (int4)
+    side = (4 if shape.wdtype != "bf16" else 0) + (1 if shape.wdtype == "int4" else 0)
+    wbytes = int(active * 3 * d * f * eb) + active * (2 * f + d) * side
     return {
         "router_bytes": T * d * 2 + (shape.hash_dims if shape.router == "hash" else E) * d * 2 + T * k * 8,
         "dispatch_bytes": T * d * 2 + M * d * 2 + 16 * M,
@@ -91,8 +93,8 @@ def algorithmic_work(shape, counts):
         "down_flops": 2 * d * f * M,
         "combine_bytes": M * d * 4 + 8 * M + T * d * 2,
         "active_expert_weight_bytes": wbytes,
-        "gateup_weight_bytes": active * 2 * d * f * eb,
-        "down_weight_bytes": active * d * f * eb,
+        "gateup_weight_bytes": int(active * 2 * d * f * eb),
+        "down_weight_bytes": int(active * d * f * eb),
     }
 
 
@@ -288,10 +290,11 @@ def run_ours(args):
             return torch.from_numpy(a.view(np.int16)).to(device).view(torch.bfloat16)
         return torch.from_numpy(a).to(device)
 
-    w = {n: dev(getattr(layer, n)) for n in ("wr", "bias", "wg", "wu", "wd", "sg", "su", "sd", "wh")}
+    w = {n: dev(getattr(layer, n)) for n in ("wr", "bias", "wg", "wu", "wd", "sg", "su", "sd", "wh", "zg", "zu", "zd")}
     m = cb.MoELayer(shape.T, shape.d, shape.f, shape.E, shape.k, w["wr"], w["wg"], w["wu"], w["wd"],
                     router_bias=w["bias"], s_gate=w["sg"], s_up=w["su"], s_down=w["sd"], device=local,
-                    stage_timing=True, router=shape.router, w_hash=w["wh"])
+                    stage_timing=True, router=shape.router, w_hash=w["wh"], z_gate=w["zg"], z_up=w["zu"],
+                    z_down=w["zd"])
     launches_per_forward = m.kernels_per_forward()
     del w
     torch.cuda.empty_cache()
@@ -443,7 +446,7 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "int8" if shape.wdtype == "int8" else "bf16",
+        "scaling": "weak", "vs_baseline": None, "dtype": shape.wdtype,
         "data": "synthetic (seeded SplitMix64/Box-Muller; x ~ N(0,1), weights ~ N(0, 0.02^2), bf16)",
         "config": config_block(shape, args.l2_flush_mb),
         "e2e": {"value": shape.T * world * k2 / (e2e_ms / 1e3), "unit": "tokens/s",
@@ -473,7 +476,7 @@ def workload_shape(args):
     import synth
     if args.shape:
         T, d, f, E, k = (int(v) for v in args.shape.split(","))
-        name = f"custom_T{T}_d{d}_f{f}_E{E}_k{k}" + ("_int8" if args.wdtype == "int8" else "") + \
+        name = f"custom_T{T}_d{d}_f{f}_E{E}_k{k}" + (f"_{args.wdtype}" if args.wdtype != "bf16" else "") + \
             ("_bias" if args.bias else "")
         return synth.with_router(synth.custom_shape(name, T=T, d=d, f=f, E=E, k=k, wdtype=args.wdtype,
                                                     bias=args.bias, seed=1100), args.router)

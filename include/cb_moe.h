@@ -67,7 +67,14 @@ typedef enum {
                               range or a row past the workspace (cb_moe_last_error)      */
 } cb_status_t;
 
-typedef enum { CB_W_BF16 = 0, CB_W_INT8 = 1 } cb_wdtype_t;
+/* Expert weight formats.  CB_W_INT8: symmetric int8 codes q with an fp32
+ * scale s per output channel, W = s q ("lshu.cn/news/53496" §4.3).
+ * CB_W_INT4: 4-bit codes q in 0..15 with an fp32 scale s and an integer zero
+ * point z (uint8, 0..15) per output channel, W = s (q - z)
+ * ("m.nxbn.cn/news/47706" §3.2, a channel read as an output row); the codes
+ * are packed two to a byte along the input dimension, element 2m in the low
+ * nibble of byte m and element 2m + 1 in its high nibble. */
+typedef enum { CB_W_BF16 = 0, CB_W_INT8 = 1, CB_W_INT4 = 2 } cb_wdtype_t;
 
 /*
  * config.router_mode: how each token picks its experts and their weights.
@@ -118,13 +125,16 @@ typedef struct {
 typedef struct {
   const void *w_router;     /* bf16 [E][d]                                        */
   const float *router_bias; /* fp32 [E], or NULL for no bias                      */
-  const void *w_gate;       /* bf16 or int8 [E][f][d]   (w1)                      */
-  const void *w_up;         /* bf16 or int8 [E][f][d]   (w3)                      */
-  const void *w_down;       /* bf16 or int8 [E][d][f]   (w2)                      */
-  const float *s_gate;      /* fp32 [E][f]  int8 only, else NULL                  */
-  const float *s_up;        /* fp32 [E][f]  int8 only, else NULL                  */
-  const float *s_down;      /* fp32 [E][d]  int8 only, else NULL                  */
+  const void *w_gate;       /* bf16 or int8 [E][f][d]; int4 [E][f][d/2] bytes (w1)  */
+  const void *w_up;         /* bf16 or int8 [E][f][d]; int4 [E][f][d/2] bytes (w3)  */
+  const void *w_down;       /* bf16 or int8 [E][d][f]; int4 [E][d][f/2] bytes (w2)  */
+  const float *s_gate;      /* fp32 [E][f]  int8 and int4, else NULL              */
+  const float *s_up;        /* fp32 [E][f]  int8 and int4, else NULL              */
+  const float *s_down;      /* fp32 [E][d]  int8 and int4, else NULL              */
   const void *w_hash;       /* bf16 [hash_dims][d], CB_ROUTER_HASH only, else NULL */
+  const uint8_t *z_gate;    /* uint8 [E][f] zero points 0..15, int4 only, else NULL */
+  const uint8_t *z_up;      /* uint8 [E][f] zero points, int4 only, else NULL     */
+  const uint8_t *z_down;    /* uint8 [E][d] zero points, int4 only, else NULL     */
 } cb_moe_weights_t;
 
 typedef struct cb_moe cb_moe_t;   /* opaque handle */

@@ -15,7 +15,7 @@ LIB_PATH = os.path.join(HERE, "libcbmoe.so")
 
 CB_OK, CB_ERR_INVALID_ARG, CB_ERR_UNSUPPORTED, CB_ERR_ALIGNMENT = 0, 1, 2, 3
 CB_ERR_OOM, CB_ERR_CUDA, CB_ERR_TIMEOUT, CB_ERR_DEVICE = 4, 5, 6, 7
-CB_W_BF16, CB_W_INT8 = 0, 1
+CB_W_BF16, CB_W_INT8, CB_W_INT4 = 0, 1, 2
 CB_FLAG_KEEP_LOGITS = 0x1
 CB_FLAG_STAGE_TIMING = 0x2
 CB_FLAG_TEST_STALL = 0x4
@@ -45,7 +45,8 @@ class cb_moe_weights_t(ctypes.Structure):
     _fields_ = [("w_router", ctypes.c_void_p), ("router_bias", ctypes.c_void_p),
                 ("w_gate", ctypes.c_void_p), ("w_up", ctypes.c_void_p), ("w_down", ctypes.c_void_p),
                 ("s_gate", ctypes.c_void_p), ("s_up", ctypes.c_void_p), ("s_down", ctypes.c_void_p),
-                ("w_hash", ctypes.c_void_p)]
+                ("w_hash", ctypes.c_void_p),
+                ("z_gate", ctypes.c_void_p), ("z_up", ctypes.c_void_p), ("z_down", ctypes.c_void_p)]
 
 
 class cb_routing_view_t(ctypes.Structure):
@@ -204,14 +205,17 @@ class MoELayer:
 
     def __init__(self, T, d, f, E, k, w_router, w_gate, w_up, w_down, router_bias=None,
                  s_gate=None, s_up=None, s_down=None, device=0, keep_logits=False, stage_timing=False,
-                 flags=0, router="softmax", w_hash=None):
+                 flags=0, router="softmax", w_hash=None, z_gate=None, z_up=None, z_down=None):
+        """Expert weights: bf16; int8 codes with scales (s_*); or packed int4 codes (two per
+        byte along the input dimension) with scales and uint8 zero points (z_*)."""
         flags |= (CB_FLAG_KEEP_LOGITS if keep_logits else 0) | (CB_FLAG_STAGE_TIMING if stage_timing else 0)
         mode = ROUTER_MODES[router]
         hash_dims = 0 if w_hash is None else int(w_hash.shape[0])
-        self.cfg = cb_moe_config_t(T, d, f, E, k, CB_W_INT8 if s_gate is not None else CB_W_BF16,
-                                   device, flags, mode, hash_dims)
+        wdtype = CB_W_INT4 if z_gate is not None else CB_W_INT8 if s_gate is not None else CB_W_BF16
+        self.cfg = cb_moe_config_t(T, d, f, E, k, wdtype, device, flags, mode, hash_dims)
         w = cb_moe_weights_t(_ptr(w_router), _ptr(router_bias), _ptr(w_gate), _ptr(w_up), _ptr(w_down),
-                             _ptr(s_gate), _ptr(s_up), _ptr(s_down), _ptr(w_hash))
+                             _ptr(s_gate), _ptr(s_up), _ptr(s_down), _ptr(w_hash),
+                             _ptr(z_gate), _ptr(z_up), _ptr(z_down))
         st, h = cb_moe_init(self.cfg, w)
         if st != CB_OK:
             raise CbMoeError(st, "cb_moe_init")

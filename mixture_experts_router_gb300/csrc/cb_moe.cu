@@ -33,6 +33,7 @@ struct cb_moe {
   void* wgu;  // [E][f/B][2][B][d]: gate rows then up rows per B-row block (B = 128 bf16; int8: 16 or 64)
   void* wd;   // [E][d][f]
   float *sg, *su, *sd;
+  uint8_t *zg, *zu, *zd;  // int4 zero points
   // workspace
   uint16_t* xp;  // [mpad][d]
   uint16_t* hb;  // [mpad][f]
@@ -72,7 +73,7 @@ struct cb_moe {
 namespace {
 
 struct Layout {
-  uint64_t off_wr, off_bias, off_wgu, off_wd, off_sg, off_su, off_sd, off_wh;
+  uint64_t off_wr, off_bias, off_wgu, off_wd, off_sg, off_su, off_sd, off_wh, off_zg, off_zu, off_zd;
   uint64_t off_xp, off_hb, off_y, off_ids, off_w, off_logits, off_rpart, off_chunk, off_counts, off_offsets, off_mtile_off,
       off_mtile_expert, off_ptile_off, off_ptile_expert, off_tok, off_inv, off_err, off_xs, off_os;
   uint64_t total;
@@ -84,7 +85,8 @@ uint64_t align256(uint64_t v) { return (v + 255) & ~uint64_t(255); }
 Layout plan(const cb_moe_config_t& c) {
   Layout L{};
   const uint64_t T = c.n_tokens, d = c.d_model, f = c.d_ff, E = c.n_experts, k = c.top_k;
-  const uint64_t eb = (c.wdtype == CB_W_INT8) ? 1 : 2;
+  const uint64_t wbits = c.wdtype == CB_W_INT8 ? 8 : c.wdtype == CB_W_INT4 ? 4 : 16;  // bits per weight
+  const bool quant = c.wdtype != CB_W_BF16;
   const uint64_t M = T * k;
   L.max_mtiles = static_cast<int32_t>((M + E * (kTileM - 1)) / kTileM + 1);
   L.n_chunks = static_cast<int32_t>((M + kDispatchChunk - 1) / kDispatchChunk);
@@ -97,11 +99,14 @@ Layout plan(const cb_moe_config_t& c) {
   };
   L.off_wr = take(E * d * 2);
   L.off_bias = take(E * 4);
-  L.off_wgu = take(E * 2 * f * d * eb);
-  L.off_wd = take(E * d * f * eb);
-  L.off_sg = take(c.wdtype == CB_W_INT8 ? E * f * 4 : 0);
-  L.off_su = take(c.wdtype == CB_W_INT8 ? E * f * 4 : 0);
-  L.off_sd = take(c.wdtype == CB_W_INT8 ? E * d * 4 : 0);
+  L.off_wgu = take(E * 2 * f * d * wbits / 8);
+  L.off_wd = take(E * d * f * wbits / 8);
+  L.off_sg = take(quant ? E * f * 4 : 0);
+  L.off_su = take(quant ? E * f * 4 : 0);
+  L.off_sd = take(quant ? E * d * 4 : 0);
+  L.off_zg = take(c.wdtype == CB_W_INT4 ? E * f : 0);
+  L.off_zu = take(c.wdtype == CB_W_INT4 ? E * f : 0);
+  L.off_zd = take(c.wdtype == CB_W_INT4 ? E * d : 0);
   L.off_wh = take(c.router_mode == CB_ROUTER_HASH ? static_cast<uint64_t>(c.hash_dims) * d * 4 : 0);  // fp32
   L.off_xp = take(mpad * d * 2);
   L.off_hb = take(mpad * f * 2);
@@ -135,7 +140,7 @@ cb_status_t validate_config(const cb_moe_config_t* c) {
   if (c->n_tokens < 0 || c->d_model <= 0 || c->d_ff <= 0 || c->n_experts <= 0 || c->top_k <= 0)
     return CB_ERR_INVALID_ARG;
   if (c->top_k > c->n_experts) return CB_ERR_INVALID_ARG;
-  if (c->wdtype != CB_W_BF16 && c->wdtype != CB_W_INT8) return CB_ERR_INVALID_ARG;
+  if (c->wdtype != CB_W_BF16 && c->wdtype != CB_W_INT8 && c->wdtype != CB_W_INT4) return CB_ERR_INVALID_ARG;
   if (c->d_model % 256 != 0 || c->d_ff % 256 != 0) return CB_ERR_UNSUPPORTED;
   if (c->n_experts > 256 || c->top_k > 16) return CB_ERR_UNSUPPORTED;
   if (c->router_mode < CB_ROUTER_SOFTMAX_TOPK || c->router_mode > CB_ROUTER_HASH) return CB_ERR_INVALID_ARG;
@@ -284,7 +289,9 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
   da.n_rank_blocks = h->n_rank_blocks;
   if (launch_dispatch(da, s) != cudaSuccess || !mark(2)) return CB_ERR_CUDA;
 
-  const bool int8w = c.wdtype == CB_W_INT8;
+  const bool int4w = c.wdtype == CB_W_INT4;
+  const bool int8w = c.wdtype == CB_W_INT8 || int4w;  // quantized weights (int8 or int4)
+  const int wbits = int4w ? 4 : 8;
   GemmArgs ga{};
   ga.mtile_off = h->mtile_off;
   ga.mtile_expert = h->mtile_expert;
@@ -300,6 +307,8 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
   ga.ld_out = c.d_ff;
   ga.scale0 = h->sg;
   ga.scale1 = h->su;
+  ga.zero0 = h->zg;
+  ga.zero1 = h->zu;
   ga.err = h->err;
   ga.wait_limit_ns = kWaitLimitNs;
   ga.grid = h->num_sms;
@@ -324,7 +333,7 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
   const bool pair_dn = !int8w && h->pair_dn;
   cudaError_t e1;
   if (int8w && h->int8_tm) {
-    e1 = launch_grouped_gemm_int8_tm(kGateUpSwiGLU, h->tm_a_gu, h->tm_w_gu8, ga, s);
+    e1 = launch_grouped_gemm_int8_tm(kGateUpSwiGLU, wbits, h->tm_a_gu, h->tm_w_gu8, ga, s);
   } else if (int8w) {
     e1 = launch_grouped_gemm_int8(kGateUpSwiGLU, h->tm_a_gu, h->tm_b_gu, h->tm_y, ga, s);
   } else if (pair_gu) {
@@ -348,9 +357,11 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
   gd.ld_out = c.d_model;
   gd.scale0 = h->sd;
   gd.scale1 = nullptr;
+  gd.zero0 = h->zd;
+  gd.zero1 = nullptr;
   cudaError_t e2;
   if (int8w && h->int8_tm) {
-    e2 = launch_grouped_gemm_int8_tm(kDownF32, h->tm_a_dn, h->tm_w_dn8, gd, s);
+    e2 = launch_grouped_gemm_int8_tm(kDownF32, wbits, h->tm_a_dn, h->tm_w_dn8, gd, s);
   } else if (int8w) {
     e2 = launch_grouped_gemm_int8(kDownF32, h->tm_a_dn, h->tm_b_dn, h->tm_y, gd, s);
   } else if (pair_dn) {
@@ -484,7 +495,10 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
   if (wts == nullptr || (wts->w_router == nullptr && !hashr) || wts->w_gate == nullptr || wts->w_up == nullptr ||
       wts->w_down == nullptr || (hashr && wts->w_hash == nullptr))
     return CB_ERR_INVALID_ARG;
-  const bool int8w = cfg->wdtype == CB_W_INT8;
+  const bool int4w = cfg->wdtype == CB_W_INT4;
+  const bool int8w = cfg->wdtype == CB_W_INT8 || int4w;  // quantized weights (int8 or int4)
+  if (int4w && (wts->z_gate == nullptr || wts->z_up == nullptr || wts->z_down == nullptr))
+    return CB_ERR_UNSUPPORTED;
   if (int8w && (wts->s_gate == nullptr || wts->s_up == nullptr || wts->s_down == nullptr))
     return CB_ERR_UNSUPPORTED;
   const void* ptrs[] = {wts->w_router, wts->router_bias, wts->w_gate, wts->w_up, wts->w_down,
@@ -520,6 +534,9 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
   h->sg = int8w ? reinterpret_cast<float*>(b + L.off_sg) : nullptr;
   h->su = int8w ? reinterpret_cast<float*>(b + L.off_su) : nullptr;
   h->sd = int8w ? reinterpret_cast<float*>(b + L.off_sd) : nullptr;
+  h->zg = int4w ? reinterpret_cast<uint8_t*>(b + L.off_zg) : nullptr;
+  h->zu = int4w ? reinterpret_cast<uint8_t*>(b + L.off_zu) : nullptr;
+  h->zd = int4w ? reinterpret_cast<uint8_t*>(b + L.off_zd) : nullptr;
   h->xp = reinterpret_cast<uint16_t*>(b + L.off_xp);
   h->hb = reinterpret_cast<uint16_t*>(b + L.off_hb);
   h->y = reinterpret_cast<float*>(b + L.off_y);
@@ -541,7 +558,8 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
   h->out_stage = reinterpret_cast<uint16_t*>(b + L.off_os);
 
   const uint64_t E = cfg->n_experts, d = cfg->d_model, f = cfg->d_ff;
-  const uint64_t eb = int8w ? 1 : 2;
+  const uint64_t eb = int8w ? 1 : 2;                      // element bytes of the bf16 / int8 maps
+  const uint64_t wbits = int4w ? 4 : int8w ? 8 : 16;      // bits per expert weight
   bool ok = cudaMemset(h->block + L.off_xp, 0, L.off_ids - L.off_xp) == cudaSuccess &&
             cudaMemset(h->block + L.off_ids, 0, L.total - L.off_ids) == cudaSuccess;
   if (wts->w_router != nullptr)
@@ -552,24 +570,29 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
     ok = ok && prepare_hash_weights(static_cast<const uint16_t*>(wts->w_hash), cfg->hash_dims, static_cast<int>(d),
                                     h->wh, nullptr) == cudaSuccess;
   if (ok && h->bias) ok = cudaMemcpy(h->bias, wts->router_bias, E * 4, cudaMemcpyDeviceToDevice) == cudaSuccess;
-  ok = ok && cudaMemcpy(h->wd, wts->w_down, E * d * f * eb, cudaMemcpyDeviceToDevice) == cudaSuccess;
+  ok = ok && cudaMemcpy(h->wd, wts->w_down, E * d * f * wbits / 8, cudaMemcpyDeviceToDevice) == cudaSuccess;
   if (ok && int8w) {
     ok = cudaMemcpy(h->sg, wts->s_gate, E * f * 4, cudaMemcpyDeviceToDevice) == cudaSuccess &&
          cudaMemcpy(h->su, wts->s_up, E * f * 4, cudaMemcpyDeviceToDevice) == cudaSuccess &&
          cudaMemcpy(h->sd, wts->s_down, E * d * 4, cudaMemcpyDeviceToDevice) == cudaSuccess;
   }
+  if (ok && int4w) {
+    ok = cudaMemcpy(h->zg, wts->z_gate, E * f, cudaMemcpyDeviceToDevice) == cudaSuccess &&
+         cudaMemcpy(h->zu, wts->z_up, E * f, cudaMemcpyDeviceToDevice) == cudaSuccess &&
+         cudaMemcpy(h->zd, wts->z_down, E * d, cudaMemcpyDeviceToDevice) == cudaSuccess;
+  }
   // gate/up interleave: block n of expert e = gate rows [Bn, Bn+B) then the same up rows
   // int8 expert GEMMs: weights converted into tensor memory as the MMA's A
   // operand (default), or CB_MOE_INT8=smem for the kernel that converts them
   // into shared memory as the B operand; the two interleave gate and up rows
-  // in blocks of different sizes
+  // in blocks of different sizes.  int4 weights have the first kernel only.
   {
     const char* iv = std::getenv("CB_MOE_INT8");
-    h->int8_tm = !(iv != nullptr && std::strcmp(iv, "smem") == 0);
+    h->int8_tm = int4w || !(iv != nullptr && std::strcmp(iv, "smem") == 0);
   }
   const uint64_t brows =
       int8w ? (h->int8_tm ? grouped_gemm_int8_tm_gateup_block() : grouped_gemm_int8_gateup_block()) : 128;
-  const uint64_t blk = brows * d * eb;  // bytes of one block of weight rows
+  const uint64_t blk = brows * d * wbits / 8;  // bytes of one block of weight rows
   const uint64_t nblk = E * (f / brows);
   ok = ok && cudaMemcpy2D(h->wgu, 2 * blk, wts->w_gate, blk, blk, nblk, cudaMemcpyDeviceToDevice) == cudaSuccess;
   ok = ok && cudaMemcpy2D(static_cast<char*>(h->wgu) + blk, 2 * blk, wts->w_up, blk, blk, nblk,
@@ -579,14 +602,16 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
   ok = ok && make_tmap(&h->tm_a_gu, h->xp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, mpad, 64, 128);
   const CUtensorMapSwizzle wsw = int8w ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B;
   const uint32_t brows_box = int8w ? 128 : 256;
-  ok = ok && make_tmap(&h->tm_b_gu, h->wgu, wdt, eb, d, E * 2 * f, 64, brows_box, wsw);
   ok = ok && make_tmap(&h->tm_a_dn, h->hb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, f, mpad, 64, 128);
-  ok = ok && make_tmap(&h->tm_b_dn, h->wd, wdt, eb, f, E * d, 64, brows_box, wsw);
   ok = ok && make_tmap(&h->tm_y, h->y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, mpad, 32, 32);
-  ok = ok && make_tmap(&h->tm_b_dn64, h->wd, wdt, eb, f, E * d, 64, 64, wsw);
-  if (int8w) {
-    ok = ok && make_tmap(&h->tm_w_gu8, h->wgu, wdt, 1, d, E * 2 * f, 128, 128);
-    ok = ok && make_tmap(&h->tm_w_dn8, h->wd, wdt, 1, f, E * d, 128, 128);
+  if (!int4w) {  // the bf16 and shared-memory int8 GEMMs' weight maps
+    ok = ok && make_tmap(&h->tm_b_gu, h->wgu, wdt, eb, d, E * 2 * f, 64, brows_box, wsw);
+    ok = ok && make_tmap(&h->tm_b_dn, h->wd, wdt, eb, f, E * d, 64, brows_box, wsw);
+    ok = ok && make_tmap(&h->tm_b_dn64, h->wd, wdt, eb, f, E * d, 64, 64, wsw);
+  }
+  if (int8w) {  // the tensor-memory int8 / int4 GEMMs: rows of bytes (K or K/2 of them)
+    ok = ok && make_tmap(&h->tm_w_gu8, h->wgu, wdt, 1, d * wbits / 8, E * 2 * f, 128, 128);
+    ok = ok && make_tmap(&h->tm_w_dn8, h->wd, wdt, 1, f * wbits / 8, E * d, 128, 128);
   }
   if (!int8w) {
     ok = ok && make_tmap(&h->tm_b_gu128, h->wgu, wdt, eb, d, E * 2 * f, 64, 128, wsw);

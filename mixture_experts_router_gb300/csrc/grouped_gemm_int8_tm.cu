@@ -1,6 +1,9 @@
 // Grouped expert GEMMs with int8 weights (symmetric per-output-channel int8,
-// "lshu.cn/news/53496" §4.3), dequantised to bf16 inside the kernel, with the
-// converted weights held in TENSOR MEMORY as the MMA's A operand.
+// "lshu.cn/news/53496" §4.3) or int4 weights (4-bit codes with a scale and a
+// zero point per output channel, "m.nxbn.cn/news/47706" §3.2), dequantised to
+// bf16 inside the kernel, with the converted weights held in TENSOR MEMORY as
+// the MMA's A operand.  An int4 row of the tile holds q - z (its zero point
+// taken off during the conversion, exact); the scale is the same as int8's.
 //
 // The GEMM is computed transposed: D[weight row][token] = W[e] * Xp^T, with
 // D in tensor memory (lane = weight row, column = token).  A tile is 128
@@ -52,12 +55,13 @@ namespace {
 constexpr int BM = kTileM;              // tokens per m-tile
 constexpr int BK = 64;                  // K per stage (one 128-byte bf16 row)
 constexpr int WROWS = 128;              // weight rows per tile (TMEM lanes)
-constexpr int WK = 128;                 // K per int8 slot (one 128-byte int8 row)
+constexpr int W_ROW_BYTES = 128;       // bytes per weight row of a slot (one TMA box row):
+                                        // K = 128 int8 or 256 int4 codes
 constexpr int STAGES = 4;
 constexpr int A_BOX = BM * BK * 2;      // 16 KB: one m-tile's 64 K of activations
 constexpr int STAGE_BYTES = 2 * A_BOX;
 constexpr int W_SLOTS = 4;
-constexpr int W_BYTES = WROWS * WK;     // 16 KB int8
+constexpr int W_BYTES = WROWS * W_ROW_BYTES;  // 16 KB
 constexpr int THREADS = 16 * 32;
 constexpr int XFORM_WARP0 = 4;
 constexpr int EPI_WARP0 = 8;
@@ -91,10 +95,11 @@ __device__ __forceinline__ PairCoord decode_pair(int tile, const GemmArgs& p) {
   return c;
 }
 
-template <int KIND>
+template <int KIND, int WBITS>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_int8_tm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                                 const GemmArgs p) {
+  constexpr int KPS = WBITS == 8 ? 2 : 4;  // k-blocks per weight slot
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* s_w = smem + STAGES * STAGE_BYTES;  // int8 weight slots (128-byte swizzled rows)
@@ -169,7 +174,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
         const PairCoord c = decode_pair(tile, p);
         const int w_row = c.e * p.b_rows_per_expert + c.n * WROWS;
-        for (int j = 0; j < p.k_blocks / 2; ++j, ++it) {
+        for (int j = 0; j < p.k_blocks / KPS; ++j, ++it) {
           const int slot = static_cast<int>(it % W_SLOTS);
           if (!mbar_wait(&w_empty[slot], static_cast<uint32_t>(((it / W_SLOTS) & 1) ^ 1), p.wait_limit_ns)) {
             set_error(p.err, kErrTimeout);
@@ -177,7 +182,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             break;
           }
           mbar_arrive_expect_tx(&w_full[slot], W_BYTES);
-          tma_load_2d(s_w + slot * W_BYTES, &tm_w, &w_full[slot], j * WK, w_row);
+          tma_load_2d(s_w + slot * W_BYTES, &tm_w, &w_full[slot], j * W_ROW_BYTES, w_row);
         }
       }
       for (int64_t i = (it > W_SLOTS ? it - W_SLOTS : 0); i < it; ++i)
@@ -223,12 +228,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!mbar_wait(mma_done, 0, p.wait_limit_ns)) set_error(p.err, kErrTimeout);
     }
   } else if (warp >= XFORM_WARP0 && warp < XFORM_WARP0 + 4) {
-    // ------------------------------------------------ int8 -> bf16 transform
+    // ------------------------------------------- int8 / int4 -> bf16 transform
     // Thread (q, lane) owns weight row r = 32q + lane of the tile, i.e. TMEM
-    // lane r.  Per int8 slot (two k-blocks) it reads the row's 128 codes
+    // lane r.  Per weight slot (KPS k-blocks) it reads the row's 128 bytes
     // (16-byte chunk c at r*128 + 16*(c ^ (r & 7)), the TMA 128-byte swizzle);
-    // per k-block it converts 64 of them exactly and stores them into the
-    // stage's weight slot, column 8c + i holding K elements 16c + 2i, 16c + 2i + 1.
+    // per k-block it converts 64 codes exactly and stores them into the
+    // stage's weight slot, column i holding K elements 2i, 2i + 1 of the
+    // k-block (int8: 4 chunks of 16 codes; int4: 2 chunks of 32 codes, minus
+    // the row's zero point).
     const int q = warp & 3;
     const int r = q * 32 + lane;
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
@@ -236,9 +243,22 @@ __global__ void __launch_bounds__(THREADS, 1)
     bool ok = true;
     uint4 v[8];
     for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+      uint32_t zz = 0;  // int4: 0x4300 | zero point, in both bf16 halves
+      if constexpr (WBITS == 4) {
+        const PairCoord c = decode_pair(tile, p);
+        int z;
+        if constexpr (KIND == kGateUpSwiGLU) {
+          // rows of group g: 16 gate rows, then the same 16 features' up rows
+          const int feat = c.n * (WROWS / 2) + (r / 32) * GATEUP_GROUP + (r % GATEUP_GROUP);
+          z = __ldg((r % 32 < GATEUP_GROUP ? p.zero0 : p.zero1) + static_cast<int64_t>(c.e) * p.ld_out + feat);
+        } else {
+          z = __ldg(p.zero0 + static_cast<int64_t>(c.e) * p.ld_out + c.n * WROWS + r);
+        }
+        zz = (0x4300u | static_cast<uint32_t>(z)) * 0x00010001u;
+      }
       for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
         const int stage = static_cast<int>(it % STAGES);
-        if ((kb & 1) == 0) {
+        if ((kb % KPS) == 0) {
           const int slot = static_cast<int>(wi % W_SLOTS);
           if (!mbar_wait(&w_full[slot], static_cast<uint32_t>((wi / W_SLOTS) & 1), p.wait_limit_ns)) {
             set_error(p.err, kErrTimeout);
@@ -259,21 +279,47 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         tc_fence_after();
         uint32_t o[32];
-        if ((kb & 1) == 0) {
+        if constexpr (WBITS == 8) {
+          if ((kb & 1) == 0) {
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            int8x4_to_bf16x4(v[cc].x, o[8 * cc + 0], o[8 * cc + 1]);
-            int8x4_to_bf16x4(v[cc].y, o[8 * cc + 2], o[8 * cc + 3]);
-            int8x4_to_bf16x4(v[cc].z, o[8 * cc + 4], o[8 * cc + 5]);
-            int8x4_to_bf16x4(v[cc].w, o[8 * cc + 6], o[8 * cc + 7]);
+            for (int cc = 0; cc < 4; ++cc) {
+              int8x4_to_bf16x4(v[cc].x, o[8 * cc + 0], o[8 * cc + 1]);
+              int8x4_to_bf16x4(v[cc].y, o[8 * cc + 2], o[8 * cc + 3]);
+              int8x4_to_bf16x4(v[cc].z, o[8 * cc + 4], o[8 * cc + 5]);
+              int8x4_to_bf16x4(v[cc].w, o[8 * cc + 6], o[8 * cc + 7]);
+            }
+          } else {
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+              int8x4_to_bf16x4(v[4 + cc].x, o[8 * cc + 0], o[8 * cc + 1]);
+              int8x4_to_bf16x4(v[4 + cc].y, o[8 * cc + 2], o[8 * cc + 3]);
+              int8x4_to_bf16x4(v[4 + cc].z, o[8 * cc + 4], o[8 * cc + 5]);
+              int8x4_to_bf16x4(v[4 + cc].w, o[8 * cc + 6], o[8 * cc + 7]);
+            }
           }
         } else {
+          // chunks 2 (kb % 4) and 2 (kb % 4) + 1: 64 codes, 32 columns
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            int8x4_to_bf16x4(v[4 + cc].x, o[8 * cc + 0], o[8 * cc + 1]);
-            int8x4_to_bf16x4(v[4 + cc].y, o[8 * cc + 2], o[8 * cc + 3]);
-            int8x4_to_bf16x4(v[4 + cc].z, o[8 * cc + 4], o[8 * cc + 5]);
-            int8x4_to_bf16x4(v[4 + cc].w, o[8 * cc + 6], o[8 * cc + 7]);
+          for (int part = 0; part < 4; ++part) {
+            if (part == (kb & 3)) {
+#pragma unroll
+              for (int cc = 0; cc < 2; ++cc) {
+                const uint4 w = v[2 * part + cc];
+                uint32_t t[4];
+                int4x8_minus_zero_to_bf16(w.x, zz, t);
+#pragma unroll
+                for (int m = 0; m < 4; ++m) o[16 * cc + m] = t[m];
+                int4x8_minus_zero_to_bf16(w.y, zz, t);
+#pragma unroll
+                for (int m = 0; m < 4; ++m) o[16 * cc + 4 + m] = t[m];
+                int4x8_minus_zero_to_bf16(w.z, zz, t);
+#pragma unroll
+                for (int m = 0; m < 4; ++m) o[16 * cc + 8 + m] = t[m];
+                int4x8_minus_zero_to_bf16(w.w, zz, t);
+#pragma unroll
+                for (int m = 0; m < 4; ++m) o[16 * cc + 12 + m] = t[m];
+              }
+            }
           }
         }
         tmem_store32(lane_addr + A_COL0 + static_cast<uint32_t>(stage) * SLOT_COLS, o);
@@ -375,20 +421,31 @@ int grouped_gemm_int8_tm_tile_n(GemmKind kind) { return kind == kGateUpSwiGLU ? 
 int grouped_gemm_int8_tm_gateup_block() { return GATEUP_GROUP; }
 
 cudaError_t grouped_gemm_int8_tm_prepare() {
-  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_int8_tm_kernel<kGateUpSwiGLU>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(grouped_gemm_int8_tm_kernel<kDownF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              SMEM_BYTES);
+  cudaError_t e = cudaSuccess;
+  auto set = [&](auto fn) {
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  };
+  set(grouped_gemm_int8_tm_kernel<kGateUpSwiGLU, 8>);
+  set(grouped_gemm_int8_tm_kernel<kDownF32, 8>);
+  set(grouped_gemm_int8_tm_kernel<kGateUpSwiGLU, 4>);
+  set(grouped_gemm_int8_tm_kernel<kDownF32, 4>);
+  return e;
 }
 
-cudaError_t launch_grouped_gemm_int8_tm(GemmKind kind, const CUtensorMap& tm_x, const CUtensorMap& tm_w,
+cudaError_t launch_grouped_gemm_int8_tm(GemmKind kind, int wbits, const CUtensorMap& tm_x, const CUtensorMap& tm_w,
                                         const GemmArgs& a, cudaStream_t s) {
-  if (a.k_blocks % 2 != 0) return cudaErrorInvalidValue;
-  if (kind == kGateUpSwiGLU)
-    launch_kernel(grouped_gemm_int8_tm_kernel<kGateUpSwiGLU>, a.grid, THREADS, SMEM_BYTES, s, tm_x, tm_w, a);
-  else
-    launch_kernel(grouped_gemm_int8_tm_kernel<kDownF32>, a.grid, THREADS, SMEM_BYTES, s, tm_x, tm_w, a);
+  if (a.k_blocks % (wbits == 8 ? 2 : 4) != 0 || (wbits != 8 && wbits != 4)) return cudaErrorInvalidValue;
+  if (wbits == 8) {
+    if (kind == kGateUpSwiGLU)
+      launch_kernel(grouped_gemm_int8_tm_kernel<kGateUpSwiGLU, 8>, a.grid, THREADS, SMEM_BYTES, s, tm_x, tm_w, a);
+    else
+      launch_kernel(grouped_gemm_int8_tm_kernel<kDownF32, 8>, a.grid, THREADS, SMEM_BYTES, s, tm_x, tm_w, a);
+  } else {
+    if (kind == kGateUpSwiGLU)
+      launch_kernel(grouped_gemm_int8_tm_kernel<kGateUpSwiGLU, 4>, a.grid, THREADS, SMEM_BYTES, s, tm_x, tm_w, a);
+    else
+      launch_kernel(grouped_gemm_int8_tm_kernel<kDownF32, 4>, a.grid, THREADS, SMEM_BYTES, s, tm_x, tm_w, a);
+  }
   return cudaGetLastError();
 }
 

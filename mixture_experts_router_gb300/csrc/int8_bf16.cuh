@@ -32,4 +32,22 @@ __device__ __forceinline__ void convert_chunk16(const uint8_t* src, uint8_t* til
   *reinterpret_cast<uint4*>(row + 16 * ((2 * c + 1) ^ (r & 7))) = o1;
 }
 
+// Eight packed 4-bit codes (one 32-bit word; byte m holds element 2m in its
+// low nibble and 2m + 1 in its high nibble) minus a zero point z -> four
+// bf16x2 words o[m] = {q_2m - z, q_2m+1 - z}, exactly.  Each nibble n sits in
+// the low byte of the bf16 word 0x4300|n = 128 + n; subtracting the word
+// 0x4300|z = 128 + z (zz holds it in both halves) leaves n - z, an integer
+// of magnitude <= 15.
+__device__ __forceinline__ void int4x8_minus_zero_to_bf16(uint32_t w, uint32_t zz, uint32_t (&o)[4]) {
+  const uint32_t lo = w & 0x0F0F0F0Fu, hi = (w >> 4) & 0x0F0F0F0Fu;
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    // bytes {lo_m, -, hi_m, -}, then 0x43 into the high byte of each half
+    const uint32_t t = __byte_perm(lo, hi, static_cast<uint32_t>(m | ((4 + m) << 8)));
+    uint32_t v;
+    asm("lop3.b32 %0, %1, 0x00FF00FF, 0x43004300, 0xEA;" : "=r"(v) : "r"(t));
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(o[m]) : "r"(v), "r"(zz));
+  }
+}
+
 }  // namespace cbmoe

@@ -183,8 +183,10 @@ struct GemmArgs {
   int32_t b_rows_per_expert;    // rows of the B operand per expert
   void* out;                    // H bf16 or Y fp32
   int64_t ld_out;               // elements per output row
-  const float* scale0;          // int8: gate (or down) per-channel scales
-  const float* scale1;          // int8: up scales
+  const float* scale0;          // int8 / int4: gate (or down) per-channel scales
+  const float* scale1;          // int8 / int4: up scales
+  const uint8_t* zero0;         // int4: gate (or down) per-channel zero points
+  const uint8_t* zero1;         // int4: up zero points
   int* err;
   uint64_t wait_limit_ns;
   int32_t grid;                 // persistent CTAs
@@ -222,7 +224,8 @@ int grouped_gemm_int8_gateup_block();  // gate/up rows interleaved in blocks of 
 // int8 weights converted into tensor memory (the MMA's A operand): tiles are
 // 128 weight rows against a pair of m-tiles; tm_x: the activations (128 x 64
 // boxes), tm_w: the int8 weights with a 128 x 128 box and the 128-byte swizzle
-cudaError_t launch_grouped_gemm_int8_tm(GemmKind kind, const CUtensorMap& tm_x, const CUtensorMap& tm_w,
+// (wbits 8: int8 codes; 4: packed int4 codes with zero points, slots of K = 256)
+cudaError_t launch_grouped_gemm_int8_tm(GemmKind kind, int wbits, const CUtensorMap& tm_x, const CUtensorMap& tm_w,
                                         const GemmArgs& a, cudaStream_t s);
 cudaError_t grouped_gemm_int8_tm_prepare();
 int grouped_gemm_int8_tm_tile_n(GemmKind kind);

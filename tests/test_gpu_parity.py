@@ -24,6 +24,10 @@ SMALL = {
     "int8_k6": synth.custom_shape("int8_k6", T=700, d=256, f=512, E=64, k=6, wdtype="int8", seed=28),
     # int8 experts of about five m-tiles each: full and half-empty m-tile pairs
     "int8_pairs": synth.custom_shape("int8_pairs", T=1100, d=512, f=768, E=4, k=2, wdtype="int8", seed=29),
+    # int4 experts (scale and zero point per channel): one-m-tile experts, pairs, many experts
+    "int4_mid": synth.custom_shape("int4_mid", T=300, d=512, f=768, E=8, k=2, wdtype="int4", seed=30),
+    "int4_pairs": synth.custom_shape("int4_pairs", T=1100, d=512, f=768, E=4, k=2, wdtype="int4", seed=31),
+    "int4_k6": synth.custom_shape("int4_k6", T=700, d=256, f=512, E=64, k=6, wdtype="int4", seed=32),
 }
 
 FULL = {  # workload: tokens sampled for the output check
@@ -31,6 +35,7 @@ FULL = {  # workload: tokens sampled for the output check
     "skewed": 64,
     "mixtral_prefill": 24,
     "int8": 48,
+    "int4": 48,
 }
 
 
@@ -145,7 +150,7 @@ def test_both_routers(name, router, monkeypatch):
     assert rep.get("logit_max_err", 0.0) <= 5e-6
 
 
-@pytest.mark.parametrize("wdtype", ["bf16", "int8"])
+@pytest.mark.parametrize("wdtype", ["bf16", "int8", "int4"])
 def test_device_wait_timeout_is_reported_and_context_survives(wdtype):
     """A bounded device wait that nothing satisfies (CB_FLAG_TEST_STALL) ends the
     kernel with CB_ERR_TIMEOUT in the status word instead of a hang or a fault;
