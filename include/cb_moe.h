@@ -19,8 +19,10 @@
  *
  * int8 experts: W[e][j][i] = s[e][j] * Q[e][j][i] with one fp32 scale per
  * output channel (symmetric per-channel int8, "lshu.cn/news/53496" §4.3);
- * the codes become bf16 exactly inside the GEMM and the scale multiplies the
- * fp32 accumulator.
+ * int4 experts: W[e][j][i] = s[e][j] * (q[e][j][i] - z[e][j]) with a scale
+ * and an integer zero point per output channel ("m.nxbn.cn/news/47706"
+ * §3.2).  The codes (minus the zero point) become bf16 exactly inside the
+ * GEMM and the scale multiplies the fp32 accumulator.
  *
  * Conventions for every call below:
  *  - bf16 means IEEE bfloat16 stored as 16-bit words; all matrices are
