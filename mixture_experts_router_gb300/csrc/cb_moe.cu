@@ -64,6 +64,7 @@ struct cb_moe {
   bool gather_a;           // gate/up GEMM gathers its rows from x (no Xp copy)
   bool int8_tm;            // int8 GEMMs convert their weights into tensor memory
   bool use_pdl;            // programmatic dependent launch between the forward's kernels
+  bool fused_combine;      // the CTA-pair down GEMM adds its rows into the token sums
   const void* tm_x_src;    // x pointer tm_x was encoded for
   const void* tm_xg_src;   // x pointer tm_xg was encoded for
   CUtensorMap tm_a_gu, tm_b_gu, tm_a_dn, tm_b_dn, tm_b_dn64, tm_b_gu128, tm_b_dn128, tm_y, tm_x, tm_xg, tm_wr,
@@ -222,6 +223,11 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
     return !h->timing || cudaEventRecordWithFlags(h->ev[i], s, ev_flags) == cudaSuccess;
   };
   if (!mark(0)) return CB_ERR_CUDA;
+  const bool fuse = h->fused_combine && h->pair_dn && c.wdtype == CB_W_BF16;
+  const uint64_t td = static_cast<uint64_t>(c.n_tokens) * c.d_model;
+  // the fused combine's token sums (in the Y buffer, which it does not use)
+  // start from zero
+  if (fuse && cudaMemsetAsync(h->y, 0, td * 4, s) != cudaSuccess) return CB_ERR_CUDA;
 
   RouterArgs ra{};
   ra.x = static_cast<const uint16_t*>(x);
@@ -367,12 +373,27 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
   } else if (pair_dn) {
     GemmArgs gp = gd;
     gp.grid = h->pair_grid_dn;
+    if (fuse) {
+      gp.comb_acc = h->y;
+      gp.comb_ids = h->ids;
+      gp.comb_w = h->w;
+      gp.top_k = c.top_k;
+      gp.tok = h->tok;
+      gp.offsets = h->offsets;
+      gp.counts = h->counts;
+    }
     e2 = launch_grouped_gemm_pair(kDownF32, h->tm_a_dn, h->tm_b_dn128, h->tm_y, gp, s);
   } else {
     e2 = launch_grouped_gemm(kDownF32, false, h->tm_a_dn, h->tm_b_dn, h->tm_y, h->tm_b_dn64, gd, s);
   }
   if (e2 != cudaSuccess || !mark(4)) return CB_ERR_CUDA;
 
+  if (fuse) {
+    if (launch_combine_acc(h->y, static_cast<int64_t>(td), out, f32out ? 1 : 0, h->num_sms * 8, s) != cudaSuccess ||
+        !mark(5))
+      return CB_ERR_CUDA;
+    return CB_OK;
+  }
   CombineArgs ca{};
   ca.y = h->y;
   ca.w = h->w;
@@ -654,6 +675,15 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
       ok = ok && grouped_gemm_pair_prepare(h->num_sms, &h->pair_grid_gu, &h->pair_grid_dn) == cudaSuccess;
       if (h->pair_grid_gu < 2 || h->pair_grid_dn < 2) h->pair_gu = h->pair_dn = false;
     }
+    // the combine fused into the CTA-pair down GEMM with CB_MOE_FUSED_COMBINE=1
+    // (bf16 weights, layers that run the pair down kernel): each routed row
+    // adds w * Y-row into its token's fp32 sum by vector reductions, and one
+    // pass rounds the sums to the output; Y is neither stored nor re-read.
+    // Measured on GB300 it does not pay: the reductions slow the down GEMM
+    // more than the combine pass costs (128-expert layer 0.377 vs 0.348 ms,
+    // Mixtral prefill 1.900 vs 1.875 ms); off by default.
+    const char* fcv = std::getenv("CB_MOE_FUSED_COMBINE");
+    h->fused_combine = h->pair_dn && fcv != nullptr && std::strcmp(fcv, "1") == 0;
     // programmatic dependent launch between the forward's kernels with
     // CB_MOE_PDL=1.  Measured on GB300 it does not pay: decode layer -0.4 %,
     // 128-expert layer +1.7 % (the next kernel's early CTAs wait beside the

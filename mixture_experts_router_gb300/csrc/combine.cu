@@ -69,7 +69,47 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(CombineArgs a) {
   }
 }
 
+// The combine fused into the down GEMM leaves each token's fp32 sum in acc;
+// this pass rounds it once to bf16 (or copies it out as fp32).
+template <bool F32OUT>
+__global__ void __launch_bounds__(kThreads) combine_acc_kernel(const float* __restrict__ acc, int64_t n8, void* out) {
+  grid_dep_wait();
+  grid_dep_launch();
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+  for (int64_t v = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; v < n8; v += stride) {
+    const float4 p = __ldg(reinterpret_cast<const float4*>(acc) + 2 * v);
+    const float4 q = __ldg(reinterpret_cast<const float4*>(acc) + 2 * v + 1);
+    if constexpr (F32OUT) {
+      reinterpret_cast<float4*>(out)[2 * v] = p;
+      reinterpret_cast<float4*>(out)[2 * v + 1] = q;
+    } else {
+      __nv_bfloat162 b0 = __floats2bfloat162_rn(p.x, p.y);
+      __nv_bfloat162 b1 = __floats2bfloat162_rn(p.z, p.w);
+      __nv_bfloat162 b2 = __floats2bfloat162_rn(q.x, q.y);
+      __nv_bfloat162 b3 = __floats2bfloat162_rn(q.z, q.w);
+      uint4 o;
+      o.x = *reinterpret_cast<uint32_t*>(&b0);
+      o.y = *reinterpret_cast<uint32_t*>(&b1);
+      o.z = *reinterpret_cast<uint32_t*>(&b2);
+      o.w = *reinterpret_cast<uint32_t*>(&b3);
+      reinterpret_cast<uint4*>(out)[v] = o;
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_combine_acc(const float* acc, int64_t n_elems, void* out, int out_f32, int grid, cudaStream_t s) {
+  const int64_t n8 = n_elems / 8;
+  if (n8 <= 0) return cudaSuccess;
+  const int64_t need = (n8 + kThreads - 1) / kThreads;
+  const int g = static_cast<int>(need < grid ? need : grid);
+  if (out_f32)
+    launch_kernel(combine_acc_kernel<true>, g, kThreads, 0, s, acc, n8, out);
+  else
+    launch_kernel(combine_acc_kernel<false>, g, kThreads, 0, s, acc, n8, out);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s) {
   if (a.T <= 0) return cudaSuccess;

@@ -2,7 +2,10 @@
 //
 // Same math and epilogues as grouped_gemm.cu (gate/up with SwiGLU into bf16
 // H, down into fp32 Y with bulk tensor stores), run by clusters of two CTAs
-// on two SMs.  The pair computes the two m-tiles (2p, 2p+1) of one expert
+// on two SMs.  The down kernel can instead fuse the combine: each row's
+// output, times its gate weight, is added into its token's fp32 row by
+// vector reductions (the order of a token's k additions then varies from run
+// to run, which changes no result for k <= 2: 0 + a + b = 0 + b + a).  The pair computes the two m-tiles (2p, 2p+1) of one expert
 // against one 256-row weight tile with tcgen05.mma.cta_group::2 (M = 256,
 // N = 256, K = 16), issued by one thread of the even CTA:
 //
@@ -239,6 +242,33 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint4* dst = reinterpret_cast<uint4*>(out_row + c0);
 #pragma unroll
             for (int j = 0; j < 4; ++j) dst[j] = make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
+          }
+        } else if (p.comb_acc != nullptr) {
+          // combine fused: the lane's row adds its gate-weighted output into
+          // its token's accumulator row (fp32 reductions performed in L2);
+          // padding rows past the expert's count add nothing
+          const int local = (t.m_tile - p.mtile_off[t.e]) * BM + q * 32 + lane;
+          const bool live = local < p.counts[t.e];
+          float wt = 0.f;
+          float* dst = p.comb_acc;
+          if (live) {
+            const int tk = p.tok[p.offsets[t.e] + local];
+            const int64_t pr = static_cast<int64_t>(tk) * p.top_k;
+            int sl = 0;
+            while (sl + 1 < p.top_k && p.comb_ids[pr + sl] != t.e) ++sl;
+            wt = p.comb_w[pr + sl];
+            dst += static_cast<int64_t>(tk) * p.ld_out + t.n * BN;
+          }
+#pragma unroll 1
+          for (int c0 = 0; c0 < BN; c0 += 32) {
+            uint32_t r[32];
+            tmem_load32(tbase + c0, r);
+            if (live) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                red_add_f32x4(dst + c0 + 4 * j, wt * __uint_as_float(r[4 * j]), wt * __uint_as_float(r[4 * j + 1]),
+                              wt * __uint_as_float(r[4 * j + 2]), wt * __uint_as_float(r[4 * j + 3]));
+            }
           }
         } else {
           const int row0 = t.m_tile * BM + q * 32;

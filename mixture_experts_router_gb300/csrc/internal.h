@@ -170,6 +170,9 @@ struct CombineArgs {
   int out_f32;
 };
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s);
+// out[t] = round(acc[t]) for the down GEMM's fused combine: acc fp32 [T][d]
+// -> out bf16 (or fp32 when out_f32) [T][d]
+cudaError_t launch_combine_acc(const float* acc, int64_t n_elems, void* out, int out_f32, int grid, cudaStream_t s);
 
 // ------------------------------------------------------------ grouped GEMM
 struct GemmArgs {
@@ -197,6 +200,15 @@ struct GemmArgs {
   const int32_t* tok;
   const int32_t* offsets;
   const int32_t* counts;
+  // down on CTA pairs with the combine fused into its epilogue (comb_acc
+  // non-null; tok, offsets and counts set): row `local` of expert e, for
+  // local < counts[e], is token t = tok[offsets[e] + local] at the slot s with
+  // comb_ids[t k + s] = e; the epilogue adds comb_w[t k + s] * Y-row into
+  // comb_acc[t] (fp32 [T][ld_out], zero beforehand) instead of storing Y
+  float* comb_acc;
+  const int32_t* comb_ids;
+  const float* comb_w;
+  int32_t top_k;
 };
 enum GemmKind { kGateUpSwiGLU = 0, kDownF32 = 1 };
 // tm_out: the fp32 output Y [rows][d] with a 32 x 32 box and the 128-byte

@@ -125,6 +125,12 @@ __device__ __forceinline__ void bulk_wait_group() {
   asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Four fp32 additions into 16 bytes of global memory, performed in L2
+// (a relaxed reduction: no value comes back).
+__device__ __forceinline__ void red_add_f32x4(float* p, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+}
+
 // Make this thread's generic-proxy shared-memory writes visible to later
 // async-proxy reads (tensor core operands, TMA stores).
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -265,6 +265,46 @@ def test_pair_mma_path_timeout(monkeypatch):
     assert rep["f32_max_abs"] <= gh.MAX_ABS
 
 
+@pytest.mark.parametrize("name", PAIR_SMALL)
+def test_fused_combine_small(name, monkeypatch):
+    """CB_MOE_FUSED_COMBINE=1 (CTA-pair down GEMM forced on): the down
+    epilogue adds each row's gate-weighted output into its token's fp32 sum
+    and one pass rounds the sums; the same bounds against the oracle."""
+    monkeypatch.setenv("CB_MOE_PAIR", "1")
+    monkeypatch.setenv("CB_MOE_FUSED_COMBINE", "1")
+    rep = gh.full_check(synth.make_layer(SMALL[name]))
+    print(name, "fused combine", rep)
+
+
+@pytest.mark.parametrize("name", ["mixtral_prefill", "skewed"])
+def test_fused_combine_full_size(name, monkeypatch):
+    monkeypatch.setenv("CB_MOE_FUSED_COMBINE", "1")
+    rep = gh.full_check(synth.make_layer(synth.WORKLOADS[name]), sample=FULL[name])
+    print(name, "fused combine", rep)
+
+
+def test_fused_combine_repeatable_at_k2(monkeypatch):
+    """With k = 2 each token sum is 0 + a + b in either order, so repeated
+    forwards (device and host buffers) agree bit for bit."""
+    monkeypatch.setenv("CB_MOE_PAIR", "1")
+    monkeypatch.setenv("CB_MOE_FUSED_COMBINE", "1")
+    layer = synth.make_layer(SMALL["ragged_mid"])
+    gl = gh.GpuLayer(layer)
+    try:
+        gl.run(f32=False)
+        a = gl.out.clone()
+        for _ in range(3):
+            gl.run(f32=False)
+            assert torch.equal(a.view(torch.int16), gl.out.view(torch.int16))
+        xh = torch.from_numpy(layer.x.view(np.int16)).pin_memory()
+        oh = torch.empty_like(xh).pin_memory()
+        gl.m.forward_host(xh, oh)
+        torch.cuda.synchronize()
+        assert torch.equal(oh, a.view(torch.int16).cpu())
+    finally:
+        gl.close()
+
+
 @pytest.mark.parametrize("name", ["tiny", "ragged_mid", "odd_T", "int8_mid", "skewed_small", "e256_k16", "int8_k6"])
 def test_dispatch_own_ranking_small(name, monkeypatch):
     """CB_MOE_FUSED_RANKS=0: the dispatch ranks the routed pairs itself
