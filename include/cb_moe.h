@@ -109,6 +109,14 @@ typedef enum { CB_ROUTER_SOFTMAX_TOPK = 0, CB_ROUTER_RAW_LOGITS = 1, CB_ROUTER_H
                                       forward finishes (its output is garbage)
                                       and cb_moe_last_error returns
                                       CB_ERR_TIMEOUT                            */
+#define CB_FLAG_TEST_STALL_DISPATCH 0x8u /* test only: the cooperative dispatch's
+                                      grid barrier waits for one block more
+                                      than the launch has, bounded to 1 ms:
+                                      every block gives up and returns, the
+                                      routing tables keep their previous
+                                      values (zeros after init), the output is
+                                      garbage and cb_moe_last_error returns
+                                      CB_ERR_TIMEOUT                            */
 
 typedef struct {
   int32_t n_tokens;   /* T: tokens in every forward on this handle (>= 0)         */

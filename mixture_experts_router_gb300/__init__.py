@@ -19,6 +19,7 @@ CB_W_BF16, CB_W_INT8, CB_W_INT4 = 0, 1, 2
 CB_FLAG_KEEP_LOGITS = 0x1
 CB_FLAG_STAGE_TIMING = 0x2
 CB_FLAG_TEST_STALL = 0x4
+CB_FLAG_TEST_STALL_DISPATCH = 0x8
 CB_N_STAGES = 5
 STAGE_NAMES = ("router", "dispatch", "gateup_gemm", "down_gemm", "combine")
 

@@ -20,6 +20,9 @@
 //                      into per-block row bases, totals, offsets and tiles
 //   dispatch_copy    : each token's row of x into its k rows of Xp (and,
 //                      after dispatch_scan_blocks, the global ranks: inv, tok)
+//   dispatch_coop    : count, scan, ranks and row copy in one cooperative
+//                      launch with one grid barrier (the default for the
+//                      dispatch's own ranking)
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -377,6 +380,221 @@ __global__ void __launch_bounds__(kThreads) dispatch_copy(DispatchArgs a) {
   }
 }
 
+// The steps above in one cooperative launch of G co-resident blocks (the
+// launch guarantees that all of them run at once, so each block's one wait
+// at the grid barrier ends; the wait is bounded all the same).  Block b owns
+// the tokens [b tpb, (b + 1) tpb) and with them the flat pairs
+// [b tpb k, (b + 1) tpb k):
+//   1. per-warp counts per expert of its pairs (warp w: a contiguous run,
+//      as in dispatch_small), their sum to chunk[b][e]
+//   2. the grid barrier
+//   3. every block sums the G rows of counts itself: per-expert totals and
+//      its own base sum_{b' < b} chunk[b'][e]; the expert prefix and the tile
+//      maps follow (block 0 publishes them)
+//   4. ranks of its pairs in flat (token, slot) order -> tok, inv
+//   5. its tokens' rows of x into their k padded rows of Xp
+constexpr int kCoopThreads = 1024;
+constexpr int kCoopWarps = kCoopThreads / 32;
+
+__device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* p) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__global__ void __launch_bounds__(kCoopThreads) dispatch_coop(DispatchArgs a) {
+  grid_dep_wait();    // what earlier kernels in the stream wrote is visible from here
+  grid_dep_launch();
+  __shared__ int wh[kCoopWarps][256];
+  __shared__ int part_pre[kCoopThreads], part_tot[kCoopThreads];
+  __shared__ int s_off[256], s_moff[256];
+  __shared__ int tmp[kCoopWarps];
+  __shared__ int s_ok;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int G = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x), E = a.E, k = a.k;
+  const int64_t M = static_cast<int64_t>(a.T) * k;
+  const int tpb = (a.T + G - 1) / G;
+  const int t0 = static_cast<int>(min(static_cast<int64_t>(a.T), static_cast<int64_t>(b) * tpb));
+  const int t1 = min(a.T, t0 + tpb);
+  const int64_t p0 = static_cast<int64_t>(t0) * k, p1 = static_cast<int64_t>(t1) * k;
+  const int64_t per_warp = ((p1 - p0 + kCoopWarps - 1) / kCoopWarps + 31) / 32 * 32;
+  const int64_t wbase = p0 + warp * per_warp;
+  const int64_t wend = min(p1, wbase + per_warp);
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  for (int i = threadIdx.x; i < kCoopWarps * 256; i += kCoopThreads) (&wh[0][0])[i] = 0;
+  __syncthreads();
+
+  // 1. counts (the loop bound is the same for every lane of the warp)
+  for (int64_t q = wbase; q < wend; q += 32) {
+    const int64_t p = q + lane;
+    int e = p < wend ? a.ids[p] : -1;
+    if (p < wend && (e < 0 || e >= E)) set_error(a.err, kErrDevice);
+    if (e < 0 || e >= E) e = -1;
+    const uint32_t m = __match_any_sync(0xffffffffu, e);
+    if (e >= 0 && (__ffs(m) - 1) == lane) wh[warp][e] += __popc(m);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += kCoopThreads) {
+    int c = 0;
+    for (int w = 0; w < kCoopWarps; ++w) c += wh[w][e];
+    a.chunk[static_cast<int64_t>(b) * E + e] = c;
+  }
+
+  // 2. grid barrier: the block's count stores, then its arrival
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(a.bar, 1u);
+    const uint64_t start = globaltimer_ns();
+    int ok = 1;
+    while (ld_acquire_gpu(a.bar) < static_cast<unsigned int>(G + a.test_stall)) {
+      if (globaltimer_ns() - start > a.wait_limit_ns) {
+        set_error(a.err, kErrTimeout);
+        ok = 0;
+        break;
+      }
+      __nanosleep(64);
+    }
+    __threadfence();
+    s_ok = ok;
+  }
+  __syncthreads();
+  if (!s_ok) return;
+
+  // 3. column sums: thread i < P E sums expert i % E over the block rows of
+  // part i / E (P = kCoopThreads / E >= 2 parts)
+  const int P = kCoopThreads / E;
+  if (static_cast<int>(threadIdx.x) < P * E) {
+    const int e = threadIdx.x % E, q = threadIdx.x / E;
+    const int lo = q * G / P, hi = (q + 1) * G / P;
+    int pre = 0, tot = 0;
+#pragma unroll 8
+    for (int r = lo; r < hi; ++r) {
+      const int c = __ldcg(a.chunk + static_cast<int64_t>(r) * E + e);
+      tot += c;
+      pre += r < b ? c : 0;
+    }
+    part_pre[threadIdx.x] = pre;
+    part_tot[threadIdx.x] = tot;
+  }
+  __syncthreads();
+  const int e = threadIdx.x;
+  int total = 0, pre = 0;
+  if (e < E)
+    for (int q = 0; q < P; ++q) {
+      total += part_tot[q * E + e];
+      pre += part_pre[q * E + e];
+    }
+  const int mt = (total + kTileM - 1) / kTileM;
+  const int pt = (mt + 1) / 2;
+  const int off = block_exclusive_scan<kCoopWarps>(e < E ? total : 0, tmp);
+  const int moff = block_exclusive_scan<kCoopWarps>(e < E ? mt : 0, tmp);
+  const int poff = block_exclusive_scan<kCoopWarps>(e < E ? pt : 0, tmp);
+  if (e < E) {
+    s_off[e] = off;
+    s_moff[e] = moff;
+    if (b == 0) {
+      a.counts[e] = total;
+      a.offsets[e] = off;
+      a.mtile_off[e] = moff;
+      if (e == E - 1) {
+        a.offsets[E] = off + total;
+        a.mtile_off[E] = moff + mt;
+        if (moff + mt > a.max_mtiles) set_error(a.err, kErrDevice);
+      }
+      for (int i = moff; i < moff + mt && i < a.max_mtiles; ++i) a.mtile_expert[i] = e;
+      if (a.ptile_off != nullptr) {
+        a.ptile_off[e] = poff;
+        if (e == E - 1) a.ptile_off[E] = poff + pt;
+        for (int i = poff; i < poff + pt && i < a.max_mtiles; ++i) a.ptile_expert[i] = e;
+      }
+    }
+    int base = off + pre;  // this block's first row of expert e, then each warp's
+    for (int w = 0; w < kCoopWarps; ++w) {
+      const int c = wh[w][e];
+      wh[w][e] = base;
+      base += c;
+    }
+  }
+  __syncthreads();
+
+  // 4. ranks
+  for (int64_t q = wbase; q < wend; q += 32) {
+    const int64_t p = q + lane;
+    int e2 = p < wend ? a.ids[p] : -1;
+    if (e2 < 0 || e2 >= E) e2 = -1;
+    const uint32_t m = __match_any_sync(0xffffffffu, e2);
+    int rank = 0;
+    if (e2 >= 0) rank = wh[warp][e2] + __popc(m & lt_mask);
+    __syncwarp();
+    if (e2 >= 0 && (__ffs(m) - 1) == lane) wh[warp][e2] += __popc(m);
+    __syncwarp();
+    if (e2 >= 0) {
+      if (rank < 0 || rank >= M) {
+        set_error(a.err, kErrDevice);
+      } else {
+        a.tok[rank] = static_cast<int32_t>(p / k);
+        a.inv[p] = rank;
+      }
+    }
+  }
+  if (!a.copy_rows) return;
+  __syncthreads();  // this block's inv stores are visible to all its threads
+
+  // 5. row copy: items of 128 16-byte vectors of one token's row, dealt to
+  // the block's warps in turn (a whole row per warp would leave the block's
+  // last warps idle: 54 tokens over 16 warps on the 128-expert layer); each
+  // warp moves two items per round, eight 16-byte loads in flight per lane
+  constexpr int kSegVec = 128;
+  const int vec_per_row = a.d / 8;
+  const int segs = (vec_per_row + kSegVec - 1) / kSegVec;
+  const int n_items = (t1 - t0) * segs;
+  const int64_t rows = static_cast<int64_t>(a.max_mtiles) * kTileM;
+  for (int it = warp; it < n_items; it += 2 * kCoopWarps) {
+    uint4 buf[2][kSegVec / 32];
+    int64_t dst_row[2] = {-1, -1};
+    int v_base[2] = {0, 0};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int item = it + h * kCoopWarps;
+      if (item >= n_items) continue;  // the same for the whole warp
+      const int t = t0 + item / segs;
+      v_base[h] = (item % segs) * kSegVec;
+      if (lane < k) {
+        const int64_t p = static_cast<int64_t>(t) * k + lane;
+        const int ee = a.ids[p];
+        if (ee >= 0 && ee < E) {
+          dst_row[h] = static_cast<int64_t>(s_moff[ee]) * kTileM + (a.inv[p] - s_off[ee]);
+          if (dst_row[h] < 0 || dst_row[h] >= rows) {
+            set_error(a.err, kErrDevice);
+            dst_row[h] = -1;
+          }
+        }
+      }
+      const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<int64_t>(t) * a.d);
+#pragma unroll
+      for (int u = 0; u < kSegVec / 32; ++u) {
+        const int v = v_base[h] + u * 32 + lane;
+        if (v < vec_per_row) buf[h][u] = __ldg(src + v);
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      if (it + h * kCoopWarps >= n_items) continue;
+      for (int s = 0; s < k; ++s) {
+        const int64_t row = __shfl_sync(0xffffffffu, dst_row[h], s);
+        if (row < 0) continue;
+        uint4* dst = reinterpret_cast<uint4*>(a.xp + row * a.d);
+#pragma unroll
+        for (int u = 0; u < kSegVec / 32; ++u) {
+          const int v = v_base[h] + u * 32 + lane;
+          if (v < vec_per_row) dst[v] = buf[h][u];
+        }
+      }
+    }
+  }
+}
+
 }  // namespace
 
 // The per-chunk counts of dispatch_count have the layout of the router's
@@ -408,8 +626,32 @@ cudaError_t dispatch_prepare() {
                               kFusedScanWords * 4);
 }
 
+int dispatch_coop_max_blocks(int num_sms) {
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_coop, kCoopThreads, 0) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return per_sm > 0 ? num_sms : 0;
+}
+
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s) {
   if (a.n_chunks <= 0) return cudaSuccess;
+  if (a.rank_block <= 0 && a.coop_blocks > 0) {
+    if (a.E > 256 || a.bar == nullptr) return cudaErrorInvalidValue;
+    cudaError_t e = cudaMemsetAsync(a.bar, 0, sizeof(unsigned int), s);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.coop_blocks, 1, 1);
+    cfg.blockDim = dim3(kCoopThreads, 1, 1);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, dispatch_coop, a);
+  }
   if (a.rank_block > 0) {
     const int words = (a.n_rank_blocks + 1) * (a.E + 1);
     if (words > kFusedScanWords || a.E > 256) return cudaErrorInvalidValue;

@@ -147,12 +147,24 @@ struct DispatchArgs {
   // row-copy kernel turns the ranks into global ones
   int32_t rank_block;     // tokens per rank block
   int32_t n_rank_blocks;
+  // > 0: the dispatch's own ranking and the row copy run as one cooperative
+  // launch of this many blocks (chunk then holds [coop_blocks][E] counts),
+  // meeting once at a grid barrier on *bar (zeroed by the launcher)
+  int32_t coop_blocks;
+  unsigned int* bar;
+  uint64_t wait_limit_ns;
+  int32_t test_stall;     // test only: the barrier waits for one block more than exist
 };
 constexpr int kDispatchChunk = 2048;
 constexpr int64_t kDispatchSmallPairs = 16384;  // T*k ranked by the one-block kernel
 // the fused-rank scan holds (n_rank_blocks + 1) x (E + 1) counts in shared memory
 constexpr int kFusedScanWords = 49152;
 cudaError_t dispatch_prepare();  // one-time function attributes
+// routed pairs up to which the cooperative dispatch is the default
+constexpr int64_t kCoopMaxPairs = 65536;
+// blocks of the cooperative dispatch that can be resident at once on
+// num_sms SMs (at most one per SM; 0 if none)
+int dispatch_coop_max_blocks(int num_sms);
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s);
 // histogram, prefix sums and ranks only (no row gather; x and xp unused)
 cudaError_t launch_dispatch_ranks(const DispatchArgs& a, cudaStream_t s);

@@ -322,15 +322,58 @@ def test_dispatch_own_ranking_full_size(name, monkeypatch):
     print(name, "own ranking", rep)
 
 
+@pytest.mark.parametrize("name", ["tiny", "ragged_mid", "skewed_small", "e256_k16", "int8_k6", "one_expert"])
+def test_dispatch_split_kernels_small(name, monkeypatch):
+    """CB_MOE_DISPATCH=split (with the dispatch's own ranking): separate
+    count, scan, scatter and row-copy kernels instead of the cooperative
+    launch; same routing views and outputs."""
+    monkeypatch.setenv("CB_MOE_FUSED_RANKS", "0")
+    monkeypatch.setenv("CB_MOE_DISPATCH", "split")
+    rep = gh.full_check(synth.make_layer(SMALL[name]))
+    print(name, "split dispatch", rep)
+
+
+@pytest.mark.parametrize("name,mode", [("skewed", "split"), ("int8", "coop"), ("int4", "coop")])
+def test_dispatch_forced_full_size(name, mode, monkeypatch):
+    """The dispatch form that is not the default at this size: separate
+    kernels on the 128-expert layer, the cooperative launch past 65536
+    routed pairs."""
+    monkeypatch.setenv("CB_MOE_DISPATCH", mode)
+    rep = gh.full_check(synth.make_layer(synth.WORKLOADS[name]), sample=FULL[name])
+    print(name, mode, "dispatch", rep)
+
+
+def test_cooperative_dispatch_timeout():
+    """The cooperative dispatch's grid barrier, made to wait for a block that
+    does not exist (CB_FLAG_TEST_STALL_DISPATCH, 1 ms bound), ends with
+    CB_ERR_TIMEOUT and leaves the device usable; a new handle is correct."""
+    import mixture_experts_router_gb300 as cb
+    layer = synth.make_layer(SMALL["skewed_small"])
+    gl = gh.GpuLayer(layer, flags=cb.CB_FLAG_TEST_STALL_DISPATCH)
+    try:
+        assert gl.m.kernels_per_forward() == 6  # tcgen05 router: 2, cooperative dispatch: 1
+        gl.m.forward(gl.x, gl.out)
+        torch.cuda.synchronize()
+        assert gl.m.last_error() == cb.CB_ERR_TIMEOUT
+    finally:
+        gl.close()
+    rep = gh.full_check(layer)
+    assert rep["f32_max_abs"] <= gh.MAX_ABS
+
+
 @pytest.mark.parametrize("fused,name,expect", [
-    ("1", "mixtral_prefill", 6), ("1", "skewed", 9), ("0", "mixtral_prefill", 6), ("0", "skewed", 9)])
+    ("1", "mixtral_prefill", 6), ("1", "skewed", 6), ("0", "mixtral_prefill", 5), ("0", "skewed", 6),
+    ("split", "mixtral_prefill", 6), ("split", "skewed", 9)])
 def test_kernels_per_forward(fused, name, expect, monkeypatch):
     """The launch count the library reports: router (the tcgen05 router of wide
     layers: partial logits + top-k), dispatch kernels (block scan + row copy
-    after the mma router's per-block ranks; or one-block / count-scan-scatter
-    ranking + row copy), two grouped GEMMs, combine."""
-    if fused == "0":
-        monkeypatch.setenv("CB_MOE_FUSED_RANKS", fused)
+    after the mma router's per-block ranks; else one cooperative launch, or
+    with CB_MOE_DISPATCH=split one-block / count-scan-scatter ranking + row
+    copy), two grouped GEMMs, combine."""
+    if fused != "1":
+        monkeypatch.setenv("CB_MOE_FUSED_RANKS", "0")
+    if fused == "split":
+        monkeypatch.setenv("CB_MOE_DISPATCH", "split")
     shp = synth.WORKLOADS[name]
     gl = gh.GpuLayer(synth.make_layer(synth.custom_shape(name + "_n", T=shp.T, d=256, f=256, E=shp.E, k=shp.k,
                                                          seed=61)))
