@@ -170,11 +170,17 @@ def test_device_wait_timeout_is_reported_and_context_survives(wdtype):
     assert rep["f32_max_abs"] <= gh.MAX_ABS
 
 
-@pytest.mark.parametrize("name", ["ragged_mid", "skewed_small", "tiny"])
-def test_gathered_rows_path(name, monkeypatch):
+@pytest.mark.parametrize("name,dispatch", [("ragged_mid", None), ("skewed_small", None), ("tiny", None),
+                                           ("skewed_small", "split"), ("ragged_mid", "split")])
+def test_gathered_rows_path(name, dispatch, monkeypatch):
     """CB_MOE_GATHER=1: the gate/up GEMM loads its rows from x with TMA
-    tile::gather4 instead of the dispatch's row copy; same results."""
+    tile::gather4 instead of the dispatch's row copy; same results (also with
+    the separate dispatch kernels, whose copy kernel then only writes the
+    pairs' padded rows)."""
     monkeypatch.setenv("CB_MOE_GATHER", "1")
+    if dispatch is not None:
+        monkeypatch.setenv("CB_MOE_FUSED_RANKS", "0")
+        monkeypatch.setenv("CB_MOE_DISPATCH", dispatch)
     rep = gh.full_check(synth.make_layer(SMALL[name]))
     print(name, "gather", rep)
 
