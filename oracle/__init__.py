@@ -28,7 +28,7 @@ class _Layer(ctypes.Structure):
                 ("router_mode", ctypes.c_int32), ("hash_dims", ctypes.c_int32), ("wh", ctypes.c_void_p),
                 ("zg", ctypes.c_void_p), ("zu", ctypes.c_void_p), ("zd", ctypes.c_void_p)]
 
-WDTYPES = {"bf16": 0, "int8": 1, "int4": 2}
+WDTYPES = {"bf16": 0, "int8": 1, "int4": 2, "fp8": 3}
 
 ROUTER_MODES = {"softmax": 0, "raw": 1, "hash": 2}
 
@@ -58,6 +58,8 @@ def _bind(lib):
     lib.moe_oracle_dispatch.argtypes = [i64, i32, i32, vp, vp, vp, vp, vp]
     lib.moe_oracle_dispatch.restype = i32
     lib.moe_oracle_expert.argtypes = [vp, i32, vp, i32, vp]
+    lib.moe_oracle_fp8_value.argtypes = [ctypes.c_uint8]
+    lib.moe_oracle_fp8_value.restype = ctypes.c_double
     lib.moe_oracle_expert.restype = None
     lib.moe_oracle_forward.argtypes = [vp, vp, i64, i32, vp, vp, vp]
     lib.moe_oracle_forward.restype = i32

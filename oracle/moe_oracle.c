@@ -47,6 +47,13 @@
  *     W[e][j][i] = s[e][j] * (q[e][j][i] - z[e][j]) with q in 0..15 packed two
  *     to a byte along i (element 2m in the low nibble of byte m) and an
  *     integer zero point z, so g_j = s_g[e][j] * sum_i x_i (q_g - z_g).
+ *     fp8 experts (the FP8 of the roadmap in "discosf.com/news/4774337" §6.3,
+ *     read as the e4m3 format that Transformer Engine uses for forward-pass
+ *     weights, with an fp32 scale per output channel as for int8):
+ *     W[e][j][i] = s[e][j] * v(c[e][j][i]) for the byte c = sign, 4 exponent
+ *     bits E (bias 7), 3 mantissa bits M: v = (-1)^sign * (1 + M/8) * 2^(E-7)
+ *     for E > 0, (-1)^sign * (M/8) * 2^-6 for E = 0; E = 15 with M = 7 is NaN
+ *     (there is no infinity).
  *     Mode EXACT keeps h in double; mode BF16H rounds each h_j to bf16
  *     (round to nearest even) before the down projection, which is the
  *     precision the layer's bf16 down-projection operand holds.
@@ -54,8 +61,8 @@
  *     o[t] = sum_s w[t][s] * y(t, s).
  *
  * Every sum is a plain sequential loop in double.  Inputs are bf16 bit
- * patterns (uint16), or int8 or packed int4 codes with float scales (and
- * uint8 zero points for int4).
+ * patterns (uint16), or int8, packed int4 or e4m3 codes with float scales
+ * (and uint8 zero points for int4).
  */
 #include <math.h>
 #include <stdint.h>
@@ -68,7 +75,8 @@
 typedef struct {
   int32_t T, d, f, E, k;
   int32_t wdtype;                 /* 0 = bf16 weights, 1 = int8 + scales,
-                                     2 = int4 + scales + zero points      */
+                                     2 = int4 + scales + zero points,
+                                     3 = fp8 (e4m3) + scales              */
   const uint16_t *x;              /* [T][d] bf16 bits                    */
   const uint16_t *wr;             /* [E][d] bf16 bits                    */
   const float *bias;              /* [E] or NULL                         */
@@ -139,11 +147,26 @@ uint16_t moe_oracle_bf16_bits(double v) {
   return (uint16_t)(u >> 16);
 }
 
+/* Value of an e4m3 byte (sign, 4 exponent bits with bias 7, 3 mantissa
+ * bits; no infinities; exponent 15 with mantissa 7 is NaN). */
+double moe_oracle_fp8_value(uint8_t c) {
+  const int sign = c >> 7, ex = (c >> 3) & 0xF, man = c & 0x7;
+  double mag;
+  if (ex == 15 && man == 7) return NAN;
+  if (ex == 0)
+    mag = ldexp((double)man / 8.0, -6);  /* subnormal: (M/8) 2^(1-7) */
+  else
+    mag = ldexp(1.0 + (double)man / 8.0, ex - 7);
+  return sign ? -mag : mag;
+}
+
 /* Element idx of a weight tensor before its channel scale: the bf16 value,
- * the int8 code, or the int4 code minus the row's zero point `zero`. */
+ * the int8 code, the int4 code minus the row's zero point `zero`, or the
+ * value of the e4m3 byte. */
 static double weight_elem(const moe_oracle_layer_t *L, const void *w, int64_t idx, int zero) {
   if (L->wdtype == 0) return bf16_value(((const uint16_t *)w)[idx]);
   if (L->wdtype == 1) return (double)((const int8_t *)w)[idx];
+  if (L->wdtype == 3) return moe_oracle_fp8_value(((const uint8_t *)w)[idx]);
   const uint8_t byte = ((const uint8_t *)w)[idx / 2];
   const int q = (idx % 2 == 0) ? (byte & 0x0F) : (byte >> 4);
   return (double)(q - zero);

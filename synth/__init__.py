@@ -3,7 +3,7 @@
 This module is shared by the fp64 oracle's tests and by the CUDA library's
 tests and benchmark.  It holds no part of the layer's arithmetic: it only
 draws the inputs (activations, router weights, the hash router's projection,
-expert weights, int8 codes and scales, the skewed router bias) in the shapes and distributions of the five
+expert weights, int8 / int4 / e4m3 codes and scales, the skewed router bias) in the shapes and distributions of the five
 workloads below, from a counter-based stream defined in ``synth.c``.
 
 The workloads follow the layer shapes the Colibri pages discuss: a Mixtral-8x7B
@@ -41,6 +41,10 @@ SCALE_LO, SCALE_HI = 0.5e-3, 1.0e-3   # per-output-channel fp32 scales ~ U
 INT4_CODE_SCALE, INT4_CODE_LO, INT4_CODE_HI = 2.5, -6, 6
 INT4_ZERO_SCALE, INT4_ZERO_LO, INT4_ZERO_HI, INT4_ZERO_MID = 1.2, -1, 2, 7
 INT4_SCALE_LO, INT4_SCALE_HI = 0.006, 0.010
+# fp8 (e4m3) weights: codes of 32 N(0,1) rounded to the nearest e4m3 value
+# (ties to the even code), scales ~ U(0.5e-3, 1e-3) per output channel as for
+# int8
+FP8_SCALE = 32.0
 
 
 def build(force: bool = False) -> str:
@@ -125,6 +129,32 @@ def int4_weights(seed, tid_w, tid_z, rows_shape, cols):
     return pack_int4(q), z.astype(np.uint8)
 
 
+def _e4m3_grid() -> np.ndarray:
+    """The non-negative finite e4m3 values, by code 0x00..0x7E (ascending)."""
+    c = np.arange(0x7F)
+    ex, man = c >> 3, c & 7
+    return np.where(ex == 0, man / 8.0 * 2.0 ** -6, (1.0 + man / 8.0) * 2.0 ** (ex - 7))
+
+
+def fp8_codes(seed, tid, scale, shape) -> np.ndarray:
+    """e4m3 bytes of scale * N(0,1) draws."""
+    return encode_e4m3(normal_f64(seed, tid, scale, shape))
+
+
+def encode_e4m3(v) -> np.ndarray:
+    """e4m3 bytes of float values: nearest value, ties to the even code,
+    magnitudes past 448 saturated."""
+    v = np.asarray(v, np.float64)
+    a = np.abs(v)
+    grid = _e4m3_grid()
+    i = np.clip(np.searchsorted(grid, a), 1, len(grid) - 1)
+    lo, hi = grid[i - 1], grid[i]
+    up = (a - lo > hi - a) | ((a - lo == hi - a) & (i % 2 == 0))
+    code = np.where(up, i, i - 1)
+    code = np.where(a >= grid[-1], len(grid) - 1, code)
+    return (code | np.where(np.signbit(v), 0x80, 0)).astype(np.uint8)
+
+
 def raw_bits(seed, tid, n, offset=0) -> np.ndarray:
     out = np.empty(n, dtype=np.uint64)
     _load().synth_bits(seed, tid, out.ctypes.data, offset, n)
@@ -145,7 +175,7 @@ class Shape:
     f: int
     E: int
     k: int
-    wdtype: str = "bf16"       # "bf16", "int8" or "int4"
+    wdtype: str = "bf16"       # "bf16", "int8", "int4" or "fp8"
     bias: bool = False         # skewed router bias b_e = 2 ln(1/(e+1))
     seed: int = 0
     router: str = "softmax"    # "softmax" (top-k, renormalised), "raw" (raw-logit weights), "hash"
@@ -161,6 +191,8 @@ WORKLOADS = {
     "int8": Shape("int8", T=16384, d=4096, f=1536, E=64, k=6, wdtype="int8", seed=1005),
     # the int8 layer's shape with 4-bit weights (scale and zero point per channel)
     "int4": Shape("int4", T=16384, d=4096, f=1536, E=64, k=6, wdtype="int4", seed=1006),
+    # the int8 layer's shape with fp8 (e4m3) weights and a scale per channel
+    "fp8": Shape("fp8", T=16384, d=4096, f=1536, E=64, k=6, wdtype="fp8", seed=1007),
 }
 
 
@@ -176,10 +208,10 @@ class Layer:
     x: np.ndarray                 # [T][d] bf16 bits
     wr: np.ndarray                # [E][d] bf16 bits
     bias: np.ndarray | None       # [E] float32
-    wg: np.ndarray                # [E][f][d] bf16 bits or int8; int4: [E][f][d/2] packed
+    wg: np.ndarray                # [E][f][d] bf16 bits, int8 or e4m3 bytes; int4: [E][f][d/2] packed
     wu: np.ndarray                # [E][f][d]
     wd: np.ndarray                # [E][d][f]
-    sg: np.ndarray | None = None  # [E][f] float32 (int8 and int4)
+    sg: np.ndarray | None = None  # [E][f] float32 (int8, int4 and fp8)
     su: np.ndarray | None = None  # [E][f]
     sd: np.ndarray | None = None  # [E][d]
     wh: np.ndarray | None = None  # [hash_dims][d] bf16 bits (hash router only)
@@ -211,9 +243,14 @@ def make_layer(shape: Shape, seed: int | None = None, T: int | None = None) -> L
         su = uniform_f32(s, TID_SU, INT4_SCALE_LO, INT4_SCALE_HI, (E, f))
         sd = uniform_f32(s, TID_SD, INT4_SCALE_LO, INT4_SCALE_HI, (E, d))
         return Layer(shape, x, wr, bias, wg, wu, wd, sg, su, sd, wh=wh, zg=zg, zu=zu, zd=zd)
-    wg = int8_codes(s, TID_WG, INT8_SCALE, (E, f, d))
-    wu = int8_codes(s, TID_WU, INT8_SCALE, (E, f, d))
-    wd = int8_codes(s, TID_WD, INT8_SCALE, (E, d, f))
+    if shape.wdtype == "fp8":
+        wg = fp8_codes(s, TID_WG, FP8_SCALE, (E, f, d))
+        wu = fp8_codes(s, TID_WU, FP8_SCALE, (E, f, d))
+        wd = fp8_codes(s, TID_WD, FP8_SCALE, (E, d, f))
+    else:
+        wg = int8_codes(s, TID_WG, INT8_SCALE, (E, f, d))
+        wu = int8_codes(s, TID_WU, INT8_SCALE, (E, f, d))
+        wd = int8_codes(s, TID_WD, INT8_SCALE, (E, d, f))
     sg = uniform_f32(s, TID_SG, SCALE_LO, SCALE_HI, (E, f))
     su = uniform_f32(s, TID_SU, SCALE_LO, SCALE_HI, (E, f))
     sd = uniform_f32(s, TID_SD, SCALE_LO, SCALE_HI, (E, d))

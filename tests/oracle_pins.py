@@ -56,7 +56,7 @@ def make_layer_from_values(x, wr, wg, wu, wd, k, bias=None, wdtype="bf16", sg=No
     conv = f32_to_bf16_bits
     if wdtype == "bf16":
         wgb, wub, wdb = conv(wg), conv(wu), conv(wd)
-    elif wdtype == "int4":
+    elif wdtype in ("int4", "fp8"):
         wgb, wub, wdb = (np.asarray(a, np.uint8) for a in (wg, wu, wd))
     else:
         wgb = np.asarray(wg, np.int8)
@@ -298,6 +298,48 @@ def pin_int8_equals_bf16(lib):
         assert np.allclose(oi, ob, rtol=1e-13, atol=1e-15), np.abs(oi - ob).max()
 
 
+def _torch_e4m3(codes):
+    """Values of e4m3 bytes by PyTorch's float8_e4m3fn (a library decode)."""
+    import torch
+    c = torch.from_numpy(np.ascontiguousarray(codes, dtype=np.uint8))
+    return c.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def pin_fp8_decode(lib):
+    """The oracle's e4m3 decode against PyTorch's float8_e4m3fn for all 256 bytes (NaN at
+    0x7F and 0xFF), and the format's landmarks: 0x38 = 1, 0x7E = 448 (largest), 0x08 = 2^-6
+    (smallest normal), 0x01 = 2^-9 (smallest subnormal), 0x80 = -0."""
+    mine = np.array([lib.moe_oracle_fp8_value(c) for c in range(256)])
+    ref = _torch_e4m3(np.arange(256))
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(mine), nan) and set(np.flatnonzero(nan).tolist()) == {0x7F, 0xFF}
+    assert np.array_equal(mine[~nan], ref[~nan])
+    assert mine[0x38] == 1.0 and mine[0x7E] == 448.0 and mine[0x08] == 2.0 ** -6 and mine[0x01] == 2.0 ** -9
+    assert mine[0x80] == 0.0 and np.signbit(mine[0x80]) and mine[0xB8] == -1.0
+
+
+def pin_fp8_equals_bf16(lib):
+    """e4m3 codes with per-output-channel power-of-two scales equal the bf16 layer whose weights
+    are s[j] * v(c[j][i]), the values taken from PyTorch's decode (exact in bf16: at most four
+    significant bits), for gate/up (channel j) and down (channel c)."""
+    rng = np.random.default_rng(13)
+    T, d, f, E, k = 6, 16, 24, 4, 2
+    x = rng_bf16(rng, (T, d), 1.0)
+    wr = rng_bf16(rng, (E, d), 0.3)
+    finite = np.array([c for c in range(256) if c not in (0x7F, 0xFF)])
+    cg, cu, cd = rng.choice(finite, (E, f, d)), rng.choice(finite, (E, f, d)), rng.choice(finite, (E, d, f))
+    sg = 2.0 ** -rng.integers(5, 10, (E, f)); su = 2.0 ** -rng.integers(5, 10, (E, f))
+    sd = 2.0 ** -rng.integers(5, 10, (E, d))
+    Lq = make_layer_from_values(x, wr, cg, cu, cd, k, wdtype="fp8", sg=sg, su=su, sd=sd)
+    Lb = make_layer_from_values(x, wr, _torch_e4m3(cg) * sg[:, :, None], _torch_e4m3(cu) * su[:, :, None],
+                                _torch_e4m3(cd) * sd[:, :, None], k)
+    for mode in (oracle.EXACT, oracle.BF16H):
+        oq, iq, _ = oracle.Oracle(Lq, lib).forward(mode=mode)
+        ob, ib, _ = oracle.Oracle(Lb, lib).forward(mode=mode)
+        assert np.array_equal(iq, ib)
+        assert np.allclose(oq, ob, rtol=1e-13, atol=1e-15), np.abs(oq - ob).max()
+
+
 def _pack_nibbles(q):
     """The ABI's int4 layout written out: byte m of a row = q[2m] + 16 q[2m + 1]."""
     q = np.asarray(q, np.int64)
@@ -470,6 +512,6 @@ def pin_hash_invariants(lib):
 
 ALL_PINS = [pin_round_bf16, pin_gate_bruteforce, pin_gate_weights, pin_dispatch, pin_identical_experts,
             pin_one_hot_router, pin_two_expert_mix, pin_zero_input, pin_bf16_h_mode, pin_int8_equals_bf16,
-            pin_int4_equals_bf16,
+            pin_int4_equals_bf16, pin_fp8_decode, pin_fp8_equals_bf16,
             pin_token_permutation, pin_expert_relabel, pin_golden_tiny, pin_routing_invariants,
             pin_raw_gate, pin_hash_golden, pin_hash_invariants]

@@ -12,6 +12,11 @@ import oracle_pins
 SRC = os.path.join(os.path.dirname(oracle.__file__), "moe_oracle.c")
 
 MUTANTS = {
+    "fp8_exponent_bias_8": ("mag = ldexp(1.0 + (double)man / 8.0, ex - 7);",
+                            "mag = ldexp(1.0 + (double)man / 8.0, ex - 8);"),
+    "fp8_subnormal_scale": ("mag = ldexp((double)man / 8.0, -6);", "mag = ldexp((double)man / 8.0, -7);"),
+    "fp8_mantissa_sixteenths": ("mag = ldexp(1.0 + (double)man / 8.0, ex - 7);",
+                                "mag = ldexp(1.0 + (double)man / 16.0, ex - 7);"),
     "gate_up_swapped": ("double silu = g / (1.0 + exp(-g));\n    double hj = silu * u;",
                         "double silu = u / (1.0 + exp(-u));\n    double hj = silu * g;"),
     "silu_sign": ("double silu = g / (1.0 + exp(-g));", "double silu = g / (1.0 + exp(g));"),

@@ -2,6 +2,7 @@
 import math
 
 import numpy as np
+import pytest
 
 import synth
 
@@ -82,3 +83,27 @@ def test_int4_weights_ranges_and_packing():
         assert np.array_equal(synth.pack_int4(q), w)
     for s in (L.sg, L.su, L.sd):
         assert s.dtype == np.float32 and s.min() >= 0.006 and s.max() < 0.010
+
+
+def test_fp8_weights_are_rounded_e4m3_codes():
+    """fp8 layers: e4m3 bytes (never the NaN codes) of 32 N(0,1) rounded to nearest with
+    ties to the even code, the same as PyTorch's float8_e4m3fn conversion of the draws;
+    scales in [0.5e-3, 1e-3)."""
+    torch = pytest.importorskip("torch")
+    shape = synth.custom_shape("f8", T=4, d=64, f=32, E=3, k=2, wdtype="fp8", seed=5)
+    L = synth.make_layer(shape)
+    assert L.wg.shape == (3, 32, 64) and L.wd.shape == (3, 64, 32) and L.wg.dtype == np.uint8
+    for w in (L.wg, L.wu, L.wd):
+        assert not np.any((w & 0x7F) == 0x7F)
+    draws = synth.normal_f64(shape.seed, synth.TID_WG, synth.FP8_SCALE, (3, 32, 64))
+    ref = torch.from_numpy(draws).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ref, L.wg)
+    # a tie between two e4m3 values goes to the even code: 1 + 1/16 lies between
+    # 0x38 (1.0) and 0x39 (1.125), 1 + 3/16 between 0x39 and 0x3A, 2^-10 between
+    # 0x00 and 0x01 (2^-9); past 448 saturates
+    g = synth._e4m3_grid()
+    assert g[0x38] == 1.0 and g[0x39] == 1.125 and g[0x7E] == 448.0
+    got = synth.encode_e4m3([1 + 1 / 16, 1 + 3 / 16, -(1 + 1 / 16), 2.0 ** -10, 500.0, -1.0])
+    assert got.tolist() == [0x38, 0x3A, 0xB8, 0x00, 0x7E, 0xB8]
+    for s in (L.sg, L.su, L.sd):
+        assert s.dtype == np.float32 and s.min() >= 0.5e-3 and s.max() < 1e-3
