@@ -47,7 +47,8 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--shape", default=None, help="T,d,f,E,k of a custom layer (profiling cases)")
-    p.add_argument("--wdtype", default="bf16", choices=["bf16", "int8", "int4"], help="expert weights of a --shape layer")
+    p.add_argument("--wdtype", default="bf16", choices=["bf16", "int8", "int4", "fp8"],
+                   help="expert weights of a --shape layer")
     p.add_argument("--bias", action="store_true", help="skewed router bias on a --shape layer")
     p.add_argument("--router", default="softmax", choices=["softmax", "raw", "hash"],
                    help="router variant: softmax top-k (default), raw-logit weights, or the hash router (k = 1)")
@@ -81,9 +82,9 @@ def algorithmic_work(shape, counts):
     count routed rows only (padding rows of the 128-row tiles are waste)."""
     T, d, f, E, k = shape.T, shape.d, shape.f, shape.E, shape.k
     M = T * k
-    eb = {"bf16": 2.0, "int8": 1.0, "int4": 0.5}[shape.wdtype]   # bytes per expert weight
+    eb = {"bf16": 2.0, "int8": 1.0, "int4": 0.5, "fp8": 1.0}[shape.wdtype]   # bytes per expert weight
     active = sum(1 for c in counts if c > 0)
-    # + per-channel scales (int8, int4) and zero points (int4)
+    # + per-channel scales (int8, int4, fp8) and zero points (int4)
     side = (4 if shape.wdtype != "bf16" else 0) + (1 if shape.wdtype == "int4" else 0)
     wbytes = int(active * 3 * d * f * eb) + active * (2 * f + d) * side
     return {
@@ -294,7 +295,7 @@ def run_ours(args):
     m = cb.MoELayer(shape.T, shape.d, shape.f, shape.E, shape.k, w["wr"], w["wg"], w["wu"], w["wd"],
                     router_bias=w["bias"], s_gate=w["sg"], s_up=w["su"], s_down=w["sd"], device=local,
                     stage_timing=True, router=shape.router, w_hash=w["wh"], z_gate=w["zg"], z_up=w["zu"],
-                    z_down=w["zd"])
+                    z_down=w["zd"], wdtype=shape.wdtype)
     launches_per_forward = m.kernels_per_forward()
     del w
     torch.cuda.empty_cache()

@@ -21,8 +21,10 @@
  * output channel (symmetric per-channel int8, "lshu.cn/news/53496" §4.3);
  * int4 experts: W[e][j][i] = s[e][j] * (q[e][j][i] - z[e][j]) with a scale
  * and an integer zero point per output channel ("m.nxbn.cn/news/47706"
- * §3.2).  The codes (minus the zero point) become bf16 exactly inside the
- * GEMM and the scale multiplies the fp32 accumulator.
+ * §3.2); fp8 experts: W[e][j][i] = s[e][j] * v(c[e][j][i]) for e4m3 bytes c
+ * ("discosf.com/news/4774337" §6.3).  The codes (minus the zero point)
+ * become bf16 exactly inside the GEMM and the scale multiplies the fp32
+ * accumulator.
  *
  * Conventions for every call below:
  *  - bf16 means IEEE bfloat16 stored as 16-bit words; all matrices are
@@ -75,8 +77,14 @@ typedef enum {
  * point z (uint8, 0..15) per output channel, W = s (q - z)
  * ("m.nxbn.cn/news/47706" §3.2, a channel read as an output row); the codes
  * are packed two to a byte along the input dimension, element 2m in the low
- * nibble of byte m and element 2m + 1 in its high nibble. */
-typedef enum { CB_W_BF16 = 0, CB_W_INT8 = 1, CB_W_INT4 = 2 } cb_wdtype_t;
+ * nibble of byte m and element 2m + 1 in its high nibble.
+ * CB_W_FP8: one e4m3 byte per weight (sign, 4 exponent bits with bias 7, 3
+ * mantissa bits: (1 + M/8) 2^(E-7), or (M/8) 2^-6 for E = 0; the NaN bytes
+ * 0x7F and 0xFF are not valid weights) with an fp32 scale s per output
+ * channel, W = s v(byte): the FP8 of "discosf.com/news/4774337" §6.3, read
+ * as the e4m3 format Transformer Engine uses for forward-pass weights.  The
+ * layout and scales are those of CB_W_INT8. */
+typedef enum { CB_W_BF16 = 0, CB_W_INT8 = 1, CB_W_INT4 = 2, CB_W_FP8 = 3 } cb_wdtype_t;
 
 /*
  * config.router_mode: how each token picks its experts and their weights.
@@ -135,12 +143,12 @@ typedef struct {
 typedef struct {
   const void *w_router;     /* bf16 [E][d]                                        */
   const float *router_bias; /* fp32 [E], or NULL for no bias                      */
-  const void *w_gate;       /* bf16 or int8 [E][f][d]; int4 [E][f][d/2] bytes (w1)  */
-  const void *w_up;         /* bf16 or int8 [E][f][d]; int4 [E][f][d/2] bytes (w3)  */
-  const void *w_down;       /* bf16 or int8 [E][d][f]; int4 [E][d][f/2] bytes (w2)  */
-  const float *s_gate;      /* fp32 [E][f]  int8 and int4, else NULL              */
-  const float *s_up;        /* fp32 [E][f]  int8 and int4, else NULL              */
-  const float *s_down;      /* fp32 [E][d]  int8 and int4, else NULL              */
+  const void *w_gate;       /* bf16, int8 or e4m3 [E][f][d]; int4 [E][f][d/2] (w1) */
+  const void *w_up;         /* bf16, int8 or e4m3 [E][f][d]; int4 [E][f][d/2] (w3) */
+  const void *w_down;       /* bf16, int8 or e4m3 [E][d][f]; int4 [E][d][f/2] (w2) */
+  const float *s_gate;      /* fp32 [E][f]  int8, int4 and fp8, else NULL         */
+  const float *s_up;        /* fp32 [E][f]  int8, int4 and fp8, else NULL         */
+  const float *s_down;      /* fp32 [E][d]  int8, int4 and fp8, else NULL         */
   const void *w_hash;       /* bf16 [hash_dims][d], CB_ROUTER_HASH only, else NULL */
   const uint8_t *z_gate;    /* uint8 [E][f] zero points 0..15, int4 only, else NULL */
   const uint8_t *z_up;      /* uint8 [E][f] zero points, int4 only, else NULL     */

@@ -15,7 +15,8 @@ LIB_PATH = os.path.join(HERE, "libcbmoe.so")
 
 CB_OK, CB_ERR_INVALID_ARG, CB_ERR_UNSUPPORTED, CB_ERR_ALIGNMENT = 0, 1, 2, 3
 CB_ERR_OOM, CB_ERR_CUDA, CB_ERR_TIMEOUT, CB_ERR_DEVICE = 4, 5, 6, 7
-CB_W_BF16, CB_W_INT8, CB_W_INT4 = 0, 1, 2
+CB_W_BF16, CB_W_INT8, CB_W_INT4, CB_W_FP8 = 0, 1, 2, 3
+WDTYPES = {"bf16": CB_W_BF16, "int8": CB_W_INT8, "int4": CB_W_INT4, "fp8": CB_W_FP8}
 CB_FLAG_KEEP_LOGITS = 0x1
 CB_FLAG_STAGE_TIMING = 0x2
 CB_FLAG_TEST_STALL = 0x4
@@ -202,17 +203,25 @@ def _ptr(t):
 
 class MoELayer:
     """One layer handle over torch device tensors (bf16 as torch.bfloat16 or int16 bits,
-    int8 as torch.int8).  Raises CbMoeError on any non-zero status."""
+    int8 as torch.int8, e4m3 as uint8 bytes or torch.float8_e4m3fn).  Raises CbMoeError on
+    any non-zero status."""
 
     def __init__(self, T, d, f, E, k, w_router, w_gate, w_up, w_down, router_bias=None,
                  s_gate=None, s_up=None, s_down=None, device=0, keep_logits=False, stage_timing=False,
-                 flags=0, router="softmax", w_hash=None, z_gate=None, z_up=None, z_down=None):
-        """Expert weights: bf16; int8 codes with scales (s_*); or packed int4 codes (two per
-        byte along the input dimension) with scales and uint8 zero points (z_*)."""
+                 flags=0, router="softmax", w_hash=None, z_gate=None, z_up=None, z_down=None, wdtype=None):
+        """Expert weights: bf16; int8 codes with scales (s_*); packed int4 codes (two per
+        byte along the input dimension) with scales and uint8 zero points (z_*); or e4m3
+        bytes with scales (wdtype="fp8", or weights of dtype torch.float8_e4m3fn).  Without
+        `wdtype` the format follows from which of s_* and z_* are given."""
         flags |= (CB_FLAG_KEEP_LOGITS if keep_logits else 0) | (CB_FLAG_STAGE_TIMING if stage_timing else 0)
         mode = ROUTER_MODES[router]
         hash_dims = 0 if w_hash is None else int(w_hash.shape[0])
-        wdtype = CB_W_INT4 if z_gate is not None else CB_W_INT8 if s_gate is not None else CB_W_BF16
+        if wdtype is None:
+            fp8 = str(getattr(w_gate, "dtype", "")).endswith("float8_e4m3fn")
+            wdtype = (CB_W_INT4 if z_gate is not None else CB_W_FP8 if fp8 else
+                      CB_W_INT8 if s_gate is not None else CB_W_BF16)
+        elif isinstance(wdtype, str):
+            wdtype = WDTYPES[wdtype]
         self.cfg = cb_moe_config_t(T, d, f, E, k, wdtype, device, flags, mode, hash_dims)
         w = cb_moe_weights_t(_ptr(w_router), _ptr(router_bias), _ptr(w_gate), _ptr(w_up), _ptr(w_down),
                              _ptr(s_gate), _ptr(s_up), _ptr(s_down), _ptr(w_hash),

@@ -88,7 +88,7 @@ uint64_t align256(uint64_t v) { return (v + 255) & ~uint64_t(255); }
 Layout plan(const cb_moe_config_t& c) {
   Layout L{};
   const uint64_t T = c.n_tokens, d = c.d_model, f = c.d_ff, E = c.n_experts, k = c.top_k;
-  const uint64_t wbits = c.wdtype == CB_W_INT8 ? 8 : c.wdtype == CB_W_INT4 ? 4 : 16;  // bits per weight
+  const uint64_t wbits = c.wdtype == CB_W_INT4 ? 4 : c.wdtype == CB_W_BF16 ? 16 : 8;  // bits per weight
   const bool quant = c.wdtype != CB_W_BF16;
   const uint64_t M = T * k;
   L.max_mtiles = static_cast<int32_t>((M + E * (kTileM - 1)) / kTileM + 1);
@@ -144,7 +144,8 @@ cb_status_t validate_config(const cb_moe_config_t* c) {
   if (c->n_tokens < 0 || c->d_model <= 0 || c->d_ff <= 0 || c->n_experts <= 0 || c->top_k <= 0)
     return CB_ERR_INVALID_ARG;
   if (c->top_k > c->n_experts) return CB_ERR_INVALID_ARG;
-  if (c->wdtype != CB_W_BF16 && c->wdtype != CB_W_INT8 && c->wdtype != CB_W_INT4) return CB_ERR_INVALID_ARG;
+  if (c->wdtype != CB_W_BF16 && c->wdtype != CB_W_INT8 && c->wdtype != CB_W_INT4 && c->wdtype != CB_W_FP8)
+    return CB_ERR_INVALID_ARG;
   if (c->d_model % 256 != 0 || c->d_ff % 256 != 0) return CB_ERR_UNSUPPORTED;
   if (c->n_experts > 256 || c->top_k > 16) return CB_ERR_UNSUPPORTED;
   if (c->router_mode < CB_ROUTER_SOFTMAX_TOPK || c->router_mode > CB_ROUTER_HASH) return CB_ERR_INVALID_ARG;
@@ -307,8 +308,8 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
   if (launch_dispatch(da, s) != cudaSuccess || !mark(2)) return CB_ERR_CUDA;
 
   const bool int4w = c.wdtype == CB_W_INT4;
-  const bool int8w = c.wdtype == CB_W_INT8 || int4w;  // quantized weights (int8 or int4)
-  const int wbits = int4w ? 4 : 8;
+  const bool int8w = c.wdtype != CB_W_BF16;  // quantized weights (int8, int4 or fp8)
+  const WeightFormat wf = int4w ? kWInt4 : c.wdtype == CB_W_FP8 ? kWFp8 : kWInt8;
   GemmArgs ga{};
   ga.mtile_off = h->mtile_off;
   ga.mtile_expert = h->mtile_expert;
@@ -350,7 +351,7 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
   const bool pair_dn = !int8w && h->pair_dn;
   cudaError_t e1;
   if (int8w && h->int8_tm) {
-    e1 = launch_grouped_gemm_int8_tm(kGateUpSwiGLU, wbits, h->tm_a_gu, h->tm_w_gu8, ga, s);
+    e1 = launch_grouped_gemm_int8_tm(kGateUpSwiGLU, wf, h->tm_a_gu, h->tm_w_gu8, ga, s);
   } else if (int8w) {
     e1 = launch_grouped_gemm_int8(kGateUpSwiGLU, h->tm_a_gu, h->tm_b_gu, h->tm_y, ga, s);
   } else if (pair_gu) {
@@ -378,7 +379,7 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
   gd.zero1 = nullptr;
   cudaError_t e2;
   if (int8w && h->int8_tm) {
-    e2 = launch_grouped_gemm_int8_tm(kDownF32, wbits, h->tm_a_dn, h->tm_w_dn8, gd, s);
+    e2 = launch_grouped_gemm_int8_tm(kDownF32, wf, h->tm_a_dn, h->tm_w_dn8, gd, s);
   } else if (int8w) {
     e2 = launch_grouped_gemm_int8(kDownF32, h->tm_a_dn, h->tm_b_dn, h->tm_y, gd, s);
   } else if (pair_dn) {
@@ -530,7 +531,8 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
       wts->w_down == nullptr || (hashr && wts->w_hash == nullptr))
     return CB_ERR_INVALID_ARG;
   const bool int4w = cfg->wdtype == CB_W_INT4;
-  const bool int8w = cfg->wdtype == CB_W_INT8 || int4w;  // quantized weights (int8 or int4)
+  const bool fp8w = cfg->wdtype == CB_W_FP8;
+  const bool int8w = cfg->wdtype != CB_W_BF16;  // quantized weights (int8, int4 or fp8)
   if (int4w && (wts->z_gate == nullptr || wts->z_up == nullptr || wts->z_down == nullptr))
     return CB_ERR_UNSUPPORTED;
   if (int8w && (wts->s_gate == nullptr || wts->s_up == nullptr || wts->s_down == nullptr))
@@ -623,7 +625,7 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
   // in blocks of different sizes.  int4 weights have the first kernel only.
   {
     const char* iv = std::getenv("CB_MOE_INT8");
-    h->int8_tm = int4w || !(iv != nullptr && std::strcmp(iv, "smem") == 0);
+    h->int8_tm = int4w || fp8w || !(iv != nullptr && std::strcmp(iv, "smem") == 0);
   }
   const uint64_t brows =
       int8w ? (h->int8_tm ? grouped_gemm_int8_tm_gateup_block() : grouped_gemm_int8_gateup_block()) : 128;

@@ -1,9 +1,12 @@
 // Grouped expert GEMMs with int8 weights (symmetric per-output-channel int8,
-// "lshu.cn/news/53496" §4.3) or int4 weights (4-bit codes with a scale and a
-// zero point per output channel, "m.nxbn.cn/news/47706" §3.2), dequantised to
-// bf16 inside the kernel, with the converted weights held in TENSOR MEMORY as
-// the MMA's A operand.  An int4 row of the tile holds q - z (its zero point
-// taken off during the conversion, exact); the scale is the same as int8's.
+// "lshu.cn/news/53496" §4.3), int4 weights (4-bit codes with a scale and a
+// zero point per output channel, "m.nxbn.cn/news/47706" §3.2) or fp8 weights
+// (e4m3 bytes with a scale per output channel, the FP8 of
+// "discosf.com/news/4774337" §6.3), dequantised to bf16 inside the kernel,
+// with the converted weights held in TENSOR MEMORY as the MMA's A operand.
+// An int4 row of the tile holds q - z (its zero point taken off during the
+// conversion, exact), an fp8 row the e4m3 values (exact in bf16); the scale
+// is applied as for int8.
 //
 // The GEMM is computed transposed: D[weight row][token] = W[e] * Xp^T, with
 // D in tensor memory (lane = weight row, column = token).  A tile is 128
@@ -73,6 +76,15 @@ constexpr uint32_t IDESC2 = idesc_bf16_f32(WROWS, 2 * BM);
 constexpr uint32_t IDESC1 = idesc_bf16_f32(WROWS, BM);
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + W_SLOTS * W_BYTES + 1024 + 512;
 
+// Four one-byte weight codes -> four bf16 (int8 or e4m3), exactly.
+template <int WF>
+__device__ __forceinline__ void byte4_to_bf16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  if constexpr (WF == kWFp8)
+    fp8x4_to_bf16x4(w, lo, hi);
+  else
+    int8x4_to_bf16x4(w, lo, hi);
+}
+
 struct PairCoord {
   int m0;      // first m-tile (global index)
   bool two;    // second m-tile m0 + 1 is real
@@ -95,11 +107,11 @@ __device__ __forceinline__ PairCoord decode_pair(int tile, const GemmArgs& p) {
   return c;
 }
 
-template <int KIND, int WBITS>
+template <int KIND, int WF>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_int8_tm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                                 const GemmArgs p) {
-  constexpr int KPS = WBITS == 8 ? 2 : 4;  // k-blocks per weight slot
+  constexpr int KPS = WF == kWInt4 ? 4 : 2;  // k-blocks per weight slot
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* s_w = smem + STAGES * STAGE_BYTES;  // int8 weight slots (128-byte swizzled rows)
@@ -244,7 +256,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint4 v[8];
     for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
       uint32_t zz = 0;  // int4: 0x4300 | zero point, in both bf16 halves
-      if constexpr (WBITS == 4) {
+      if constexpr (WF == kWInt4) {
         const PairCoord c = decode_pair(tile, p);
         int z;
         if constexpr (KIND == kGateUpSwiGLU) {
@@ -279,22 +291,22 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         tc_fence_after();
         uint32_t o[32];
-        if constexpr (WBITS == 8) {
+        if constexpr (WF != kWInt4) {
           if ((kb & 1) == 0) {
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
-              int8x4_to_bf16x4(v[cc].x, o[8 * cc + 0], o[8 * cc + 1]);
-              int8x4_to_bf16x4(v[cc].y, o[8 * cc + 2], o[8 * cc + 3]);
-              int8x4_to_bf16x4(v[cc].z, o[8 * cc + 4], o[8 * cc + 5]);
-              int8x4_to_bf16x4(v[cc].w, o[8 * cc + 6], o[8 * cc + 7]);
+              byte4_to_bf16x4<WF>(v[cc].x, o[8 * cc + 0], o[8 * cc + 1]);
+              byte4_to_bf16x4<WF>(v[cc].y, o[8 * cc + 2], o[8 * cc + 3]);
+              byte4_to_bf16x4<WF>(v[cc].z, o[8 * cc + 4], o[8 * cc + 5]);
+              byte4_to_bf16x4<WF>(v[cc].w, o[8 * cc + 6], o[8 * cc + 7]);
             }
           } else {
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
-              int8x4_to_bf16x4(v[4 + cc].x, o[8 * cc + 0], o[8 * cc + 1]);
-              int8x4_to_bf16x4(v[4 + cc].y, o[8 * cc + 2], o[8 * cc + 3]);
-              int8x4_to_bf16x4(v[4 + cc].z, o[8 * cc + 4], o[8 * cc + 5]);
-              int8x4_to_bf16x4(v[4 + cc].w, o[8 * cc + 6], o[8 * cc + 7]);
+              byte4_to_bf16x4<WF>(v[4 + cc].x, o[8 * cc + 0], o[8 * cc + 1]);
+              byte4_to_bf16x4<WF>(v[4 + cc].y, o[8 * cc + 2], o[8 * cc + 3]);
+              byte4_to_bf16x4<WF>(v[4 + cc].z, o[8 * cc + 4], o[8 * cc + 5]);
+              byte4_to_bf16x4<WF>(v[4 + cc].w, o[8 * cc + 6], o[8 * cc + 7]);
             }
           }
         } else {
@@ -425,26 +437,32 @@ cudaError_t grouped_gemm_int8_tm_prepare() {
   auto set = [&](auto fn) {
     if (e == cudaSuccess) e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   };
-  set(grouped_gemm_int8_tm_kernel<kGateUpSwiGLU, 8>);
-  set(grouped_gemm_int8_tm_kernel<kDownF32, 8>);
-  set(grouped_gemm_int8_tm_kernel<kGateUpSwiGLU, 4>);
-  set(grouped_gemm_int8_tm_kernel<kDownF32, 4>);
+  set(grouped_gemm_int8_tm_kernel<kGateUpSwiGLU, kWInt8>);
+  set(grouped_gemm_int8_tm_kernel<kDownF32, kWInt8>);
+  set(grouped_gemm_int8_tm_kernel<kGateUpSwiGLU, kWInt4>);
+  set(grouped_gemm_int8_tm_kernel<kDownF32, kWInt4>);
+  set(grouped_gemm_int8_tm_kernel<kGateUpSwiGLU, kWFp8>);
+  set(grouped_gemm_int8_tm_kernel<kDownF32, kWFp8>);
   return e;
 }
 
-cudaError_t launch_grouped_gemm_int8_tm(GemmKind kind, int wbits, const CUtensorMap& tm_x, const CUtensorMap& tm_w,
-                                        const GemmArgs& a, cudaStream_t s) {
-  if (a.k_blocks % (wbits == 8 ? 2 : 4) != 0 || (wbits != 8 && wbits != 4)) return cudaErrorInvalidValue;
-  if (wbits == 8) {
-    if (kind == kGateUpSwiGLU)
-      launch_kernel(grouped_gemm_int8_tm_kernel<kGateUpSwiGLU, 8>, a.grid, THREADS, SMEM_BYTES, s, tm_x, tm_w, a);
-    else
-      launch_kernel(grouped_gemm_int8_tm_kernel<kDownF32, 8>, a.grid, THREADS, SMEM_BYTES, s, tm_x, tm_w, a);
-  } else {
-    if (kind == kGateUpSwiGLU)
-      launch_kernel(grouped_gemm_int8_tm_kernel<kGateUpSwiGLU, 4>, a.grid, THREADS, SMEM_BYTES, s, tm_x, tm_w, a);
-    else
-      launch_kernel(grouped_gemm_int8_tm_kernel<kDownF32, 4>, a.grid, THREADS, SMEM_BYTES, s, tm_x, tm_w, a);
+template <int WF>
+static void launch_wf(GemmKind kind, const CUtensorMap& tm_x, const CUtensorMap& tm_w, const GemmArgs& a,
+                      cudaStream_t s) {
+  if (kind == kGateUpSwiGLU)
+    launch_kernel(grouped_gemm_int8_tm_kernel<kGateUpSwiGLU, WF>, a.grid, THREADS, SMEM_BYTES, s, tm_x, tm_w, a);
+  else
+    launch_kernel(grouped_gemm_int8_tm_kernel<kDownF32, WF>, a.grid, THREADS, SMEM_BYTES, s, tm_x, tm_w, a);
+}
+
+cudaError_t launch_grouped_gemm_int8_tm(GemmKind kind, WeightFormat wf, const CUtensorMap& tm_x,
+                                        const CUtensorMap& tm_w, const GemmArgs& a, cudaStream_t s) {
+  if (a.k_blocks % (wf == kWInt4 ? 4 : 2) != 0) return cudaErrorInvalidValue;
+  switch (wf) {
+    case kWInt8: launch_wf<kWInt8>(kind, tm_x, tm_w, a, s); break;
+    case kWInt4: launch_wf<kWInt4>(kind, tm_x, tm_w, a, s); break;
+    case kWFp8: launch_wf<kWFp8>(kind, tm_x, tm_w, a, s); break;
+    default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
 }

@@ -50,4 +50,21 @@ __device__ __forceinline__ void int4x8_minus_zero_to_bf16(uint32_t w, uint32_t z
   }
 }
 
+// Four e4m3 bytes (one 32-bit word; sign, 4 exponent bits with bias 7, 3
+// mantissa bits) -> four bf16, exactly: lo = {b0, b1}, hi = {b2, b3}.  Each
+// byte's sign goes to bit 15 and its exponent and mantissa to bits 10..4 of a
+// bf16 word, which is then the byte's value times 2^-120 (exponent bias 127
+// instead of 7; an e4m3 subnormal lands on a bf16 subnormal with the same
+// mantissa bits).  The bf16 product with 2^120 restores the value; it is
+// exact, being a power-of-two scaling into bf16's normal range.  The NaN
+// bytes (exponent 15, mantissa 7) are not valid weights and map to 480.
+__device__ __forceinline__ void fp8x4_to_bf16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t t01 = __byte_perm(w, 0u, 0x4140), t23 = __byte_perm(w, 0u, 0x4342);  // {b, 0} per half
+  uint32_t v01, v23;
+  asm("lop3.b32 %0, %1, 0x80008000, %2, 0xEA;" : "=r"(v01) : "r"(t01 << 8), "r"((t01 & 0x007F007Fu) << 4));
+  asm("lop3.b32 %0, %1, 0x80008000, %2, 0xEA;" : "=r"(v23) : "r"(t23 << 8), "r"((t23 & 0x007F007Fu) << 4));
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(lo) : "r"(v01), "r"(0x7B807B80u));
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(hi) : "r"(v23), "r"(0x7B807B80u));
+}
+
 }  // namespace cbmoe

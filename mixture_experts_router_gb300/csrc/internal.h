@@ -245,12 +245,14 @@ cudaError_t launch_grouped_gemm_int8(GemmKind kind, const CUtensorMap& tm_a, con
 cudaError_t grouped_gemm_int8_prepare();
 int grouped_gemm_int8_tile_n(GemmKind kind);
 int grouped_gemm_int8_gateup_block();  // gate/up rows interleaved in blocks of this size
-// int8 weights converted into tensor memory (the MMA's A operand): tiles are
-// 128 weight rows against a pair of m-tiles; tm_x: the activations (128 x 64
-// boxes), tm_w: the int8 weights with a 128 x 128 box and the 128-byte swizzle
-// (wbits 8: int8 codes; 4: packed int4 codes with zero points, slots of K = 256)
-cudaError_t launch_grouped_gemm_int8_tm(GemmKind kind, int wbits, const CUtensorMap& tm_x, const CUtensorMap& tm_w,
-                                        const GemmArgs& a, cudaStream_t s);
+// int8, int4 or fp8 weights converted into tensor memory (the MMA's A
+// operand): tiles are 128 weight rows against a pair of m-tiles; tm_x: the
+// activations (128 x 64 boxes), tm_w: the weight bytes with a 128 x 128 box
+// and the 128-byte swizzle (kWInt8: int8 codes; kWFp8: e4m3 codes; kWInt4:
+// packed int4 codes with zero points, slots of K = 256)
+enum WeightFormat { kWInt8 = 0, kWInt4 = 1, kWFp8 = 2 };
+cudaError_t launch_grouped_gemm_int8_tm(GemmKind kind, WeightFormat wf, const CUtensorMap& tm_x,
+                                        const CUtensorMap& tm_w, const GemmArgs& a, cudaStream_t s);
 cudaError_t grouped_gemm_int8_tm_prepare();
 int grouped_gemm_int8_tm_tile_n(GemmKind kind);
 int grouped_gemm_int8_tm_gateup_block();  // gate/up rows interleaved in blocks of this size

@@ -49,7 +49,7 @@ class GpuLayer:
         self.m = cb.MoELayer(self.T, s.d, s.f, s.E, s.k, w["wr"], w["wg"], w["wu"], w["wd"], router_bias=w["bias"],
                              s_gate=w["sg"], s_up=w["su"], s_down=w["sd"], device=device, keep_logits=keep_logits,
                              flags=flags, router=s.router, w_hash=w["wh"], z_gate=w["zg"], z_up=w["zu"],
-                             z_down=w["zd"])
+                             z_down=w["zd"], wdtype=s.wdtype)
         del w
         self.x = to_dev(layer.x, self.dev)
         self.out = torch.empty((self.T, s.d), dtype=torch.bfloat16, device=self.dev)

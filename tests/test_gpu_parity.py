@@ -28,6 +28,10 @@ SMALL = {
     "int4_mid": synth.custom_shape("int4_mid", T=300, d=512, f=768, E=8, k=2, wdtype="int4", seed=30),
     "int4_pairs": synth.custom_shape("int4_pairs", T=1100, d=512, f=768, E=4, k=2, wdtype="int4", seed=31),
     "int4_k6": synth.custom_shape("int4_k6", T=700, d=256, f=512, E=64, k=6, wdtype="int4", seed=32),
+    # fp8 (e4m3) experts with a scale per channel: the same three layouts
+    "fp8_mid": synth.custom_shape("fp8_mid", T=300, d=512, f=768, E=8, k=2, wdtype="fp8", seed=34),
+    "fp8_pairs": synth.custom_shape("fp8_pairs", T=1100, d=512, f=768, E=4, k=2, wdtype="fp8", seed=35),
+    "fp8_k6": synth.custom_shape("fp8_k6", T=700, d=256, f=512, E=64, k=6, wdtype="fp8", seed=36),
 }
 
 FULL = {  # workload: tokens sampled for the output check
@@ -36,6 +40,7 @@ FULL = {  # workload: tokens sampled for the output check
     "mixtral_prefill": 24,
     "int8": 48,
     "int4": 48,
+    "fp8": 48,
 }
 
 
@@ -150,7 +155,25 @@ def test_both_routers(name, router, monkeypatch):
     assert rep.get("logit_max_err", 0.0) <= 5e-6
 
 
-@pytest.mark.parametrize("wdtype", ["bf16", "int8", "int4"])
+def test_fp8_every_code():
+    """fp8 weights drawn uniformly from all 254 finite e4m3 bytes (both zeros, every
+    subnormal, the largest values), each about 2000 times: the kernel's byte -> bf16
+    conversion is exact for every code, so the layer matches the oracle."""
+    import dataclasses
+    shape = synth.custom_shape("fp8_codes", T=300, d=256, f=512, E=4, k=2, wdtype="fp8", seed=33)
+    layer = synth.make_layer(shape)
+    rng = np.random.default_rng(33)
+    finite = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8)
+    wg, wu, wd = (rng.choice(finite, a.shape).astype(np.uint8) for a in (layer.wg, layer.wu, layer.wd))
+    assert all(len(np.unique(w)) == len(finite) for w in (wg, wu, wd))
+    small = lambda s: (s * np.float32(0.2)).astype(np.float32)  # weights of about 0.02 spread
+    layer = dataclasses.replace(layer, wg=wg, wu=wu, wd=wd, sg=small(layer.sg), su=small(layer.su),
+                                sd=small(layer.sd))
+    rep = gh.full_check(layer)
+    print("fp8 every code", rep)
+
+
+@pytest.mark.parametrize("wdtype", ["bf16", "int8", "int4", "fp8"])
 def test_device_wait_timeout_is_reported_and_context_survives(wdtype):
     """A bounded device wait that nothing satisfies (CB_FLAG_TEST_STALL) ends the
     kernel with CB_ERR_TIMEOUT in the status word instead of a hang or a fault;
@@ -339,7 +362,7 @@ def test_dispatch_split_kernels_small(name, monkeypatch):
     print(name, "split dispatch", rep)
 
 
-@pytest.mark.parametrize("name,mode", [("skewed", "split"), ("int8", "coop"), ("int4", "coop")])
+@pytest.mark.parametrize("name,mode", [("skewed", "split"), ("int8", "coop"), ("int4", "coop"), ("fp8", "coop")])
 def test_dispatch_forced_full_size(name, mode, monkeypatch):
     """The dispatch form that is not the default at this size: separate
     kernels on the 128-expert layer, the cooperative launch past 65536
