@@ -18,9 +18,17 @@
 // Barriers: the TMA loads of both CTAs signal the even CTA's `full` barrier
 // (whose producer expects both CTAs' bytes); the MMA thread's commits arrive
 // on `empty` (stage free) and `tfull` (accumulator ready) in both CTAs; the
-// epilogue warps of both CTAs arrive on the even CTA's `tempty`.  In a pair
-// whose second m-tile does not exist (an expert with an odd number of
-// m-tiles), the odd CTA loads a repeat of the first tile and stores nothing.
+// epilogue warps of both CTAs arrive on the even CTA's `tempty`.
+//
+// A pair whose second m-tile does not exist (the last pair of an expert with
+// an odd number of m-tiles) runs the M = 128 form of the 2-SM MMA instead:
+// CTA r stages rows [64 r, 64 r + 64) of the single m-tile, and the MMA takes
+// half the time.  Its accumulator (measured on GB300) holds, in each CTA,
+// the CTA's 64 rows in TMEM lanes 0..63 against weight rows 0..127 and again
+// in lanes 64..127 against weight rows 128..255, both in columns 0..127.  So
+// in the down epilogue each warp stores its own 128-column half of Y, and in
+// the gate/up epilogue (gate in lanes 0..63, up in lanes 64..127) the up
+// warps hand their values to the gate warps through shared memory.
 //
 // Roles per CTA: warp 0 TMA producer, warp 1 TMEM allocation for the pair
 // (and, in the even CTA, the MMA issuer), warps 2..5 epilogue.  All waits
@@ -47,6 +55,8 @@ constexpr int THREADS = 192;
 constexpr int EPI_WARPS = 4;
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr uint32_t IDESC = idesc_bf16_f32(2 * BM, BN);
+constexpr uint32_t IDESC_HALF = idesc_bf16_f32(BM, BN);  // M = 128: 64 rows per CTA
+constexpr uint32_t EPI_BAR = 1;                          // named barrier of the epilogue warps
 constexpr uint16_t PAIR_MASK = 0x3;
 constexpr int STG_BYTES = EPI_WARPS * 2 * 32 * 128;
 
@@ -64,8 +74,9 @@ struct Cfg {
 static_assert(Cfg<kGateUpSwiGLU>::BYTES <= 232448 && Cfg<kDownF32>::BYTES <= 232448, "shared memory per CTA");
 
 struct PairTile {
-  int m_tile;  // this CTA's m-tile (a repeat of the pair's first when !valid)
+  int m_tile;  // this CTA's m-tile (for a half pair, the pair's single m-tile)
   bool valid;
+  bool half;   // the pair has one m-tile: M = 128, 64 of its rows per CTA
   int e;
   int n;
 };
@@ -83,8 +94,9 @@ __device__ __forceinline__ PairTile decode_pair_tile(int tile, const GemmArgs& p
   t.n = local / np;
   const int mt_e = p.mtile_off[e + 1] - p.mtile_off[e];
   const int idx = 2 * pair + rank;
-  t.valid = idx < mt_e;
-  t.m_tile = p.mtile_off[e] + (t.valid ? idx : 2 * pair);
+  t.half = 2 * pair + 1 == mt_e;
+  t.valid = t.half || idx < mt_e;
+  t.m_tile = p.mtile_off[e] + (idx < mt_e ? idx : 2 * pair);
   return t;
 }
 
@@ -143,7 +155,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       bool ok = true;
       for (int tile = cluster; ok && tile < total_tiles; tile += n_clusters) {
         const PairTile t = decode_pair_tile(tile, p, rank);
-        const int a_row = t.m_tile * BM;
+        const int a_row = t.m_tile * BM + (t.half ? rank * (BM / 2) : 0);
         const int b_row = t.e * p.b_rows_per_expert + t.n * BN + rank * HALF_ROWS;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           const int stage = static_cast<int>(issued % STAGES);
@@ -177,6 +189,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int tile = cluster; ok && tile < total_tiles; tile += n_clusters) {
+        const uint32_t idesc = decode_pair_tile(tile, p, 0).half ? IDESC_HALF : IDESC;
         if (!mbar_wait_cluster(&tempty[acc], p.test_stall ? acc_phase : acc_phase ^ 1u, p.wait_limit_ns)) {
           set_error(p.err, kErrTimeout);
           break;
@@ -194,7 +207,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint64_t bdesc = sw128_desc(smem_u32(sb + stage * BH_BYTES));
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
-            tc_mma_f16_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, IDESC, (kb | k) != 0 ? 1u : 0u);
+            tc_mma_f16_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
           tc_commit_pair_multicast(&empty[stage], PAIR_MASK);
           if (++stage == STAGES) {
             stage = 0;
@@ -223,7 +236,61 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       tc_fence_after();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      if (t.valid) {
+      if (t.valid && KIND == kGateUpSwiGLU && t.half) {
+        // half pair: gate in lanes 0..63, up of the same rows in lanes 64..127
+        // (columns 0..127 both).  Warp q < 2 (gate) computes features 0..63
+        // of rows 32q.., warp q + 2 (up) features 64..127 of the same rows;
+        // per round j each hands the partner the 32-column chunk it needs
+        // through a shared-memory slot (rows of 128 B, 16-byte chunks
+        // swizzled by the row)
+        const bool gate_warp = q < 2;
+        uint8_t* mine = staging + ((q & 1) * 2 + (gate_warp ? 0 : 1)) * 4096;    // written by this warp
+        uint8_t* theirs = staging + ((q & 1) * 2 + (gate_warp ? 1 : 0)) * 4096;  // written by the partner
+        const int64_t row = static_cast<int64_t>(t.m_tile) * BM + rank * (BM / 2) + (q & 1) * 32 + lane;
+        uint16_t* out_row = static_cast<uint16_t*>(p.out) + row * p.ld_out + t.n * (BN / 2);
+#pragma unroll 1
+        for (int j = 0; j < 2; ++j) {
+          const int give = (gate_warp ? 2 + j : j) * 32;  // chunk the partner computes with
+          const int keep = (gate_warp ? j : 2 + j) * 32;  // chunk this warp computes
+          uint32_t v[32];
+          tmem_load32(tbase + give, v);
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(mine + lane * 128 + 16 * (c ^ (lane & 7))) =
+                make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+          tmem_load32(tbase + keep, v);
+          named_bar_sync(EPI_BAR, EPI_WARPS * 32);
+          uint32_t w[32];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 x = *reinterpret_cast<const uint4*>(theirs + lane * 128 + 16 * (c ^ (lane & 7)));
+            w[4 * c] = x.x;
+            w[4 * c + 1] = x.y;
+            w[4 * c + 2] = x.z;
+            w[4 * c + 3] = x.w;
+          }
+          named_bar_sync(EPI_BAR, EPI_WARPS * 32);
+          // gate warp: v = gate, w = up; up warp: v = up, w = gate
+          uint32_t h[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float g0 = __uint_as_float(gate_warp ? v[2 * i] : w[2 * i]);
+            const float u0 = __uint_as_float(gate_warp ? w[2 * i] : v[2 * i]);
+            const float g1 = __uint_as_float(gate_warp ? v[2 * i + 1] : w[2 * i + 1]);
+            const float u1 = __uint_as_float(gate_warp ? w[2 * i + 1] : v[2 * i + 1]);
+            h[i] = pack_bf16x2(silu(g0) * u0, silu(g1) * u1);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(out_row + keep);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+        }
+      } else if (t.valid) {
+        // this lane's row within the m-tile, and the accumulator columns it
+        // holds: all 256 for a full pair; for a half pair 128 of them, the
+        // weight rows [128 (q / 2), +128) of the tile in columns 0..127
+        const int row_in = t.half ? rank * (BM / 2) + (q & 1) * 32 : q * 32;
+        const int ncols = t.half ? BN / 2 : BN;
+        const int col0 = t.half ? (q >> 1) * (BN / 2) : 0;
         if constexpr (KIND == kGateUpSwiGLU) {
           const int64_t row = static_cast<int64_t>(t.m_tile) * BM + q * 32 + lane;
           uint16_t* out_row = static_cast<uint16_t*>(p.out) + row * p.ld_out + t.n * (BN / 2);
@@ -247,7 +314,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           // combine fused: the lane's row adds its gate-weighted output into
           // its token's accumulator row (fp32 reductions performed in L2);
           // padding rows past the expert's count add nothing
-          const int local = (t.m_tile - p.mtile_off[t.e]) * BM + q * 32 + lane;
+          const int local = (t.m_tile - p.mtile_off[t.e]) * BM + row_in + lane;
           const bool live = local < p.counts[t.e];
           float wt = 0.f;
           float* dst = p.comb_acc;
@@ -257,10 +324,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             int sl = 0;
             while (sl + 1 < p.top_k && p.comb_ids[pr + sl] != t.e) ++sl;
             wt = p.comb_w[pr + sl];
-            dst += static_cast<int64_t>(tk) * p.ld_out + t.n * BN;
+            dst += static_cast<int64_t>(tk) * p.ld_out + t.n * BN + col0;
           }
 #pragma unroll 1
-          for (int c0 = 0; c0 < BN; c0 += 32) {
+          for (int c0 = 0; c0 < ncols; c0 += 32) {
             uint32_t r[32];
             tmem_load32(tbase + c0, r);
             if (live) {
@@ -271,9 +338,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
           }
         } else {
-          const int row0 = t.m_tile * BM + q * 32;
+          const int row0 = t.m_tile * BM + row_in;
 #pragma unroll 1
-          for (int c0 = 0; c0 < BN; c0 += 32, ++n_stores) {
+          for (int c0 = 0; c0 < ncols; c0 += 32, ++n_stores) {
             uint32_t r[32];
             tmem_load32(tbase + c0, r);
             uint8_t* buf = staging + (q * 2 + (n_stores & 1)) * 4096;
@@ -288,7 +355,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              tma_store_2d(&tm_out, buf, t.n * BN + c0, row0);
+              tma_store_2d(&tm_out, buf, t.n * BN + col0 + c0, row0);
               bulk_commit_group();
             }
           }

@@ -264,8 +264,8 @@ PAIR_SMALL = ["tiny", "ragged_mid", "one_expert", "k_equals_E", "skewed_small", 
 @pytest.mark.parametrize("name", PAIR_SMALL)
 def test_pair_mma_path_small(name, monkeypatch):
     """CB_MOE_PAIR=1: bf16 expert GEMMs on CTA pairs with the 2-SM MMA
-    (M = 256 over two m-tiles of one expert); odd m-tile counts leave the
-    second CTA of a pair without rows to store."""
+    (M = 256 over two m-tiles of one expert); an expert's last m-tile without
+    a partner runs the M = 128 form, 64 of its rows on each CTA."""
     monkeypatch.setenv("CB_MOE_PAIR", "1")
     rep = gh.full_check(synth.make_layer(SMALL[name]))
     print(name, "pair", rep)
