@@ -18,6 +18,9 @@ SMALL = {
     # skewed bias: most of the 128 experts get no rows
     "skewed_small": synth.custom_shape("skewed_small", T=1000, d=256, f=256, E=128, k=4, bias=True, seed=24),
     "e256_k16": synth.custom_shape("e256_k16", T=257, d=256, f=256, E=256, k=16, seed=25),
+    # wide routers on a handful of tokens: the cooperative dispatch with 1 and 3 blocks
+    "one_token_e32": synth.custom_shape("one_token_e32", T=1, d=256, f=256, E=32, k=4, seed=37),
+    "three_tokens_e64": synth.custom_shape("three_tokens_e64", T=3, d=512, f=256, E=64, k=6, seed=38),
     "odd_T": synth.custom_shape("odd_T", T=1, d=512, f=512, E=8, k=2, seed=26),
     # int8 experts with per-channel scales: several tiles, ragged tails
     "int8_mid": synth.custom_shape("int8_mid", T=300, d=512, f=768, E=8, k=2, wdtype="int8", seed=27),
