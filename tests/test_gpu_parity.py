@@ -19,6 +19,8 @@ SMALL = {
     "skewed_small": synth.custom_shape("skewed_small", T=1000, d=256, f=256, E=128, k=4, bias=True, seed=24),
     "e256_k16": synth.custom_shape("e256_k16", T=257, d=256, f=256, E=256, k=16, seed=25),
     # wide routers on a handful of tokens: the cooperative dispatch with 1 and 3 blocks
+    # about 300 rows per expert: three m-tiles, a full CTA pair and a half pair
+    "three_mtiles": synth.custom_shape("three_mtiles", T=600, d=512, f=768, E=4, k=2, seed=39),
     "one_token_e32": synth.custom_shape("one_token_e32", T=1, d=256, f=256, E=32, k=4, seed=37),
     "three_tokens_e64": synth.custom_shape("three_tokens_e64", T=3, d=512, f=256, E=64, k=6, seed=38),
     "odd_T": synth.custom_shape("odd_T", T=1, d=512, f=512, E=8, k=2, seed=26),
@@ -261,7 +263,7 @@ def test_graph_replay_matches_direct_launches():
         gl.close()
 
 
-PAIR_SMALL = ["tiny", "ragged_mid", "one_expert", "k_equals_E", "skewed_small", "e256_k16", "odd_T"]
+PAIR_SMALL = ["tiny", "ragged_mid", "one_expert", "k_equals_E", "skewed_small", "e256_k16", "odd_T", "three_mtiles"]
 
 
 @pytest.mark.parametrize("name", PAIR_SMALL)
