@@ -175,19 +175,23 @@ CB_API cb_status_t cb_moe_init(const cb_moe_config_t *cfg, const cb_moe_weights_
  * reported later by cb_moe_last_error.
  */
 CB_API cb_status_t cb_moe_forward(cb_moe_t *h, const void *x, void *out, void *stream);
+/* The forwards of one handle share its workspace.  Each waits for the
+ * handle's previous forward, on whatever stream that one ran, unless `stream`
+ * is being captured into a graph (then the caller's graph orders them). */
 
 /* Same pass with the combine storing fp32 instead of bf16: out fp32 [T][d]. */
 CB_API cb_status_t cb_moe_forward_f32out(cb_moe_t *h, const void *x, float *out, void *stream);
 
 /*
- * Same pass from host memory: copies x_host (bf16 [T][d]) to a handle-owned
- * device buffer and runs cb_moe_forward, all on `stream`.  When out_host is
- * page-locked memory that CUDA maps into the device's address space
- * (cudaHostAlloc / cudaHostRegister, as torch's pin_memory does), the combine
- * writes the bf16 result straight into it; otherwise the result goes to a
- * handle-owned device buffer and is copied back.  Asynchronous when both host
- * buffers are pinned; the caller synchronises the stream before reading
- * out_host.
+ * Same pass from host memory: x_host (bf16 [T][d]) in, out_host (bf16 [T][d])
+ * back.  The input copy, the layer and the output copy run on three streams
+ * of the handle, through two handle-owned device staging slots that
+ * successive calls alternate between, so one call's copies run beside the
+ * next or previous call's layer.  The call does not wait for earlier work on
+ * `stream`; later work on `stream` waits for out_host to be written.  With
+ * page-locked host buffers the call returns before the copies finish: both
+ * buffers must stay untouched until `stream` has been synchronised.
+ * CB_ERR_UNSUPPORTED while `stream` is being captured into a graph.
  */
 CB_API cb_status_t cb_moe_forward_host(cb_moe_t *h, const void *x_host, void *out_host, void *stream);
 

@@ -46,7 +46,15 @@ struct cb_moe {
   int* err;
   unsigned int* coop_bar;  // grid barrier of the cooperative dispatch
   int32_t coop_blocks;     // > 0: the dispatch's own ranking runs as one cooperative launch
-  uint16_t *x_stage, *out_stage;
+  uint16_t *x_stage[2], *out_stage[2];  // host-buffer forwards: double-buffered device copies of x and out
+  // Host-buffer forwards run on the handle's own streams: the copy of x in,
+  // the layer, the copy of out back.  Successive calls alternate between the
+  // two staging slots, so one call's copies overlap another call's layer.
+  cudaStream_t hs_in, hs_comp, hs_out;
+  cudaEvent_t hin_done[2], hfwd_done[2], hout_done[2];
+  int host_slot;
+  cudaEvent_t ev_last;     // completion of the last forward enqueued on this handle
+  bool last_valid;
   int32_t max_mtiles, n_chunks;
   cudaEvent_t ev[CB_N_STAGES + 1];
   bool timing;             // record the stage events in forwards now
@@ -62,7 +70,7 @@ struct cb_moe {
     const void* b;
     bool timing;           // captured with the stage events
     cudaGraphExec_t exec;
-  } graphs[3];             // bf16 forward, fp32-out forward, host-buffer forward
+  } graphs[4];             // bf16 forward, fp32-out forward, host-buffer forward (two staging slots)
   bool gather_a;           // gate/up GEMM gathers its rows from x (no Xp copy)
   bool int8_tm;            // int8 GEMMs convert their weights into tensor memory
   bool use_pdl;            // programmatic dependent launch between the forward's kernels
@@ -133,8 +141,8 @@ Layout plan(const cb_moe_config_t& c) {
   L.off_inv = take(M * 4);
   L.off_err = take(64);
   L.off_bar = take(64);
-  L.off_xs = take(T * d * 2);
-  L.off_os = take(T * d * 2);
+  L.off_xs = take(2 * T * d * 2);
+  L.off_os = take(2 * T * d * 2);
   L.total = o;
   return L;
 }
@@ -476,6 +484,62 @@ cb_status_t check_forward_args(const cb_moe_t* h, const void* x, const void* out
   return CB_OK;
 }
 
+bool create_sync_objects(cb_moe_t* h) {
+  bool ok = true;
+  for (cudaStream_t* s : {&h->hs_in, &h->hs_comp, &h->hs_out})
+    ok = ok && cudaStreamCreateWithFlags(s, cudaStreamNonBlocking) == cudaSuccess;
+  for (int i = 0; i < 2; ++i)
+    for (cudaEvent_t* e : {&h->hin_done[i], &h->hfwd_done[i], &h->hout_done[i]})
+      ok = ok && cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess;
+  ok = ok && cudaEventCreateWithFlags(&h->ev_last, cudaEventDisableTiming) == cudaSuccess;
+  // the events start out complete, so the first calls wait on nothing
+  for (int i = 0; ok && i < 2; ++i)
+    for (cudaEvent_t e : {h->hin_done[i], h->hfwd_done[i], h->hout_done[i]})
+      ok = ok && cudaEventRecord(e, h->hs_comp) == cudaSuccess;
+  return ok;
+}
+
+void destroy_sync_objects(cb_moe_t* h) {
+  for (cudaStream_t s : {h->hs_in, h->hs_comp, h->hs_out})
+    if (s != nullptr) cudaStreamDestroy(s);
+  for (int i = 0; i < 2; ++i)
+    for (cudaEvent_t e : {h->hin_done[i], h->hfwd_done[i], h->hout_done[i]})
+      if (e != nullptr) cudaEventDestroy(e);
+  if (h->ev_last != nullptr) cudaEventDestroy(h->ev_last);
+}
+
+// Forwards of one handle share its workspace, so each waits for the last one
+// enqueued, whichever stream ran it, and then becomes the last one.  A stream
+// that the caller is capturing into a graph is left to the caller's ordering.
+bool capturing(cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return cs != cudaStreamCaptureStatusNone;
+}
+
+bool wait_last_forward(cb_moe_t* h, cudaStream_t s) {
+  return !h->last_valid || cudaStreamWaitEvent(s, h->ev_last, 0) == cudaSuccess;
+}
+
+bool mark_last_forward(cb_moe_t* h, cudaStream_t s) {
+  if (cudaEventRecord(h->ev_last, s) != cudaSuccess) return false;
+  h->last_valid = true;
+  return true;
+}
+
+// A device forward (bf16 or fp32 output) on the caller's stream.
+template <class Body>
+cb_status_t device_forward(cb_moe_t* h, int slot, const void* x, void* out, cudaStream_t s, Body body) {
+  const bool cap = capturing(s);
+  if (!cap && !wait_last_forward(h, s)) return CB_ERR_CUDA;
+  const cb_status_t st = run_graphed(h, slot, x, out, s, body);
+  if (st == CB_OK && !cap && !mark_last_forward(h, s)) return CB_ERR_CUDA;
+  return st;
+}
+
 }  // namespace
 
 extern "C" {
@@ -591,8 +655,10 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
   h->inv = reinterpret_cast<int32_t*>(b + L.off_inv);
   h->err = reinterpret_cast<int*>(b + L.off_err);
   h->coop_bar = reinterpret_cast<unsigned int*>(b + L.off_bar);
-  h->x_stage = reinterpret_cast<uint16_t*>(b + L.off_xs);
-  h->out_stage = reinterpret_cast<uint16_t*>(b + L.off_os);
+  for (int i = 0; i < 2; ++i) {
+    h->x_stage[i] = reinterpret_cast<uint16_t*>(b + L.off_xs) + static_cast<uint64_t>(i) * cfg->n_tokens * cfg->d_model;
+    h->out_stage[i] = reinterpret_cast<uint16_t*>(b + L.off_os) + static_cast<uint64_t>(i) * cfg->n_tokens * cfg->d_model;
+  }
 
   const uint64_t E = cfg->n_experts, d = cfg->d_model, f = cfg->d_ff;
   const uint64_t eb = int8w ? 1 : 2;                      // element bytes of the bf16 / int8 maps
@@ -749,9 +815,11 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
   h->timing = (cfg->flags & CB_FLAG_STAGE_TIMING) != 0;
   h->timing_events = h->timing;
   for (int i = 0; ok && h->timing && i <= CB_N_STAGES; ++i) ok = cudaEventCreate(&h->ev[i]) == cudaSuccess;
+  ok = ok && create_sync_objects(h);
   ok = ok && cudaDeviceSynchronize() == cudaSuccess;
   if (!ok) {
     cudaGetLastError();
+    destroy_sync_objects(h);
     cudaFree(h->block);
     delete h;
     return CB_ERR_CUDA;
@@ -767,8 +835,8 @@ cb_status_t cb_moe_forward(cb_moe_t* h, const void* x, void* out, void* stream) 
   if (fault_injected("launch")) return CB_ERR_CUDA;
   DeviceGuard guard(h->cfg.device);
   if (!guard.ok) return CB_ERR_CUDA;
-  return run_graphed(h, 0, x, out, static_cast<cudaStream_t>(stream),
-                     [&](cudaStream_t s) { return enqueue_forward(h, x, out, false, s); });
+  return device_forward(h, 0, x, out, static_cast<cudaStream_t>(stream),
+                        [&](cudaStream_t s) { return enqueue_forward(h, x, out, false, s); });
 }
 
 cb_status_t cb_moe_forward_f32out(cb_moe_t* h, const void* x, float* out, void* stream) {
@@ -778,42 +846,44 @@ cb_status_t cb_moe_forward_f32out(cb_moe_t* h, const void* x, float* out, void* 
   if (fault_injected("launch")) return CB_ERR_CUDA;
   DeviceGuard guard(h->cfg.device);
   if (!guard.ok) return CB_ERR_CUDA;
-  return run_graphed(h, 1, x, out, static_cast<cudaStream_t>(stream),
-                     [&](cudaStream_t s) { return enqueue_forward(h, x, out, true, s); });
+  return device_forward(h, 1, x, out, static_cast<cudaStream_t>(stream),
+                        [&](cudaStream_t s) { return enqueue_forward(h, x, out, true, s); });
 }
-
-namespace {
-// Device address of host memory that CUDA maps into the device's address
-// space (pinned by cudaHostAlloc / cudaHostRegister), or nullptr (pageable
-// memory, or a pointer CUDA does not know).
-void* mapped_host_ptr(void* host) {
-  cudaPointerAttributes a;
-  if (cudaPointerGetAttributes(&a, host) != cudaSuccess) {
-    cudaGetLastError();
-    return nullptr;
-  }
-  if (a.type != cudaMemoryTypeHost || a.devicePointer == nullptr || !aligned16(a.devicePointer)) return nullptr;
-  return a.devicePointer;
-}
-}  // namespace
 
 cb_status_t cb_moe_forward_host(cb_moe_t* h, const void* x_host, void* out_host, void* stream) {
   if (h == nullptr || x_host == nullptr || out_host == nullptr) return CB_ERR_INVALID_ARG;
   if (h->cfg.n_tokens == 0) return CB_OK;
   if (fault_injected("launch")) return CB_ERR_CUDA;
+  const cudaStream_t user = static_cast<cudaStream_t>(stream);
+  if (capturing(user)) return CB_ERR_UNSUPPORTED;  // the copies run on the handle's own streams
   DeviceGuard guard(h->cfg.device);
   if (!guard.ok) return CB_ERR_CUDA;
   const uint64_t bytes = static_cast<uint64_t>(h->cfg.n_tokens) * h->cfg.d_model * 2;
-  // A mapped output buffer receives the combine's rows directly over the
-  // host link, in place of a staging copy back after the combine.
-  void* out_mapped = mapped_host_ptr(out_host);
-  return run_graphed(h, 2, x_host, out_host, static_cast<cudaStream_t>(stream), [&](cudaStream_t s) {
-    if (cudaMemcpyAsync(h->x_stage, x_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return CB_ERR_CUDA;
-    const cb_status_t st2 = enqueue_forward(h, h->x_stage, out_mapped ? out_mapped : h->out_stage, false, s);
-    if (st2 != CB_OK || out_mapped != nullptr) return st2;
-    if (cudaMemcpyAsync(out_host, h->out_stage, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) return CB_ERR_CUDA;
-    return CB_OK;
+  const int b = h->host_slot;
+  h->host_slot ^= 1;
+  // 1. x into staging slot b, once the layer that last read the slot is done
+  if (cudaStreamWaitEvent(h->hs_in, h->hfwd_done[b], 0) != cudaSuccess ||
+      cudaMemcpyAsync(h->x_stage[b], x_host, bytes, cudaMemcpyHostToDevice, h->hs_in) != cudaSuccess ||
+      cudaEventRecord(h->hin_done[b], h->hs_in) != cudaSuccess)
+    return CB_ERR_CUDA;
+  // 2. the layer, after its input copy, after the copy out of the slot's
+  // previous result, and after the handle's last forward
+  if (cudaStreamWaitEvent(h->hs_comp, h->hin_done[b], 0) != cudaSuccess ||
+      cudaStreamWaitEvent(h->hs_comp, h->hout_done[b], 0) != cudaSuccess || !wait_last_forward(h, h->hs_comp))
+    return CB_ERR_CUDA;
+  const cb_status_t st = run_graphed(h, 2 + b, h->x_stage[b], h->out_stage[b], h->hs_comp, [&](cudaStream_t s) {
+    return enqueue_forward(h, h->x_stage[b], h->out_stage[b], false, s);
   });
+  if (st != CB_OK) return st;
+  if (cudaEventRecord(h->hfwd_done[b], h->hs_comp) != cudaSuccess || !mark_last_forward(h, h->hs_comp))
+    return CB_ERR_CUDA;
+  // 3. out back to the host, then the caller's stream waits for it
+  if (cudaStreamWaitEvent(h->hs_out, h->hfwd_done[b], 0) != cudaSuccess ||
+      cudaMemcpyAsync(out_host, h->out_stage[b], bytes, cudaMemcpyDeviceToHost, h->hs_out) != cudaSuccess ||
+      cudaEventRecord(h->hout_done[b], h->hs_out) != cudaSuccess ||
+      cudaStreamWaitEvent(user, h->hout_done[b], 0) != cudaSuccess)
+    return CB_ERR_CUDA;
+  return CB_OK;
 }
 
 cb_status_t cb_moe_routing(const cb_moe_t* h, cb_routing_view_t* v) {
@@ -866,6 +936,7 @@ cb_status_t cb_moe_free(cb_moe_t* h) {
       if (h->ev[i] != nullptr) cudaEventDestroy(h->ev[i]);
     for (auto& g : h->graphs)
       if (g.exec != nullptr) cudaGraphExecDestroy(g.exec);
+    destroy_sync_objects(h);
     if (cudaFree(h->block) != cudaSuccess) st = CB_ERR_CUDA;
   }
   delete h;

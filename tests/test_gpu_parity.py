@@ -79,6 +79,37 @@ def test_deterministic_and_host_entry_point():
         gl.close()
 
 
+def test_host_forwards_pipelined():
+    """Back-to-back host-buffer forwards of different inputs (their copies overlap the
+    neighbouring calls' layers through the two staging slots), with a device forward
+    on another stream in between: every result equals the device forward of its input."""
+    layer = synth.make_layer(SMALL["ragged_mid"])
+    gl = gh.GpuLayer(layer)
+    try:
+        gen = torch.Generator().manual_seed(4)
+        xs = [gl.x[torch.randperm(gl.T, generator=gen).to(gl.x.device)].contiguous() for _ in range(5)]
+        refs = []
+        for x in xs:
+            gl.m.forward(x, gl.out)
+            torch.cuda.synchronize()
+            refs.append(gl.out.clone().view(torch.int16).cpu())
+        xh = [x.view(torch.int16).cpu().pin_memory() for x in xs]
+        oh = [torch.empty_like(a).pin_memory() for a in xh]
+        side = torch.cuda.Stream()
+        dev_out = torch.empty_like(gl.out)
+        for i in range(5):
+            gl.m.forward_host(xh[i], oh[i])
+            if i == 2:
+                with torch.cuda.stream(side):
+                    gl.m.forward(xs[0], dev_out, stream=side)
+        torch.cuda.synchronize()
+        for i in range(5):
+            assert torch.equal(oh[i], refs[i]), i
+        assert torch.equal(dev_out.view(torch.int16).cpu(), refs[0])
+    finally:
+        gl.close()
+
+
 def test_token_permutation_equivariance():
     layer = synth.make_layer(SMALL["ragged_mid"])
     gl = gh.GpuLayer(layer)
