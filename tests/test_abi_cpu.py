@@ -28,6 +28,18 @@ def test_header_declares_the_abi():
     assert declared_symbols() == sorted(cb.ABI_SYMBOLS)
 
 
+def test_header_constants_match_the_binding():
+    """Every CB_FLAG_* and the weight-format, router-mode and status enumerators of the
+    header have the values the Python binding uses."""
+    text = open(HEADER).read()
+    flags = {n: int(v, 16) for n, v in re.findall(r"#define\s+(CB_FLAG_\w+)\s+(0x[0-9a-fA-F]+)u", text)}
+    assert flags and all(getattr(cb, n) == v for n, v in flags.items()), flags
+    enums = dict((n, int(v)) for n, v in re.findall(r"\b(CB_(?:W|ROUTER|OK|ERR)\w*)\s*=\s*(\d+)", text))
+    for name in ("CB_W_BF16", "CB_W_INT8", "CB_W_INT4", "CB_W_FP8", "CB_OK", "CB_ERR_TIMEOUT", "CB_ERR_DEVICE"):
+        assert name in enums and getattr(cb, name) == enums[name], name
+    assert cb.WDTYPES == {"bf16": 0, "int8": 1, "int4": 2, "fp8": 3}
+
+
 def test_library_exports_every_declared_symbol(lib):
     raw = ctypes.CDLL(cb.LIB_PATH)
     for name in declared_symbols():
@@ -57,6 +69,10 @@ def cfg(**kw):
     (dict(n_experts=257, top_k=2), cb.CB_ERR_UNSUPPORTED),
     (dict(n_experts=32, top_k=17), cb.CB_ERR_UNSUPPORTED),
     (dict(wdtype=5), cb.CB_ERR_INVALID_ARG),
+    (dict(wdtype=4), cb.CB_ERR_INVALID_ARG),
+    (dict(wdtype=3), cb.CB_OK),
+    (dict(flags=0x8), cb.CB_OK),
+    (dict(flags=0x10), cb.CB_ERR_INVALID_ARG),
     (dict(flags=0x80), cb.CB_ERR_INVALID_ARG),
     (dict(router_mode=1), cb.CB_OK),
     (dict(router_mode=2, top_k=1, hash_dims=8), cb.CB_OK),
@@ -79,6 +95,18 @@ def test_device_bytes_cover_the_workspace(lib):
     assert st == cb.CB_OK
     weights = 3 * 8 * 4096 * 14336 * 2
     assert weights < nbytes < weights + 2 * 10**9
+
+
+def test_device_bytes_by_weight_format(lib):
+    """fp8 and int8 experts take one byte per weight (plus the same fp32 scales), int4 half a
+    byte plus uint8 zero points, bf16 two bytes."""
+    big = dict(n_tokens=64, d_model=1024, d_ff=2048, n_experts=8, top_k=2)
+    sizes = {w: cb.cb_moe_device_bytes(cfg(wdtype=w, **big)) for w in (0, 1, 2, 3)}
+    assert all(st == cb.CB_OK for st, _ in sizes.values())
+    n_w = 3 * 8 * 1024 * 2048
+    assert sizes[3][1] == sizes[1][1]
+    assert abs((sizes[0][1] - sizes[1][1]) - n_w) < 64 * 1024 + 8 * 3 * 2048 * 4
+    assert sizes[2][1] < sizes[1][1]
 
 
 def test_device_bytes_hold_the_hash_projection(lib):
