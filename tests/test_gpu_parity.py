@@ -110,6 +110,37 @@ def test_host_forwards_pipelined():
         gl.close()
 
 
+def test_forwards_inside_a_caller_graph():
+    """A device forward captured into the caller's own CUDA graph replays to the same
+    bits (the handle's ordering event is left to the caller's graph); the host-buffer
+    forward, whose copies run on the handle's streams, refuses a capturing stream."""
+    import mixture_experts_router_gb300 as cb
+    layer = synth.make_layer(SMALL["ragged_mid"])
+    gl = gh.GpuLayer(layer)
+    try:
+        gl.run(f32=False)
+        ref = gl.out.clone()
+        out = torch.zeros_like(gl.out)
+        s = torch.cuda.Stream()
+        xh = torch.from_numpy(layer.x.view(np.int16)).pin_memory()
+        oh = torch.empty_like(xh).pin_memory()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            gl.m.forward(gl.x, out, stream=s)
+            st = cb.cb_moe_forward_host(gl.m.handle, xh.data_ptr(), oh.data_ptr(), s.cuda_stream)
+        assert st == cb.CB_ERR_UNSUPPORTED
+        for _ in range(2):
+            out.zero_()
+            g.replay()
+            torch.cuda.synchronize()
+            assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+        assert gl.m.last_error() == cb.CB_OK
+        gl.run(f32=False)                  # the handle still runs outside the graph
+        assert torch.equal(gl.out.view(torch.int16), ref.view(torch.int16))
+    finally:
+        gl.close()
+
+
 def test_token_permutation_equivariance():
     layer = synth.make_layer(SMALL["ragged_mid"])
     gl = gh.GpuLayer(layer)
