@@ -34,8 +34,10 @@
  *    device, 16-byte aligned; "host" pointers are ordinary host memory
  *    (pinned for asynchronous copies).
  *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
- *    stream).  All work is enqueued on it; no call below synchronises the
- *    device except cb_moe_init, cb_moe_free and cb_moe_last_error.
+ *    stream).  Work is enqueued on it (the host-buffer forward uses the
+ *    handle's own streams and makes `stream` wait for its result); no call
+ *    below synchronises the device except cb_moe_init, cb_moe_free,
+ *    cb_moe_last_error and cb_moe_check_guards.
  *  - Errors in arguments are reported before anything is enqueued.  A
  *    non-zero status never leaves a partial forward behind.
  *  - A handle is not thread safe; one forward may be in flight per handle
@@ -117,6 +119,10 @@ typedef enum { CB_ROUTER_SOFTMAX_TOPK = 0, CB_ROUTER_RAW_LOGITS = 1, CB_ROUTER_H
                                       forward finishes (its output is garbage)
                                       and cb_moe_last_error returns
                                       CB_ERR_TIMEOUT                            */
+#define CB_FLAG_GUARDS 0x10u       /* testing and debugging: a 4096-byte band of
+                                      0xA5 follows every workspace region;
+                                      cb_moe_check_guards reports whether a
+                                      kernel wrote into one                     */
 #define CB_FLAG_TEST_STALL_DISPATCH 0x8u /* test only: the cooperative dispatch's
                                       grid barrier waits for one block more
                                       than the launch has, bounded to 1 ms:
@@ -238,6 +244,12 @@ CB_API cb_status_t cb_moe_set_stage_timing(cb_moe_t *h, int32_t on);
 /* Synchronise the device, return the handle's device status word (CB_OK,
  * CB_ERR_TIMEOUT or CB_ERR_DEVICE) and clear it. */
 CB_API cb_status_t cb_moe_last_error(cb_moe_t *h);
+
+/* On a handle created with CB_FLAG_GUARDS: synchronises the device and checks
+ * every guard band.  CB_OK when all are intact, CB_ERR_DEVICE when a byte of
+ * one changed (a kernel wrote past the end of a workspace region),
+ * CB_ERR_INVALID_ARG on a handle without guards. */
+CB_API cb_status_t cb_moe_check_guards(cb_moe_t *h);
 
 /*
  * Dispatch without any device allocation (the pages have no counterpart of

@@ -21,6 +21,7 @@ CB_FLAG_KEEP_LOGITS = 0x1
 CB_FLAG_STAGE_TIMING = 0x2
 CB_FLAG_TEST_STALL = 0x4
 CB_FLAG_TEST_STALL_DISPATCH = 0x8
+CB_FLAG_GUARDS = 0x10
 CB_N_STAGES = 5
 STAGE_NAMES = ("router", "dispatch", "gateup_gemm", "down_gemm", "combine")
 
@@ -28,7 +29,7 @@ STAGE_NAMES = ("router", "dispatch", "gateup_gemm", "down_gemm", "combine")
 ABI_SYMBOLS = ("cb_moe_init", "cb_moe_forward", "cb_moe_forward_f32out", "cb_moe_forward_host",
                "cb_moe_routing", "cb_moe_stage_times", "cb_moe_last_error", "cb_moe_device_bytes",
                "cb_moe_free", "cb_status_string", "cb_moe_dispatch_noalloc", "cb_moe_kernels_per_forward",
-               "cb_moe_set_stage_timing")
+               "cb_moe_set_stage_timing", "cb_moe_check_guards")
 
 
 CB_ROUTER_SOFTMAX_TOPK, CB_ROUTER_RAW_LOGITS, CB_ROUTER_HASH = 0, 1, 2
@@ -83,6 +84,7 @@ def load_library(path: str = LIB_PATH):
     lib.cb_moe_routing.argtypes = [vp, ctypes.POINTER(cb_routing_view_t)]
     lib.cb_moe_stage_times.argtypes = [vp, ctypes.POINTER(ctypes.c_float), ctypes.c_int32]
     lib.cb_moe_last_error.argtypes = [vp]
+    lib.cb_moe_check_guards.argtypes = [vp]
     lib.cb_moe_device_bytes.argtypes = [ctypes.POINTER(cb_moe_config_t), ctypes.POINTER(ctypes.c_uint64)]
     lib.cb_moe_free.argtypes = [vp]
     lib.cb_moe_kernels_per_forward.argtypes = [vp, ctypes.POINTER(i32)]
@@ -92,7 +94,7 @@ def load_library(path: str = LIB_PATH):
     lib.cb_moe_dispatch_noalloc.restype = i32
     for name in ("cb_moe_init", "cb_moe_forward", "cb_moe_forward_f32out", "cb_moe_forward_host",
                  "cb_moe_routing", "cb_moe_stage_times", "cb_moe_last_error", "cb_moe_device_bytes",
-                 "cb_moe_free", "cb_moe_kernels_per_forward", "cb_moe_set_stage_timing"):
+                 "cb_moe_free", "cb_moe_kernels_per_forward", "cb_moe_set_stage_timing", "cb_moe_check_guards"):
         getattr(lib, name).restype = i32
     lib.cb_status_string.argtypes = [i32]
     lib.cb_status_string.restype = ctypes.c_char_p
@@ -139,6 +141,10 @@ def cb_moe_stage_times(handle):
 
 def cb_moe_last_error(handle) -> int:
     return load_library().cb_moe_last_error(handle)
+
+
+def cb_moe_check_guards(handle) -> int:
+    return load_library().cb_moe_check_guards(handle)
 
 
 def cb_moe_device_bytes(cfg: cb_moe_config_t):
@@ -266,6 +272,10 @@ class MoELayer:
 
     def last_error(self) -> int:
         return cb_moe_last_error(self.handle)
+
+    def check_guards(self) -> int:
+        """CB_OK when every guard band of a CB_FLAG_GUARDS handle is intact."""
+        return cb_moe_check_guards(self.handle)
 
     def kernels_per_forward(self) -> int:
         st, n = cb_moe_kernels_per_forward(self.handle)

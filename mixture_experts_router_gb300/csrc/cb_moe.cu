@@ -15,6 +15,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <new>
+#include <vector>
 
 #include "cb_moe.h"
 #include "internal.h"
@@ -46,6 +47,8 @@ struct cb_moe {
   int* err;
   unsigned int* coop_bar;  // grid barrier of the cooperative dispatch
   int32_t coop_blocks;     // > 0: the dispatch's own ranking runs as one cooperative launch
+  uint64_t guard_off[48];  // CB_FLAG_GUARDS: offsets of the guard bands in the block
+  int32_t n_guards;
   uint16_t *x_stage[2], *out_stage[2];  // host-buffer forwards: double-buffered device copies of x and out
   // Host-buffer forwards run on the handle's own streams: the copy of x in,
   // the layer, the copy of out back.  Successive calls alternate between the
@@ -83,7 +86,15 @@ struct cb_moe {
 
 namespace {
 
+// CB_FLAG_GUARDS: a band of this many bytes of kGuardByte after every
+// non-empty workspace region
+constexpr uint64_t kGuardBytes = 4096;
+constexpr int kGuardByte = 0xA5;
+constexpr int kMaxGuards = 48;
+
 struct Layout {
+  uint64_t guard_off[kMaxGuards];
+  int32_t n_guards;
   uint64_t off_wr, off_bias, off_wgu, off_wd, off_sg, off_su, off_sd, off_wh, off_zg, off_zu, off_zd;
   uint64_t off_xp, off_hb, off_y, off_ids, off_w, off_logits, off_rpart, off_chunk, off_counts, off_offsets, off_mtile_off,
       off_mtile_expert, off_ptile_off, off_ptile_expert, off_tok, off_inv, off_err, off_bar, off_xs, off_os;
@@ -103,9 +114,14 @@ Layout plan(const cb_moe_config_t& c) {
   L.n_chunks = static_cast<int32_t>((M + kDispatchChunk - 1) / kDispatchChunk);
   const uint64_t mpad = static_cast<uint64_t>(L.max_mtiles) * kTileM;
   uint64_t o = 0;
+  const uint64_t guard = (c.flags & CB_FLAG_GUARDS) ? kGuardBytes : 0;
   auto take = [&](uint64_t bytes) {
     const uint64_t at = o;
     o = align256(o + bytes);
+    if (guard != 0 && bytes != 0 && L.n_guards < kMaxGuards) {
+      L.guard_off[L.n_guards++] = o;
+      o += guard;
+    }
     return at;
   };
   L.off_wr = take(E * d * 2);
@@ -161,7 +177,7 @@ cb_status_t validate_config(const cb_moe_config_t* c) {
       (c->top_k != 1 || c->hash_dims < 1 || c->hash_dims > CB_MAX_HASH_DIMS))
     return CB_ERR_INVALID_ARG;
   if ((c->flags & ~(CB_FLAG_KEEP_LOGITS | CB_FLAG_STAGE_TIMING | CB_FLAG_TEST_STALL |
-                   CB_FLAG_TEST_STALL_DISPATCH)) != 0)
+                   CB_FLAG_TEST_STALL_DISPATCH | CB_FLAG_GUARDS)) != 0)
     return CB_ERR_INVALID_ARG;
   // 32-bit row and tile indices everywhere
   const uint64_t M = static_cast<uint64_t>(c->n_tokens) * c->top_k;
@@ -615,6 +631,9 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
   const Layout L = plan(*cfg);
   cb_moe_t* h = new (std::nothrow) cb_moe_t();
   if (h == nullptr) return CB_ERR_OOM;
+  static_assert(sizeof(h->guard_off) / sizeof(h->guard_off[0]) == kMaxGuards, "guard table");
+  for (int i = 0; i < L.n_guards; ++i) h->guard_off[i] = L.guard_off[i];
+  h->n_guards = L.n_guards;
   h->cfg = *cfg;
   h->num_sms = prop.multiProcessorCount;
   h->max_mtiles = L.max_mtiles;
@@ -815,6 +834,9 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
   h->timing = (cfg->flags & CB_FLAG_STAGE_TIMING) != 0;
   h->timing_events = h->timing;
   for (int i = 0; ok && h->timing && i <= CB_N_STAGES; ++i) ok = cudaEventCreate(&h->ev[i]) == cudaSuccess;
+  // the guard bands last: the workspace memsets above span them
+  for (int i = 0; ok && i < h->n_guards; ++i)
+    ok = cudaMemset(h->block + h->guard_off[i], kGuardByte, kGuardBytes) == cudaSuccess;
   ok = ok && create_sync_objects(h);
   ok = ok && cudaDeviceSynchronize() == cudaSuccess;
   if (!ok) {
@@ -912,6 +934,20 @@ cb_status_t cb_moe_stage_times(cb_moe_t* h, float* ms, int32_t n) {
 cb_status_t cb_moe_set_stage_timing(cb_moe_t* h, int32_t on) {
   if (h == nullptr || !h->timing_events) return CB_ERR_INVALID_ARG;
   h->timing = on != 0;
+  return CB_OK;
+}
+
+cb_status_t cb_moe_check_guards(cb_moe_t* h) {
+  if (h == nullptr || h->n_guards == 0) return CB_ERR_INVALID_ARG;
+  DeviceGuard guard(h->cfg.device);
+  if (!guard.ok || cudaDeviceSynchronize() != cudaSuccess) return CB_ERR_CUDA;
+  std::vector<uint8_t> band(kGuardBytes);
+  for (int i = 0; i < h->n_guards; ++i) {
+    if (cudaMemcpy(band.data(), h->block + h->guard_off[i], kGuardBytes, cudaMemcpyDeviceToHost) != cudaSuccess)
+      return CB_ERR_CUDA;
+    for (uint8_t v : band)
+      if (v != kGuardByte) return CB_ERR_DEVICE;
+  }
   return CB_OK;
 }
 

@@ -72,7 +72,8 @@ def cfg(**kw):
     (dict(wdtype=4), cb.CB_ERR_INVALID_ARG),
     (dict(wdtype=3), cb.CB_OK),
     (dict(flags=0x8), cb.CB_OK),
-    (dict(flags=0x10), cb.CB_ERR_INVALID_ARG),
+    (dict(flags=0x10), cb.CB_OK),
+    (dict(flags=0x20), cb.CB_ERR_INVALID_ARG),
     (dict(flags=0x80), cb.CB_ERR_INVALID_ARG),
     (dict(router_mode=1), cb.CB_OK),
     (dict(router_mode=2, top_k=1, hash_dims=8), cb.CB_OK),
@@ -107,6 +108,15 @@ def test_device_bytes_by_weight_format(lib):
     assert sizes[3][1] == sizes[1][1]
     assert abs((sizes[0][1] - sizes[1][1]) - n_w) < 64 * 1024 + 8 * 3 * 2048 * 4
     assert sizes[2][1] < sizes[1][1]
+
+
+def test_device_bytes_with_guard_bands(lib):
+    """CB_FLAG_GUARDS adds a 4096-byte band after each non-empty workspace region."""
+    st, plain = cb.cb_moe_device_bytes(cfg())
+    st2, guarded = cb.cb_moe_device_bytes(cfg(flags=cb.CB_FLAG_GUARDS))
+    assert st == st2 == cb.CB_OK
+    extra = guarded - plain
+    assert extra % 4096 == 0 and 20 <= extra // 4096 <= 48
 
 
 def test_device_bytes_hold_the_hash_projection(lib):

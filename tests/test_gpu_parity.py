@@ -141,6 +141,39 @@ def test_forwards_inside_a_caller_graph():
         gl.close()
 
 
+GUARD_CASES = [
+    ("tiny", {}), ("odd_T", {}), ("ragged_mid", {"CB_MOE_PAIR": "1"}),
+    ("ragged_mid", {"CB_MOE_PAIR": "1", "CB_MOE_FUSED_COMBINE": "1"}), ("ragged_mid", {"CB_MOE_GATHER": "1"}),
+    ("three_mtiles", {"CB_MOE_PAIR": "1"}), ("skewed_small", {}), ("skewed_small", {"CB_MOE_DISPATCH": "split"}),
+    ("e256_k16", {}), ("one_token_e32", {}), ("int8_k6", {}), ("int8_mid", {"CB_MOE_INT8": "smem"}),
+    ("int4_k6", {}), ("fp8_mid", {}), ("hash", {}),
+]
+
+
+@pytest.mark.parametrize("name,env", GUARD_CASES, ids=[f"{n}-{'-'.join(e.values()) or 'default'}" for n, e in GUARD_CASES])
+def test_kernels_stay_inside_the_workspace(name, env, monkeypatch):
+    """With CB_FLAG_GUARDS a 4 KB band of 0xA5 follows every workspace region; after
+    bf16, fp32 and host-buffer forwards on every kernel path none of them has changed
+    (a check of out-of-range writes, with compute-sanitizer unavailable)."""
+    import mixture_experts_router_gb300 as cb
+    for k, v in env.items():
+        monkeypatch.setenv(k, v)
+    shape = synth.with_router(SMALL["ragged_mid"], "hash") if name == "hash" else SMALL[name]
+    layer = synth.make_layer(shape)
+    gl = gh.GpuLayer(layer, flags=cb.CB_FLAG_GUARDS)
+    try:
+        gl.run()
+        xh = torch.from_numpy(layer.x.view(np.int16)).pin_memory()
+        oh = torch.empty_like(xh).pin_memory()
+        gl.m.forward_host(xh, oh)
+        torch.cuda.synchronize()
+        assert gl.m.last_error() == cb.CB_OK
+        assert gl.m.check_guards() == cb.CB_OK
+        assert torch.equal(oh, gl.out.view(torch.int16).cpu())
+    finally:
+        gl.close()
+
+
 def test_token_permutation_equivariance():
     layer = synth.make_layer(SMALL["ragged_mid"])
     gl = gh.GpuLayer(layer)
