@@ -12,6 +12,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <new>
@@ -845,6 +846,23 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
     cudaFree(h->block);
     delete h;
     return CB_ERR_CUDA;
+  }
+  // CB_MOE_LOG=1: one line on stderr with the paths this handle runs
+  const char* lv = std::getenv("CB_MOE_LOG");
+  if (lv != nullptr && std::strcmp(lv, "1") == 0) {
+    static const char* const kW[] = {"bf16", "int8", "int4", "fp8"};
+    static const char* const kR[] = {"softmax", "raw", "hash"};
+    const char* router = cfg->router_mode == CB_ROUTER_HASH ? "hash" : h->router_tc ? "tcgen05" : "mma";
+    const char* dispatch = h->rank_block > 0 ? "router-ranked" : h->coop_blocks > 0 ? "cooperative" : "split";
+    const char* gemm = int8w ? (h->int8_tm ? "tensor-memory quantised" : "shared-memory int8")
+                             : (h->pair_gu || h->pair_dn) ? "cta-pair" : "single-cta";
+    std::fprintf(stderr,
+                 "cbmoe: T=%d d=%d f=%d E=%d k=%d weights=%s gate=%s router=%s dispatch=%s gemm=%s "
+                 "pair=%d/%d graphs=%d pdl=%d fused_combine=%d guards=%d workspace=%.1f MB sms=%d\n",
+                 cfg->n_tokens, cfg->d_model, cfg->d_ff, cfg->n_experts, cfg->top_k, kW[cfg->wdtype],
+                 kR[cfg->router_mode], router, dispatch, gemm, h->pair_gu ? 1 : 0, h->pair_dn ? 1 : 0,
+                 h->use_graphs ? 1 : 0, h->use_pdl ? 1 : 0, h->fused_combine ? 1 : 0, h->n_guards,
+                 static_cast<double>(L.total) / 1e6, h->num_sms);
   }
   *out = h;
   return CB_OK;

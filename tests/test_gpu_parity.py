@@ -174,6 +174,23 @@ def test_kernels_stay_inside_the_workspace(name, env, monkeypatch):
         gl.close()
 
 
+@pytest.mark.parametrize("name,expect", [
+    ("skewed_small", "T=1000 d=256 f=256 E=128 k=4 weights=bf16 gate=softmax router=tcgen05 dispatch=cooperative "
+                     "gemm=single-cta"),
+    ("ragged_mid", "T=300 d=512 f=768 E=8 k=2 weights=bf16 gate=softmax router=mma dispatch=router-ranked"),
+    ("fp8_mid", "weights=fp8 gate=softmax router=mma dispatch=router-ranked gemm=tensor-memory quantised"),
+])
+def test_init_log_line(name, expect, monkeypatch, capfd):
+    """CB_MOE_LOG=1: cb_moe_init prints one stderr line naming the paths the handle runs."""
+    monkeypatch.setenv("CB_MOE_LOG", "1")
+    gl = gh.GpuLayer(synth.make_layer(SMALL[name]))
+    try:
+        err = capfd.readouterr().err
+        assert "cbmoe: " in err and expect in err, err
+    finally:
+        gl.close()
+
+
 def test_token_permutation_equivariance():
     layer = synth.make_layer(SMALL["ragged_mid"])
     gl = gh.GpuLayer(layer)
