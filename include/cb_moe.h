@@ -261,7 +261,10 @@ CB_API cb_status_t cb_moe_check_guards(cb_moe_t *h);
  * writes counts[E], offsets[E+1], tok[T*k] and inv[T][k] exactly as the
  * dispatch of cb_moe_forward does (rows of expert e in ascending token
  * order).  `status` (device int32, or NULL) receives 0 or CB_ERR_DEVICE
- * (an id out of range) once the stream has run the call.  All pointers are
+ * (an id out of range) once the stream has run the call.  With status ==
+ * NULL that error is not reported anywhere: the call still returns CB_OK,
+ * and the pairs with bad ids are missing from tok and inv.  Pass a status
+ * word unless the ids are known to be in range.  All pointers are
  * caller-owned device memory, 4-byte aligned; the call is asynchronous on
  * `stream` and runs on the current device.
  *
@@ -270,8 +273,10 @@ CB_API cb_status_t cb_moe_check_guards(cb_moe_t *h);
  * without launching anything when
  *   ceil(T*k/2048)*E + (E+1) + ((T*k + 127*E)/128 + 1) + 1
  * 32-bit words exceed it (about T*k <= 2 million pairs at E = 256).  The
- * first call on each device looks the array's address up (and may load the
- * library's kernels there): make it before any stream capture.  All calls
+ * first call on each device (and the first after that device's context has
+ * changed, e.g. after cudaDeviceReset) looks the array's address up and sets
+ * a kernel attribute (no allocation; it may load the library's kernels onto
+ * the device): make it before any stream capture.  All calls
  * share the array, so calls that overlap on the GPU race: keep them on one
  * stream.  Returns CB_ERR_INVALID_ARG / CB_ERR_UNSUPPORTED / CB_ERR_ALIGNMENT
  * on bad arguments, CB_ERR_CUDA if a launch fails.

@@ -603,22 +603,21 @@ __global__ void __launch_bounds__(kCoopThreads) dispatch_coop(DispatchArgs a) {
 // dispatch_prepare, else the 48 KB a launch gets without it); its columns are
 // scanned by whole warps, where dispatch_scan walks each expert's chunks with
 // one thread.
-static void launch_chunk_scan(const DispatchArgs& a, int max_words, cudaStream_t s) {
+static cudaError_t launch_chunk_scan(const DispatchArgs& a, int max_words, cudaStream_t s) {
   if ((a.n_chunks + 1) * (a.E + 1) <= max_words && a.E <= 256) {
     DispatchArgs b = a;
     b.n_rank_blocks = a.n_chunks;
-    launch_kernel(dispatch_scan_blocks, 1, kScanThreads, (b.n_rank_blocks + 1) * (b.E + 1) * 4, s, b);
-  } else {
-    launch_kernel(dispatch_scan, 1, kThreads, 0, s, a);
+    return launch_kernel(dispatch_scan_blocks, 1, kScanThreads, (b.n_rank_blocks + 1) * (b.E + 1) * 4, s, b);
   }
+  return launch_kernel(dispatch_scan, 1, kThreads, 0, s, a);
 }
 
-cudaError_t launch_dispatch_ranks(const DispatchArgs& a, cudaStream_t s) {
+cudaError_t launch_dispatch_ranks(const DispatchArgs& a, int scan_words, cudaStream_t s) {
   if (a.n_chunks <= 0) return cudaSuccess;
-  launch_kernel(dispatch_count, a.n_chunks, kThreads, 0, s, a);
-  launch_chunk_scan(a, 12 * 1024, s);
-  launch_kernel(dispatch_scatter, a.n_chunks, kThreads, 0, s, a);
-  return cudaGetLastError();
+  cudaError_t e = launch_kernel(dispatch_count, a.n_chunks, kThreads, 0, s, a);
+  if (e == cudaSuccess) e = launch_chunk_scan(a, scan_words, s);
+  if (e == cudaSuccess) e = launch_kernel(dispatch_scatter, a.n_chunks, kThreads, 0, s, a);
+  return e;
 }
 
 cudaError_t dispatch_prepare() {

@@ -17,9 +17,14 @@
 //
 // In host code the array's name is only a host-side stand-in, so the device
 // address is looked up with cudaGetSymbolAddress once per device, with that
-// device current; the first call on each device does this set-up (which
-// may also load the library's kernels onto the device), so make that first
-// call before any stream capture.
+// device current.  The same set-up raises the shared-memory limit of the
+// block-scan kernel (cudaFuncSetAttribute, which allocates nothing), so the
+// call does not depend on a handle having been made on the device.  The
+// first call on each device does this set-up (which may also load the
+// library's kernels onto the device), so make that first call before any
+// stream capture.  The set-up is keyed on the device's current CUDA context
+// as well: after cudaDeviceReset the next call looks the address up again
+// in the new context.
 //
 // All calls share the one array and it keeps the last call's contents.
 // Every scratch word a call reads is written earlier in the same call, and
@@ -42,22 +47,55 @@ constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) int32_t g_dispatch_scratch[kScratchWords];
 
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
+// cuCtxGetCurrent through the runtime's driver entry points (the library
+// links no driver library), or nullptr if it cannot be had.
+CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+      cudaGetLastError();
+      return static_cast<CtxGetCurrentFn>(nullptr);
+    }
+    return reinterpret_cast<CtxGetCurrentFn>(p);
+  }();
+  return fn;
+}
+
+CUcontext current_context() {
+  CUcontext c = nullptr;
+  CtxGetCurrentFn fn = ctx_get_current();
+  if (fn == nullptr || fn(&c) != CUDA_SUCCESS) return nullptr;
+  return c;
+}
+
 // Device address of g_dispatch_scratch on `device` (the current device), or
-// nullptr when the lookup fails.  Looked up once per device.
+// nullptr when the set-up fails.  Set up once per device and context: the
+// address lookup, and the block scan's shared-memory limit.  Without a way to
+// name the context the set-up runs on every call.
 int32_t* scratch_on(int device) {
+  struct Entry {
+    CUcontext ctx;
+    int32_t* addr;
+  };
   static std::mutex mu;
-  static int32_t* addr[kMaxDevices] = {};
+  static Entry cache[kMaxDevices] = {};
   if (device < 0 || device >= kMaxDevices) return nullptr;
   std::lock_guard<std::mutex> lock(mu);
-  if (addr[device] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_dispatch_scratch) != cudaSuccess) {
-      cudaGetLastError();
-      return nullptr;
-    }
-    addr[device] = static_cast<int32_t*>(p);
+  Entry& en = cache[device];
+  const CUcontext before = current_context();
+  if (before != nullptr && en.ctx == before && en.addr != nullptr) return en.addr;
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_dispatch_scratch) != cudaSuccess || dispatch_prepare() != cudaSuccess) {
+    cudaGetLastError();
+    en = Entry{nullptr, nullptr};
+    return nullptr;
   }
-  return addr[device];
+  en = Entry{current_context(), static_cast<int32_t*>(p)};
+  return en.addr;
 }
 
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
@@ -115,5 +153,5 @@ extern "C" cb_status_t cb_moe_dispatch_noalloc(const int32_t* ids, int32_t n_tok
   a.tok = tok;
   a.inv = inv;
   a.err = err;
-  return launch_dispatch_ranks(a, s) == cudaSuccess ? CB_OK : CB_ERR_CUDA;
+  return launch_dispatch_ranks(a, kFusedScanWords, s) == cudaSuccess ? CB_OK : CB_ERR_CUDA;
 }

@@ -166,8 +166,11 @@ constexpr int64_t kCoopMaxPairs = 65536;
 // num_sms SMs (at most one per SM; 0 if none)
 int dispatch_coop_max_blocks(int num_sms);
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s);
-// histogram, prefix sums and ranks only (no row gather; x and xp unused)
-cudaError_t launch_dispatch_ranks(const DispatchArgs& a, cudaStream_t s);
+// histogram, prefix sums and ranks only (no row gather; x and xp unused);
+// the block scan is used up to scan_words words of shared memory
+// (kFusedScanWords once dispatch_prepare has run on the device); returns the
+// first launch's error, launching nothing after it
+cudaError_t launch_dispatch_ranks(const DispatchArgs& a, int scan_words, cudaStream_t s);
 
 // ----------------------------------------------------------------- combine
 struct CombineArgs {

@@ -1,22 +1,30 @@
-"""cb_moe_dispatch_noalloc against the dispatch of cb_moe_forward.
+"""cb_moe_dispatch_noalloc against the oracle's dispatch and the forward's own.
 
 The no-allocation entry point is for callers that cannot call cudaMalloc (for
 example a host program whose own allocator has reserved the GPU's memory).
 It keeps its scratch in one static device array that every call reuses, so
-this test makes two calls in a row on different routings and checks each
-against the existing entry point's dispatch, bit for bit (integer work).  It
-sits in a file of its own, collected last, and builds everything it needs, so
-it passes alone in a fresh process and after the other tests.
+these tests make calls in a row on different routings and check each one,
+bit for bit (integer work), against the oracle's dispatch of the same ids and
+against the dispatch inside cb_moe_forward.  One test runs in a child process
+that never creates a layer handle, at the sizes where the entry point's
+kernels change form.  The file is collected last and builds everything it
+needs, so it passes alone in a fresh process and after the other tests.
 """
+import os
+import subprocess
+import sys
+
 import numpy as np
 import pytest
 import torch
 
+import oracle
 import synth
 
 pytestmark = pytest.mark.gpu
 
 gh = pytest.importorskip("gpu_harness")
+HERE = os.path.dirname(os.path.abspath(__file__))
 
 
 def _routing_of_forward(shape):
@@ -47,16 +55,25 @@ def _noalloc(ids_np, E):
     return counts.cpu().numpy(), offsets.cpu().numpy(), tok.cpu().numpy(), inv.cpu().numpy().reshape(T, k)
 
 
-def test_noalloc_dispatch_matches_forward_twice_in_a_row():
+def test_noalloc_dispatch_matches_oracle_and_forward_twice_in_a_row():
     shapes = [synth.custom_shape("noalloc_a", T=3000, d=256, f=256, E=128, k=4, bias=True, seed=31),
               synth.custom_shape("noalloc_b", T=300, d=512, f=256, E=8, k=2, seed=32)]
-    for shape in shapes:       # two calls in a row; the second sees the first call's leftovers
+    for shape in shapes:       # calls in a row; the second sees the first call's leftovers
         r = _routing_of_forward(shape)
-        cnt, off, tok, inv = _noalloc(r["ids"], shape.E)
-        assert np.array_equal(cnt, r["counts"])
-        assert np.array_equal(off, r["offsets"])
-        assert np.array_equal(tok, r["tok"])
-        assert np.array_equal(inv, r["inv"])
+        want = oracle.dispatch(r["ids"], shape.E)
+        got = _noalloc(r["ids"], shape.E)
+        for g, w, f, name in zip(got, want, (r["counts"], r["offsets"], r["tok"], r["inv"]),
+                                 ("counts", "offsets", "tok", "inv")):
+            assert np.array_equal(g, w), name
+            assert np.array_equal(g, f), name
+
+
+def test_noalloc_in_a_process_without_handles():
+    """48 KB shared-memory band, the one-thread scan past the block scan, a
+    size near the scratch limit and an out-of-range id, in a fresh process."""
+    r = subprocess.run([sys.executable, os.path.join(HERE, "noalloc_fresh_process.py")], capture_output=True,
+                       text=True, timeout=600)
+    assert r.returncode == 0 and "NOALLOC_OK" in r.stdout, r.stdout + r.stderr
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
