@@ -6,8 +6,11 @@ One step = one forward of the whole layer over one batch of T tokens of the
 workload (default: the Mixtral-8x7B-shaped prefill layer, T=4096, d=4096,
 f=14336, E=8, top-2, bf16).  Inputs are seeded synthetic data resident in HBM;
 L2 is flushed (a 512 MB write) between timed steps, outside the timed events.
+After the headline layer the metric's other layers are timed the same way
+(decode-size weight streaming, the skewed 128-expert layer, the int8 layer)
+and reported under "workloads"; `--workloads none` skips them.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--workloads A,B|none] [--impl reference]
 
 Under torchrun each rank runs an independent replica of the layer on its own
 GPU over its own T tokens (weak scaling, no collective in the data path); the
@@ -34,6 +37,9 @@ sys.path.insert(0, ROOT)
 
 METRIC = "MoE-layer tokens/s; grouped-GEMM % of bf16 TC peak; decode weight GB/s % HBM"
 DEFAULT_WORKLOAD = "mixtral_prefill"
+# the metric's other layers: decode-size weight streaming, the skewed
+# 128-expert layer and the int8 layer
+EXTRA_WORKLOADS = ("mixtral_decode", "skewed", "int8")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 GEMM_SOURCES = [os.path.join(ROOT, "mixture_experts_router_gb300", "csrc", n)
                 for n in ("grouped_gemm.cu", "grouped_gemm_pair.cu")]
@@ -57,6 +63,10 @@ def parse_args(argv=None):
     p.add_argument("--e2e-steps", type=int, default=50)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU work of the oracle baseline")
+    p.add_argument("--workloads", default=",".join(EXTRA_WORKLOADS),
+                   help="further workloads timed after the headline one ('none' for the headline only)")
+    p.add_argument("--sub-cpu-seconds", type=float, default=4.0,
+                   help="target CPU work of each further workload's oracle sample")
     return p.parse_args(argv)
 
 
@@ -90,6 +100,8 @@ def algorithmic_work(shape, counts):
     return {
         "router_bytes": T * d * 2 + (shape.hash_dims if shape.router == "hash" else E) * d * 2 + T * k * 8,
         "dispatch_bytes": T * d * 2 + M * d * 2 + 16 * M,
+        # router and dispatch in one launch: x crosses HBM once
+        "route_dispatch_fused_bytes": T * d * 2 + E * d * 2 + T * k * 8 + M * d * 2 + 16 * M,
         "gateup_flops": 4 * d * f * M,
         "down_flops": 2 * d * f * M,
         "combine_bytes": M * d * 4 + 8 * M + T * d * 2,
@@ -260,7 +272,7 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded SplitMix64/Box-Muller, bf16 inputs)",
-            "config": config_block(shape, 0),
+            "config": config_block(shape, args.l2_flush_mb),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.get_threads(lib), "kind": "oracle",
                              "sample": f"{per_step} tokens per step of the {shape.T}-token batch"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -269,19 +281,86 @@ def run_reference(args):
 
 
 # ---------------------------------------------------------------- our arm
-def run_ours(args):
+def stage_report(shape, work, mean, names, pk, fused_rd=False):
+    """Per-stage times with their algorithmic rates and roofline fractions.
+    With fused_rd the router's launch also dispatches: the router stage holds
+    both and the dispatch stage is empty."""
+    hbm, tc_burst, tc_sus = pk["hbm_gbs"], pk["bf16_tflops"], pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+    stages = {}
+    for i, n in enumerate(names):
+        s = mean[i] / 1e3
+        if fused_rd and n == "router":
+            b = work["route_dispatch_fused_bytes"]
+            stages[n] = {"ms": mean[i], "gbs": b / s / 1e9, "frac_hbm": b / s / 1e9 / hbm,
+                         "about": "router and dispatch in one launch (x read from HBM once)"}
+        elif fused_rd and n == "dispatch":
+            stages[n] = {"ms": mean[i], "about": "in the router's launch"}
+        elif n in ("gateup_gemm", "down_gemm"):
+            fl = work["gateup_flops" if n == "gateup_gemm" else "down_flops"]
+            wb = work["gateup_weight_bytes" if n == "gateup_gemm" else "down_weight_bytes"]
+            stages[n] = {"ms": mean[i], "tflops": fl / s / 1e12, "frac_tc": fl / s / 1e12 / tc_burst,
+                         "frac_tc_sustained": fl / s / 1e12 / tc_sus,
+                         "weight_gbs": wb / s / 1e9, "frac_hbm_weights": wb / s / 1e9 / hbm}
+        else:
+            b = work[n + "_bytes"]
+            stages[n] = {"ms": mean[i], "gbs": b / s / 1e9, "frac_hbm": b / s / 1e9 / hbm}
+    gemm_s = (mean[2] + mean[3]) / 1e3
+    fl = work["gateup_flops"] + work["down_flops"]
+    stages["grouped_gemms"] = {"ms": mean[2] + mean[3], "tflops": fl / gemm_s / 1e12,
+                               "frac_tc": fl / gemm_s / 1e12 / tc_burst,
+                               "frac_tc_sustained": fl / gemm_s / 1e12 / tc_sus,
+                               "weight_gbs": work["active_expert_weight_bytes"] / gemm_s / 1e9,
+                               "frac_hbm_weights": work["active_expert_weight_bytes"] / gemm_s / 1e9 / hbm}
+    rd_s = (mean[0] + mean[1]) / 1e3
+    rd_b = work["route_dispatch_fused_bytes"] if fused_rd else work["router_bytes"] + work["dispatch_bytes"]
+    stages["router_dispatch"] = {"ms": mean[0] + mean[1], "gbs": rd_b / rd_s / 1e9, "frac_hbm": rd_b / rd_s / 1e9 / hbm,
+                                 "bytes": rd_b}
+    return stages
+
+
+def roofline_of(shape, work, mean, names, pk, pk_kind, fused_rd=False):
+    """The dominant (longest) stage against its roofline.  A GEMM whose FLOPs
+    per weight byte exceed the ridge point is tensor-bound and is compared with
+    the burst bf16 peak (it runs inside a millisecond-scale step); below the
+    ridge (decode sizes) it streams weights and is compared with HBM."""
+    hbm, tc_burst, tc_sus = pk["hbm_gbs"], pk["bf16_tflops"], pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+    dom = max(range(len(names)), key=lambda i: mean[i])
+    dname = names[dom]
+    intensity = (work["gateup_flops"] + work["down_flops"]) / max(1, work["active_expert_weight_bytes"])
+    ridge = tc_burst * 1e12 / (hbm * 1e9)
+    if dname in ("gateup_gemm", "down_gemm") and intensity >= ridge:
+        fl = work["gateup_flops" if dname == "gateup_gemm" else "down_flops"]
+        achieved = fl / (mean[dom] / 1e3) / 1e12
+        roof = {"kernel": dname, "bound": "tensor", "achieved": achieved, "peak": tc_burst, "unit": "TFLOP/s",
+                "frac": achieved / tc_burst, "peak_kind": f"{pk_kind} bf16 dense burst",
+                "peak_sustained": tc_sus, "frac_of_sustained": achieved / tc_sus}
+        alg = fl
+    elif dname in ("gateup_gemm", "down_gemm"):
+        wb = work["gateup_weight_bytes" if dname == "gateup_gemm" else "down_weight_bytes"]
+        achieved = wb / (mean[dom] / 1e3) / 1e9
+        roof = {"kernel": dname, "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm, "peak_kind": f"{pk_kind} HBM copy"}
+        alg = wb
+    else:
+        alg = work["route_dispatch_fused_bytes"] if (fused_rd and dname == "router") else work[dname + "_bytes"]
+        achieved = alg / (mean[dom] / 1e3) / 1e9
+        roof = {"kernel": dname, "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm, "peak_kind": f"{pk_kind} HBM copy"}
+    roof["traffic"] = measured_traffic(f"{dname}:{shape.name}")
+    roof["algorithmic_per_launch"] = alg
+    return roof
+
+
+def run_workload(shape, args, device, world, cpu_seconds):
+    """Time one workload: the timed steps (no stage events), a stage-timed pass,
+    host-buffer forwards end to end, and optionally the oracle on a sample.
+    Returns the record (rank 0) or None."""
     import numpy as np
     import torch
     import mixture_experts_router_gb300 as cb
     import synth
 
-    world, rank, local = dist_env()
-    torch.cuda.set_device(local)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    device = torch.device("cuda", local)
-    shape = workload_shape(args)
+    local = device.index
     layer = synth.make_layer(shape)
 
     def dev(a):
@@ -364,8 +443,9 @@ def run_ours(args):
 
         # end to end through the host-buffer entry point (pinned host memory): k2
         # back-to-back calls, each copying its x in and its out back, timed by the
-        # host clock between two device synchronisations (no L2 flush: every
-        # workload's per-step traffic is larger than L2)
+        # host clock between two device synchronisations (no L2 flush: per step
+        # every workload but decode moves more than L2, and decode streams 2.8 GB
+        # of weights)
         xh = torch.from_numpy(layer.x.view(np.int16)).pin_memory()
         oh = torch.empty_like(xh).pin_memory()
         k2 = max(1, min(args.e2e_steps, args.steps))
@@ -388,86 +468,92 @@ def run_ours(args):
         counts = counts.cpu().tolist()
 
     m.close()
+    del x, out, flush, xh, oh
+    torch.cuda.empty_cache()
+    if int(os.environ.get("RANK", "0")) != 0:
+        return None
+
+    pk, pk_kind = peaks()
+    work = algorithmic_work(shape, counts)
+    mean = [statistics.mean(s[i] for s in stage_ms) for i in range(5)]
+    # router (1 launch) + dispatch + two GEMMs + combine: 4 launches means the
+    # router's launch also dispatched
+    fused_rd = shape.router != "hash" and launches_per_forward == 4
+    names = cb.STAGE_NAMES
+    value = shape.T * world * args.steps / (total_ms / 1e3)
+    ms = total_ms / args.steps
+    rec = {
+        "value": value, "unit": "tokens/s", "ms_per_step": ms, "steps": args.steps, "warmup": args.warmup,
+        "dtype": shape.wdtype, "config": config_block(shape, args.l2_flush_mb),
+        "e2e": {"value": shape.T * world * k2 / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": shape.T * shape.d * 2, "d2h_bytes_per_step": shape.T * shape.d * 2,
+                "steps": k2, "timing": "host clock over back-to-back calls",
+                "api": "cb_moe_forward_host (pinned host x and out; input copy, layer and output copy on the "
+                       "handle's three streams, successive calls overlapping)"},
+        "gpu_launches": launches_per_forward * args.steps,
+        "roofline": roofline_of(shape, work, mean, names, pk, pk_kind, fused_rd),
+        "stages": stage_report(shape, work, mean, names, pk, fused_rd),
+        "stage_pass": {"ms_per_step": stage_step_ms / args.steps,
+                       "about": "the stage times and the roofline come from a second pass of the same steps "
+                                "with CUDA events between the stages; ms_per_step and value from the first, "
+                                "without them"},
+        "layer_weight_streaming": {"active_expert_weight_bytes": work["active_expert_weight_bytes"],
+                                   "gbs": work["active_expert_weight_bytes"] / (ms / 1e3) / 1e9,
+                                   "frac_hbm": work["active_expert_weight_bytes"] / (ms / 1e3) / 1e9 / pk["hbm_gbs"],
+                                   "about": "activated-expert weight bytes over the whole layer's step time"},
+        "expert_rows": {"active_experts": sum(1 for c in counts if c > 0), "max_rows": max(counts),
+                        "min_rows": min(counts)},
+        "clocks": clocks,
+    }
+    if world == 1 and cpu_seconds > 0:
+        rec["cpu_baseline"] = oracle_baseline(shape, layer, cpu_seconds)
+    return rec
+
+
+def run_ours(args):
+    import torch
+    import synth
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    device = torch.device("cuda", local)
+    shape = workload_shape(args)
+    head = run_workload(shape, args, device, world, 0.0 if args.no_cpu_baseline else args.cpu_seconds)
+    extra = {}
+    names = [] if args.shape or args.workloads in ("", "none") else \
+        [n for n in args.workloads.split(",") if n != shape.name]
+    for name in names:
+        sub = synth.with_router(synth.WORKLOADS[name], args.router)
+        rec = run_workload(sub, args, device, world, 0.0 if args.no_cpu_baseline else args.sub_cpu_seconds)
+        if rec is not None:
+            extra[name] = rec
     if rank != 0:
         if world > 1:
             torch.distributed.destroy_process_group()
         return 0
 
     pk, pk_kind = peaks()
-    hbm = pk["hbm_gbs"]
-    tc_sus = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
-    tc_burst = pk["bf16_tflops"]
-    work = algorithmic_work(shape, counts)
-    mean = [statistics.mean(s[i] for s in stage_ms) for i in range(5)]
-    names = cb.STAGE_NAMES
-    stages = {}
-    for i, n in enumerate(names):
-        s = mean[i] / 1e3
-        if n in ("gateup_gemm", "down_gemm"):
-            fl = work["gateup_flops" if n == "gateup_gemm" else "down_flops"]
-            wb = work["gateup_weight_bytes" if n == "gateup_gemm" else "down_weight_bytes"]
-            stages[n] = {"ms": mean[i], "tflops": fl / s / 1e12, "frac_tc_sustained": fl / s / 1e12 / tc_sus,
-                         "weight_gbs": wb / s / 1e9, "frac_hbm_weights": wb / s / 1e9 / hbm}
-        else:
-            b = work[n + "_bytes"]
-            stages[n] = {"ms": mean[i], "gbs": b / s / 1e9, "frac_hbm": b / s / 1e9 / hbm}
-    gemm_s = (mean[2] + mean[3]) / 1e3
-    stages["grouped_gemms"] = {"ms": mean[2] + mean[3],
-                               "tflops": (work["gateup_flops"] + work["down_flops"]) / gemm_s / 1e12,
-                               "frac_tc_sustained": (work["gateup_flops"] + work["down_flops"]) / gemm_s / 1e12 / tc_sus,
-                               "weight_gbs": work["active_expert_weight_bytes"] / gemm_s / 1e9,
-                               "frac_hbm_weights": work["active_expert_weight_bytes"] / gemm_s / 1e9 / hbm}
-
-    # dominant kernel: the longest stage
-    dom = max(range(5), key=lambda i: mean[i])
-    dname = names[dom]
-    # a GEMM is tensor-bound when its FLOPs per weight byte exceed the ridge point
-    intensity = (work["gateup_flops"] + work["down_flops"]) / max(1, work["active_expert_weight_bytes"])
-    ridge = tc_sus * 1e12 / (hbm * 1e9)
-    if dname in ("gateup_gemm", "down_gemm") and intensity >= ridge:
-        fl = work["gateup_flops" if dname == "gateup_gemm" else "down_flops"]
-        achieved = fl / (mean[dom] / 1e3) / 1e12
-        roof = {"kernel": dname, "bound": "tensor", "achieved": achieved, "peak": tc_sus, "unit": "TFLOP/s",
-                "frac": achieved / tc_sus, "peak_kind": f"{pk_kind} bf16 sustained",
-                "frac_of_burst": achieved / tc_burst}
-    elif dname in ("gateup_gemm", "down_gemm"):
-        wb = work["gateup_weight_bytes" if dname == "gateup_gemm" else "down_weight_bytes"]
-        achieved = wb / (mean[dom] / 1e3) / 1e9
-        roof = {"kernel": dname, "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                "frac": achieved / hbm, "peak_kind": f"{pk_kind} HBM copy"}
-    else:
-        b = work[dname + "_bytes"]
-        achieved = b / (mean[dom] / 1e3) / 1e9
-        roof = {"kernel": dname, "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                "frac": achieved / hbm, "peak_kind": f"{pk_kind} HBM copy"}
-    roof["traffic"] = measured_traffic(f"{dname}:{shape.name}")
-    roof["algorithmic_per_launch"] = (work["gateup_flops"] if dname == "gateup_gemm" else
-                                      work["down_flops"] if dname == "down_gemm" else work[dname + "_bytes"])
-
-    value = shape.T * world * args.steps / (total_ms / 1e3)
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": shape.wdtype,
         "data": "synthetic (seeded SplitMix64/Box-Muller; x ~ N(0,1), weights ~ N(0, 0.02^2), bf16)",
-        "config": config_block(shape, args.l2_flush_mb),
-        "e2e": {"value": shape.T * world * k2 / (e2e_ms / 1e3), "unit": "tokens/s",
-                "h2d_bytes_per_step": shape.T * shape.d * 2, "d2h_bytes_per_step": shape.T * shape.d * 2,
-                "steps": k2, "timing": "host clock over back-to-back calls", "api": "cb_moe_forward_host (pinned host x and out; input copy, layer and output copy on the handle's three streams, successive calls overlapping)"},
-        "gpu_launches": launches_per_forward * args.steps,
-        "roofline": roof,
-        "stages": stages,
-        "stage_pass": {"ms_per_step": stage_step_ms / args.steps,
-                       "about": "the stage times and the roofline come from a second pass of the same steps "
-                                "with CUDA events between the stages; ms_per_step and value from the first, "
-                                "without them"},
-        "expert_rows": {"active_experts": sum(1 for c in counts if c > 0), "max_rows": max(counts),
-                        "min_rows": min(counts)},
-        "clocks": clocks,
-        "peaks": {"hbm_gbs": hbm, "bf16_tflops": tc_burst, "bf16_tflops_sustained": tc_sus, "kind": pk_kind},
+        "config": head["config"],
     }
-    if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = oracle_baseline(shape, layer, args.cpu_seconds)
+    for key in ("e2e", "gpu_launches", "roofline", "stages", "stage_pass", "layer_weight_streaming",
+                "expert_rows", "clocks", "cpu_baseline"):
+        if key in head:
+            line[key] = head[key]
+    line["peaks"] = {"hbm_gbs": pk["hbm_gbs"], "bf16_tflops": pk["bf16_tflops"],
+                     "bf16_tflops_sustained": pk.get("bf16_tflops_sustained"), "kind": pk_kind}
+    if extra:
+        line["workloads"] = extra
+        line["workloads_about"] = ("the other layers of the metric, each timed the same way after the headline "
+                                   "one (its own steps, stages, roofline, clocks, end-to-end leg and oracle "
+                                   "sample); value and e2e above are the headline layer's")
     print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
