@@ -66,6 +66,7 @@ struct cb_moe {
   bool router_tc;          // tcgen05 router (else the mma.sync router)
   bool use_graphs;         // replay each forward variant from a captured CUDA graph
   bool pair_gu, pair_dn;   // bf16 gate/up, down GEMMs on CTA pairs (2-SM MMA)
+  int32_t rd_grid;         // > 0: router and dispatch run as one cooperative launch of this many blocks
   int32_t rank_block;      // > 0: the router ranks pairs in blocks of this many tokens
   int32_t n_rank_blocks;
   int pair_grid_gu, pair_grid_dn;
@@ -295,7 +296,7 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
     }
     if (launch_router_tc(h->tm_x, h->tm_wr, ra, h->rpart, h->num_sms, s) != cudaSuccess || !mark(1))
       return CB_ERR_CUDA;
-  } else {
+  } else if (h->rd_grid <= 0) {
     if (launch_router(ra, s) != cudaSuccess || !mark(1)) return CB_ERR_CUDA;
   }
 
@@ -330,7 +331,15 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
     da.test_stall = 1;
     da.wait_limit_ns = 1000000ull;  // 1 ms
   }
-  if (launch_dispatch(da, s) != cudaSuccess || !mark(2)) return CB_ERR_CUDA;
+  if (h->rd_grid > 0 && c.router_mode != CB_ROUTER_HASH && !h->router_tc) {
+    // router and dispatch in one launch: the router stage ends with it and
+    // the dispatch stage is empty
+    ra.blk_counts = nullptr;
+    ra.local_rank = nullptr;
+    if (launch_route_dispatch(ra, da, h->rd_grid, s) != cudaSuccess || !mark(1) || !mark(2)) return CB_ERR_CUDA;
+  } else if (launch_dispatch(da, s) != cudaSuccess || !mark(2)) {
+    return CB_ERR_CUDA;
+  }
 
   const bool int4w = c.wdtype == CB_W_INT4;
   const bool int8w = c.wdtype != CB_W_BF16;  // quantized weights (int8, int4 or fp8)
@@ -583,7 +592,9 @@ cb_status_t cb_moe_kernels_per_forward(const cb_moe_t* h, int32_t* n) {
     return CB_OK;
   }
   int32_t dispatch;
-  if (h->rank_block > 0)
+  if (h->rd_grid > 0 && c.router_mode != CB_ROUTER_HASH && !h->router_tc)
+    dispatch = 0;  // in the router's launch
+  else if (h->rank_block > 0)
     dispatch = 2;  // block-count scan + row copy (which also finalises the ranks)
   else if (h->coop_blocks > 0)
     dispatch = 1;  // count, scan, ranks and row copy in one cooperative launch
@@ -742,7 +753,8 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
   }
   ok = ok && grouped_gemm_prepare() == cudaSuccess && grouped_gemm_int8_prepare() == cudaSuccess &&
        grouped_gemm_int8_tm_prepare() == cudaSuccess &&
-       router_prepare() == cudaSuccess && router_tc_prepare() == cudaSuccess && dispatch_prepare() == cudaSuccess;
+       router_prepare() == cudaSuccess && router_tc_prepare() == cudaSuccess && dispatch_prepare() == cudaSuccess &&
+       route_dispatch_prepare() == cudaSuccess;
   // router: tcgen05 for wide expert counts, the mma.sync split-K router for
   // E <= 16 (bound by reading x, where more CTAs help); CB_MOE_ROUTER=tc|mma
   // overrides the choice
@@ -807,10 +819,24 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
     const int64_t nb = (static_cast<int64_t>(cfg->n_tokens) + rb - 1) / rb;
     h->rank_block = 0;
     h->n_rank_blocks = 0;
-    if (!h->router_tc && !hashr && (nb + 1) * (cfg->n_experts + 1) <= kFusedScanWords &&
-        !(fv != nullptr && std::strcmp(fv, "0") == 0)) {
+    const bool fused_ranks = !(fv != nullptr && std::strcmp(fv, "0") == 0);
+    if (!h->router_tc && !hashr && (nb + 1) * (cfg->n_experts + 1) <= kFusedScanWords && fused_ranks) {
       h->rank_block = rb;
       h->n_rank_blocks = static_cast<int32_t>(nb);
+    }
+    // With the mma router and up to 16 experts (d a multiple of 512), the
+    // router, the ranking and the row copy run as one cooperative launch that
+    // reads x from HBM once (the copy finds its rows in L2) and needs no scan
+    // kernel in between.  CB_MOE_ROUTE_DISPATCH=0 keeps the separate router
+    // and dispatch kernels; CB_MOE_FUSED_RANKS=0 implies it.
+    const char* rdv = std::getenv("CB_MOE_ROUTE_DISPATCH");
+    h->rd_grid = 0;
+    if (!h->router_tc && !hashr && fused_ranks && !(rdv != nullptr && std::strcmp(rdv, "0") == 0) &&
+        static_cast<int64_t>(cfg->n_tokens) * cfg->top_k + 128ll * cfg->n_experts < (1ll << 31) &&
+        route_dispatch_supported(cfg->n_tokens, cfg->d_model, cfg->n_experts, cfg->top_k, h->num_sms)) {
+      h->rd_grid = route_dispatch_grid(cfg->n_tokens, h->num_sms);
+      h->rank_block = 0;
+      h->n_rank_blocks = 0;
     }
     // Otherwise (tcgen05 and hash routers, or CB_MOE_FUSED_RANKS=0) the
     // dispatch ranks the pairs itself.  Up to 65536 routed pairs its
@@ -823,7 +849,7 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
     const char* dv = std::getenv("CB_MOE_DISPATCH");
     const bool coop_pref = dv != nullptr ? std::strcmp(dv, "coop") == 0 : routed <= kCoopMaxPairs;
     h->coop_blocks = 0;
-    if (h->rank_block == 0 && cfg->n_experts <= 256 && coop_pref) {
+    if (h->rank_block == 0 && h->rd_grid == 0 && cfg->n_experts <= 256 && coop_pref) {
       int g = dispatch_coop_max_blocks(h->num_sms);
       g = std::min(g, kFusedScanWords / cfg->n_experts);  // rows of counts the chunk buffer holds
       g = std::min(g, cfg->n_tokens);
@@ -853,7 +879,8 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
     static const char* const kW[] = {"bf16", "int8", "int4", "fp8"};
     static const char* const kR[] = {"softmax", "raw", "hash"};
     const char* router = cfg->router_mode == CB_ROUTER_HASH ? "hash" : h->router_tc ? "tcgen05" : "mma";
-    const char* dispatch = h->rank_block > 0 ? "router-ranked" : h->coop_blocks > 0 ? "cooperative" : "split";
+    const char* dispatch = h->rd_grid > 0 ? "fused-with-router" : h->rank_block > 0 ? "router-ranked"
+                           : h->coop_blocks > 0 ? "cooperative" : "split";
     const char* gemm = int8w ? (h->int8_tm ? "tensor-memory quantised" : "shared-memory int8")
                              : (h->pair_gu || h->pair_dn) ? "cta-pair" : "single-cta";
     std::fprintf(stderr,

@@ -23,6 +23,7 @@
 //   dispatch_coop    : count, scan, ranks and row copy in one cooperative
 //                      launch with one grid barrier (the default for the
 //                      dispatch's own ranking)
+#include "grid_barrier.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -396,12 +397,6 @@ __global__ void __launch_bounds__(kThreads) dispatch_copy(DispatchArgs a) {
 constexpr int kCoopThreads = 1024;
 constexpr int kCoopWarps = kCoopThreads / 32;
 
-__device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* p) {
-  unsigned int v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
 __global__ void __launch_bounds__(kCoopThreads) dispatch_coop(DispatchArgs a) {
   grid_dep_wait();    // what earlier kernels in the stream wrote is visible from here
   grid_dep_launch();
@@ -440,26 +435,14 @@ __global__ void __launch_bounds__(kCoopThreads) dispatch_coop(DispatchArgs a) {
     a.chunk[static_cast<int64_t>(b) * E + e] = c;
   }
 
-  // 2. grid barrier: the block's count stores, then its arrival
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    atomicAdd(a.bar, 1u);
-    const uint64_t start = globaltimer_ns();
-    int ok = 1;
-    while (ld_acquire_gpu(a.bar) < static_cast<unsigned int>(G + a.test_stall)) {
-      if (globaltimer_ns() - start > a.wait_limit_ns) {
-        set_error(a.err, kErrTimeout);
-        ok = 0;
-        break;
-      }
-      __nanosleep(64);
-    }
-    __threadfence();
-    s_ok = ok;
+  // 2. grid barrier (the words reset themselves: no memset before the
+  // launch); the block's last thread counts its departure while the others
+  // start the column sums
+  if (!grid_barrier_wait(a.bar, static_cast<unsigned>(G + a.test_stall), a.wait_limit_ns, a.err, &s_ok)) {
+    if (threadIdx.x == 0) grid_barrier_depart(a.bar, static_cast<unsigned>(G));
+    return;
   }
-  __syncthreads();
-  if (!s_ok) return;
+  if (threadIdx.x == kCoopThreads - 1) grid_barrier_depart(a.bar, static_cast<unsigned>(G));
 
   // 3. column sums: thread i < P E sums expert i % E over the block rows of
   // part i / E (P = kCoopThreads / E >= 2 parts)
@@ -638,8 +621,6 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s) {
   if (a.n_chunks <= 0) return cudaSuccess;
   if (a.rank_block <= 0 && a.coop_blocks > 0) {
     if (a.E > 256 || a.bar == nullptr) return cudaErrorInvalidValue;
-    cudaError_t e = cudaMemsetAsync(a.bar, 0, sizeof(unsigned int), s);
-    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.coop_blocks, 1, 1);
     cfg.blockDim = dim3(kCoopThreads, 1, 1);

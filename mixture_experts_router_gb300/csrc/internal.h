@@ -149,7 +149,8 @@ struct DispatchArgs {
   int32_t n_rank_blocks;
   // > 0: the dispatch's own ranking and the row copy run as one cooperative
   // launch of this many blocks (chunk then holds [coop_blocks][E] counts),
-  // meeting once at a grid barrier on *bar (zeroed by the launcher)
+  // meeting once at a grid barrier on bar[0..1] (zero between launches: the
+  // kernel sets the words back itself, grid_barrier.cuh)
   int32_t coop_blocks;
   unsigned int* bar;
   uint64_t wait_limit_ns;
@@ -171,6 +172,18 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s);
 // (kFusedScanWords once dispatch_prepare has run on the device); returns the
 // first launch's error, launching nothing after it
 cudaError_t launch_dispatch_ranks(const DispatchArgs& a, int scan_words, cudaStream_t s);
+
+// ---------------------------------------------- router + dispatch, fused
+// The mma router and the dispatch (ranks, tok/inv, tile maps, row copy) in
+// one cooperative launch of `grid` blocks, one per SM, for E <= 16 and d a
+// multiple of 512 (route_dispatch_supported checks the shared memory and the
+// residency).  Uses a.chunk ([grid][E]), a.bar (the grid barrier's two words),
+// a.test_stall and a.wait_limit_ns; the router's blk_counts/local_rank are
+// unused.
+bool route_dispatch_supported(int T, int d, int E, int k, int num_sms);
+int route_dispatch_grid(int T, int num_sms);
+cudaError_t route_dispatch_prepare();  // one-time function attributes
+cudaError_t launch_route_dispatch(const RouterArgs& r, const DispatchArgs& a, int grid, cudaStream_t s);
 
 // ----------------------------------------------------------------- combine
 struct CombineArgs {

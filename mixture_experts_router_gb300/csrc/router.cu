@@ -28,32 +28,14 @@
 #include "internal.h"
 #include "ptx.cuh"
 #include "route_ranks.cuh"
+#include "router_common.cuh"
 
 namespace cbmoe {
 namespace {
 
+using namespace router_detail;
+
 constexpr int kMaxWarps = 16;
-
-struct Cand {
-  float v;
-  int idx;
-  int cls;  // 0 number, 1 NaN, 2 not available (padding or already taken)
-};
-
-__device__ __forceinline__ bool ranks_before(const Cand& a, const Cand& b) {
-  if (a.cls != b.cls) return a.cls < b.cls;
-  if (a.cls == 0 && a.v != b.v) return a.v > b.v;
-  return a.idx < b.idx;
-}
-
-__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-      "{%0, %1, %2, %3};\n"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
 
 // NT: n-tiles of 8 experts in total (E padded to 8 NT); KS: d split; NS:
 // expert split; MTB: 16-token m-tiles per block; the block has KS NS MTB
@@ -88,46 +70,10 @@ __global__ void __launch_bounds__(RCfg<NT, KS, NS, MTB>::THREADS) router_mma_ker
   const int dslice = a.d / KS;
   const int dbeg = ks * dslice;
 
-  const int r0 = tok0 + g, r1 = tok0 + g + 8;
-  const uint4* xa_ptr = reinterpret_cast<const uint4*>(a.x + static_cast<int64_t>(min(r0, a.T - 1)) * a.d + dbeg + 8 * q);
-  const uint4* xb_ptr = reinterpret_cast<const uint4*>(a.x + static_cast<int64_t>(min(r1, a.T - 1)) * a.d + dbeg + 8 * q);
-  const bool va = r0 < a.T, vb = r1 < a.T;
-  const uint4* w_ptr[NTW];
-  bool wv[NTW];
-#pragma unroll
-  for (int j = 0; j < NTW; ++j) {
-    const int e = (ns * NTW + j) * 8 + g;
-    wv[j] = e < a.E;
-    w_ptr[j] = reinterpret_cast<const uint4*>(a.wr + static_cast<int64_t>(min(e, a.E - 1)) * a.d + dbeg + 8 * q);
-  }
-
-  float acc[NTW][4];
-#pragma unroll
-  for (int j = 0; j < NTW; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-
-  // UNR 32-element steps per iteration: all their loads are issued before
-  // any MMA, so each thread keeps several 16-byte loads in flight.
+  // UNR 32-element steps per iteration: more loads in flight for fewer n-tiles
   constexpr int UNR = NTW <= 2 ? 8 : (NTW <= 4 ? 2 : 1);
-  const uint4 zero = make_uint4(0, 0, 0, 0);
-  for (int c = 0; c < dslice; c += 32 * UNR) {
-    uint4 xa[UNR], xb[UNR], wr[UNR][NTW];
-#pragma unroll
-    for (int u = 0; u < UNR; ++u) {
-      const bool in = c + 32 * u < dslice;
-      const int off = (c + 32 * u) / 8;  // in uint4 units
-      xa[u] = (in && va) ? __ldg(xa_ptr + off) : zero;
-      xb[u] = (in && vb) ? __ldg(xb_ptr + off) : zero;
-#pragma unroll
-      for (int j = 0; j < NTW; ++j) wr[u][j] = (in && wv[j]) ? __ldg(w_ptr[j] + off) : zero;
-    }
-#pragma unroll
-    for (int u = 0; u < UNR; ++u)
-#pragma unroll
-      for (int j = 0; j < NTW; ++j) {
-        mma_bf16(acc[j], xa[u].x, xb[u].x, xa[u].y, xb[u].y, wr[u][j].x, wr[u][j].y);
-        mma_bf16(acc[j], xa[u].z, xb[u].z, xa[u].w, xb[u].w, wr[u][j].z, wr[u][j].w);
-      }
-  }
+  float acc[NTW][4];
+  tile_logits<NTW, UNR>(a.x, a.wr, a.T, a.d, a.E, tok0, ns * NTW * 8, dbeg, dslice, acc);
 
   // partial logits -> shared memory
   float* mine = part + (static_cast<int64_t>(ks) * TB + mt * 16) * EP;
@@ -164,50 +110,12 @@ __global__ void __launch_bounds__(RCfg<NT, KS, NS, MTB>::THREADS) router_mma_ker
   for (int r = warp; r < TB; r += kWarps) {
     const int t = t_base + r;
     if (t >= a.T) break;
-    Cand cand[PER];
-#pragma unroll
-    for (int p = 0; p < PER; ++p) {
-      const int e = lane + 32 * p;
-      if (e < a.E) {
-        const float v = ls[r * EP + e];
-        cand[p] = Cand{v, e, isnan(v) ? 1 : 0};
-      } else {
-        cand[p] = Cand{0.f, e, 2};
-      }
-    }
-    float my_v = 0.f, l0 = 0.f;
-    int my_i = 0;
-    for (int s = 0; s < a.k; ++s) {
-      Cand b = cand[0];
-#pragma unroll
-      for (int p = 1; p < PER; ++p)
-        if (ranks_before(cand[p], b)) b = cand[p];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        Cand other;
-        other.v = __shfl_xor_sync(0xffffffffu, b.v, o);
-        other.idx = __shfl_xor_sync(0xffffffffu, b.idx, o);
-        other.cls = __shfl_xor_sync(0xffffffffu, b.cls, o);
-        if (ranks_before(other, b)) b = other;
-      }
-      if ((b.idx & 31) == lane) {
-#pragma unroll
-        for (int p = 0; p < PER; ++p)
-          if (p == (b.idx >> 5)) cand[p].cls = 2;
-      }
-      if (s == 0) l0 = b.v;
-      if (lane == s) {
-        my_v = b.v;
-        my_i = b.idx;
-      }
-    }
-    const float ex = (lane < a.k) ? expf(my_v - l0) : 0.f;
-    float sum = ex;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    int my_i;
+    float my_w;
+    warp_gate<PER>(ls + r * EP, a.E, a.k, a.raw_weights, my_i, my_w);
     if (lane < a.k) {
       a.ids[static_cast<int64_t>(t) * a.k + lane] = my_i;
-      a.w[static_cast<int64_t>(t) * a.k + lane] = a.raw_weights ? my_v : ex / sum;
+      a.w[static_cast<int64_t>(t) * a.k + lane] = my_w;
       s_ids[r * 16 + lane] = my_i;
     }
   }

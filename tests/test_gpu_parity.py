@@ -37,6 +37,10 @@ SMALL = {
     "fp8_mid": synth.custom_shape("fp8_mid", T=300, d=512, f=768, E=8, k=2, wdtype="fp8", seed=34),
     "fp8_pairs": synth.custom_shape("fp8_pairs", T=1100, d=512, f=768, E=4, k=2, wdtype="fp8", seed=35),
     "fp8_k6": synth.custom_shape("fp8_k6", T=700, d=256, f=512, E=64, k=6, wdtype="fp8", seed=36),
+    # router and dispatch in one launch: several 16-token units per block, and 16 experts
+    "many_units": synth.custom_shape("many_units", T=10000, d=512, f=256, E=8, k=2, seed=91),
+    "e16_d512": synth.custom_shape("e16_d512", T=700, d=512, f=256, E=16, k=4, seed=95),
+    "e3_k3_d1024": synth.custom_shape("e3_k3_d1024", T=77, d=1024, f=256, E=3, k=3, seed=93),
 }
 
 FULL = {  # workload: random tokens checked beyond the first and last row of every m-tile (None: every token)
@@ -142,7 +146,8 @@ def test_forwards_inside_a_caller_graph():
 
 
 GUARD_CASES = [
-    ("tiny", {}), ("odd_T", {}), ("ragged_mid", {"CB_MOE_PAIR": "1"}),
+    ("tiny", {}), ("odd_T", {}), ("ragged_mid", {"CB_MOE_PAIR": "1"}), ("ragged_mid", {"CB_MOE_ROUTE_DISPATCH": "0"}),
+    ("many_units", {}),
     ("ragged_mid", {"CB_MOE_PAIR": "1", "CB_MOE_FUSED_COMBINE": "1"}), ("ragged_mid", {"CB_MOE_GATHER": "1"}),
     ("three_mtiles", {"CB_MOE_PAIR": "1"}), ("skewed_small", {}), ("skewed_small", {"CB_MOE_DISPATCH": "split"}),
     ("e256_k16", {}), ("one_token_e32", {}), ("int8_k6", {}), ("int8_mid", {"CB_MOE_INT8": "smem"}),
@@ -177,8 +182,9 @@ def test_kernels_stay_inside_the_workspace(name, env, monkeypatch):
 @pytest.mark.parametrize("name,expect", [
     ("skewed_small", "T=1000 d=256 f=256 E=128 k=4 weights=bf16 gate=softmax router=tcgen05 dispatch=cooperative "
                      "gemm=single-cta"),
-    ("ragged_mid", "T=300 d=512 f=768 E=8 k=2 weights=bf16 gate=softmax router=mma dispatch=router-ranked"),
-    ("fp8_mid", "weights=fp8 gate=softmax router=mma dispatch=router-ranked gemm=tensor-memory quantised"),
+    ("ragged_mid", "T=300 d=512 f=768 E=8 k=2 weights=bf16 gate=softmax router=mma dispatch=fused-with-router"),
+    ("tiny", "T=64 d=256 f=512 E=8 k=2 weights=bf16 gate=softmax router=mma dispatch=router-ranked"),
+    ("fp8_mid", "weights=fp8 gate=softmax router=mma dispatch=fused-with-router gemm=tensor-memory quantised"),
 ])
 def test_init_log_line(name, expect, monkeypatch, capfd):
     """CB_MOE_LOG=1: cb_moe_init prints one stderr line naming the paths the handle runs."""
@@ -507,21 +513,26 @@ def test_cooperative_dispatch_timeout():
     assert rep["f32_max_abs"] <= gh.MAX_ABS
 
 
-@pytest.mark.parametrize("fused,name,expect", [
-    ("1", "mixtral_prefill", 6), ("1", "skewed", 6), ("0", "mixtral_prefill", 5), ("0", "skewed", 6),
-    ("split", "mixtral_prefill", 6), ("split", "skewed", 9)])
-def test_kernels_per_forward(fused, name, expect, monkeypatch):
+@pytest.mark.parametrize("fused,name,d,expect", [
+    ("1", "mixtral_prefill", 256, 6), ("1", "skewed", 256, 6), ("0", "mixtral_prefill", 256, 5),
+    ("0", "skewed", 256, 6), ("split", "mixtral_prefill", 256, 6), ("split", "skewed", 256, 9),
+    ("1", "mixtral_prefill", 512, 4), ("1", "mixtral_decode", 512, 4), ("rd0", "mixtral_prefill", 512, 6),
+    ("1", "skewed", 512, 6)])
+def test_kernels_per_forward(fused, name, d, expect, monkeypatch):
     """The launch count the library reports: router (the tcgen05 router of wide
-    layers: partial logits + top-k), dispatch kernels (block scan + row copy
-    after the mma router's per-block ranks; else one cooperative launch, or
-    with CB_MOE_DISPATCH=split one-block / count-scan-scatter ranking + row
-    copy), two grouped GEMMs, combine."""
-    if fused != "1":
+    layers: partial logits + top-k), dispatch kernels (none when the router's
+    launch also dispatches: up to 16 experts and d a multiple of 512; block
+    scan + row copy after the mma router's per-block ranks; else one
+    cooperative launch, or with CB_MOE_DISPATCH=split one-block /
+    count-scan-scatter ranking + row copy), two grouped GEMMs, combine."""
+    if fused in ("0", "split"):
         monkeypatch.setenv("CB_MOE_FUSED_RANKS", "0")
     if fused == "split":
         monkeypatch.setenv("CB_MOE_DISPATCH", "split")
+    if fused == "rd0":
+        monkeypatch.setenv("CB_MOE_ROUTE_DISPATCH", "0")
     shp = synth.WORKLOADS[name]
-    gl = gh.GpuLayer(synth.make_layer(synth.custom_shape(name + "_n", T=shp.T, d=256, f=256, E=shp.E, k=shp.k,
+    gl = gh.GpuLayer(synth.make_layer(synth.custom_shape(name + "_n", T=shp.T, d=d, f=256, E=shp.E, k=shp.k,
                                                          seed=61)))
     try:
         assert gl.m.kernels_per_forward() == expect
@@ -671,3 +682,62 @@ def test_programmatic_dependent_launch(name, monkeypatch):
         gl.close()
     rep = gh.full_check(layer)
     print(name, "pdl", rep)
+
+
+ROUTE_DISPATCH_SMALL = ["ragged_mid", "three_mtiles", "odd_T", "int8_mid", "many_units", "e16_d512", "e3_k3_d1024"]
+
+
+@pytest.mark.parametrize("name", ROUTE_DISPATCH_SMALL)
+def test_separate_router_and_dispatch_small(name, monkeypatch):
+    """CB_MOE_ROUTE_DISPATCH=0: the router kernel (with its per-block ranks),
+    the block-count scan and the row copy as separate launches instead of the
+    one cooperative launch; same routing views and outputs."""
+    monkeypatch.setenv("CB_MOE_ROUTE_DISPATCH", "0")
+    rep = gh.full_check(synth.make_layer(SMALL[name]))
+    print(name, "separate router and dispatch", rep)
+
+
+@pytest.mark.parametrize("name", ["mixtral_prefill", "mixtral_decode"])
+def test_separate_router_and_dispatch_full_size(name, monkeypatch):
+    monkeypatch.setenv("CB_MOE_ROUTE_DISPATCH", "0")
+    rep = gh.full_check(synth.make_layer(synth.WORKLOADS[name]), sample=FULL[name])
+    print(name, "separate router and dispatch", rep)
+
+
+def test_fused_route_dispatch_matches_separate_kernels_bit_for_bit(monkeypatch):
+    """The one-launch router + dispatch gives the same ids, weights, logits,
+    dispatch arrays and outputs, bit for bit, as the separate kernels."""
+    layer = synth.make_layer(SMALL["many_units"])
+    outs = []
+    for rd in ("1", "0"):
+        monkeypatch.setenv("CB_MOE_ROUTE_DISPATCH", rd)
+        gl = gh.GpuLayer(layer)
+        try:
+            assert gl.m.kernels_per_forward() == (4 if rd == "1" else 6)
+            gl.run()
+            outs.append((gl.routing(), gl.out.clone(), gl.out32.clone()))
+        finally:
+            gl.close()
+    (ra, oa, fa), (rb, ob, fb) = outs
+    for key in ra:
+        assert np.array_equal(ra[key], rb[key]), key
+    assert torch.equal(oa.view(torch.int16), ob.view(torch.int16))
+    assert torch.equal(fa, fb)
+
+
+def test_fused_route_dispatch_timeout():
+    """The grid barrier of the router + dispatch launch, made to wait for a
+    block that does not exist (CB_FLAG_TEST_STALL_DISPATCH, 1 ms bound), ends
+    with CB_ERR_TIMEOUT and leaves the device usable."""
+    import mixture_experts_router_gb300 as cb
+    layer = synth.make_layer(SMALL["ragged_mid"])
+    gl = gh.GpuLayer(layer, flags=cb.CB_FLAG_TEST_STALL_DISPATCH)
+    try:
+        assert gl.m.kernels_per_forward() == 4
+        gl.m.forward(gl.x, gl.out)
+        torch.cuda.synchronize()
+        assert gl.m.last_error() == cb.CB_ERR_TIMEOUT
+    finally:
+        gl.close()
+    rep = gh.full_check(layer)
+    assert rep["f32_max_abs"] <= gh.MAX_ABS
