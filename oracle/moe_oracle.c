@@ -160,13 +160,24 @@ double moe_oracle_fp8_value(uint8_t c) {
   return sign ? -mag : mag;
 }
 
+/* moe_oracle_fp8_value of every byte, filled once before the first parallel
+ * loop that reads fp8 weights (the same values, looked up). */
+static double fp8_table[256];
+static int fp8_table_ready = 0;
+
+static void fp8_table_fill(void) {
+  if (fp8_table_ready) return;
+  for (int c = 0; c < 256; ++c) fp8_table[c] = moe_oracle_fp8_value((uint8_t)c);
+  fp8_table_ready = 1;
+}
+
 /* Element idx of a weight tensor before its channel scale: the bf16 value,
  * the int8 code, the int4 code minus the row's zero point `zero`, or the
  * value of the e4m3 byte. */
 static double weight_elem(const moe_oracle_layer_t *L, const void *w, int64_t idx, int zero) {
   if (L->wdtype == 0) return bf16_value(((const uint16_t *)w)[idx]);
   if (L->wdtype == 1) return (double)((const int8_t *)w)[idx];
-  if (L->wdtype == 3) return moe_oracle_fp8_value(((const uint8_t *)w)[idx]);
+  if (L->wdtype == 3) return fp8_table[((const uint8_t *)w)[idx]];
   const uint8_t byte = ((const uint8_t *)w)[idx / 2];
   const int q = (idx % 2 == 0) ? (byte & 0x0F) : (byte >> 4);
   return (double)(q - zero);
@@ -373,6 +384,7 @@ static void expert_row(const moe_oracle_layer_t *L, int e, const double *xv, int
 
 /* Expert e applied to an arbitrary bf16 row (d elements). */
 void moe_oracle_expert(const moe_oracle_layer_t *L, int e, const uint16_t *xrow, int mode, double *y) {
+  fp8_table_fill();
   double *xv = (double *)malloc(sizeof(double) * (size_t)L->d);
   double *h = (double *)malloc(sizeof(double) * (size_t)L->f);
   for (int i = 0; i < L->d; ++i) xv[i] = bf16_value(xrow[i]);
@@ -388,6 +400,7 @@ int moe_oracle_forward(const moe_oracle_layer_t *L, const int32_t *tokens, int64
                        double *out, int32_t *ids_out, double *w_out) {
   const int d = L->d, E = L->E, k = L->k;
   int bad = 0;
+  fp8_table_fill();
   #pragma omp parallel
   {
     double *l = (double *)malloc(sizeof(double) * (size_t)E);
