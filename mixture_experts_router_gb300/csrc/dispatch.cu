@@ -444,18 +444,27 @@ __global__ void __launch_bounds__(kCoopThreads) dispatch_coop(DispatchArgs a) {
   }
   if (threadIdx.x == kCoopThreads - 1) grid_barrier_depart(a.bar, static_cast<unsigned>(G));
 
-  // 3. column sums: thread i < P E sums expert i % E over the block rows of
-  // part i / E (P = kCoopThreads / E >= 2 parts)
+  // 3. column sums: thread i < P E sums expert i % E over the rows
+  // i / E, i / E + P, ... (consecutive threads read consecutive words of a
+  // row; P = kCoopThreads / E >= 4 parts), up to kSumLoads loads in flight
+  // at a time, then thread e adds the P parts
+  constexpr int kSumLoads = 20;
   const int P = kCoopThreads / E;
   if (static_cast<int>(threadIdx.x) < P * E) {
     const int e = threadIdx.x % E, q = threadIdx.x / E;
-    const int lo = q * G / P, hi = (q + 1) * G / P;
     int pre = 0, tot = 0;
-#pragma unroll 8
-    for (int r = lo; r < hi; ++r) {
-      const int c = __ldcg(a.chunk + static_cast<int64_t>(r) * E + e);
-      tot += c;
-      pre += r < b ? c : 0;
+    for (int r0 = q; r0 < G; r0 += P * kSumLoads) {
+      int c[kSumLoads];
+#pragma unroll
+      for (int i = 0; i < kSumLoads; ++i) {
+        const int r = r0 + i * P;
+        c[i] = r < G ? __ldcg(a.chunk + static_cast<int64_t>(r) * E + e) : 0;
+      }
+#pragma unroll
+      for (int i = 0; i < kSumLoads; ++i) {
+        tot += c[i];
+        pre += r0 + i * P < b ? c[i] : 0;
+      }
     }
     part_pre[threadIdx.x] = pre;
     part_tot[threadIdx.x] = tot;

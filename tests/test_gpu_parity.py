@@ -41,6 +41,12 @@ SMALL = {
     "many_units": synth.custom_shape("many_units", T=10000, d=512, f=256, E=8, k=2, seed=91),
     "e16_d512": synth.custom_shape("e16_d512", T=700, d=512, f=256, E=16, k=4, seed=95),
     "e3_k3_d1024": synth.custom_shape("e3_k3_d1024", T=77, d=1024, f=256, E=3, k=3, seed=93),
+    "rd_one_expert": synth.custom_shape("rd_one_expert", T=130, d=512, f=256, E=1, k=1, seed=101),
+    "rd_k_equals_E": synth.custom_shape("rd_k_equals_E", T=200, d=512, f=256, E=4, k=4, seed=102),
+    # about 16 units per block, 272 owned tokens
+    "rd_long": synth.custom_shape("rd_long", T=40000, d=512, f=256, E=8, k=2, seed=103),
+    "rd_e16_k16": synth.custom_shape("rd_e16_k16", T=333, d=1024, f=256, E=16, k=16, seed=104),
+    "rd_bias": synth.custom_shape("rd_bias", T=500, d=512, f=256, E=12, k=3, bias=True, seed=105),
 }
 
 FULL = {  # workload: random tokens checked beyond the first and last row of every m-tile (None: every token)
@@ -684,7 +690,8 @@ def test_programmatic_dependent_launch(name, monkeypatch):
     print(name, "pdl", rep)
 
 
-ROUTE_DISPATCH_SMALL = ["ragged_mid", "three_mtiles", "odd_T", "int8_mid", "many_units", "e16_d512", "e3_k3_d1024"]
+ROUTE_DISPATCH_SMALL = ["ragged_mid", "three_mtiles", "odd_T", "int8_mid", "many_units", "e16_d512", "e3_k3_d1024",
+                        "rd_one_expert", "rd_k_equals_E", "rd_long", "rd_e16_k16", "rd_bias"]
 
 
 @pytest.mark.parametrize("name", ROUTE_DISPATCH_SMALL)
@@ -741,3 +748,22 @@ def test_fused_route_dispatch_timeout():
         gl.close()
     rep = gh.full_check(layer)
     assert rep["f32_max_abs"] <= gh.MAX_ABS
+
+
+@pytest.mark.parametrize("name", ["rd_one_expert", "rd_k_equals_E", "rd_long", "rd_e16_k16", "rd_bias"])
+def test_fused_route_dispatch_edges(name):
+    """The one-launch router + dispatch on its edges: one expert, k = E, a long
+    layer whose blocks own many units, 16 experts with k = 16, a router bias
+    (and the raw-logit gate on the same layer)."""
+    import mixture_experts_router_gb300 as cb
+    layer = synth.make_layer(SMALL[name])
+    gl = gh.GpuLayer(layer)
+    try:
+        assert gl.m.kernels_per_forward() == 4
+    finally:
+        gl.close()
+    rep = gh.full_check(layer)
+    print(name, "fused", rep)
+    if name == "rd_bias":
+        rep = gh.full_check(synth.make_layer(synth.with_router(SMALL[name], "raw")))
+        print(name, "fused raw", rep)
