@@ -21,6 +21,8 @@ Tolerances (bf16 in/out, fp32 accumulate):
 """
 from __future__ import annotations
 
+import os
+
 import numpy as np
 import torch
 
@@ -31,6 +33,10 @@ import synth
 GAP = 1e-5
 MAX_ABS = 2e-2
 MEAN_REL = 5e-3
+
+# (test id, layer name, report) of every full_check of the session, printed
+# by tests/conftest.py at the end of the run
+REPORTS = []
 
 
 def to_dev(a, device="cuda"):
@@ -214,4 +220,5 @@ def full_check(layer: synth.Layer, sample=None, report=None):
             assert report["mtiles_checked"] == hit_max, report
     finally:
         gl.close()
+    REPORTS.append((os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0], layer.shape, dict(report)))
     return report
