@@ -452,13 +452,20 @@ def run_workload(shape, args, device, world, cpu_seconds):
         for _ in range(3):
             m.forward_host(xh, oh, stream=stream)
         torch.cuda.synchronize()
+        e2e_sampler = ClockSampler(local)
+        time.sleep(0.3)
         if world > 1:
             torch.distributed.barrier()
+        t_e0 = time.time()
         t0 = time.perf_counter()
         for i in range(k2):
             m.forward_host(xh, oh, stream=stream)
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3, world)
+        t_e1 = time.time()
+        time.sleep(0.2)
+        e2e_sampler.stop()
+        e2e_clocks = e2e_sampler.summary(t_e0, t_e1)
         st = m.last_error()
         if st != cb.CB_OK:
             raise cb.CbMoeError(st, "host forward")
@@ -487,7 +494,7 @@ def run_workload(shape, args, device, world, cpu_seconds):
         "dtype": shape.wdtype, "config": config_block(shape, args.l2_flush_mb),
         "e2e": {"value": shape.T * world * k2 / (e2e_ms / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": shape.T * shape.d * 2, "d2h_bytes_per_step": shape.T * shape.d * 2,
-                "steps": k2, "timing": "host clock over back-to-back calls",
+                "steps": k2, "timing": "host clock over back-to-back calls", "clocks": e2e_clocks,
                 "api": "cb_moe_forward_host (pinned host x and out; input copy, layer and output copy on the "
                        "handle's three streams, successive calls overlapping)"},
         "gpu_launches": launches_per_forward * args.steps,

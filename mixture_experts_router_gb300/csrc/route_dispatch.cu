@@ -5,27 +5,27 @@
 // then the dispatch of the first page's §2.3 (per-expert histogram, prefix
 // sum, stable permutation, row copy), without a kernel boundary between them.
 //
-// One block per SM.  Each block owns a contiguous run of 16-token units (one
-// mma.sync m-tile each), and so a contiguous run of tokens:
-//   1. per unit: the logit GEMM, its 16 warps splitting d 16 ways, partial
-//      logits summed in a fixed order in shared memory, the bias, one warp
-//      per token for the gate; the block keeps its tokens' ids;
-//   2. ranks of the block's pairs within the block, in (token, slot) order
-//      (match-any groups per warp, then a scan over the warps), written to
-//      inv, and its per-expert counts -> chunk[b][e];
+// One block per SM.  Block b owns the tokens [b T / G, (b + 1) T / G) of the
+// G blocks (an even share: at decode size 64 tokens spread over 64 blocks):
+//   1. the logits and gate of its tokens, 16 at a time (one mma.sync
+//      m-tile, the last one of a block possibly partial): the 16 warps split
+//      d 16 ways, the partial logits are summed in a fixed order in shared
+//      memory, the bias added, one warp per token takes the gate; the block
+//      keeps its tokens' ids;
+//   2. ranks of its pairs within the block, in (token, slot) order
+//      (match-any groups per warp, then a scan over the warps), and its
+//      per-expert counts -> chunk[b][e];
 //   3. one grid barrier (the cooperative launch keeps every block resident;
 //      the wait is bounded by wall time all the same; the barrier words reset
 //      themselves, so the launch needs no memset before it);
 //   4. every block scans the count rows itself (one warp per expert): expert
-//      totals and each block's base sum_{b' < b} chunk[b'][e]; block 0
-//      publishes the counts, offsets and 128-row tile maps;
-//   5. the pairs of an even share of the tokens (not its own units: at
-//      decode size a few blocks own all the tokens) get their global ranks
-//      (base of the owning block + in-block rank) in tok and inv, and their
-//      rows are copied, Xp[row(t, s)] = x[t].  Those rows were read in step 1
-//      a few microseconds earlier, so they come from L2: x crosses HBM once,
-//      where the separate router and row-copy kernels read it twice, and the
-//      one-block scan kernel between them is gone.
+//      totals and its own base sum_{b' < b} chunk[b'][e]; block 0 publishes
+//      the counts, offsets and 128-row tile maps;
+//   5. the global ranks of its pairs (base + in-block rank) into tok and inv,
+//      and the copy of its tokens' rows, Xp[row(t, s)] = x[t].  Those rows
+//      were read in step 1 a few microseconds earlier, so they come from L2:
+//      x crosses HBM once, where the separate router and row-copy kernels
+//      read it twice, and the one-block scan kernel between them is gone.
 // The results are those of the separate router and dispatch kernels: the same
 // logit sums in the same order, the same gate, and ranks in the canonical
 // order (expert ascending, then token ascending).
@@ -62,26 +62,21 @@ __device__ __forceinline__ int warp_exclusive_scan(int v) {
   return x - v;
 }
 
-// The block that owns unit u: the largest b with floor(b units / G) <= u.
-__device__ __forceinline__ int owner_of_unit(int u, int units, int G) {
-  return static_cast<int>((static_cast<int64_t>(u + 1) * G - 1) / units);
-}
-
 // NT n-tiles of 8 experts (E <= 8 NT); d a multiple of 512.  Dynamic shared
-// memory: partial logits [16][16][8 NT] fp32, the block's ids [own_max][k],
-// the rows of its copy share [copy_max][k], and the blocks' bases [G][E]
-// (int32).
+// memory: partial logits [16][16][8 NT] fp32, the block's ids and their
+// in-block ranks (then padded rows), [own_max][k] int32 each, and the
+// blocks' bases [G][E] int32.
 template <int NT>
 __global__ void __launch_bounds__(kRdThreads, 1) route_dispatch_kernel(RouterArgs r, DispatchArgs a,
-                                                                       int32_t own_max, int32_t copy_max) {
+                                                                       int32_t own_max) {
   grid_dep_wait();    // what earlier kernels in the stream wrote is visible from here
   grid_dep_launch();
   constexpr int EP = NT * 8;
   extern __shared__ __align__(16) unsigned char rd_smem[];
   float* part = reinterpret_cast<float*>(rd_smem);                // [16][16][EP]
   int* s_ids = reinterpret_cast<int*>(part + kRdWarps * kUnit * EP);
-  int* s_row = s_ids + own_max * r.k;                              // [copy_max][k]
-  int* s_pref = s_row + copy_max * r.k;                            // [G][E]
+  int* s_row = s_ids + own_max * r.k;                              // [own_max][k]
+  int* s_pref = s_row + own_max * r.k;                             // [G][E]
   __shared__ int s_cnt[kMaxExperts], s_off[kMaxExperts], s_moff[kMaxExperts];
   __shared__ int s_wcnt[kRdWarps][kMaxExperts];
   __shared__ int s_ok;
@@ -91,29 +86,17 @@ __global__ void __launch_bounds__(kRdThreads, 1) route_dispatch_kernel(RouterArg
   const int G = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
   const int T = r.T, E = r.E, k = r.k, d = r.d;
   const int64_t M = static_cast<int64_t>(T) * k;
-  const int units = (T + kUnit - 1) / kUnit;
-  const int u_lo = static_cast<int>(static_cast<int64_t>(b) * units / G);
-  const int u_hi = static_cast<int>(static_cast<int64_t>(b + 1) * units / G);
-  const int t_lo = u_lo * kUnit;
-  const int t_hi = min(T, u_hi * kUnit);
-  const int own = max(0, t_hi - t_lo);
+  const int t_lo = static_cast<int>(static_cast<int64_t>(b) * T / G);
+  const int t_hi = static_cast<int>(static_cast<int64_t>(b + 1) * T / G);
+  const int own = t_hi - t_lo;
 
-  // 1. logits and gate, unit by unit.  First the block's whole run of x is
-  // requested into L2 in one asynchronous bulk prefetch, so HBM streams it at
-  // full rate while the warps' loads below find it in L2.
-  if (threadIdx.x == 0 && own > 0) {
-    const uint8_t* xb = reinterpret_cast<const uint8_t*>(r.x) + static_cast<int64_t>(t_lo) * d * 2;
-    int64_t left = static_cast<int64_t>(own) * d * 2;
-    constexpr int64_t kMaxPrefetch = 1 << 20;
-    for (; left > 0; xb += kMaxPrefetch, left -= kMaxPrefetch)
-      bulk_prefetch_l2(xb, static_cast<uint32_t>(left < kMaxPrefetch ? left : kMaxPrefetch));
-  }
+  // 1. logits and gate of the block's tokens, 16 at a time (rows at or past
+  // t_hi read as zero)
   const int dslice = d / kRdWarps;
   const int dbeg = warp * dslice;
-  for (int u = u_lo; u < u_hi; ++u) {
-    const int tok0 = u * kUnit;
+  for (int tok0 = t_lo; tok0 < t_hi; tok0 += kUnit) {
     float acc[NT][4];
-    tile_logits<NT, 8>(r.x, r.wr, T, d, E, tok0, 0, dbeg, dslice, acc);
+    tile_logits<NT, 8>(r.x, r.wr, t_hi, d, E, tok0, 0, dbeg, dslice, acc);
     float* mine = part + warp * kUnit * EP;
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
@@ -137,12 +120,12 @@ __global__ void __launch_bounds__(kRdThreads, 1) route_dispatch_kernel(RouterArg
     if (r.logits != nullptr) {
       for (int i = threadIdx.x; i < kUnit * E; i += kRdThreads) {
         const int rr = i / E, e = i % E, t = tok0 + rr;
-        if (t < T) r.logits[static_cast<int64_t>(t) * E + e] = part[rr * EP + e];
+        if (t < t_hi) r.logits[static_cast<int64_t>(t) * E + e] = part[rr * EP + e];
       }
     }
     {
       const int t = tok0 + warp;  // one token per warp
-      if (t < T) {
+      if (t < t_hi) {
         int id;
         float wt;
         warp_gate<1>(part + warp * EP, E, k, r.raw_weights, id, wt);
@@ -153,13 +136,12 @@ __global__ void __launch_bounds__(kRdThreads, 1) route_dispatch_kernel(RouterArg
         }
       }
     }
-    __syncthreads();  // part is rewritten by the next unit
+    __syncthreads();  // part is rewritten by the next group
   }
 
   // 2. ranks in the block, in flat (token, slot) order: 512 pairs per round,
   // match-any groups inside each warp, then an exclusive scan over the
-  // warps per expert on top of the earlier rounds' counts -> inv; the block's
-  // counts
+  // warps per expert on top of the earlier rounds' counts; the block's counts
   const uint32_t lt_mask = (1u << lane) - 1u;
   if (threadIdx.x < E) s_cnt[threadIdx.x] = 0;
   const int npairs = own * k;
@@ -182,7 +164,7 @@ __global__ void __launch_bounds__(kRdThreads, 1) route_dispatch_kernel(RouterArg
       s_cnt[threadIdx.x] = run;
     }
     __syncthreads();
-    if (e >= 0) a.inv[static_cast<int64_t>(t_lo) * k + p] = s_wcnt[warp][e] + __popc(m & lt_mask);
+    if (e >= 0) s_row[p] = s_wcnt[warp][e] + __popc(m & lt_mask);
     __syncthreads();  // s_wcnt is rewritten by the next round
   }
   if (threadIdx.x < E) a.chunk[static_cast<int64_t>(b) * E + threadIdx.x] = s_cnt[threadIdx.x];
@@ -255,22 +237,17 @@ __global__ void __launch_bounds__(kRdThreads, 1) route_dispatch_kernel(RouterArg
   }
   __syncthreads();
 
-  // 5. this block's copy share: tokens [c_lo, c_hi); global ranks -> tok,
-  // inv; each pair's padded row; then the row copy
-  const int c_lo = static_cast<int>(static_cast<int64_t>(b) * T / G);
-  const int c_hi = static_cast<int>(static_cast<int64_t>(b + 1) * T / G);
-  const int ncopy = c_hi - c_lo;
+  // 5. global ranks of the block's pairs -> tok, inv; each pair's padded row;
+  // then the row copy
   const int64_t rows = static_cast<int64_t>(a.max_mtiles) * kTileM;
-  for (int i = threadIdx.x; i < ncopy * k; i += kRdThreads) {
-    const int t = c_lo + i / k;
-    const int64_t p = static_cast<int64_t>(t) * k + i % k;
-    const int e = __ldcg(r.ids + p);
+  for (int i = threadIdx.x; i < own * k; i += kRdThreads) {
+    const int t = t_lo + i / k;
+    const int e = s_ids[i];
     int row = -1;
     if (e >= 0 && e < E) {
-      const int ob = owner_of_unit(t / kUnit, units, G);
-      const int rank = s_off[e] + s_pref[ob * E + e] + __ldcg(a.inv + p);
+      const int rank = s_off[e] + s_pref[b * E + e] + s_row[i];
       if (rank >= 0 && rank < M) {
-        a.inv[p] = rank;
+        a.inv[static_cast<int64_t>(t) * k + i % k] = rank;
         a.tok[rank] = t;
         const int64_t rw = static_cast<int64_t>(s_moff[e]) * kTileM + (rank - s_off[e]);
         if (rw >= 0 && rw < rows) row = static_cast<int>(rw);
@@ -285,7 +262,7 @@ __global__ void __launch_bounds__(kRdThreads, 1) route_dispatch_kernel(RouterArg
   // turn; each warp moves two items per round (eight loads in flight per lane)
   const int vec_per_row = d / 8;
   const int segs = (vec_per_row + kSegVec - 1) / kSegVec;
-  const int n_items = ncopy * segs;
+  const int n_items = own * segs;
   for (int it = warp; it < n_items; it += 2 * kRdWarps) {
     uint4 buf[2][kSegVec / 32];
     int tl[2] = {-1, -1};
@@ -296,7 +273,7 @@ __global__ void __launch_bounds__(kRdThreads, 1) route_dispatch_kernel(RouterArg
       if (item >= n_items) continue;  // the same for the whole warp
       tl[h] = item / segs;
       v_base[h] = (item % segs) * kSegVec;
-      const uint4* src = reinterpret_cast<const uint4*>(r.x + static_cast<int64_t>(c_lo + tl[h]) * d);
+      const uint4* src = reinterpret_cast<const uint4*>(r.x + static_cast<int64_t>(t_lo + tl[h]) * d);
 #pragma unroll
       for (int u = 0; u < kSegVec / 32; ++u) {
         const int v = v_base[h] + u * 32 + lane;
@@ -321,30 +298,22 @@ __global__ void __launch_bounds__(kRdThreads, 1) route_dispatch_kernel(RouterArg
 }
 
 template <int NT>
-size_t smem_bytes(int own_max, int copy_max, int k, int G, int E) {
-  return static_cast<size_t>(kRdWarps) * kUnit * NT * 8 * 4 + 4ull * (own_max + copy_max) * k +
-         4ull * G * E;
+size_t smem_bytes(int own_max, int k, int G, int E) {
+  return static_cast<size_t>(kRdWarps) * kUnit * NT * 8 * 4 + 8ull * own_max * k + 4ull * G * E;
 }
-
-int copy_max_of(int T, int G) { return G > 0 ? (T + G - 1) / G : 0; }
 
 }  // namespace
 
 int route_dispatch_grid(int T, int num_sms) { return T > 0 ? std::min(num_sms, 32 * kMaxGridRounds) : 0; }
 
-int route_dispatch_own_max(int T, int grid) {
-  if (grid <= 0) return 0;
-  const int units = (T + kUnit - 1) / kUnit;
-  return kUnit * ((units + grid - 1) / grid);
-}
+// tokens of the largest block share
+int route_dispatch_own_max(int T, int grid) { return grid > 0 ? (T + grid - 1) / grid : 0; }
 
 bool route_dispatch_supported(int T, int d, int E, int k, int num_sms) {
   if (E < 1 || E > kMaxExperts || k < 1 || k > E || d % 512 != 0 || T < 1) return false;
   const int grid = route_dispatch_grid(T, num_sms);
   const int own_max = route_dispatch_own_max(T, grid);
-  const int copy_max = copy_max_of(T, grid);
-  const size_t smem = E <= 8 ? smem_bytes<1>(own_max, copy_max, k, grid, E)
-                             : smem_bytes<2>(own_max, copy_max, k, grid, E);
+  const size_t smem = E <= 8 ? smem_bytes<1>(own_max, k, grid, E) : smem_bytes<2>(own_max, k, grid, E);
   if (smem > kSmemLimit) return false;
   int per_sm = 0;
   cudaError_t e = E <= 8 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, route_dispatch_kernel<1>,
@@ -379,13 +348,12 @@ cudaError_t launch_route_dispatch(const RouterArgs& r, const DispatchArgs& a, in
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const int copy_max = copy_max_of(r.T, grid);
   if (r.E <= 8) {
-    cfg.dynamicSmemBytes = smem_bytes<1>(own_max, copy_max, r.k, grid, r.E);
-    return cudaLaunchKernelEx(&cfg, route_dispatch_kernel<1>, r, a, own_max, copy_max);
+    cfg.dynamicSmemBytes = smem_bytes<1>(own_max, r.k, grid, r.E);
+    return cudaLaunchKernelEx(&cfg, route_dispatch_kernel<1>, r, a, own_max);
   }
-  cfg.dynamicSmemBytes = smem_bytes<2>(own_max, copy_max, r.k, grid, r.E);
-  return cudaLaunchKernelEx(&cfg, route_dispatch_kernel<2>, r, a, own_max, copy_max);
+  cfg.dynamicSmemBytes = smem_bytes<2>(own_max, r.k, grid, r.E);
+  return cudaLaunchKernelEx(&cfg, route_dispatch_kernel<2>, r, a, own_max);
 }
 
 }  // namespace cbmoe
