@@ -67,6 +67,7 @@ struct cb_moe {
   bool use_graphs;         // replay each forward variant from a captured CUDA graph
   bool pair_gu, pair_dn;   // bf16 gate/up, down GEMMs on CTA pairs (2-SM MMA)
   int32_t rd_grid;         // > 0: router and dispatch run as one cooperative launch of this many blocks
+  bool short_a;            // 1-CTA bf16 GEMMs load 32-row A boxes for m-tiles of at most 32 routed rows
   int32_t rank_block;      // > 0: the router ranks pairs in blocks of this many tokens
   int32_t n_rank_blocks;
   int pair_grid_gu, pair_grid_dn;
@@ -83,6 +84,7 @@ struct cb_moe {
   const void* tm_x_src;    // x pointer tm_x was encoded for
   const void* tm_xg_src;   // x pointer tm_xg was encoded for
   CUtensorMap tm_a_gu, tm_b_gu, tm_a_dn, tm_b_dn, tm_b_dn64, tm_b_gu128, tm_b_dn128, tm_y, tm_x, tm_xg, tm_wr,
+      tm_a_gu32, tm_a_dn32,
       tm_w_gu8, tm_w_dn8;
 };
 
@@ -393,7 +395,9 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
     gp.grid = h->pair_grid_gu;
     e1 = launch_grouped_gemm_pair(kGateUpSwiGLU, h->tm_a_gu, h->tm_b_gu128, h->tm_y, gp, s);
   } else {
-    e1 = launch_grouped_gemm(kGateUpSwiGLU, false, *tm_a_gu, h->tm_b_gu, h->tm_y, h->tm_b_dn64, ga, s);
+    GemmArgs g1 = ga;
+    if (!h->gather_a && h->short_a) g1.counts = h->counts;  // 32-row A boxes for tiles of few rows
+    e1 = launch_grouped_gemm(kGateUpSwiGLU, false, *tm_a_gu, h->tm_b_gu, h->tm_y, h->tm_b_dn64, h->tm_a_gu32, g1, s);
   }
   if (e1 != cudaSuccess || !mark(3)) return CB_ERR_CUDA;
 
@@ -430,7 +434,9 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
     }
     e2 = launch_grouped_gemm_pair(kDownF32, h->tm_a_dn, h->tm_b_dn128, h->tm_y, gp, s);
   } else {
-    e2 = launch_grouped_gemm(kDownF32, false, h->tm_a_dn, h->tm_b_dn, h->tm_y, h->tm_b_dn64, gd, s);
+    GemmArgs g2 = gd;
+    g2.counts = h->short_a ? h->counts : nullptr;
+    e2 = launch_grouped_gemm(kDownF32, false, h->tm_a_dn, h->tm_b_dn, h->tm_y, h->tm_b_dn64, h->tm_a_dn32, g2, s);
   }
   if (e2 != cudaSuccess || !mark(4)) return CB_ERR_CUDA;
 
@@ -737,6 +743,10 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
   const CUtensorMapSwizzle wsw = int8w ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B;
   const uint32_t brows_box = int8w ? 128 : 256;
   ok = ok && make_tmap(&h->tm_a_dn, h->hb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, f, mpad, 64, 128);
+  // 32-row boxes of the same activations, for the 1-CTA GEMMs' m-tiles of at
+  // most 32 routed rows
+  ok = ok && make_tmap(&h->tm_a_gu32, h->xp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, mpad, 64, 32);
+  ok = ok && make_tmap(&h->tm_a_dn32, h->hb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, f, mpad, 64, 32);
   ok = ok && make_tmap(&h->tm_y, h->y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, mpad, 32, 32);
   if (!int4w) {  // the bf16 and shared-memory int8 GEMMs' weight maps
     ok = ok && make_tmap(&h->tm_b_gu, h->wgu, wdt, eb, d, E * 2 * f, 64, brows_box, wsw);
@@ -789,6 +799,12 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
       ok = ok && grouped_gemm_pair_prepare(h->num_sms, &h->pair_grid_gu, &h->pair_grid_dn) == cudaSuccess;
       if (h->pair_grid_gu < 2 || h->pair_grid_dn < 2) h->pair_gu = h->pair_dn = false;
     }
+    // The 1-CTA bf16 GEMMs load only the first 32 rows of an m-tile that has
+    // at most 32 routed rows (decode sizes: 8 rows per expert at T = 64, k =
+    // 2, E = 8), so their load traffic is almost all weights.
+    // CB_MOE_SHORT_A=0 loads whole 128-row tiles.
+    const char* sav = std::getenv("CB_MOE_SHORT_A");
+    h->short_a = !(sav != nullptr && std::strcmp(sav, "0") == 0);
     // the combine fused into the CTA-pair down GEMM with CB_MOE_FUSED_COMBINE=1
     // (bf16 weights, layers that run the pair down kernel): each routed row
     // adds w * Y-row into its token's fp32 sum by vector reductions, and one

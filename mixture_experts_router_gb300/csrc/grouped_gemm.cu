@@ -44,6 +44,8 @@ constexpr int BK = 64;                   // 64 bf16 = one 128-byte swizzled row
 constexpr int BN = 256;                  // accumulator columns per tile
 constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;     // 16 KB
+constexpr int A32_ROWS = 32;              // rows of the short A box (tiles of few routed rows)
+constexpr int A32_BYTES = A32_ROWS * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;     // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int THREADS = 192;
@@ -116,7 +118,7 @@ template <int KIND>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                         const __grid_constant__ CUtensorMap tm_out, const __grid_constant__ CUtensorMap tm_b64,
-                        const GemmArgs p) {
+                        const __grid_constant__ CUtensorMap tm_a32, const GemmArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sa = smem;
@@ -141,6 +143,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     fence_barrier_init();
     prefetch_tensormap(&tm_a);
     prefetch_tensormap(&tm_b);
+    if (p.counts != nullptr) prefetch_tensormap(&tm_a32);
     if (KIND == kDownF32) {
       prefetch_tensormap(&tm_out);
       prefetch_tensormap(&tm_b64);
@@ -217,14 +220,20 @@ __global__ void __launch_bounds__(THREADS, 1)
         const Work w = decode_work(u, p, full_tiles, split);
         const int a_row = w.c.m_tile * BM;
         const int b_row = w.c.e * p.b_rows_per_expert + w.col0;
+        // A tile holding at most 32 routed rows (decode sizes) loads only its
+        // first 32 rows: the accumulator's other rows are padding that no one
+        // reads, and the SM's load traffic is then almost all weights
+        const bool a32 = p.counts != nullptr &&
+                         p.counts[w.c.e] - (w.c.m_tile - p.mtile_off[w.c.e]) * BM <= A32_ROWS;
+        const uint32_t a_bytes = a32 ? A32_BYTES : A_BYTES;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, p.wait_limit_ns)) {
             set_error(p.err, kErrTimeout);
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[stage], A_BYTES + w.nsub * BK * 2);
-          tma_load_2d(sa + stage * A_BYTES, &tm_a, &full[stage], kb * BK, a_row);
+          mbar_arrive_expect_tx(&full[stage], a_bytes + w.nsub * BK * 2);
+          tma_load_2d(sa + stage * A_BYTES, a32 ? &tm_a32 : &tm_a, &full[stage], kb * BK, a_row);
           if (w.nsub == BN) {
             tma_load_2d(sb + stage * B_BYTES, &tm_b, &full[stage], kb * BK, b_row);
           } else {
@@ -381,13 +390,15 @@ cudaError_t grouped_gemm_prepare() {
 }
 
 cudaError_t launch_grouped_gemm(GemmKind kind, bool int8_weights, const CUtensorMap& tm_a, const CUtensorMap& tm_b,
-                                const CUtensorMap& tm_out, const CUtensorMap& tm_b64, const GemmArgs& a,
-                                cudaStream_t s) {
+                                const CUtensorMap& tm_out, const CUtensorMap& tm_b64, const CUtensorMap& tm_a32,
+                                const GemmArgs& a, cudaStream_t s) {
   if (int8_weights) return cudaErrorNotSupported;
   if (kind == kGateUpSwiGLU)
-    launch_kernel(grouped_gemm_kernel<kGateUpSwiGLU>, a.grid, THREADS, Smem<kGateUpSwiGLU>::BYTES, s, tm_a, tm_b, tm_out, tm_b64, a);
+    launch_kernel(grouped_gemm_kernel<kGateUpSwiGLU>, a.grid, THREADS, Smem<kGateUpSwiGLU>::BYTES, s, tm_a, tm_b,
+                  tm_out, tm_b64, tm_a32, a);
   else
-    launch_kernel(grouped_gemm_kernel<kDownF32>, a.grid, THREADS, Smem<kDownF32>::BYTES, s, tm_a, tm_b, tm_out, tm_b64, a);
+    launch_kernel(grouped_gemm_kernel<kDownF32>, a.grid, THREADS, Smem<kDownF32>::BYTES, s, tm_a, tm_b, tm_out,
+                  tm_b64, tm_a32, a);
   return cudaGetLastError();
 }
 

@@ -242,10 +242,11 @@ enum GemmKind { kGateUpSwiGLU = 0, kDownF32 = 1 };
 // tm_out: the fp32 output Y [rows][d] with a 32 x 32 box and the 128-byte
 // swizzle, used by the down kernels' TMA-store epilogue; tm_b64: the down
 // weights with a 64-row box, for the narrower tail tiles (both ignored by
-// gate/up)
+// gate/up); tm_a32: the A operand with a 32-row box, for m-tiles of at most
+// 32 routed rows (used when a.counts is set; not with gathered rows)
 cudaError_t launch_grouped_gemm(GemmKind kind, bool int8_weights, const CUtensorMap& tm_a,
                                 const CUtensorMap& tm_b, const CUtensorMap& tm_out, const CUtensorMap& tm_b64,
-                                const GemmArgs& a, cudaStream_t s);
+                                const CUtensorMap& tm_a32, const GemmArgs& a, cudaStream_t s);
 cudaError_t grouped_gemm_prepare();  // one-time function attributes
 int grouped_gemm_tile_n(GemmKind kind);  // output columns per tile
 // bf16 on CTA pairs with the 2-SM MMA (M = 256 over m-tiles 2p, 2p+1 of one

@@ -767,3 +767,23 @@ def test_fused_route_dispatch_edges(name):
     if name == "rd_bias":
         rep = gh.full_check(synth.make_layer(synth.with_router(SMALL[name], "raw")))
         print(name, "fused raw", rep)
+
+
+@pytest.mark.parametrize("name", ["tiny", "skewed_small", "one_token_e32"])
+def test_short_activation_boxes_match_whole_tiles(name, monkeypatch):
+    """The 1-CTA GEMMs load 32-row activation boxes for m-tiles of at most 32
+    routed rows (the other accumulator rows are padding); each output row
+    depends on its own activation row only, so the outputs equal, bit for
+    bit, those of whole 128-row boxes (CB_MOE_SHORT_A=0)."""
+    layer = synth.make_layer(SMALL[name])
+    outs = []
+    for v in ("1", "0"):
+        monkeypatch.setenv("CB_MOE_SHORT_A", v)
+        gl = gh.GpuLayer(layer)
+        try:
+            gl.run()
+            outs.append((gl.out.clone(), gl.out32.clone()))
+        finally:
+            gl.close()
+    assert torch.equal(outs[0][0].view(torch.int16), outs[1][0].view(torch.int16))
+    assert torch.equal(outs[0][1], outs[1][1])
