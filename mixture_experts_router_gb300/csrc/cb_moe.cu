@@ -387,7 +387,9 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
   const bool pair_dn = !int8w && h->pair_dn;
   cudaError_t e1;
   if (int8w && h->int8_tm) {
-    e1 = launch_grouped_gemm_int8_tm(kGateUpSwiGLU, wf, h->tm_a_gu, h->tm_w_gu8, ga, s);
+    GemmArgs g1 = ga;
+    g1.counts = h->short_a ? h->counts : nullptr;  // 32-row activation boxes for single m-tiles of few rows
+    e1 = launch_grouped_gemm_int8_tm(kGateUpSwiGLU, wf, h->tm_a_gu, h->tm_w_gu8, h->tm_a_gu32, g1, s);
   } else if (int8w) {
     e1 = launch_grouped_gemm_int8(kGateUpSwiGLU, h->tm_a_gu, h->tm_b_gu, h->tm_y, ga, s);
   } else if (pair_gu) {
@@ -417,7 +419,9 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
   gd.zero1 = nullptr;
   cudaError_t e2;
   if (int8w && h->int8_tm) {
-    e2 = launch_grouped_gemm_int8_tm(kDownF32, wf, h->tm_a_dn, h->tm_w_dn8, gd, s);
+    GemmArgs g2 = gd;
+    g2.counts = h->short_a ? h->counts : nullptr;
+    e2 = launch_grouped_gemm_int8_tm(kDownF32, wf, h->tm_a_dn, h->tm_w_dn8, h->tm_a_dn32, g2, s);
   } else if (int8w) {
     e2 = launch_grouped_gemm_int8(kDownF32, h->tm_a_dn, h->tm_b_dn, h->tm_y, gd, s);
   } else if (pair_dn) {
@@ -799,10 +803,10 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
       ok = ok && grouped_gemm_pair_prepare(h->num_sms, &h->pair_grid_gu, &h->pair_grid_dn) == cudaSuccess;
       if (h->pair_grid_gu < 2 || h->pair_grid_dn < 2) h->pair_gu = h->pair_dn = false;
     }
-    // The 1-CTA bf16 GEMMs load only the first 32 rows of an m-tile that has
-    // at most 32 routed rows (decode sizes: 8 rows per expert at T = 64, k =
-    // 2, E = 8), so their load traffic is almost all weights.
-    // CB_MOE_SHORT_A=0 loads whole 128-row tiles.
+    // The 1-CTA bf16 GEMMs and the quantised GEMMs load only the first 32
+    // rows of an m-tile that has at most 32 routed rows (decode sizes: 8 rows
+    // per expert at T = 64, k = 2, E = 8), so their load traffic is almost
+    // all weights.  CB_MOE_SHORT_A=0 loads whole 128-row tiles.
     const char* sav = std::getenv("CB_MOE_SHORT_A");
     h->short_a = !(sav != nullptr && std::strcmp(sav, "0") == 0);
     // the combine fused into the CTA-pair down GEMM with CB_MOE_FUSED_COMBINE=1

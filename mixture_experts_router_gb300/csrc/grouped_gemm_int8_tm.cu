@@ -63,6 +63,8 @@ constexpr int W_ROW_BYTES = 128;       // bytes per weight row of a slot (one TM
 constexpr int STAGES = 4;
 constexpr int A_BOX = BM * BK * 2;      // 16 KB: one m-tile's 64 K of activations
 constexpr int STAGE_BYTES = 2 * A_BOX;
+constexpr int A32_ROWS = 32;            // rows of the short activation box
+constexpr int A32_BOX = A32_ROWS * BK * 2;
 constexpr int W_SLOTS = 4;
 constexpr int W_BYTES = WROWS * W_ROW_BYTES;  // 16 KB
 constexpr int THREADS = 16 * 32;
@@ -110,7 +112,7 @@ __device__ __forceinline__ PairCoord decode_pair(int tile, const GemmArgs& p) {
 template <int KIND, int WF>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_int8_tm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
-                                const GemmArgs p) {
+                                const __grid_constant__ CUtensorMap tm_x32, const GemmArgs p) {
   constexpr int KPS = WF == kWInt4 ? 4 : 2;  // k-blocks per weight slot
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -140,6 +142,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     fence_barrier_init();
     prefetch_tensormap(&tm_x);
     prefetch_tensormap(&tm_w);
+    if (p.counts != nullptr) prefetch_tensormap(&tm_x32);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, TMEM_COLS);
@@ -160,6 +163,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
         const PairCoord c = decode_pair(tile, p);
+        // a single m-tile of at most 32 routed rows (decode sizes) loads only
+        // its first 32 rows: the other token columns of the accumulator are
+        // padding that no one reads, and the SM's loads are then mostly the
+        // weights
+        const bool a32 = p.counts != nullptr && !c.two &&
+                         p.counts[c.e] - (c.m0 - p.mtile_off[c.e]) * BM <= A32_ROWS;
         for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
           const int stage = static_cast<int>(it % STAGES);
           if (!mbar_wait(&empty[stage], static_cast<uint32_t>(((it / STAGES) & 1) ^ 1), p.wait_limit_ns)) {
@@ -168,8 +177,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             break;
           }
           uint8_t* st = smem + stage * STAGE_BYTES;
-          mbar_arrive_expect_tx(&full[stage], c.two ? 2 * A_BOX : A_BOX);
-          tma_load_2d(st, &tm_x, &full[stage], kb * BK, c.m0 * BM);
+          mbar_arrive_expect_tx(&full[stage], c.two ? 2 * A_BOX : (a32 ? A32_BOX : A_BOX));
+          tma_load_2d(st, a32 ? &tm_x32 : &tm_x, &full[stage], kb * BK, c.m0 * BM);
           if (c.two) tma_load_2d(st + A_BOX, &tm_x, &full[stage], kb * BK, (c.m0 + 1) * BM);
         }
       }
@@ -447,21 +456,23 @@ cudaError_t grouped_gemm_int8_tm_prepare() {
 }
 
 template <int WF>
-static void launch_wf(GemmKind kind, const CUtensorMap& tm_x, const CUtensorMap& tm_w, const GemmArgs& a,
-                      cudaStream_t s) {
+static void launch_wf(GemmKind kind, const CUtensorMap& tm_x, const CUtensorMap& tm_w, const CUtensorMap& tm_x32,
+                      const GemmArgs& a, cudaStream_t s) {
   if (kind == kGateUpSwiGLU)
-    launch_kernel(grouped_gemm_int8_tm_kernel<kGateUpSwiGLU, WF>, a.grid, THREADS, SMEM_BYTES, s, tm_x, tm_w, a);
+    launch_kernel(grouped_gemm_int8_tm_kernel<kGateUpSwiGLU, WF>, a.grid, THREADS, SMEM_BYTES, s, tm_x, tm_w, tm_x32,
+                  a);
   else
-    launch_kernel(grouped_gemm_int8_tm_kernel<kDownF32, WF>, a.grid, THREADS, SMEM_BYTES, s, tm_x, tm_w, a);
+    launch_kernel(grouped_gemm_int8_tm_kernel<kDownF32, WF>, a.grid, THREADS, SMEM_BYTES, s, tm_x, tm_w, tm_x32, a);
 }
 
 cudaError_t launch_grouped_gemm_int8_tm(GemmKind kind, WeightFormat wf, const CUtensorMap& tm_x,
-                                        const CUtensorMap& tm_w, const GemmArgs& a, cudaStream_t s) {
+                                        const CUtensorMap& tm_w, const CUtensorMap& tm_x32, const GemmArgs& a,
+                                        cudaStream_t s) {
   if (a.k_blocks % (wf == kWInt4 ? 4 : 2) != 0) return cudaErrorInvalidValue;
   switch (wf) {
-    case kWInt8: launch_wf<kWInt8>(kind, tm_x, tm_w, a, s); break;
-    case kWInt4: launch_wf<kWInt4>(kind, tm_x, tm_w, a, s); break;
-    case kWFp8: launch_wf<kWFp8>(kind, tm_x, tm_w, a, s); break;
+    case kWInt8: launch_wf<kWInt8>(kind, tm_x, tm_w, tm_x32, a, s); break;
+    case kWInt4: launch_wf<kWInt4>(kind, tm_x, tm_w, tm_x32, a, s); break;
+    case kWFp8: launch_wf<kWFp8>(kind, tm_x, tm_w, tm_x32, a, s); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();

@@ -268,8 +268,11 @@ int grouped_gemm_int8_gateup_block();  // gate/up rows interleaved in blocks of 
 // and the 128-byte swizzle (kWInt8: int8 codes; kWFp8: e4m3 codes; kWInt4:
 // packed int4 codes with zero points, slots of K = 256)
 enum WeightFormat { kWInt8 = 0, kWInt4 = 1, kWFp8 = 2 };
+// (tm_x32: the activations with a 32-row box, for a single m-tile of at most
+// 32 routed rows; used when a.counts is set)
 cudaError_t launch_grouped_gemm_int8_tm(GemmKind kind, WeightFormat wf, const CUtensorMap& tm_x,
-                                        const CUtensorMap& tm_w, const GemmArgs& a, cudaStream_t s);
+                                        const CUtensorMap& tm_w, const CUtensorMap& tm_x32, const GemmArgs& a,
+                                        cudaStream_t s);
 cudaError_t grouped_gemm_int8_tm_prepare();
 int grouped_gemm_int8_tm_tile_n(GemmKind kind);
 int grouped_gemm_int8_tm_gateup_block();  // gate/up rows interleaved in blocks of this size
