@@ -68,6 +68,7 @@ struct cb_moe {
   bool pair_gu, pair_dn;   // bf16 gate/up, down GEMMs on CTA pairs (2-SM MMA)
   int32_t rd_grid;         // > 0: router and dispatch run as one cooperative launch of this many blocks
   bool short_a;            // 1-CTA bf16 GEMMs load 32-row A boxes for m-tiles of at most 32 routed rows
+  bool quant_wide;         // quantised GEMMs take one m-tile against two weight blocks per tile
   int32_t rank_block;      // > 0: the router ranks pairs in blocks of this many tokens
   int32_t n_rank_blocks;
   int pair_grid_gu, pair_grid_dn;
@@ -389,6 +390,10 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
   if (int8w && h->int8_tm) {
     GemmArgs g1 = ga;
     g1.counts = h->short_a ? h->counts : nullptr;  // 32-row activation boxes for single m-tiles of few rows
+    if (h->quant_wide) {  // one m-tile against two weight blocks per tile
+      g1.wide = 1;
+      g1.n_tiles = ga.n_tiles / 2;
+    }
     e1 = launch_grouped_gemm_int8_tm(kGateUpSwiGLU, wf, h->tm_a_gu, h->tm_w_gu8, h->tm_a_gu32, g1, s);
   } else if (int8w) {
     e1 = launch_grouped_gemm_int8(kGateUpSwiGLU, h->tm_a_gu, h->tm_b_gu, h->tm_y, ga, s);
@@ -421,6 +426,10 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
   if (int8w && h->int8_tm) {
     GemmArgs g2 = gd;
     g2.counts = h->short_a ? h->counts : nullptr;
+    if (h->quant_wide) {
+      g2.wide = 1;
+      g2.n_tiles = gd.n_tiles / 2;
+    }
     e2 = launch_grouped_gemm_int8_tm(kDownF32, wf, h->tm_a_dn, h->tm_w_dn8, h->tm_a_dn32, g2, s);
   } else if (int8w) {
     e2 = launch_grouped_gemm_int8(kDownF32, h->tm_a_dn, h->tm_b_dn, h->tm_y, gd, s);
@@ -809,6 +818,14 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
     // all weights.  CB_MOE_SHORT_A=0 loads whole 128-row tiles.
     const char* sav = std::getenv("CB_MOE_SHORT_A");
     h->short_a = !(sav != nullptr && std::strcmp(sav, "0") == 0);
+    // With at most 128 tokens every expert has at most one m-tile (a token's
+    // k experts are distinct), and the quantised GEMMs are bound by their
+    // per-k-block handshake, not the tensor core: each of their tiles then
+    // pairs the m-tile with two weight blocks, twice the weight bytes per
+    // handshake.  CB_MOE_WIDE_QUANT=0 keeps one weight block per tile.
+    const char* wqv = std::getenv("CB_MOE_WIDE_QUANT");
+    h->quant_wide = int8w && h->int8_tm && cfg->n_tokens <= kTileM &&
+                    !(wqv != nullptr && std::strcmp(wqv, "0") == 0);
     // the combine fused into the CTA-pair down GEMM with CB_MOE_FUSED_COMBINE=1
     // (bf16 weights, layers that run the pair down kernel): each routed row
     // adds w * Y-row into its token's fp32 sum by vector reductions, and one

@@ -45,6 +45,18 @@
 // weight slot s in tensor memory: full[s] completes on the TMA bytes and the
 // four transform warps' arrivals, empty[s] on the MMAs' commit.
 // Every wait is bounded (CB_ERR_TIMEOUT in the status word on expiry).
+//
+// WIDE tiles (layers of at most 128 tokens, where every expert has at most
+// one m-tile): a tile is the single m-tile against TWO 128-row weight blocks,
+// two M=128 N=128 MMAs per K step into two accumulators (columns 0..127 and
+// 128..255), so each k-block's handshake moves twice the weight bytes (at
+// decode sizes the per-k-block waits, not the tensor core, bound the
+// kernel).  A stage is then one activation box and a weight slot two 128-row
+// boxes (the same 192 KB of shared memory); per stage the two converted
+// blocks take 64 tensor-memory columns (256..511).  The conversion warps read
+// each k-block's codes of both rows from shared memory and release the slot
+// after its last k-block; the epilogue's two halves are the two weight blocks
+// of the same tokens.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -109,15 +121,21 @@ __device__ __forceinline__ PairCoord decode_pair(int tile, const GemmArgs& p) {
   return c;
 }
 
-template <int KIND, int WF>
+template <int KIND, int WF, bool WIDE>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_int8_tm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                                 const __grid_constant__ CUtensorMap tm_x32, const GemmArgs p) {
   constexpr int KPS = WF == kWInt4 ? 4 : 2;  // k-blocks per weight slot
+  constexpr int kStageBytes = WIDE ? A_BOX : STAGE_BYTES;     // activation boxes of a stage
+  constexpr int kWBytes = WIDE ? 2 * W_BYTES : W_BYTES;        // weight boxes of a slot
+  constexpr uint32_t kSlotCols = WIDE ? 2 * SLOT_COLS : SLOT_COLS;  // tensor-memory columns per stage
+  static_assert(STAGES * kStageBytes + W_SLOTS * kWBytes == STAGES * STAGE_BYTES + W_SLOTS * W_BYTES,
+                "both tilings use the same shared memory");
+  static_assert(A_COL0 + STAGES * kSlotCols <= TMEM_COLS, "weight slots fit the tensor memory");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* s_w = smem + STAGES * STAGE_BYTES;  // int8 weight slots (128-byte swizzled rows)
-  uint64_t* full = reinterpret_cast<uint64_t*>(s_w + W_SLOTS * W_BYTES);
+  uint8_t* s_w = smem + STAGES * kStageBytes;  // int8 weight slots (128-byte swizzled rows)
+  uint64_t* full = reinterpret_cast<uint64_t*>(s_w + W_SLOTS * kWBytes);
   uint64_t* empty = full + STAGES;
   uint64_t* w_full = empty + STAGES;
   uint64_t* w_empty = w_full + W_SLOTS;
@@ -176,7 +194,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             ok = false;
             break;
           }
-          uint8_t* st = smem + stage * STAGE_BYTES;
+          uint8_t* st = smem + stage * kStageBytes;
           mbar_arrive_expect_tx(&full[stage], c.two ? 2 * A_BOX : (a32 ? A32_BOX : A_BOX));
           tma_load_2d(st, a32 ? &tm_x32 : &tm_x, &full[stage], kb * BK, c.m0 * BM);
           if (c.two) tma_load_2d(st + A_BOX, &tm_x, &full[stage], kb * BK, (c.m0 + 1) * BM);
@@ -194,7 +212,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
         const PairCoord c = decode_pair(tile, p);
-        const int w_row = c.e * p.b_rows_per_expert + c.n * WROWS;
+        const int w_row = c.e * p.b_rows_per_expert + c.n * (WIDE ? 2 * WROWS : WROWS);
         for (int j = 0; j < p.k_blocks / KPS; ++j, ++it) {
           const int slot = static_cast<int>(it % W_SLOTS);
           if (!mbar_wait(&w_empty[slot], static_cast<uint32_t>(((it / W_SLOTS) & 1) ^ 1), p.wait_limit_ns)) {
@@ -202,8 +220,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&w_full[slot], W_BYTES);
-          tma_load_2d(s_w + slot * W_BYTES, &tm_w, &w_full[slot], j * W_ROW_BYTES, w_row);
+          mbar_arrive_expect_tx(&w_full[slot], kWBytes);
+          tma_load_2d(s_w + slot * kWBytes, &tm_w, &w_full[slot], j * W_ROW_BYTES, w_row);
+          if constexpr (WIDE) tma_load_2d(s_w + slot * kWBytes + W_BYTES, &tm_w, &w_full[slot], j * W_ROW_BYTES, w_row + WROWS);
         }
       }
       for (int64_t i = (it > W_SLOTS ? it - W_SLOTS : 0); i < it; ++i)
@@ -224,7 +243,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t idesc = c.two ? IDESC2 : IDESC1;
+        [[maybe_unused]] const uint32_t idesc = c.two ? IDESC2 : IDESC1;
         for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
           const int stage = static_cast<int>(it % STAGES);
           if (!mbar_wait(&full[stage], static_cast<uint32_t>((it / STAGES) & 1), p.wait_limit_ns)) {
@@ -233,11 +252,18 @@ __global__ void __launch_bounds__(THREADS, 1)
             break;
           }
           tc_fence_after();
-          const uint64_t b = sw128_desc(smem_u32(smem + stage * STAGE_BYTES));
-          const uint32_t a = tmem_base + A_COL0 + static_cast<uint32_t>(stage) * SLOT_COLS;
+          const uint64_t b = sw128_desc(smem_u32(smem + stage * kStageBytes));
+          const uint32_t a = tmem_base + A_COL0 + static_cast<uint32_t>(stage) * kSlotCols;
 #pragma unroll
-          for (int ks = 0; ks < BK / 16; ++ks)
-            tc_mma_f16_ts(tmem_base, a + 8 * ks, b + 2 * ks, idesc, (kb | ks) != 0 ? 1u : 0u);
+          for (int ks = 0; ks < BK / 16; ++ks) {
+            if constexpr (WIDE) {
+              const uint32_t acc = (kb | ks) != 0 ? 1u : 0u;
+              tc_mma_f16_ts(tmem_base, a + 8 * ks, b + 2 * ks, IDESC1, acc);
+              tc_mma_f16_ts(tmem_base + BM, a + SLOT_COLS + 8 * ks, b + 2 * ks, IDESC1, acc);
+            } else {
+              tc_mma_f16_ts(tmem_base, a + 8 * ks, b + 2 * ks, idesc, (kb | ks) != 0 ? 1u : 0u);
+            }
+          }
           tc_commit(&empty[stage]);
         }
         if (!ok) break;
@@ -248,7 +274,102 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_commit(mma_done);
       if (!mbar_wait(mma_done, 0, p.wait_limit_ns)) set_error(p.err, kErrTimeout);
     }
-  } else if (warp >= XFORM_WARP0 && warp < XFORM_WARP0 + 4) {
+  } else if (WIDE && warp >= XFORM_WARP0 && warp < XFORM_WARP0 + 4) {
+    // ---------------------------- int8 / int4 / fp8 -> bf16, wide tiles
+    // Thread (q, lane) owns row r = 32q + lane of both weight blocks (TMEM
+    // lane r of both regions).  Per k-block it reads that k-block's codes of
+    // both rows from the slot (the TMA 128-byte swizzle as below), converts
+    // them and stores them into the stage's two 32-column regions; the slot
+    // is released after its last k-block.
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    int64_t it = 0, wi = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+      uint32_t zz[2] = {0u, 0u};  // int4: 0x4300 | zero point of block 0's and block 1's row r
+      if constexpr (WF == kWInt4) {
+        const PairCoord c = decode_pair(tile, p);
+#pragma unroll
+        for (int blk = 0; blk < 2; ++blk) {
+          const int nb = 2 * c.n + blk;
+          int z;
+          if constexpr (KIND == kGateUpSwiGLU) {
+            const int feat = nb * (WROWS / 2) + (r / 32) * GATEUP_GROUP + (r % GATEUP_GROUP);
+            z = __ldg((r % 32 < GATEUP_GROUP ? p.zero0 : p.zero1) + static_cast<int64_t>(c.e) * p.ld_out + feat);
+          } else {
+            z = __ldg(p.zero0 + static_cast<int64_t>(c.e) * p.ld_out + nb * WROWS + r);
+          }
+          zz[blk] = (0x4300u | static_cast<uint32_t>(z)) * 0x00010001u;
+        }
+      }
+      int slot = 0;
+      for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
+        const int stage = static_cast<int>(it % STAGES);
+        if ((kb % KPS) == 0) {
+          slot = static_cast<int>(wi % W_SLOTS);
+          if (!mbar_wait(&w_full[slot], static_cast<uint32_t>((wi / W_SLOTS) & 1), p.wait_limit_ns)) {
+            set_error(p.err, kErrTimeout);
+            ok = false;
+            break;
+          }
+          ++wi;
+        }
+        if (!mbar_wait(&empty[stage], static_cast<uint32_t>(((it / STAGES) & 1) ^ 1), p.wait_limit_ns)) {
+          set_error(p.err, kErrTimeout);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int blk = 0; blk < 2; ++blk) {
+          const uint8_t* row = s_w + slot * kWBytes + blk * W_BYTES + r * 128;
+          uint32_t o[32];
+          if constexpr (WF != kWInt4) {
+            const int c0 = (kb & 1) * 4;  // 16-byte chunks c0..c0+3: this k-block's 64 codes
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+              const uint4 w = *reinterpret_cast<const uint4*>(row + (((c0 + cc) ^ (r & 7)) << 4));
+              byte4_to_bf16x4<WF>(w.x, o[8 * cc + 0], o[8 * cc + 1]);
+              byte4_to_bf16x4<WF>(w.y, o[8 * cc + 2], o[8 * cc + 3]);
+              byte4_to_bf16x4<WF>(w.z, o[8 * cc + 4], o[8 * cc + 5]);
+              byte4_to_bf16x4<WF>(w.w, o[8 * cc + 6], o[8 * cc + 7]);
+            }
+          } else {
+            const int part = kb & 3;  // chunks 2 part, 2 part + 1: 64 codes
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+              const uint4 w = *reinterpret_cast<const uint4*>(row + (((2 * part + cc) ^ (r & 7)) << 4));
+              uint32_t t[4];
+              int4x8_minus_zero_to_bf16(w.x, zz[blk], t);
+#pragma unroll
+              for (int m = 0; m < 4; ++m) o[16 * cc + m] = t[m];
+              int4x8_minus_zero_to_bf16(w.y, zz[blk], t);
+#pragma unroll
+              for (int m = 0; m < 4; ++m) o[16 * cc + 4 + m] = t[m];
+              int4x8_minus_zero_to_bf16(w.z, zz[blk], t);
+#pragma unroll
+              for (int m = 0; m < 4; ++m) o[16 * cc + 8 + m] = t[m];
+              int4x8_minus_zero_to_bf16(w.w, zz[blk], t);
+#pragma unroll
+              for (int m = 0; m < 4; ++m) o[16 * cc + 12 + m] = t[m];
+            }
+          }
+          tmem_store32(lane_addr + A_COL0 + static_cast<uint32_t>(stage) * kSlotCols +
+                           static_cast<uint32_t>(blk) * SLOT_COLS,
+                       o);
+        }
+        if ((kb % KPS) == KPS - 1) {  // the slot's last k-block: its codes are all read
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&w_empty[slot]);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[stage]);
+      }
+    }
+  } else if (!WIDE && warp >= XFORM_WARP0 && warp < XFORM_WARP0 + 4) {
     // ------------------------------------------- int8 / int4 -> bf16 transform
     // Thread (q, lane) owns weight row r = 32q + lane of the tile, i.e. TMEM
     // lane r.  Per weight slot (KPS k-blocks) it reads the row's 128 bytes
@@ -366,14 +487,16 @@ __global__ void __launch_bounds__(THREADS, 1)
         break;
       }
       tc_fence_after();
-      const bool active = half == 0 || c.two;
-      const int64_t row0 = static_cast<int64_t>(c.m0 + half) * BM;
+      // WIDE: the halves are the two weight blocks of the same tokens
+      const bool active = WIDE || half == 0 || c.two;
+      const int64_t row0 = static_cast<int64_t>(c.m0 + (WIDE ? 0 : half)) * BM;
+      const int nblk = WIDE ? 2 * c.n + half : c.n;  // weight block of this half
       if constexpr (KIND == kGateUpSwiGLU) {
         // lane j < 16 holds gate feature n*64 + 16q + j, lane j + 16 its up row:
         // per token pair (2m, 2m+1) a shuffle gives the gate lane u(2m) and
         // the up lane g(2m+1); each computes one h
         const bool gate = lane < GATEUP_GROUP;
-        const int64_t feat = static_cast<int64_t>(c.n) * (WROWS / 2) + q * GATEUP_GROUP + (lane & (GATEUP_GROUP - 1));
+        const int64_t feat = static_cast<int64_t>(nblk) * (WROWS / 2) + q * GATEUP_GROUP + (lane & (GATEUP_GROUP - 1));
         uint32_t hp[32];  // chunk ci, pair k: h of tokens ci*32 + 4k + (0|1) + {0, 2}
         if (active) {
           const float scale = __ldg((gate ? p.scale0 : p.scale1) + static_cast<int64_t>(c.e) * p.ld_out + feat);
@@ -408,7 +531,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       } else {
         if (active) {
-          const int64_t col = static_cast<int64_t>(c.n) * WROWS + q * 32 + lane;
+          const int64_t col = static_cast<int64_t>(nblk) * WROWS + q * 32 + lane;
           const float scale = __ldg(p.scale0 + static_cast<int64_t>(c.e) * p.ld_out + col);
           float* ycol = static_cast<float*>(p.out) + row0 * p.ld_out + col;
 #pragma unroll 1
@@ -446,23 +569,39 @@ cudaError_t grouped_gemm_int8_tm_prepare() {
   auto set = [&](auto fn) {
     if (e == cudaSuccess) e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   };
-  set(grouped_gemm_int8_tm_kernel<kGateUpSwiGLU, kWInt8>);
-  set(grouped_gemm_int8_tm_kernel<kDownF32, kWInt8>);
-  set(grouped_gemm_int8_tm_kernel<kGateUpSwiGLU, kWInt4>);
-  set(grouped_gemm_int8_tm_kernel<kDownF32, kWInt4>);
-  set(grouped_gemm_int8_tm_kernel<kGateUpSwiGLU, kWFp8>);
-  set(grouped_gemm_int8_tm_kernel<kDownF32, kWFp8>);
+  set(grouped_gemm_int8_tm_kernel<kGateUpSwiGLU, kWInt8, false>);
+  set(grouped_gemm_int8_tm_kernel<kDownF32, kWInt8, false>);
+  set(grouped_gemm_int8_tm_kernel<kGateUpSwiGLU, kWInt4, false>);
+  set(grouped_gemm_int8_tm_kernel<kDownF32, kWInt4, false>);
+  set(grouped_gemm_int8_tm_kernel<kGateUpSwiGLU, kWFp8, false>);
+  set(grouped_gemm_int8_tm_kernel<kDownF32, kWFp8, false>);
+  set(grouped_gemm_int8_tm_kernel<kGateUpSwiGLU, kWInt8, true>);
+  set(grouped_gemm_int8_tm_kernel<kDownF32, kWInt8, true>);
+  set(grouped_gemm_int8_tm_kernel<kGateUpSwiGLU, kWInt4, true>);
+  set(grouped_gemm_int8_tm_kernel<kDownF32, kWInt4, true>);
+  set(grouped_gemm_int8_tm_kernel<kGateUpSwiGLU, kWFp8, true>);
+  set(grouped_gemm_int8_tm_kernel<kDownF32, kWFp8, true>);
   return e;
 }
 
-template <int WF>
+template <int WF, bool WIDE>
 static void launch_wf(GemmKind kind, const CUtensorMap& tm_x, const CUtensorMap& tm_w, const CUtensorMap& tm_x32,
                       const GemmArgs& a, cudaStream_t s) {
   if (kind == kGateUpSwiGLU)
-    launch_kernel(grouped_gemm_int8_tm_kernel<kGateUpSwiGLU, WF>, a.grid, THREADS, SMEM_BYTES, s, tm_x, tm_w, tm_x32,
-                  a);
+    launch_kernel(grouped_gemm_int8_tm_kernel<kGateUpSwiGLU, WF, WIDE>, a.grid, THREADS, SMEM_BYTES, s, tm_x, tm_w,
+                  tm_x32, a);
   else
-    launch_kernel(grouped_gemm_int8_tm_kernel<kDownF32, WF>, a.grid, THREADS, SMEM_BYTES, s, tm_x, tm_w, tm_x32, a);
+    launch_kernel(grouped_gemm_int8_tm_kernel<kDownF32, WF, WIDE>, a.grid, THREADS, SMEM_BYTES, s, tm_x, tm_w,
+                  tm_x32, a);
+}
+
+template <int WF>
+static void launch_w(GemmKind kind, const CUtensorMap& tm_x, const CUtensorMap& tm_w, const CUtensorMap& tm_x32,
+                     const GemmArgs& a, cudaStream_t s) {
+  if (a.wide)
+    launch_wf<WF, true>(kind, tm_x, tm_w, tm_x32, a, s);
+  else
+    launch_wf<WF, false>(kind, tm_x, tm_w, tm_x32, a, s);
 }
 
 cudaError_t launch_grouped_gemm_int8_tm(GemmKind kind, WeightFormat wf, const CUtensorMap& tm_x,
@@ -470,9 +609,9 @@ cudaError_t launch_grouped_gemm_int8_tm(GemmKind kind, WeightFormat wf, const CU
                                         cudaStream_t s) {
   if (a.k_blocks % (wf == kWInt4 ? 4 : 2) != 0) return cudaErrorInvalidValue;
   switch (wf) {
-    case kWInt8: launch_wf<kWInt8>(kind, tm_x, tm_w, tm_x32, a, s); break;
-    case kWInt4: launch_wf<kWInt4>(kind, tm_x, tm_w, tm_x32, a, s); break;
-    case kWFp8: launch_wf<kWFp8>(kind, tm_x, tm_w, tm_x32, a, s); break;
+    case kWInt8: launch_w<kWInt8>(kind, tm_x, tm_w, tm_x32, a, s); break;
+    case kWInt4: launch_w<kWInt4>(kind, tm_x, tm_w, tm_x32, a, s); break;
+    case kWFp8: launch_w<kWFp8>(kind, tm_x, tm_w, tm_x32, a, s); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();

@@ -237,6 +237,10 @@ struct GemmArgs {
   const int32_t* comb_ids;
   const float* comb_w;
   int32_t top_k;
+  // quantised tensor-memory GEMMs: tiles of one m-tile against two weight
+  // blocks (every expert must have at most one m-tile; n_tiles counts pairs
+  // of weight blocks)
+  int32_t wide;
 };
 enum GemmKind { kGateUpSwiGLU = 0, kDownF32 = 1 };
 // tm_out: the fp32 output Y [rows][d] with a 32 x 32 box and the 128-byte

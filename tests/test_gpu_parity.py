@@ -47,6 +47,11 @@ SMALL = {
     "rd_long": synth.custom_shape("rd_long", T=40000, d=512, f=256, E=8, k=2, seed=103),
     "rd_e16_k16": synth.custom_shape("rd_e16_k16", T=333, d=1024, f=256, E=16, k=16, seed=104),
     "rd_bias": synth.custom_shape("rd_bias", T=500, d=512, f=256, E=12, k=3, bias=True, seed=105),
+    # quantised layers of at most 128 tokens: wide tiles (one m-tile, two weight blocks)
+    "int8_wide": synth.custom_shape("int8_wide", T=100, d=512, f=768, E=8, k=2, wdtype="int8", seed=111),
+    "int4_wide": synth.custom_shape("int4_wide", T=64, d=256, f=512, E=8, k=2, wdtype="int4", seed=112),
+    "fp8_wide": synth.custom_shape("fp8_wide", T=128, d=512, f=512, E=4, k=2, wdtype="fp8", seed=113),
+    "int8_wide_e64": synth.custom_shape("int8_wide_e64", T=100, d=256, f=512, E=64, k=6, wdtype="int8", seed=114),
 }
 
 FULL = {  # workload: random tokens checked beyond the first and last row of every m-tile (None: every token)
@@ -152,7 +157,7 @@ def test_forwards_inside_a_caller_graph():
 
 
 GUARD_CASES = [
-    ("tiny", {}), ("odd_T", {}), ("ragged_mid", {"CB_MOE_PAIR": "1"}), ("ragged_mid", {"CB_MOE_ROUTE_DISPATCH": "0"}),
+    ("tiny", {}), ("odd_T", {}), ("int8_wide", {}), ("int4_wide", {}), ("ragged_mid", {"CB_MOE_PAIR": "1"}), ("ragged_mid", {"CB_MOE_ROUTE_DISPATCH": "0"}),
     ("many_units", {}),
     ("ragged_mid", {"CB_MOE_PAIR": "1", "CB_MOE_FUSED_COMBINE": "1"}), ("ragged_mid", {"CB_MOE_GATHER": "1"}),
     ("three_mtiles", {"CB_MOE_PAIR": "1"}), ("skewed_small", {}), ("skewed_small", {"CB_MOE_DISPATCH": "split"}),
@@ -787,3 +792,59 @@ def test_short_activation_boxes_match_whole_tiles(name, monkeypatch):
             gl.close()
     assert torch.equal(outs[0][0].view(torch.int16), outs[1][0].view(torch.int16))
     assert torch.equal(outs[0][1], outs[1][1])
+
+
+WIDE_SMALL = ["int8_wide", "int4_wide", "fp8_wide", "int8_wide_e64"]
+
+
+@pytest.mark.parametrize("name", WIDE_SMALL)
+def test_wide_quantised_tiles_small(name):
+    """Quantised layers of at most 128 tokens: each tile pairs the single
+    m-tile with two weight blocks (two accumulators, twice the weight bytes
+    per k-block handshake); same routing and outputs as the oracle."""
+    rep = gh.full_check(synth.make_layer(SMALL[name]))
+    print(name, "wide", rep)
+
+
+@pytest.mark.parametrize("wdtype", ["int8", "int4", "fp8"])
+def test_wide_quantised_tiles_decode_shape(wdtype):
+    """The Mixtral decode shape (T=64, d=4096, f=14336, E=8, top-2) with
+    quantised weights, every token checked against the oracle."""
+    shape = synth.custom_shape(f"{wdtype}_decode", T=64, d=4096, f=14336, E=8, k=2, wdtype=wdtype, seed=115)
+    rep = gh.full_check(synth.make_layer(shape))
+    print(wdtype, "decode shape wide", rep)
+
+
+@pytest.mark.parametrize("name", WIDE_SMALL)
+def test_wide_quantised_tiles_match_one_block_tiles(name, monkeypatch):
+    """Wide tiles run the same M=128 N=128 MMAs in the same K order as tiles of
+    one weight block (CB_MOE_WIDE_QUANT=0): the outputs agree bit for bit."""
+    layer = synth.make_layer(SMALL[name])
+    outs = []
+    for v in ("1", "0"):
+        monkeypatch.setenv("CB_MOE_WIDE_QUANT", v)
+        gl = gh.GpuLayer(layer)
+        try:
+            gl.run()
+            outs.append((gl.out.clone(), gl.out32.clone()))
+        finally:
+            gl.close()
+    assert torch.equal(outs[0][0].view(torch.int16), outs[1][0].view(torch.int16))
+    assert torch.equal(outs[0][1], outs[1][1])
+
+
+@pytest.mark.parametrize("wdtype", ["int8", "int4"])
+def test_wide_quantised_tiles_timeout(wdtype):
+    """A bounded device wait that nothing satisfies, on the wide tiles: the
+    kernel ends with CB_ERR_TIMEOUT and the context stays usable."""
+    import mixture_experts_router_gb300 as cb
+    layer = synth.make_layer(SMALL[f"{wdtype}_wide"])
+    gl = gh.GpuLayer(layer, flags=cb.CB_FLAG_TEST_STALL)
+    try:
+        gl.m.forward(gl.x, gl.out)
+        torch.cuda.synchronize()
+        assert gl.m.last_error() == cb.CB_ERR_TIMEOUT
+    finally:
+        gl.close()
+    rep = gh.full_check(layer)
+    assert rep["f32_max_abs"] <= gh.MAX_ABS
