@@ -67,6 +67,7 @@ struct cb_moe {
   bool use_graphs;         // replay each forward variant from a captured CUDA graph
   bool pair_gu, pair_dn;   // bf16 gate/up, down GEMMs on CTA pairs (2-SM MMA)
   int32_t rd_grid;         // > 0: router and dispatch run as one cooperative launch of this many blocks
+  int32_t rd_box;          // the tcgen05 form's x box rows (a block's token share)
   bool short_a;            // 1-CTA bf16 GEMMs load 32-row A boxes for m-tiles of at most 32 routed rows
   bool quant_wide;         // quantised GEMMs take one m-tile against two weight blocks per tile
   int32_t rank_block;      // > 0: the router ranks pairs in blocks of this many tokens
@@ -293,11 +294,13 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
     if (launch_router_hash(ha, s) != cudaSuccess || !mark(1)) return CB_ERR_CUDA;
   } else if (h->router_tc) {
     if (h->tm_x_src != x) {
-      if (!make_tmap(&h->tm_x, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c.d_model, c.n_tokens, 64, 128))
+      const uint32_t box = h->rd_grid > 0 ? static_cast<uint32_t>(h->rd_box) : 128u;
+      if (!make_tmap(&h->tm_x, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c.d_model, c.n_tokens, 64, box))
         return CB_ERR_CUDA;
       h->tm_x_src = x;
     }
-    if (launch_router_tc(h->tm_x, h->tm_wr, ra, h->rpart, h->num_sms, s) != cudaSuccess || !mark(1))
+    if (h->rd_grid <= 0 &&
+        (launch_router_tc(h->tm_x, h->tm_wr, ra, h->rpart, h->num_sms, s) != cudaSuccess || !mark(1)))
       return CB_ERR_CUDA;
   } else if (h->rd_grid <= 0) {
     if (launch_router(ra, s) != cudaSuccess || !mark(1)) return CB_ERR_CUDA;
@@ -334,12 +337,14 @@ cb_status_t enqueue_forward(cb_moe_t* h, const void* x, void* out, bool f32out, 
     da.test_stall = 1;
     da.wait_limit_ns = 1000000ull;  // 1 ms
   }
-  if (h->rd_grid > 0 && c.router_mode != CB_ROUTER_HASH && !h->router_tc) {
+  if (h->rd_grid > 0 && c.router_mode != CB_ROUTER_HASH) {
     // router and dispatch in one launch: the router stage ends with it and
     // the dispatch stage is empty
     ra.blk_counts = nullptr;
     ra.local_rank = nullptr;
-    if (launch_route_dispatch(ra, da, h->rd_grid, s) != cudaSuccess || !mark(1) || !mark(2)) return CB_ERR_CUDA;
+    const cudaError_t e = h->router_tc ? launch_route_dispatch_tc(h->tm_x, h->tm_wr, ra, da, h->rd_grid, h->rd_box, s)
+                                       : launch_route_dispatch(ra, da, h->rd_grid, s);
+    if (e != cudaSuccess || !mark(1) || !mark(2)) return CB_ERR_CUDA;
   } else if (launch_dispatch(da, s) != cudaSuccess || !mark(2)) {
     return CB_ERR_CUDA;
   }
@@ -611,7 +616,8 @@ cb_status_t cb_moe_kernels_per_forward(const cb_moe_t* h, int32_t* n) {
     return CB_OK;
   }
   int32_t dispatch;
-  if (h->rd_grid > 0 && c.router_mode != CB_ROUTER_HASH && !h->router_tc)
+  const bool fused = h->rd_grid > 0 && c.router_mode != CB_ROUTER_HASH;
+  if (fused)
     dispatch = 0;  // in the router's launch
   else if (h->rank_block > 0)
     dispatch = 2;  // block-count scan + row copy (which also finalises the ranks)
@@ -619,7 +625,8 @@ cb_status_t cb_moe_kernels_per_forward(const cb_moe_t* h, int32_t* n) {
     dispatch = 1;  // count, scan, ranks and row copy in one cooperative launch
   else
     dispatch = (static_cast<int64_t>(c.n_tokens) * c.top_k <= kDispatchSmallPairs ? 1 : 3) + (h->gather_a ? 0 : 1);
-  const int32_t router = (h->router_tc && c.router_mode != CB_ROUTER_HASH) ? 2 : 1;  // tcgen05: partials + top-k
+  // the separate tcgen05 router: partials + top-k
+  const int32_t router = (h->router_tc && c.router_mode != CB_ROUTER_HASH && !fused) ? 2 : 1;
   *n = router + dispatch + 2 + 1;
   return CB_OK;
 }
@@ -777,7 +784,7 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
   ok = ok && grouped_gemm_prepare() == cudaSuccess && grouped_gemm_int8_prepare() == cudaSuccess &&
        grouped_gemm_int8_tm_prepare() == cudaSuccess &&
        router_prepare() == cudaSuccess && router_tc_prepare() == cudaSuccess && dispatch_prepare() == cudaSuccess &&
-       route_dispatch_prepare() == cudaSuccess;
+       route_dispatch_prepare() == cudaSuccess && route_dispatch_tc_prepare() == cudaSuccess;
   // router: tcgen05 for wide expert counts, the mma.sync split-K router for
   // E <= 16 (bound by reading x, where more CTAs help); CB_MOE_ROUTER=tc|mma
   // overrides the choice
@@ -861,19 +868,26 @@ cb_status_t cb_moe_init(const cb_moe_config_t* cfg, const cb_moe_weights_t* wts,
       h->rank_block = rb;
       h->n_rank_blocks = static_cast<int32_t>(nb);
     }
-    // With the mma router and up to 16 experts (d a multiple of 512), the
-    // router, the ranking and the row copy run as one cooperative launch that
-    // reads x from HBM once (the copy finds its rows in L2) and needs no scan
-    // kernel in between.  CB_MOE_ROUTE_DISPATCH=0 keeps the separate router
-    // and dispatch kernels; CB_MOE_FUSED_RANKS=0 implies it.
+    // The router, the ranking and the row copy run as one cooperative launch
+    // that reads x from HBM once (the copy finds its rows in L2) and needs no
+    // scan kernel in between: with the mma router for up to 16 experts (d a
+    // multiple of 512), with the tcgen05 router for 17 to 256 (d a multiple
+    // of 64).  CB_MOE_ROUTE_DISPATCH=0 keeps the separate router and dispatch
+    // kernels; CB_MOE_FUSED_RANKS=0 implies it.
     const char* rdv = std::getenv("CB_MOE_ROUTE_DISPATCH");
     h->rd_grid = 0;
-    if (!h->router_tc && !hashr && fused_ranks && !(rdv != nullptr && std::strcmp(rdv, "0") == 0) &&
-        static_cast<int64_t>(cfg->n_tokens) * cfg->top_k + 128ll * cfg->n_experts < (1ll << 31) &&
+    h->rd_box = 0;
+    const bool rd_ok = !hashr && fused_ranks && !(rdv != nullptr && std::strcmp(rdv, "0") == 0) &&
+                       static_cast<int64_t>(cfg->n_tokens) * cfg->top_k + 128ll * cfg->n_experts < (1ll << 31);
+    if (rd_ok && !h->router_tc &&
         route_dispatch_supported(cfg->n_tokens, cfg->d_model, cfg->n_experts, cfg->top_k, h->num_sms)) {
       h->rd_grid = route_dispatch_grid(cfg->n_tokens, h->num_sms);
       h->rank_block = 0;
       h->n_rank_blocks = 0;
+    } else if (rd_ok && h->router_tc &&
+               route_dispatch_tc_supported(cfg->n_tokens, cfg->d_model, cfg->n_experts, cfg->top_k, h->num_sms)) {
+      h->rd_grid = route_dispatch_tc_grid(cfg->n_tokens, h->num_sms);
+      h->rd_box = route_dispatch_tc_box_rows(cfg->n_tokens, h->rd_grid);
     }
     // Otherwise (tcgen05 and hash routers, or CB_MOE_FUSED_RANKS=0) the
     // dispatch ranks the pairs itself.  Up to 65536 routed pairs its

@@ -184,6 +184,20 @@ bool route_dispatch_supported(int T, int d, int E, int k, int num_sms);
 int route_dispatch_grid(int T, int num_sms);
 cudaError_t route_dispatch_prepare();  // one-time function attributes
 cudaError_t launch_route_dispatch(const RouterArgs& r, const DispatchArgs& a, int grid, cudaStream_t s);
+// tokens of the largest block share of a launch of `grid` blocks
+int route_dispatch_own_max(int T, int grid);
+// The tcgen05 router and the dispatch in one cooperative launch, for
+// 16 < E <= 256 and d a multiple of 64 (route_dispatch_tc_supported checks
+// the shared memory, the count rows and the residency).  tm_x: x, bf16
+// [T][d], box 64 x route_dispatch_tc_box_rows(T, grid) (the rows a block
+// owns); tm_w: the router weights, box 64 x router_tc_rows(E).  Uses
+// a.chunk ([grid][E]), a.bar, a.test_stall and a.wait_limit_ns.
+bool route_dispatch_tc_supported(int T, int d, int E, int k, int num_sms);
+int route_dispatch_tc_grid(int T, int num_sms);
+int route_dispatch_tc_box_rows(int T, int grid);
+cudaError_t route_dispatch_tc_prepare();  // one-time function attributes
+cudaError_t launch_route_dispatch_tc(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const RouterArgs& r,
+                                     const DispatchArgs& a, int grid, int box_rows, cudaStream_t s);
 
 // ----------------------------------------------------------------- combine
 struct CombineArgs {

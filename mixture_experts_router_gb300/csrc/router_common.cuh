@@ -15,18 +15,6 @@
 namespace cbmoe {
 namespace router_detail {
 
-struct Cand {
-  float v;
-  int idx;
-  int cls;  // 0 number, 1 NaN, 2 not available (padding or already taken)
-};
-
-__device__ __forceinline__ bool ranks_before(const Cand& a, const Cand& b) {
-  if (a.cls != b.cls) return a.cls < b.cls;
-  if (a.cls == 0 && a.v != b.v) return a.v > b.v;
-  return a.idx < b.idx;
-}
-
 __device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -89,47 +77,61 @@ __device__ __forceinline__ void tile_logits(const uint16_t* x, const uint16_t* w
   }
 }
 
+// Order of a logit as an unsigned key, larger first: numbers by value (-0
+// folded into +0, so the two zeros tie), then NaN (1); 0 is left for a
+// candidate that is padding or already taken.
+__device__ __forceinline__ uint32_t gate_key(float v) {
+  if (isnan(v)) return 1u;
+  uint32_t b = __float_as_uint(v);
+  if (b == 0x80000000u) b = 0u;
+  const uint32_t h = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  return h < 2u ? 2u : h;  // numbers stay above NaN (only NaN bit patterns could map lower)
+}
+
 // The gate of one token from its logits row ls[0..E) (shared memory), by one
-// warp: k rounds of a warp arg-max.  Lane s < k returns the s-th expert in
-// (id) and its weight (w); other lanes return id = -1.
+// warp: k rounds of a warp arg-max.  Lane l holds experts l, l + 32, ...
+// (PER of them); a round takes the largest key in the lane (the lower
+// expert on equal keys), then the warp's largest key and, among the lanes
+// holding it, the lowest expert index (two warp reductions).  Lane s < k
+// returns the s-th expert in (id) and its weight (w); other lanes return
+// id = -1.  Registers only: the candidates are never indexed by a value.
 template <int PER>
 __device__ __forceinline__ void warp_gate(const float* ls, int E, int k, int raw_weights, int& id, float& w) {
   const int lane = threadIdx.x % 32;
-  Cand cand[PER];
+  float v[PER];
+  uint32_t key[PER];
 #pragma unroll
   for (int p = 0; p < PER; ++p) {
     const int e = lane + 32 * p;
-    if (e < E) {
-      const float v = ls[e];
-      cand[p] = Cand{v, e, isnan(v) ? 1 : 0};
-    } else {
-      cand[p] = Cand{0.f, e, 2};
-    }
+    v[p] = e < E ? ls[e] : 0.f;
+    key[p] = e < E ? gate_key(v[p]) : 0u;
   }
   float my_v = 0.f, l0 = 0.f;
   int my_i = -1;
   for (int s = 0; s < k; ++s) {
-    Cand b = cand[0];
+    uint32_t bk = key[0];
+    int bj = 0;
+    float bv = v[0];
 #pragma unroll
     for (int p = 1; p < PER; ++p)
-      if (ranks_before(cand[p], b)) b = cand[p];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      Cand other;
-      other.v = __shfl_xor_sync(0xffffffffu, b.v, o);
-      other.idx = __shfl_xor_sync(0xffffffffu, b.idx, o);
-      other.cls = __shfl_xor_sync(0xffffffffu, b.cls, o);
-      if (ranks_before(other, b)) b = other;
-    }
-    if ((b.idx & 31) == lane) {
+      if (key[p] > bk) {  // strictly larger: the lower expert keeps a tie
+        bk = key[p];
+        bj = p;
+        bv = v[p];
+      }
+    const uint32_t wk = __reduce_max_sync(0xffffffffu, bk);
+    const uint32_t we = __reduce_min_sync(0xffffffffu, bk == wk ? static_cast<uint32_t>(lane + 32 * bj) : ~0u);
+    const int owner = static_cast<int>(we & 31u);
+    const float sv = __shfl_sync(0xffffffffu, bv, owner);
+    if (lane == owner) {
 #pragma unroll
       for (int p = 0; p < PER; ++p)
-        if (p == (b.idx >> 5)) cand[p].cls = 2;
+        if (p == bj) key[p] = 0u;
     }
-    if (s == 0) l0 = b.v;
+    if (s == 0) l0 = sv;
     if (lane == s) {
-      my_v = b.v;
-      my_i = b.idx;
+      my_v = sv;
+      my_i = static_cast<int>(we);
     }
   }
   const float ex = (lane < k) ? expf(my_v - l0) : 0.f;
@@ -138,6 +140,75 @@ __device__ __forceinline__ void warp_gate(const float* ls, int E, int k, int raw
   for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
   id = lane < k ? my_i : -1;
   w = raw_weights ? my_v : ex / sum;
+}
+
+// warp_gate for up to N rows at once (rows ls, ls + stride, ...; the first
+// nrows of them are tokens): the same steps for each row, interleaved so
+// that the rows' reductions overlap.  Lane s < k of row n returns its s-th
+// expert in id[n] and its weight in w[n]; rows past nrows return nothing
+// meaningful.
+template <int PER, int N>
+__device__ __forceinline__ void warp_gate_rows(const float* ls, int stride, int nrows, int E, int k,
+                                               int raw_weights, int (&id)[N], float (&w)[N]) {
+  const int lane = threadIdx.x % 32;
+  float v[N][PER];
+  uint32_t key[N][PER];
+#pragma unroll
+  for (int n = 0; n < N; ++n)
+#pragma unroll
+    for (int p = 0; p < PER; ++p) {
+      const int e = lane + 32 * p;
+      const bool in = n < nrows && e < E;
+      v[n][p] = in ? ls[n * stride + e] : 0.f;
+      key[n][p] = in ? gate_key(v[n][p]) : 0u;
+    }
+  float my_v[N], l0[N];
+  int my_i[N];
+#pragma unroll
+  for (int n = 0; n < N; ++n) {
+    my_v[n] = 0.f;
+    l0[n] = 0.f;
+    my_i[n] = -1;
+  }
+  for (int s = 0; s < k; ++s) {
+#pragma unroll
+    for (int n = 0; n < N; ++n) {
+      uint32_t bk = key[n][0];
+      int bj = 0;
+      float bv = v[n][0];
+#pragma unroll
+      for (int p = 1; p < PER; ++p)
+        if (key[n][p] > bk) {  // strictly larger: the lower expert keeps a tie
+          bk = key[n][p];
+          bj = p;
+          bv = v[n][p];
+        }
+      const uint32_t wk = __reduce_max_sync(0xffffffffu, bk);
+      const uint32_t we =
+          __reduce_min_sync(0xffffffffu, bk == wk ? static_cast<uint32_t>(lane + 32 * bj) : ~0u);
+      const int owner = static_cast<int>(we & 31u);
+      const float sv = __shfl_sync(0xffffffffu, bv, owner);
+      if (lane == owner) {
+#pragma unroll
+        for (int p = 0; p < PER; ++p)
+          if (p == bj) key[n][p] = 0u;
+      }
+      if (s == 0) l0[n] = sv;
+      if (lane == s) {
+        my_v[n] = sv;
+        my_i[n] = static_cast<int>(we);
+      }
+    }
+  }
+#pragma unroll
+  for (int n = 0; n < N; ++n) {
+    const float ex = (lane < k) ? expf(my_v[n] - l0[n]) : 0.f;
+    float sum = ex;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    id[n] = lane < k ? my_i[n] : -1;
+    w[n] = raw_weights ? my_v[n] : ex / sum;
+  }
 }
 
 }  // namespace router_detail

@@ -125,7 +125,16 @@ def run_layer(layer):
     return gl
 
 
-ROUTERS = ["mma", "tc"]
+# mma: the mma.sync router (E <= 16: in one launch with the dispatch); tc: the
+# tcgen05 router (17..256 experts: in one launch with the dispatch);
+# tc-separate: the split-K tcgen05 router and top-k kernels, then the dispatch
+ROUTERS = ["mma", "tc", "tc-separate"]
+
+
+def set_router(monkeypatch, router):
+    monkeypatch.setenv("CB_MOE_ROUTER", router.split("-")[0])
+    if router.endswith("-separate"):
+        monkeypatch.setenv("CB_MOE_ROUTE_DISPATCH", "0")
 
 
 # ------------------------------------------------------------- exact ties
@@ -142,7 +151,7 @@ TIE_SHAPES = {
 @pytest.mark.parametrize("router", ROUTERS)
 @pytest.mark.parametrize("name", list(TIE_SHAPES))
 def test_exact_logit_ties_go_to_the_lower_index(name, router, monkeypatch):
-    monkeypatch.setenv("CB_MOE_ROUTER", router)
+    set_router(monkeypatch, router)
     shape = synth.custom_shape("ties_" + name, seed=81, **TIE_SHAPES[name])
     x, wr = grid_router(np.random.default_rng(81), shape.T, shape.d, shape.E)
     rep = gh.full_check(make_layer(shape, x=x, wr=wr))
@@ -156,7 +165,7 @@ def test_exact_logit_ties_go_to_the_lower_index(name, router, monkeypatch):
 @pytest.mark.parametrize("E,k,bias", [(8, 2, 0.25), (8, 3, None), (40, 3, -1.5), (256, 16, 0.0)])
 def test_zero_router_weights_equal_bias(E, k, bias, router, monkeypatch):
     """Every expert ties: experts 0..k-1 in slot order, w = 1/k."""
-    monkeypatch.setenv("CB_MOE_ROUTER", router)
+    set_router(monkeypatch, router)
     shape = synth.custom_shape(f"zero_router_e{E}", T=333, d=256, f=256, E=E, k=k, seed=82)
     layer = make_layer(shape, wr=np.zeros((E, 256), np.float32),
                        bias=None if bias is None else np.full(E, bias, np.float32))
@@ -247,7 +256,7 @@ def test_zero_input_gives_zero_output(E, k, wdtype):
 @pytest.mark.parametrize("router", ROUTERS)
 @pytest.mark.parametrize("wdtype", ["bf16", "int8"])
 def test_softmax_top1_weight_is_exactly_one(wdtype, router, monkeypatch):
-    monkeypatch.setenv("CB_MOE_ROUTER", router)
+    set_router(monkeypatch, router)
     shape = synth.custom_shape(f"top1_{wdtype}", T=500, d=512, f=768, E=8, k=1, wdtype=wdtype, seed=86)
     layer = make_layer(shape)
     xv = synth.bf16_bits_to_f32(layer.x).astype(np.float64)

@@ -52,6 +52,13 @@ SMALL = {
     "int4_wide": synth.custom_shape("int4_wide", T=64, d=256, f=512, E=8, k=2, wdtype="int4", seed=112),
     "fp8_wide": synth.custom_shape("fp8_wide", T=128, d=512, f=512, E=4, k=2, wdtype="fp8", seed=113),
     "int8_wide_e64": synth.custom_shape("int8_wide_e64", T=100, d=256, f=512, E=64, k=6, wdtype="int8", seed=114),
+    # the tcgen05 router and dispatch in one launch: blocks of 264 tokens (passes of 128, 128
+    # and 8), 200 experts (padded to 256), 17 experts with one expert per token, 20 tokens on
+    # two blocks
+    "rdt_multi_pass": synth.custom_shape("rdt_multi_pass", T=40000, d=256, f=256, E=24, k=2, bias=True, seed=121),
+    "rdt_e200": synth.custom_shape("rdt_e200", T=900, d=768, f=256, E=200, k=8, seed=122),
+    "rdt_e17_k1": synth.custom_shape("rdt_e17_k1", T=500, d=256, f=256, E=17, k=1, seed=123),
+    "rdt_small_T": synth.custom_shape("rdt_small_T", T=20, d=512, f=256, E=64, k=6, seed=124),
 }
 
 FULL = {  # workload: random tokens checked beyond the first and last row of every m-tile (None: every token)
@@ -160,7 +167,8 @@ GUARD_CASES = [
     ("tiny", {}), ("odd_T", {}), ("int8_wide", {}), ("int4_wide", {}), ("ragged_mid", {"CB_MOE_PAIR": "1"}), ("ragged_mid", {"CB_MOE_ROUTE_DISPATCH": "0"}),
     ("many_units", {}),
     ("ragged_mid", {"CB_MOE_PAIR": "1", "CB_MOE_FUSED_COMBINE": "1"}), ("ragged_mid", {"CB_MOE_GATHER": "1"}),
-    ("three_mtiles", {"CB_MOE_PAIR": "1"}), ("skewed_small", {}), ("skewed_small", {"CB_MOE_DISPATCH": "split"}),
+    ("three_mtiles", {"CB_MOE_PAIR": "1"}), ("skewed_small", {}), ("skewed_small", {"CB_MOE_ROUTE_DISPATCH": "0"}),
+    ("skewed_small", {"CB_MOE_ROUTE_DISPATCH": "0", "CB_MOE_DISPATCH": "split"}), ("rdt_multi_pass", {}), ("rdt_e200", {}),
     ("e256_k16", {}), ("one_token_e32", {}), ("int8_k6", {}), ("int8_mid", {"CB_MOE_INT8": "smem"}),
     ("int4_k6", {}), ("fp8_mid", {}), ("hash", {}),
 ]
@@ -191,8 +199,9 @@ def test_kernels_stay_inside_the_workspace(name, env, monkeypatch):
 
 
 @pytest.mark.parametrize("name,expect", [
-    ("skewed_small", "T=1000 d=256 f=256 E=128 k=4 weights=bf16 gate=softmax router=tcgen05 dispatch=cooperative "
-                     "gemm=single-cta"),
+    ("skewed_small", "T=1000 d=256 f=256 E=128 k=4 weights=bf16 gate=softmax router=tcgen05 "
+                     "dispatch=fused-with-router gemm=single-cta"),
+    ("int8_k6", "E=64 k=6 weights=int8 gate=softmax router=tcgen05 dispatch=fused-with-router"),
     ("ragged_mid", "T=300 d=512 f=768 E=8 k=2 weights=bf16 gate=softmax router=mma dispatch=fused-with-router"),
     ("tiny", "T=64 d=256 f=512 E=8 k=2 weights=bf16 gate=softmax router=mma dispatch=router-ranked"),
     ("fp8_mid", "weights=fp8 gate=softmax router=mma dispatch=fused-with-router gemm=tensor-memory quantised"),
@@ -498,19 +507,21 @@ def test_dispatch_split_kernels_small(name, monkeypatch):
 
 @pytest.mark.parametrize("name,mode", [("skewed", "split"), ("int8", "coop"), ("int4", "coop"), ("fp8", "coop")])
 def test_dispatch_forced_full_size(name, mode, monkeypatch):
-    """The dispatch form that is not the default at this size: separate
-    kernels on the 128-expert layer, the cooperative launch past 65536
-    routed pairs."""
+    """With the separate router and dispatch launches, the dispatch form that
+    is not the default at this size: separate kernels on the 128-expert layer,
+    the cooperative launch past 65536 routed pairs."""
+    monkeypatch.setenv("CB_MOE_ROUTE_DISPATCH", "0")
     monkeypatch.setenv("CB_MOE_DISPATCH", mode)
     rep = gh.full_check(synth.make_layer(synth.WORKLOADS[name]), sample=FULL[name])
     print(name, mode, "dispatch", rep)
 
 
-def test_cooperative_dispatch_timeout():
+def test_cooperative_dispatch_timeout(monkeypatch):
     """The cooperative dispatch's grid barrier, made to wait for a block that
     does not exist (CB_FLAG_TEST_STALL_DISPATCH, 1 ms bound), ends with
     CB_ERR_TIMEOUT and leaves the device usable; a new handle is correct."""
     import mixture_experts_router_gb300 as cb
+    monkeypatch.setenv("CB_MOE_ROUTE_DISPATCH", "0")
     layer = synth.make_layer(SMALL["skewed_small"])
     gl = gh.GpuLayer(layer, flags=cb.CB_FLAG_TEST_STALL_DISPATCH)
     try:
@@ -525,17 +536,18 @@ def test_cooperative_dispatch_timeout():
 
 
 @pytest.mark.parametrize("fused,name,d,expect", [
-    ("1", "mixtral_prefill", 256, 6), ("1", "skewed", 256, 6), ("0", "mixtral_prefill", 256, 5),
+    ("1", "mixtral_prefill", 256, 6), ("1", "skewed", 256, 4), ("0", "mixtral_prefill", 256, 5),
     ("0", "skewed", 256, 6), ("split", "mixtral_prefill", 256, 6), ("split", "skewed", 256, 9),
     ("1", "mixtral_prefill", 512, 4), ("1", "mixtral_decode", 512, 4), ("rd0", "mixtral_prefill", 512, 6),
-    ("1", "skewed", 512, 6)])
+    ("1", "skewed", 512, 4), ("rd0", "skewed", 512, 6), ("1", "int8", 512, 4)])
 def test_kernels_per_forward(fused, name, d, expect, monkeypatch):
-    """The launch count the library reports: router (the tcgen05 router of wide
-    layers: partial logits + top-k), dispatch kernels (none when the router's
-    launch also dispatches: up to 16 experts and d a multiple of 512; block
-    scan + row copy after the mma router's per-block ranks; else one
-    cooperative launch, or with CB_MOE_DISPATCH=split one-block /
-    count-scan-scatter ranking + row copy), two grouped GEMMs, combine."""
+    """The launch count the library reports: router (the separate tcgen05
+    router of wide layers: partial logits + top-k), dispatch kernels (none
+    when the router's launch also dispatches: up to 16 experts and d a
+    multiple of 512, or 17 to 256 experts; block scan + row copy after the
+    mma router's per-block ranks; else one cooperative launch, or with
+    CB_MOE_DISPATCH=split one-block / count-scan-scatter ranking + row copy),
+    two grouped GEMMs, combine."""
     if fused in ("0", "split"):
         monkeypatch.setenv("CB_MOE_FUSED_RANKS", "0")
     if fused == "split":
@@ -696,7 +708,8 @@ def test_programmatic_dependent_launch(name, monkeypatch):
 
 
 ROUTE_DISPATCH_SMALL = ["ragged_mid", "three_mtiles", "odd_T", "int8_mid", "many_units", "e16_d512", "e3_k3_d1024",
-                        "rd_one_expert", "rd_k_equals_E", "rd_long", "rd_e16_k16", "rd_bias"]
+                        "rd_one_expert", "rd_k_equals_E", "rd_long", "rd_e16_k16", "rd_bias",
+                        "skewed_small", "e256_k16", "int8_k6", "one_token_e32", "rdt_multi_pass", "rdt_e200"]
 
 
 @pytest.mark.parametrize("name", ROUTE_DISPATCH_SMALL)
@@ -709,7 +722,7 @@ def test_separate_router_and_dispatch_small(name, monkeypatch):
     print(name, "separate router and dispatch", rep)
 
 
-@pytest.mark.parametrize("name", ["mixtral_prefill", "mixtral_decode"])
+@pytest.mark.parametrize("name", ["mixtral_prefill", "mixtral_decode", "skewed"])
 def test_separate_router_and_dispatch_full_size(name, monkeypatch):
     monkeypatch.setenv("CB_MOE_ROUTE_DISPATCH", "0")
     rep = gh.full_check(synth.make_layer(synth.WORKLOADS[name]), sample=FULL[name])
@@ -753,6 +766,44 @@ def test_fused_route_dispatch_timeout():
         gl.close()
     rep = gh.full_check(layer)
     assert rep["f32_max_abs"] <= gh.MAX_ABS
+
+
+def test_fused_tc_route_dispatch_timeout():
+    """The grid barrier of the tcgen05 router + dispatch launch, made to wait
+    for a block that does not exist (CB_FLAG_TEST_STALL_DISPATCH, 1 ms
+    bound), ends with CB_ERR_TIMEOUT and leaves the device usable."""
+    import mixture_experts_router_gb300 as cb
+    layer = synth.make_layer(SMALL["skewed_small"])
+    gl = gh.GpuLayer(layer, flags=cb.CB_FLAG_TEST_STALL_DISPATCH)
+    try:
+        assert gl.m.kernels_per_forward() == 4
+        gl.m.forward(gl.x, gl.out)
+        torch.cuda.synchronize()
+        assert gl.m.last_error() == cb.CB_ERR_TIMEOUT
+    finally:
+        gl.close()
+    rep = gh.full_check(layer)
+    assert rep["f32_max_abs"] <= gh.MAX_ABS
+
+
+@pytest.mark.parametrize("name", ["rdt_multi_pass", "rdt_e200", "rdt_e17_k1", "rdt_small_T", "one_token_e32",
+                                  "three_tokens_e64", "e256_k16", "int8_wide_e64"])
+def test_fused_tc_route_dispatch_edges(name):
+    """The tcgen05 router + dispatch launch on its edges: blocks of several
+    128-token passes (with a bias, and the raw-logit gate on the same layer),
+    expert counts that pad to 256 and to 32, one expert per token, one to
+    twenty tokens, 256 experts with k = 16."""
+    layer = synth.make_layer(SMALL[name])
+    gl = gh.GpuLayer(layer)
+    try:
+        assert gl.m.kernels_per_forward() == 4
+    finally:
+        gl.close()
+    rep = gh.full_check(layer)
+    print(name, "fused tcgen05", rep)
+    if name == "rdt_multi_pass":
+        rep = gh.full_check(synth.make_layer(synth.with_router(SMALL[name], "raw")))
+        print(name, "fused tcgen05 raw", rep)
 
 
 @pytest.mark.parametrize("name", ["rd_one_expert", "rd_k_equals_E", "rd_long", "rd_e16_k16", "rd_bias"])
