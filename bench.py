@@ -112,7 +112,7 @@ def algorithmic_work(shape, counts):
 
 
 class ClockSampler:
-    """nvidia-smi samples (every 100 ms) of SM clock and throttle reasons."""
+    """nvidia-smi samples (every 20 ms) of SM clock and throttle reasons."""
 
     FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -122,7 +122,7 @@ class ClockSampler:
         self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                                          "-lms", "100", "-i", str(device)], stdout=self.file,
+                                          "-lms", "20", "-i", str(device)], stdout=self.file,
                                          stderr=subprocess.DEVNULL)
         except (FileNotFoundError, OSError):
             self.proc = None
@@ -149,13 +149,19 @@ class ClockSampler:
                 except ValueError:
                     continue
         os.unlink(self.file.name)
-        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05] or rows
+        inside = [r for r in rows if t0 - 0.02 <= r[0] <= t1 + 0.02]
+        nearest = not inside
+        if nearest:  # a timed region shorter than the sampling interval: the samples closest to it
+            inside = sorted(rows, key=lambda r: abs(r[0] - 0.5 * (t0 + t1)))[:2]
         if not inside:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({n for r in inside for n, v in zip(names, r[3]) if v.lower().startswith("active")})
-        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
-                "reasons": reasons, "samples": len(inside)}
+        out = {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+               "reasons": reasons, "samples": len(inside)}
+        if nearest:
+            out["nearest"] = True
+        return out
 
 
 def gemm_source_digest(sources=None) -> str:
