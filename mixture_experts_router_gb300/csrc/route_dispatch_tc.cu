@@ -7,16 +7,17 @@
 //
 // One block per SM.  Block b owns the tokens [b T / G, (b + 1) T / G):
 //   1. the logits of its tokens on the tensor cores, up to 128 tokens per
-//      pass: TMA streams the block's rows of x (a box of just the rows it
-//      owns, so no SM loads a neighbour's rows) and the router weights (E
-//      padded to NP rows, the padding read as zeros) through a ring of
-//      shared-memory stages; one thread issues M = 128, N = NP MMAs into
-//      TMEM, each K step of 16 into the next of 512 / NP accumulators (in
-//      turn), so that consecutive MMAs are independent and no fp32
-//      accumulation chain inside the tensor core runs longer than
-//      d / (16 * 512 / NP) steps.  The epilogue sums the accumulators in
-//      a fixed order, adds the bias and leaves the logits in shared memory
-//      (over the then idle ring); one warp per token takes the gate;
+//      pass: two producer threads stream, by TMA, the block's rows of x (a
+//      box of just the rows it owns, so no SM loads a neighbour's rows) and
+//      the router weights (E padded to NP rows, the padding read as zeros)
+//      through two rings of shared-memory stages; one thread issues
+//      M = 128, N = NP MMAs into TMEM, each K step of 16 into the next of
+//      512 / NP accumulators (in turn), so that consecutive MMAs are
+//      independent and no fp32 accumulation chain inside the tensor core
+//      runs longer than d / (16 * 512 / NP) steps.  The epilogue sums the
+//      accumulators in a fixed order, adds the bias and leaves the logits in
+//      shared memory (over the then idle rings); one warp per 2 to 8 tokens
+//      takes the gate;
 //   2. ranks of its pairs within the block, in (token, slot) order
 //      (match-any groups per warp, then a scan over the warps), and its
 //      per-expert counts -> chunk[b][e];
@@ -28,7 +29,9 @@
 //      maps follow by a scan, which block 0 publishes;
 //   5. the global ranks of its pairs (offset + base + in-block rank) into tok
 //      and inv, and the copy of its tokens' rows, Xp[row(t, s)] = x[t], whose
-//      rows were read in step 1 a few microseconds earlier and come from L2.
+//      rows were read in step 1 a few microseconds earlier and come from L2
+//      when x fits there (33.6 MB of the 128-expert layer does; the int8
+//      layer's 134 MB is read from HBM again).
 // Compared with the separate tcgen05 router (split-K partial logits, then a
 // top-k kernel) and the cooperative dispatch, x crosses HBM once instead of
 // twice and two kernel boundaries are gone.  The ranks are the canonical
