@@ -180,6 +180,42 @@ def test_zero_router_weights_equal_bias(E, k, bias, router, monkeypatch):
     assert rep["exact_tie_tokens"] == shape.T
 
 
+# ------------------------------------------------------------ NaN logits
+BF16_NAN = 0x7FC0
+
+
+@pytest.mark.parametrize("router", ROUTERS)
+@pytest.mark.parametrize("E,k", [(8, 2), (40, 3)])
+def test_nan_logits_rank_after_every_number(E, k, router, monkeypatch):
+    """A router row of NaN (expert 5's logit NaN for every token) and a token
+    whose x is NaN (all its logits NaN).  NaN ranks after every number and,
+    among NaNs, the lower index first: expert 5 is never chosen while numbers
+    are left, and the NaN token takes experts 0..k-1 in slot order with NaN
+    weights.  Every other token's ids (slot order) and weights match the
+    oracle's; with this seed no other token has a gap below 2e-4."""
+    import oracle
+    set_router(monkeypatch, router)
+    shape = synth.custom_shape(f"nan_e{E}_k{k}", T=200, d=256, f=256, E=E, k=k, seed=89)
+    layer = synth.make_layer(shape)
+    layer.wr = layer.wr.copy()
+    layer.wr[5, :] = BF16_NAN
+    layer.x = layer.x.copy()
+    layer.x[7, :] = BF16_NAN
+    oids, ow, _, _ = oracle.Oracle(layer).route()
+    gl = run_layer(layer)
+    try:
+        r = gl.routing()
+        ids, w = r["ids"], r["w"]
+        assert np.array_equal(ids[7], np.arange(k, dtype=np.int32))
+        assert np.all(np.isnan(w[7]))
+        rest = np.arange(shape.T) != 7
+        assert not np.any(ids[rest] == 5)
+        assert np.array_equal(ids, oids)
+        assert np.abs(w[rest] - ow[rest]).max() <= 1e-5
+    finally:
+        gl.close()
+
+
 # --------------------------------------------------------- closed forms
 IDENTICAL = [  # (name, shape kwargs, environment)
     ("bf16_e8", dict(T=300, d=512, f=768, E=8, k=2), {}),
